@@ -1,0 +1,484 @@
+// C ABI of the split-residency MoE layer: context, banks, row maps, usage
+// table, swaps and probes.  Kernels live in route_split.cu, ffn_simt.cu,
+// ffn_tc.cu and finalize.cu.
+#include "moe_internal.cuh"
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <thread>
+
+namespace moe {
+
+std::atomic<int64_t> g_launches{0};
+static thread_local std::string g_last_error = "ok";
+
+int set_error(int code, const std::string &msg) {
+    g_last_error = msg;
+    return code;
+}
+
+int cuda_error(cudaError_t e, const char *what) {
+    std::string m = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    if (e == cudaErrorMemoryAllocation) return set_error(MOE_ENOMEM, m);
+    return set_error(MOE_ECUDA, m);
+}
+
+// Run f(i) for i in [0, n) on up to `threads` host threads.
+template <class F>
+static void parallel_for(int n, F f) {
+    int threads = (int)std::max(1u, std::min(32u, std::thread::hardware_concurrency()));
+    threads = std::min(threads, n);
+    if (threads <= 1) {
+        for (int i = 0; i < n; ++i) f(i);
+        return;
+    }
+    std::atomic<int> next{0};
+    std::vector<std::thread> pool;
+    for (int t = 0; t < threads; ++t)
+        pool.emplace_back([&]() {
+            for (int i = next.fetch_add(1); i < n; i = next.fetch_add(1)) f(i);
+        });
+    for (auto &th : pool) th.join();
+}
+
+// Logical MXFP4 expert -> tiled device layout (see moe_internal.cuh).
+// Returns false if a scale byte lies outside [104, 140].
+static bool repack_expert(const Geom &g, const uint8_t *w13_q, const uint8_t *w13_s,
+                          const uint8_t *w2_q, const uint8_t *w2_s, uint8_t *dst) {
+    const int H = g.H, I = g.I;
+    bool ok = true;
+    for (int mt = 0; mt < g.mt13; ++mt) {
+        for (int c = 0; c < g.kc13; ++c) {
+            uint8_t *chunk = dst + ((int64_t)mt * g.kc13 + c) * kChunkBytes;
+            for (int m = 0; m < kMT; ++m) {
+                int w = m / 32, l = m % 32;
+                int64_t row = (l < 16 ? 0 : I) + 64 * mt + 16 * w + (l % 16);
+                const uint8_t *q = w13_q + row * (H / 2) + c * 32;
+                std::memcpy(chunk + m * 16, q, 16);
+                std::memcpy(chunk + 2048 + m * 16, q + 16, 16);
+                const uint8_t *s = w13_s + row * (H / 32) + 2 * c;
+                chunk[kChunkQBytes + 2 * m] = s[0];
+                chunk[kChunkQBytes + 2 * m + 1] = s[1];
+                ok &= s[0] >= 104 && s[0] <= 140 && s[1] >= 104 && s[1] <= 140;
+            }
+        }
+    }
+    for (int mt = 0; mt < g.mt2; ++mt) {
+        for (int c = 0; c < g.kc2; ++c) {
+            uint8_t *chunk = dst + g.w2_off + ((int64_t)mt * g.kc2 + c) * kChunkBytes;
+            for (int m = 0; m < kMT; ++m) {
+                int64_t row = (int64_t)kMT * mt + m;
+                const uint8_t *q = w2_q + row * (I / 2) + c * 32;
+                std::memcpy(chunk + m * 16, q, 16);
+                std::memcpy(chunk + 2048 + m * 16, q + 16, 16);
+                const uint8_t *s = w2_s + row * (I / 32) + 2 * c;
+                chunk[kChunkQBytes + 2 * m] = s[0];
+                chunk[kChunkQBytes + 2 * m + 1] = s[1];
+                ok &= s[0] >= 104 && s[0] <= 140 && s[1] >= 104 && s[1] <= 140;
+            }
+        }
+    }
+    return ok;
+}
+
+static void free_layer(moe::Layer &L) {
+    if (L.hot) cudaFree(L.hot);
+    if (L.cold_host) cudaFreeHost(L.cold_host);
+    if (L.rowmap_dev) cudaFree(L.rowmap_dev);
+    L = moe::Layer();
+}
+
+static int check_ctx(const moe_ctx *ctx) {
+    if (!ctx) return set_error(MOE_EINVAL, "null context");
+    return MOE_OK;
+}
+
+static int check_layer(moe_ctx *ctx, int layer, bool need_init) {
+    if (int r = check_ctx(ctx)) return r;
+    if (layer < 0 || layer >= ctx->g.L) return set_error(MOE_EINVAL, "layer out of range");
+    if (need_init && !ctx->layers[layer].init)
+        return set_error(MOE_ESTATE, "layer has no banks (call moe_init_banks first)");
+    return MOE_OK;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        cudaGetDevice(&prev);
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_last_error(void) { return g_last_error.c_str(); }
+
+int64_t moe_expert_bytes(int32_t hidden, int32_t inter) {
+    int64_t n = 2LL * inter * hidden + (int64_t)hidden * inter;
+    return n / 2 + n / 32;
+}
+
+int moe_create(const moe_geom *geom, int device, moe_ctx **out) {
+    if (!geom || !out) return set_error(MOE_EINVAL, "null argument");
+    *out = nullptr;
+    const moe_geom &g = *geom;
+    if (g.layers < 1 || g.experts < 2 || g.experts > 1024 || g.top_k < 1 || g.top_k > 16 ||
+        g.top_k > g.experts || g.hidden < 128 || g.hidden % 128 || g.inter < 64 || g.inter % 64 ||
+        g.max_tokens < 1 || g.count_tmax < 0)
+        return set_error(MOE_EINVAL, "invalid geometry (need E in 2..1024, k in 1..min(16,E), "
+                                     "H % 128 == 0, I % 64 == 0, T_max >= 1)");
+    if ((int64_t)g.max_tokens * g.top_k > (1 << 24))
+        return set_error(MOE_EINVAL, "max_tokens * top_k too large");
+    int ndev = 0;
+    MOE_CUDA_TRY(cudaGetDeviceCount(&ndev));
+    if (device < 0 || device >= ndev) return set_error(MOE_EINVAL, "no such CUDA device");
+    DeviceGuard guard(device);
+    moe_ctx *ctx = new moe_ctx();
+    ctx->g = make_geom(g);
+    ctx->device = device;
+    ctx->layers.resize(g.layers);
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDeviceProperties(&prop, device);
+    if (e == cudaSuccess) ctx->sms = prop.multiProcessorCount;
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->counts_dev, sizeof(int32_t) * g.layers * g.experts);
+    if (e == cudaSuccess) e = cudaMemset(ctx->counts_dev, 0, sizeof(int32_t) * g.layers * g.experts);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->staging, ctx->g.eb);
+    if (e == cudaSuccess) e = cudaMalloc(&ctx->status_dev, sizeof(int32_t) * 4);
+    if (e == cudaSuccess) e = cudaMemset(ctx->status_dev, 0, sizeof(int32_t) * 4);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        int r = cuda_error(e, "moe_create allocation");
+        moe_destroy(ctx);
+        return r;
+    }
+    *out = ctx;
+    return MOE_OK;
+}
+
+int moe_destroy(moe_ctx *ctx) {
+    if (!ctx) return MOE_OK;
+    DeviceGuard guard(ctx->device);
+    cudaDeviceSynchronize();
+    for (auto &L : ctx->layers) free_layer(L);
+    if (ctx->counts_dev) cudaFree(ctx->counts_dev);
+    if (ctx->staging) cudaFree(ctx->staging);
+    if (ctx->status_dev) cudaFree(ctx->status_dev);
+    if (ctx->probe_host) cudaFreeHost(ctx->probe_host);
+    if (ctx->probe_dev) cudaFree(ctx->probe_dev);
+    delete ctx;
+    return MOE_OK;
+}
+
+int moe_set_ffn_impl(moe_ctx *ctx, int impl) {
+    if (int r = check_ctx(ctx)) return r;
+    if (impl != MOE_FFN_TCGEN05 && impl != MOE_FFN_SIMT) return set_error(MOE_EINVAL, "unknown FFN impl");
+    ctx->ffn_impl = impl;
+    return MOE_OK;
+}
+
+int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t *w13_s,
+                   const uint8_t *w2_q, const uint8_t *w2_s, const uint8_t *is_hot, void *stream) {
+    if (int r = check_layer(ctx, layer, false)) return r;
+    if (!w13_q || !w13_s || !w2_q || !w2_s || !is_hot) return set_error(MOE_EINVAL, "null weight pointer");
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    const Geom &g = ctx->g;
+    Layer &L = ctx->layers[layer];
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    free_layer(L);
+
+    std::vector<int32_t> rowmap(g.E);
+    std::vector<int> hot_ids, cold_ids;
+    for (int e = 0; e < g.E; ++e) {
+        if (is_hot[e]) { rowmap[e] = (int32_t)hot_ids.size(); hot_ids.push_back(e); }
+        else { rowmap[e] = -1 - (int32_t)cold_ids.size(); cold_ids.push_back(e); }
+    }
+    const size_t q13 = (size_t)2 * g.I * (g.H / 2), s13 = (size_t)2 * g.I * (g.H / 32);
+    const size_t q2 = (size_t)g.H * (g.I / 2), s2 = (size_t)g.H * (g.I / 32);
+    auto repack = [&](int e, uint8_t *dst) {
+        return repack_expert(g, w13_q + e * q13, w13_s + e * s13, w2_q + e * q2, w2_s + e * s2, dst);
+    };
+
+    Layer nl;
+    nl.n_hot = (int)hot_ids.size();
+    nl.n_cold = (int)cold_ids.size();
+    cudaError_t e = cudaSuccess;
+    std::atomic<bool> scales_ok{true};
+    if (nl.n_hot) e = cudaMalloc(&nl.hot, (size_t)nl.n_hot * g.eb);
+    if (e == cudaSuccess && nl.n_cold) {
+        e = cudaHostAlloc(&nl.cold_host, (size_t)nl.n_cold * g.eb, cudaHostAllocMapped | cudaHostAllocPortable);
+        if (e == cudaSuccess) e = cudaHostGetDevicePointer((void **)&nl.cold_dev, nl.cold_host, 0);
+    }
+    if (e == cudaSuccess) e = cudaMalloc(&nl.rowmap_dev, sizeof(int32_t) * g.E);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(nl.rowmap_dev, rowmap.data(), sizeof(int32_t) * g.E, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) {
+        int r = cuda_error(e, "moe_init_banks allocation");
+        free_layer(nl);
+        return r;
+    }
+    // cold rows: repack straight into the pinned bank
+    parallel_for((int)cold_ids.size(), [&](int i) {
+        if (!repack(cold_ids[i], nl.cold_host + (size_t)i * g.eb)) scales_ok = false;
+    });
+    // hot rows: repack into pinned staging, batch by batch, then copy to HBM
+    if (nl.n_hot) {
+        const int batch = std::min(nl.n_hot, 16);
+        uint8_t *pin = nullptr;
+        e = cudaHostAlloc(&pin, (size_t)batch * g.eb, cudaHostAllocDefault);
+        for (int b0 = 0; e == cudaSuccess && b0 < nl.n_hot; b0 += batch) {
+            int nb = std::min(batch, nl.n_hot - b0);
+            parallel_for(nb, [&](int i) {
+                if (!repack(hot_ids[b0 + i], pin + (size_t)i * g.eb)) scales_ok = false;
+            });
+            e = cudaMemcpyAsync(nl.hot + (size_t)b0 * g.eb, pin, (size_t)nb * g.eb, cudaMemcpyHostToDevice, s);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        }
+        if (pin) cudaFreeHost(pin);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        int r = cuda_error(e, "moe_init_banks copy");
+        free_layer(nl);
+        return r;
+    }
+    if (!scales_ok) {
+        free_layer(nl);
+        return set_error(MOE_EINVAL, "e8m0 scale byte outside [104, 140]");
+    }
+    nl.rowmap = std::move(rowmap);
+    nl.init = true;
+    L = std::move(nl);
+    return MOE_OK;
+}
+
+int moe_workspace_bytes(const moe_ctx *ctx, int T, size_t *bytes) {
+    if (int r = check_ctx(ctx)) return r;
+    if (!bytes || T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "T out of range");
+    *bytes = ws_layout(ctx->g, T).total;
+    return MOE_OK;
+}
+
+int moe_route_split_count(moe_ctx *ctx, int layer, const float *logits, int T, int count_on,
+                          int32_t *ids, float *w, void *ws, void *stream) {
+    if (int r = check_layer(ctx, layer, true)) return r;
+    if (T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "T out of range");
+    if (T > 0 && (!logits || !ids || !w || !ws)) return set_error(MOE_EINVAL, "null pointer");
+    if (!ws) return set_error(MOE_EINVAL, "null workspace");
+    if ((uintptr_t)ws % 256) return set_error(MOE_EINVAL, "workspace must be 256-byte aligned");
+    DeviceGuard guard(ctx->device);
+    return launch_route_split(ctx, layer, logits, T, count_on, ids, w, (uint8_t *)ws, (cudaStream_t)stream);
+}
+
+int moe_read_split(moe_ctx *ctx, const void *ws, int T, int bank, int32_t *n_act, int32_t *n_picks,
+                   int32_t *act_row, int32_t *act_off, int32_t *picks, void *stream) {
+    if (int r = check_ctx(ctx)) return r;
+    if (!ws || T < 0 || T > ctx->g.Tmax || (bank != 0 && bank != 1) || !n_act || !n_picks || !act_row ||
+        !act_off || !picks)
+        return set_error(MOE_EINVAL, "bad moe_read_split arguments");
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    const WsLayout lay = ws_layout(ctx->g, T);
+    const size_t P = (size_t)T * ctx->g.k;
+    const uint8_t *base = (const uint8_t *)ws;
+    int32_t hdr[kHdrWords];
+    MOE_CUDA_TRY(cudaMemcpyAsync(hdr, base + lay.hdr, sizeof hdr, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    *n_act = hdr[kHdrNAct + bank];
+    *n_picks = hdr[kHdrNPicks + bank];
+    if (*n_act < 0 || (size_t)*n_act > P || *n_picks < 0 || (size_t)*n_picks > P)
+        return set_error(MOE_ESTATE, "workspace does not hold a routed step of this T");
+    MOE_CUDA_TRY(cudaMemcpyAsync(act_row, base + lay.act_row + bank * P * 4, sizeof(int32_t) * *n_act,
+                                 cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaMemcpyAsync(act_off, base + lay.act_off + bank * (P + 1) * 4, sizeof(int32_t) * (*n_act + 1),
+                                 cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaMemcpyAsync(picks, base + lay.picks + bank * P * 4, sizeof(int32_t) * *n_picks,
+                                 cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    return MOE_OK;
+}
+
+int moe_expert_ffn_bank(moe_ctx *ctx, int layer, int bank, const uint16_t *x, int T, void *ws,
+                        uint16_t *Y, void *stream) {
+    if (int r = check_layer(ctx, layer, true)) return r;
+    if (bank != MOE_BANK_HOT && bank != MOE_BANK_COLD) return set_error(MOE_EINVAL, "bank must be 0 or 1");
+    if (T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "T out of range");
+    if (!ws || (uintptr_t)ws % 256) return set_error(MOE_EINVAL, "workspace must be non-null and 256-byte aligned");
+    if (T > 0 && (!x || !Y)) return set_error(MOE_EINVAL, "null pointer");
+    if (((uintptr_t)x | (uintptr_t)Y) % 16) return set_error(MOE_EINVAL, "x and Y must be 16-byte aligned");
+    Layer &L = ctx->layers[layer];
+    const uint8_t *base = bank == MOE_BANK_HOT ? L.hot : L.cold_dev;
+    int rows = bank == MOE_BANK_HOT ? L.n_hot : L.n_cold;
+    if (T == 0 || rows == 0) return MOE_OK;
+    DeviceGuard guard(ctx->device);
+    if (ctx->ffn_impl == MOE_FFN_SIMT)
+        return launch_ffn_simt(ctx, base, bank, x, T, (uint8_t *)ws, Y, (cudaStream_t)stream);
+    return launch_ffn_tc(ctx, base, bank, x, T, (uint8_t *)ws, Y, (cudaStream_t)stream);
+}
+
+int moe_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_t *out, void *stream) {
+    if (T < 0 || k < 1 || k > 16 || H < 8 || H % 8) return set_error(MOE_EINVAL, "bad finalize shape (H % 8 == 0)");
+    if (T == 0) return MOE_OK;
+    if (!Y || !w || !out) return set_error(MOE_EINVAL, "null pointer");
+    if (((uintptr_t)Y | (uintptr_t)out) % 16) return set_error(MOE_EINVAL, "Y and out must be 16-byte aligned");
+    return launch_finalize(Y, w, T, k, H, out, (cudaStream_t)stream);
+}
+
+int moe_swap_rows(moe_ctx *ctx, int layer, int n, const int32_t *promote, const int32_t *demote,
+                  int32_t *applied, void *stream) {
+    if (int r = check_layer(ctx, layer, true)) return r;
+    if (n < 0 || (n > 0 && (!promote || !demote))) return set_error(MOE_EINVAL, "bad swap list");
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    Layer &L = ctx->layers[layer];
+    const Geom &g = ctx->g;
+    int done = 0;
+    for (int i = 0; i < n; ++i) {
+        int32_t c = promote[i], h = demote[i];
+        bool ok = c >= 0 && c < g.E && h >= 0 && h < g.E && c != h && L.rowmap[c] < 0 && L.rowmap[h] >= 0;
+        if (applied) applied[i] = ok ? 1 : 0;
+        if (!ok) continue;
+        int32_t hot_row = L.rowmap[h];
+        int32_t cold_row = -1 - L.rowmap[c];
+        uint8_t *hot_p = L.hot + (size_t)hot_row * g.eb;
+        uint8_t *cold_p = L.cold_host + (size_t)cold_row * g.eb;
+        MOE_CUDA_TRY(cudaMemcpyAsync(ctx->staging, hot_p, g.eb, cudaMemcpyDeviceToDevice, s));
+        MOE_CUDA_TRY(cudaMemcpyAsync(hot_p, cold_p, g.eb, cudaMemcpyHostToDevice, s));
+        MOE_CUDA_TRY(cudaMemcpyAsync(cold_p, ctx->staging, g.eb, cudaMemcpyDeviceToHost, s));
+        if (int r = launch_rowmap_write(L.rowmap_dev, c, hot_row, h, -1 - cold_row, s)) return r;
+        L.rowmap[c] = hot_row;
+        L.rowmap[h] = -1 - cold_row;
+        ++done;
+    }
+    return done;
+}
+
+int moe_read_counts(moe_ctx *ctx, int32_t *host_out, void *stream) {
+    if (int r = check_ctx(ctx)) return r;
+    if (!host_out) return set_error(MOE_EINVAL, "null output");
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    MOE_CUDA_TRY(cudaMemcpyAsync(host_out, ctx->counts_dev, sizeof(int32_t) * ctx->g.L * ctx->g.E,
+                                 cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    return MOE_OK;
+}
+
+int moe_reset_counts(moe_ctx *ctx, void *stream) {
+    if (int r = check_ctx(ctx)) return r;
+    DeviceGuard guard(ctx->device);
+    MOE_CUDA_TRY(cudaMemsetAsync(ctx->counts_dev, 0, sizeof(int32_t) * ctx->g.L * ctx->g.E, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+int moe_bank_rows(moe_ctx *ctx, int layer, int32_t *n_hot, int32_t *n_cold) {
+    if (int r = check_layer(ctx, layer, true)) return r;
+    if (n_hot) *n_hot = ctx->layers[layer].n_hot;
+    if (n_cold) *n_cold = ctx->layers[layer].n_cold;
+    return MOE_OK;
+}
+
+int moe_get_rowmap(moe_ctx *ctx, int layer, int32_t *host_out) {
+    if (int r = check_layer(ctx, layer, true)) return r;
+    if (!host_out) return set_error(MOE_EINVAL, "null output");
+    std::memcpy(host_out, ctx->layers[layer].rowmap.data(), sizeof(int32_t) * ctx->g.E);
+    return MOE_OK;
+}
+
+int moe_read_rowmap_device(moe_ctx *ctx, int layer, int32_t *host_out, void *stream) {
+    if (int r = check_layer(ctx, layer, true)) return r;
+    if (!host_out) return set_error(MOE_EINVAL, "null output");
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    MOE_CUDA_TRY(cudaMemcpyAsync(host_out, ctx->layers[layer].rowmap_dev, sizeof(int32_t) * ctx->g.E,
+                                 cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    return MOE_OK;
+}
+
+int moe_read_bank_row(moe_ctx *ctx, int layer, int bank, int row, uint8_t *host_out, void *stream) {
+    if (int r = check_layer(ctx, layer, true)) return r;
+    Layer &L = ctx->layers[layer];
+    int rows = bank == MOE_BANK_HOT ? L.n_hot : (bank == MOE_BANK_COLD ? L.n_cold : -1);
+    if (row < 0 || row >= rows || !host_out) return set_error(MOE_EINVAL, "bank/row out of range");
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    if (bank == MOE_BANK_HOT) {
+        MOE_CUDA_TRY(cudaMemcpyAsync(host_out, L.hot + (size_t)row * ctx->g.eb, ctx->g.eb, cudaMemcpyDeviceToHost, s));
+        MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    } else {
+        std::memcpy(host_out, L.cold_host + (size_t)row * ctx->g.eb, ctx->g.eb);
+    }
+    return MOE_OK;
+}
+
+int moe_probe_link(moe_ctx *ctx, size_t bytes, int iters, double *gbps, double *hbm_gbps) {
+    if (int r = check_ctx(ctx)) return r;
+    if (!gbps || bytes < (1 << 20) || iters < 1) return set_error(MOE_EINVAL, "bad probe arguments");
+    bytes &= ~size_t(4095);
+    DeviceGuard guard(ctx->device);
+    if (ctx->probe_bytes < bytes) {
+        if (ctx->probe_host) cudaFreeHost(ctx->probe_host);
+        if (ctx->probe_dev) cudaFree(ctx->probe_dev);
+        ctx->probe_host = nullptr;
+        ctx->probe_dev = nullptr;
+        ctx->probe_bytes = 0;
+        MOE_CUDA_TRY(cudaHostAlloc(&ctx->probe_host, bytes, cudaHostAllocMapped | cudaHostAllocPortable));
+        std::memset(ctx->probe_host, 0x5A, bytes);
+        MOE_CUDA_TRY(cudaMalloc(&ctx->probe_dev, bytes));
+        MOE_CUDA_TRY(cudaMemset(ctx->probe_dev, 0x5A, bytes));
+        ctx->probe_bytes = bytes;
+    }
+    uint8_t *host_dev = nullptr;
+    MOE_CUDA_TRY(cudaHostGetDevicePointer((void **)&host_dev, ctx->probe_host, 0));
+    uint64_t *sink = nullptr;
+    MOE_CUDA_TRY(cudaMalloc(&sink, sizeof(uint64_t) * 65536));
+    cudaEvent_t a, b;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    int blocks = ctx->sms * 8;
+    auto measure = [&](const uint8_t *src, double *best) -> int {
+        *best = 0.0;
+        for (int it = 0; it < iters + 1; ++it) {
+            cudaEventRecord(a, 0);
+            if (int r = launch_probe_read(src, bytes, sink, blocks, 0)) return r;
+            cudaEventRecord(b, 0);
+            MOE_CUDA_TRY(cudaEventSynchronize(b));
+            float ms = 0.f;
+            cudaEventElapsedTime(&ms, a, b);
+            if (it > 0) *best = std::max(*best, (double)bytes / (ms * 1e-3) / 1e9);
+        }
+        return MOE_OK;
+    };
+    int r = measure(host_dev, gbps);
+    if (!r && hbm_gbps) r = measure(ctx->probe_dev, hbm_gbps);
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    cudaFree(sink);
+    return r;
+}
+
+int moe_device_status(moe_ctx *ctx, int32_t *status) {
+    if (int r = check_ctx(ctx)) return r;
+    DeviceGuard guard(ctx->device);
+    int32_t v[4] = {0, 0, 0, 0};
+    MOE_CUDA_TRY(cudaDeviceSynchronize());
+    MOE_CUDA_TRY(cudaMemcpy(v, ctx->status_dev, sizeof v, cudaMemcpyDeviceToHost));
+    MOE_CUDA_TRY(cudaMemset(ctx->status_dev, 0, sizeof v));
+    if (status) *status = v[0];
+    return MOE_OK;
+}
+
+int64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+"""Layer-step orchestration over the C ABI (streams and buffers only).
+
+One layer-step ("vLLM: Pin Hot Experts", Results):
+    route + split + count            (moe_route_split_count, main stream)
+    hot-bank FFN   || cold-bank FFN  (moe_expert_ffn_bank on the main stream
+                                      and on a second stream, joined by events)
+    finalize                         (moe_finalize, main stream)
+The hot bank streams HBM and the cold bank streams the host link, so the two
+run concurrently.  PyTorch provides the device buffers and streams.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (MOE_BANK_COLD, MOE_BANK_HOT, moe_expert_ffn_bank, moe_finalize,
+               moe_route_split_count, moe_workspace_bytes)
+
+
+class StepBuffers:
+    """Device buffers of one layer-step of up to T_max tokens."""
+
+    def __init__(self, ctx, E, k, H, T_max, device="cuda"):
+        self.E, self.k, self.H, self.T_max = E, k, H, T_max
+        dev = torch.device(device)
+        self.logits = torch.zeros((T_max, E), dtype=torch.float32, device=dev)
+        self.x = torch.zeros((T_max, H), dtype=torch.int16, device=dev)        # bf16 bits
+        self.ids = torch.zeros((T_max, k), dtype=torch.int32, device=dev)
+        self.w = torch.zeros((T_max, k), dtype=torch.float32, device=dev)
+        self.Y = torch.zeros((T_max, k, H), dtype=torch.int16, device=dev)     # bf16 bits
+        self.out = torch.zeros((T_max, H), dtype=torch.int16, device=dev)      # bf16 bits
+        nbytes = moe_workspace_bytes(ctx, T_max)
+        self.ws = torch.zeros(nbytes + 256, dtype=torch.uint8, device=dev)
+        off = (-self.ws.data_ptr()) % 256
+        self.ws_ptr = self.ws.data_ptr() + off
+
+
+class LayerStep:
+    """Runs layer-steps on a main stream plus a second stream for the cold bank."""
+
+    def __init__(self, ctx, E, k, H, T_max, device="cuda"):
+        self.ctx = ctx
+        self.buf = StepBuffers(ctx, E, k, H, T_max, device)
+        self.cold_stream = torch.cuda.Stream(device=device)
+        self.ev_routed = torch.cuda.Event()
+        self.ev_cold = torch.cuda.Event()
+
+    def run(self, layer, T, count_on=True, stream=None, split=True):
+        """Enqueue one layer-step of T tokens from buf.logits / buf.x into
+        buf.out (and buf.ids, buf.w, buf.Y).  ``split=False`` runs both banks
+        on the main stream one after the other."""
+        b = self.buf
+        main = stream if stream is not None else torch.cuda.current_stream()
+        moe_route_split_count(self.ctx, layer, b.logits, T, count_on, b.ids, b.w, b.ws_ptr, main)
+        if split:
+            self.ev_routed.record(main)
+            self.cold_stream.wait_event(self.ev_routed)
+            moe_expert_ffn_bank(self.ctx, layer, MOE_BANK_COLD, b.x, T, b.ws_ptr, b.Y, self.cold_stream)
+            self.ev_cold.record(self.cold_stream)
+            moe_expert_ffn_bank(self.ctx, layer, MOE_BANK_HOT, b.x, T, b.ws_ptr, b.Y, main)
+            main.wait_event(self.ev_cold)
+        else:
+            moe_expert_ffn_bank(self.ctx, layer, MOE_BANK_HOT, b.x, T, b.ws_ptr, b.Y, main)
+            moe_expert_ffn_bank(self.ctx, layer, MOE_BANK_COLD, b.x, T, b.ws_ptr, b.Y, main)
+        moe_finalize(b.Y, b.w, T, b.k, b.H, b.out, main)

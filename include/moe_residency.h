@@ -1,0 +1,215 @@
+/*
+ * moe_residency.h -- C ABI of the split-residency routed MoE layer for one
+ * GB300 GPU (sm_103a).
+ *
+ * The layer (write-up "vLLM: Pin Hot Experts", section "Results, September 17"
+ * and "The one open door: two tensors and a row map"): each MoE layer keeps
+ * its experts in two banks -- a hot bank in HBM and a cold bank in pinned host
+ * memory that the GPU reads in place through a mapped (UVA) device pointer --
+ * plus a device row map from global expert id to (bank, row).  A layer-step
+ * routes each token to its top-k experts, splits the picks by residency
+ * (counting them into a usage table, write-up "We Built the Counter",
+ * section 2), runs the MXFP4 expert FFN once per bank without finalize, and
+ * finalizes each token's k expert rows in fixed k order.  Between steps, rows
+ * move between banks by true swaps ("vLLM: Pin Hot Experts", section "Making
+ * it follow the traffic"; "We Built the Counter", section 2).
+ *
+ * Conventions for every entry point:
+ *  - Return value: MOE_OK (0) or a negative MOE_E* code; moe_last_error()
+ *    gives a message for the calling thread.  Nothing throws across the ABI.
+ *  - "device" pointers are CUDA device (or mapped) addresses on the context's
+ *    device; "host" pointers are ordinary CPU memory.  The caller owns every
+ *    pointer it passes; the library owns the banks, row maps, usage table and
+ *    swap staging row it allocates in moe_create / moe_init_banks.
+ *  - stream: a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls marked "async" only enqueue work on it.
+ *  - bf16 tensors are passed as uint16_t bit patterns.
+ *  - Expert weights use the logical MXFP4 layout (OCP MX v1.0): for one
+ *    expert, w13_q [2I][H/2] and w2_q [H][I/2] bytes, where byte b of a row
+ *    holds K elements 2b (low nibble) and 2b+1 (high nibble); w13_s [2I][H/32]
+ *    and w2_s [H][I/32] are e8m0 scales, one per 32 contiguous K elements.
+ *    Rows 0..I-1 of W13 are the gate projection, rows I..2I-1 the up one.
+ *  - Row map encoding: row_map[e] >= 0 is hot-bank row row_map[e];
+ *    row_map[e] < 0 is cold-bank row -1 - row_map[e].
+ */
+#ifndef MOE_RESIDENCY_H
+#define MOE_RESIDENCY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    MOE_OK = 0,
+    MOE_EINVAL = -1,    /* bad argument, shape or id                        */
+    MOE_ENOMEM = -2,    /* a device or pinned-host allocation failed         */
+    MOE_ECUDA = -3,     /* a CUDA runtime call failed                        */
+    MOE_ESTALE = -4,    /* (per swap pair) the rows moved since the decision */
+    MOE_ETIMEOUT = -5,  /* a bounded device wait gave up                     */
+    MOE_ESTATE = -6     /* call out of order (e.g. layer has no banks yet)   */
+};
+
+enum { MOE_BANK_HOT = 0, MOE_BANK_COLD = 1 };
+
+/* FFN kernel implementation: tensor cores (tcgen05 + TMEM, default) or a
+ * CUDA-core kernel kept for cross-checking. */
+enum { MOE_FFN_TCGEN05 = 0, MOE_FFN_SIMT = 1 };
+
+typedef struct moe_ctx moe_ctx;
+
+typedef struct moe_geom {
+    int32_t layers;      /* L: MoE layers managed by this context            */
+    int32_t experts;     /* E: routed experts per layer (<= 1024)             */
+    int32_t top_k;       /* k: experts per token (1..16)                      */
+    int32_t hidden;      /* H: model width, a multiple of 128                 */
+    int32_t inter;       /* I: expert intermediate width, a multiple of 64    */
+    int32_t count_tmax;  /* count only steps with T <= count_tmax (256)       */
+    int32_t max_tokens;  /* T_max: largest T any call will pass               */
+} moe_geom;
+
+/* Message for the last failing call on this thread (never NULL). */
+const char *moe_last_error(void);
+
+/* Bytes of one expert (weights + scales); 18,800,640 at H=4096, I=2880
+ * ("vLLM: Pin Hot Experts": 17.93 MiB per MXFP4 expert). */
+int64_t moe_expert_bytes(int32_t hidden, int32_t inter);
+
+/* Create a context on CUDA device `device`: validates the geometry and
+ * allocates the [L x E] int32 usage table (zeroed) and one HBM staging row
+ * for swaps.  *out receives the context. */
+int moe_create(const moe_geom *geom, int device, moe_ctx **out);
+
+/* Free everything the context allocated.  Synchronizes the device. */
+int moe_destroy(moe_ctx *ctx);
+
+/* Select the FFN kernel implementation (MOE_FFN_*) for later calls. */
+int moe_set_ffn_impl(moe_ctx *ctx, int impl);
+
+/* Place one layer's experts ("vLLM: Pin Hot Experts", The one open door):
+ * experts with is_hot[e] != 0 go to an HBM bank, the rest to a pinned host
+ * bank mapped into the device address space; hot rows are assigned in
+ * increasing expert id, cold rows likewise, and the device row map written.
+ * Inputs are HOST pointers to all E experts stacked ([E][...] each, logical
+ * layout above); the library repacks them into its tiled device layout and
+ * does not keep the pointers.  Re-initialising a layer frees its old banks.
+ * Scale bytes must lie in [104, 140] (the range the FFN's f16 operand holds
+ * exactly); other values return MOE_EINVAL.  Synchronous. */
+int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t *w13_s,
+                   const uint8_t *w2_q, const uint8_t *w2_s, const uint8_t *is_hot,
+                   void *stream);
+
+/* Bytes of the caller-owned device workspace for steps of up to T tokens
+ * (split lists, per-bank scratch for the FFN's intermediate rows). */
+int moe_workspace_bytes(const moe_ctx *ctx, int T, size_t *bytes);
+
+/* Route, split and count (async).  "vLLM: Pin Hot Experts", Results (split
+ * each token's k ids by residency); "We Built the Counter", section 2 (one
+ * masked relaxed atomic add per pick into the usage table; only steps of at
+ * most count_tmax tokens are counted).
+ *   logits: device fp32 [T][E].  Top-k per token (ties: lower expert id
+ *           first); w = softmax over the k picked logits in fp32.
+ *   ids:    device int32 [T][k] out, descending logit order (the k order).
+ *   w:      device fp32  [T][k] out.
+ *   ws:     device workspace (moe_workspace_bytes) receiving both banks'
+ *           pick lists grouped by (bank row, slot t*k+j).
+ *   count_on: nonzero adds 1 per pick to usage[layer][id] when
+ *           T <= count_tmax. */
+int moe_route_split_count(moe_ctx *ctx, int layer, const float *logits, int T, int count_on,
+                          int32_t *ids, float *w, void *ws, void *stream);
+
+/* Copy one bank's pick lists from a routed workspace to host memory and
+ * synchronize `stream`: *n_act active rows (increasing), act_off [n_act+1]
+ * offsets into picks, picks [n_picks] slot indices t*k+j.  Host arrays must
+ * hold T*k (+1) entries.  T must be the routed step's T. */
+int moe_read_split(moe_ctx *ctx, const void *ws, int T, int bank, int32_t *n_act, int32_t *n_picks,
+                   int32_t *act_row, int32_t *act_off, int32_t *picks, void *stream);
+
+/* Expert FFN over one bank without finalize (async).  "vLLM: Pin Hot
+ * Experts", Results: the routed MXFP4 expert kernel runs once on the hot
+ * tensor and once on the cold one, unfinalized.  For every pick (t, j) whose
+ * expert lives in `bank`: Y[t][j][:] = bf16( W2 (silu(W_gate x_t) * (W_up x_t)) ).
+ * Rows of the other bank are not touched, so the two banks' calls may run on
+ * two streams at once (each uses its own part of ws).  A bank with no picks
+ * is a no-op on the device.
+ *   x: device bf16 [T][H];  Y: device bf16 [T][k][H] out;  ws as routed. */
+int moe_expert_ffn_bank(moe_ctx *ctx, int layer, int bank, const uint16_t *x, int T, void *ws,
+                        uint16_t *Y, void *stream);
+
+/* Finalize (async).  "vLLM: Pin Hot Experts", Results: accumulate each
+ * token's k bf16 expert rows in fp32 with fma in the original k order and
+ * cast once:  out[t][c] = bf16(fma(w[t][k-1], Y[t][k-1][c], ... fma(w[t][0],
+ * Y[t][0][c], 0.0f))).  Y device bf16 [T][k][H], w device fp32 [T][k],
+ * out device bf16 [T][H]. */
+int moe_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_t *out,
+                 void *stream);
+
+/* True swaps between steps ("vLLM: Pin Hot Experts", Making it follow the
+ * traffic and E4/E4b; "We Built the Counter", section 2).  For each pair i in
+ * order: promote[i] must be cold and demote[i] hot in the library's CPU copy
+ * of the placement, else applied[i] = 0 (stale, nothing changes).  An applied
+ * pair enqueues on `stream`: hot row -> HBM staging, cold row -> the hot
+ * slot, staging -> the cold slot (weights and scales together), then a
+ * two-element device row-map write ordered after the copies.  promote,
+ * demote: host int32 [n]; applied: host int32 [n] out (may be NULL).  Returns
+ * the number applied (>= 0) or an error code.  Never call it while a step of
+ * this layer is in flight on another stream. */
+int moe_swap_rows(moe_ctx *ctx, int layer, int n, const int32_t *promote, const int32_t *demote,
+                  int32_t *applied, void *stream);
+
+/* Copy the [L][E] usage table to host_out and synchronize `stream` (the
+ * counts are exact after the sync).  Counts only grow; a reader uses deltas. */
+int moe_read_counts(moe_ctx *ctx, int32_t *host_out, void *stream);
+
+/* Zero the usage table (async). */
+int moe_reset_counts(moe_ctx *ctx, void *stream);
+
+/* Placement queries.  moe_get_rowmap gives the library's CPU copy;
+ * moe_read_rowmap_device copies the device row map (synchronizes stream). */
+int moe_bank_rows(moe_ctx *ctx, int layer, int32_t *n_hot, int32_t *n_cold);
+int moe_get_rowmap(moe_ctx *ctx, int layer, int32_t *host_out);
+int moe_read_rowmap_device(moe_ctx *ctx, int layer, int32_t *host_out, void *stream);
+
+/* Copy one bank row (one expert in the library's device layout,
+ * moe_expert_bytes long) to host memory; synchronizes stream. */
+int moe_read_bank_row(moe_ctx *ctx, int layer, int bank, int row, uint8_t *host_out,
+                      void *stream);
+
+/* Host-link probe: a kernel that reads `bytes` of the layer-independent
+ * pinned probe buffer (mapped host memory) with 16-byte loads, `iters`
+ * times; *gbps receives the best read rate.  Also measures an HBM read of
+ * the same size into *hbm_gbps (may be NULL).  Synchronous. */
+int moe_probe_link(moe_ctx *ctx, size_t bytes, int iters, double *gbps, double *hbm_gbps);
+
+/* Read and clear the device status word that bounded device waits set
+ * (MOE_OK or MOE_ETIMEOUT).  Synchronizes the device. */
+int moe_device_status(moe_ctx *ctx, int32_t *status);
+
+/* Number of kernels this library has launched in this process. */
+int64_t moe_kernel_launches(void);
+
+/* ---- adaptive policy (host, between steps) ----
+ * "We Built the Counter", sections 2 and 9: read the usage table every N
+ * steps, keep a decaying average, queue swaps decided against a CPU copy of
+ * the hot/cold lists.  At each read, per expert: delta = counts - last
+ * (uint32), acc = d*acc + delta, wsum = d*wsum + 1 with
+ * d = 0.5^(read_every/half_life); avg = acc/wsum (picks per read).  Cold
+ * experts with avg >= min_avg (descending avg) pair with hot experts
+ * (ascending avg), ties by lower expert id, while avg_cold > hysteresis *
+ * avg_hot and fewer than max_pairs pairs were taken. */
+typedef struct moe_policy moe_policy;
+int moe_policy_create(int experts, double read_every, double half_life, double hysteresis,
+                      double min_avg, int max_pairs, const int32_t *counts_now,
+                      moe_policy **out);
+int moe_policy_destroy(moe_policy *p);
+/* counts: host int32 [E] of one layer; row_map: host int32 [E] (the CPU
+ * copy); promote/demote: host int32 [E] out.  Returns the pair count. */
+int moe_policy_read(moe_policy *p, const int32_t *counts, const int32_t *row_map,
+                    int32_t *promote, int32_t *demote);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_RESIDENCY_H */

@@ -1,0 +1,84 @@
+"""The C ABI without a GPU: the library builds for sm_103a and loads, every
+symbol include/moe_residency.h declares is exported, argument validation
+fails cleanly, and the native host policy takes the oracle's decisions."""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+import cold_expert_residency_gb300 as moe
+import oracle
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe.build()
+    return moe.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = moe.exported_symbols()
+    assert len(names) >= 20
+    for n in ["moe_init_banks", "moe_route_split_count", "moe_expert_ffn_bank", "moe_finalize",
+              "moe_swap_rows", "moe_read_counts"]:
+        assert n in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_expert_bytes(lib):
+    assert moe.moe_expert_bytes(4096, 2880) == 18_800_640
+    assert moe.moe_expert_bytes(256, 128) == oracle.expert_bytes(256, 128)
+
+
+def test_bad_geometry_is_rejected(lib):
+    bad = [dict(layers=0), dict(experts=1), dict(top_k=0), dict(top_k=17), dict(hidden=100),
+           dict(inter=96), dict(max_tokens=0), dict(experts=2000)]
+    base = dict(layers=1, experts=16, top_k=2, hidden=256, inter=128, max_tokens=8)
+    for b in bad:
+        kw = dict(base, **b)
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_create(kw["layers"], kw["experts"], kw["top_k"], kw["hidden"], kw["inter"], kw["max_tokens"])
+        assert ei.value.code == moe.MOE_EINVAL
+
+
+def test_null_and_shape_checks_fail_cleanly(lib):
+    assert lib.moe_finalize(None, None, 4, 0, 64, None, None) == moe.MOE_EINVAL
+    assert lib.moe_finalize(None, None, 4, 2, 60, None, None) == moe.MOE_EINVAL
+    assert lib.moe_finalize(None, None, 0, 2, 64, None, None) == moe.MOE_OK     # empty step
+    assert lib.moe_swap_rows(None, 0, 0, None, None, None, None) == moe.MOE_EINVAL
+    assert lib.moe_read_counts(None, None, None) == moe.MOE_EINVAL
+    assert b"context" in lib.moe_last_error()
+    assert lib.moe_policy_create(0, 64.0, 500.0, 1.5, 8.0, 2, None, C.byref(C.c_void_p())) == moe.MOE_EINVAL
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_native_policy_matches_oracle_policy(lib, seed):
+    rng = np.random.default_rng(seed)
+    E = 64
+    is_hot = np.zeros(E, np.uint8)
+    is_hot[rng.permutation(E)[:48]] = 1
+    rm, _, _ = oracle.initial_rowmap(is_hot)
+    params = dict(read_every=16.0, half_life=200.0, hysteresis=1.5, min_avg=8.0, max_pairs=8)
+    ref = oracle.Policy(E, **params)
+    nat = moe.moe_policy(E, **params)
+    counts = np.zeros(E, np.int64)
+    p = rng.dirichlet(np.full(E, 0.3))
+    for read in range(12):
+        if read == 6:
+            p = rng.dirichlet(np.full(E, 0.3))       # traffic shift
+        counts += rng.multinomial(16 * 42, p)
+        a = ref.read(counts.astype(np.int32), rm)
+        b = nat.read(counts.astype(np.int32), rm)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), read
+        oracle.swap(rm, a[0], a[1])
+
+
+def test_policy_counts_wrap_as_uint32(lib):
+    rm, _, _ = oracle.initial_rowmap(np.array([1, 0], np.uint8))
+    start = np.array([2**31 - 5, 2**31 - 5], np.int64).astype(np.int32)
+    nat = moe.moe_policy(2, read_every=1, half_life=1e9, min_avg=8, max_pairs=1, counts_now=start)
+    ref = oracle.Policy(2, counts=start, read_every=1, half_life=1e9, min_avg=8, max_pairs=1)
+    now = (np.array([2**31 - 5 + 2, 2**31 - 5 + 40], np.int64) & 0xFFFFFFFF).astype(np.uint32).view(np.int32)
+    assert [x.tolist() for x in nat.read(now, rm)] == [[1], [0]]
+    assert [x.tolist() for x in ref.read(now, rm)] == [[1], [0]]

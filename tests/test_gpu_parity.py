@@ -1,0 +1,245 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on seeded inputs.
+
+Bit-exact: routing ids, the residency split (pick lists), the usage table,
+the finalize given the same Y and w, split vs unsplit and swapped vs unsplit
+outputs.  Tolerance (relative L2 <= 5e-3, max |diff| <= 2e-2 of max |ref|):
+the FFN rows Y and the layer output against the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import Harness, assert_close_bf16, f32
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+IMPLS = [0, 1]   # MOE_FFN_TCGEN05, MOE_FFN_SIMT
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import cold_expert_residency_gb300 as moe
+    moe.build()
+
+
+def _check_routing(h, cfg, res, lg, T, counts_before=None, count_on=True):
+    ids_ref, w_ref = oracle.route(lg, cfg.k)
+    assert np.array_equal(res["ids"], ids_ref)
+    assert np.allclose(res["w"], w_ref, rtol=4e-7, atol=0)
+    assert np.all(np.abs(res["w"].astype(np.float64).sum(1) - 1.0) <= 1e-6)
+    rm = h.moe.moe_get_rowmap(h.ctx, 0, cfg.E)
+    assert np.array_equal(h.moe.moe_read_rowmap_device(h.ctx, 0, cfg.E), rm)
+    sp_ref = oracle.split(rm, ids_ref)
+    sp = h.split_lists(T)
+    for b in range(2):
+        for key in ("n_act", "n_picks"):
+            assert sp[b][key] == sp_ref[b][key], (b, key)
+        for key in ("act_row", "act_off", "picks"):
+            assert np.array_equal(sp[b][key], sp_ref[b][key]), (b, key)
+    return ids_ref, w_ref
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_tiny_layer_step_matches_oracle(impl):
+    cfg = synth.get_config("tiny")
+    h = Harness(cfg, impl=impl)
+    try:
+        lg = synth.router_logits(cfg, 0, 0)
+        x = synth.activations(cfg, 0, 0)
+        res = h.run(0, lg, x)
+        _check_routing(h, cfg, res, lg, cfg.T)
+        counts = np.zeros(cfg.E, np.int32)
+        ids_ref, w_ref, Y_ref, out_ref = oracle.layer_step(h.weights[0], lg, x, cfg.k, counts=counts)
+        got = h.moe.moe_read_counts(h.ctx, 1, cfg.E)[0]
+        assert np.array_equal(got, counts)
+        assert_close_bf16(res["Y"], Y_ref, "Y")
+        assert_close_bf16(res["out"], out_ref, "out")
+        # the finalize is bit-exact given the same Y and w
+        assert np.array_equal(res["out"], oracle.finalize(res["Y"], res["w"]))
+    finally:
+        h.close()
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_split_equals_unsplit_bitwise(impl):
+    cfg = synth.get_config("tiny")
+    w = synth.layer_weights(cfg, 0)
+    split = Harness(cfg, weights={0: w}, impl=impl)
+    unsplit = Harness(cfg, weights={0: w}, masks={0: np.ones(cfg.E, np.uint8)}, impl=impl)
+    try:
+        for step in range(3):
+            lg = synth.router_logits(cfg, 0, step)
+            x = synth.activations(cfg, 0, step)
+            a = split.run(0, lg, x)
+            b = unsplit.run(0, lg, x)
+            c = split.run(0, lg, x, split=False)
+            assert np.array_equal(a["Y"], b["Y"]) and np.array_equal(a["out"], b["out"])
+            assert np.array_equal(a["out"], c["out"])
+    finally:
+        split.close()
+        unsplit.close()
+
+
+def test_tc_and_simt_agree_within_tolerance():
+    cfg = synth.get_config("tiny")
+    w = synth.layer_weights(cfg, 0)
+    a = Harness(cfg, weights={0: w}, impl=0)
+    b = Harness(cfg, weights={0: w}, impl=1)
+    try:
+        lg = synth.router_logits(cfg, 0, 1)
+        x = synth.activations(cfg, 0, 1)
+        ra, rb = a.run(0, lg, x), b.run(0, lg, x)
+        assert_close_bf16(ra["Y"], rb["Y"], "tc vs simt")
+    finally:
+        a.close()
+        b.close()
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_swaps_bit_identical_and_negative_control(impl):
+    cfg = synth.get_config("tiny")
+    w = synth.layer_weights(cfg, 0)
+    mask = synth.hot_mask(cfg, 0)
+    h = Harness(cfg, weights={0: w}, impl=impl)
+    ref = Harness(cfg, weights={0: w}, masks={0: np.ones(cfg.E, np.uint8)}, impl=impl)
+    try:
+        lg = synth.router_logits(cfg, 0, 0)
+        x = synth.activations(cfg, 0, 0)
+        base = ref.run(0, lg, x)
+        cold = [int(e) for e in np.flatnonzero(mask == 0)]
+        hot = [int(e) for e in np.flatnonzero(mask == 1)]
+        rm = h.moe.moe_get_rowmap(h.ctx, 0, cfg.E).copy()
+        for i in range(5):     # five ordered swaps, output checked after each
+            pro, dem = cold[i % len(cold)], hot[i]
+            n, applied = h.moe.moe_swap_rows(h.ctx, 0, [pro], [dem])
+            exp = oracle.swap(rm, [pro], [dem])
+            assert applied.tolist() == exp.tolist()
+            assert np.array_equal(h.moe.moe_get_rowmap(h.ctx, 0, cfg.E), rm)
+            res = h.run(0, lg, x)
+            assert np.array_equal(h.moe.moe_read_rowmap_device(h.ctx, 0, cfg.E), rm)
+            assert np.array_equal(res["out"], base["out"]) and np.array_equal(res["Y"], base["Y"])
+        # a stale pair is refused and changes nothing
+        n, applied = h.moe.moe_swap_rows(h.ctx, 0, [hot[-1]], [cold[-1]])
+        assert n == 0 and applied.tolist() == [0]
+        # bank contents follow the map: a fresh placement with the final map
+        # holds the same bytes row for row
+        eb = h.moe.moe_expert_bytes(cfg.H, cfg.I)
+        fresh = Harness(cfg, weights={0: w}, masks={0: (rm >= 0).astype(np.uint8)}, impl=impl)
+        try:
+            frm = fresh.moe.moe_get_rowmap(fresh.ctx, 0, cfg.E)
+            for e in range(cfg.E):
+                bank_a, row_a = (0, rm[e]) if rm[e] >= 0 else (1, -1 - rm[e])
+                bank_b, row_b = (0, frm[e]) if frm[e] >= 0 else (1, -1 - frm[e])
+                ra = h.moe.moe_read_bank_row(h.ctx, 0, bank_a, int(row_a), eb)
+                rb = fresh.moe.moe_read_bank_row(fresh.ctx, 0, bank_b, int(row_b), eb)
+                assert np.array_equal(ra, rb), e
+        finally:
+            fresh.close()
+        # negative control: a map that names the other expert's rows (a map
+        # flip without the copies) changes the output
+        bad = list(w)
+        e0, e1 = int(base["ids"][0, 0]), int(base["ids"][0, 1])
+        for arr in bad:
+            tmp = arr[e0].copy()
+            arr[e0] = arr[e1]
+            arr[e1] = tmp
+        neg = Harness(cfg, weights={0: bad}, impl=impl)
+        try:
+            r = neg.run(0, lg, x)
+            assert not np.array_equal(r["out"], base["out"])
+        finally:
+            neg.close()
+    finally:
+        h.close()
+        ref.close()
+
+
+def test_counts_only_for_small_steps_and_when_on():
+    cfg = synth.get_config("tiny")
+    h = Harness(cfg, T_max=300)
+    try:
+        x = synth.activations(cfg, 0, 0, T=300)
+        lg = synth.router_logits(cfg, 0, 0, T=300)
+        h.run(0, lg[:256], x[:256], count_on=True)
+        c1 = h.moe.moe_read_counts(h.ctx, 1, cfg.E)[0]
+        assert c1.sum() == 256 * cfg.k
+        h.run(0, lg[:8], x[:8], count_on=False)
+        assert np.array_equal(h.moe.moe_read_counts(h.ctx, 1, cfg.E)[0], c1)
+        res = h.run(0, lg, x, count_on=True)          # 300 tokens: not counted
+        assert np.array_equal(h.moe.moe_read_counts(h.ctx, 1, cfg.E)[0], c1)
+        # the multi-kernel route/split path (T > 256) matches the oracle too
+        _check_routing(h, cfg, res, lg, 300)
+        ids_ref, w_ref, Y_ref, out_ref = oracle.layer_step(h.weights[0], lg, x, cfg.k)
+        assert_close_bf16(res["out"], out_ref, "out T=300")
+        h.moe.moe_reset_counts(h.ctx)
+        assert h.moe.moe_read_counts(h.ctx, 1, cfg.E).sum() == 0
+    finally:
+        h.close()
+
+
+@pytest.mark.parametrize("T", [1, 5, 33, 64, 65, 130])
+def test_token_counts_and_ragged_tiles(T):
+    """Several N-tile widths (16 / 64 / 256 variants) and ragged token counts."""
+    cfg = synth.get_config("tiny", T=T)
+    h = Harness(cfg)
+    try:
+        lg = synth.router_logits(cfg, 0, 3, T=T)
+        x = synth.activations(cfg, 0, 3, T=T)
+        res = h.run(0, lg, x)
+        _check_routing(h, cfg, res, lg, T)
+        _, _, Y_ref, out_ref = oracle.layer_step(h.weights[0], lg, x, cfg.k)
+        assert_close_bf16(res["Y"], Y_ref, f"Y T={T}")
+        assert_close_bf16(res["out"], out_ref, f"out T={T}")
+    finally:
+        h.close()
+
+
+def test_all_cold_and_all_hot_banks():
+    cfg = synth.get_config("tiny")
+    w = synth.layer_weights(cfg, 0)
+    lg = synth.router_logits(cfg, 0, 0)
+    x = synth.activations(cfg, 0, 0)
+    outs = []
+    for mask in (np.zeros(cfg.E, np.uint8), np.ones(cfg.E, np.uint8)):
+        h = Harness(cfg, weights={0: w}, masks={0: mask})
+        try:
+            outs.append(h.run(0, lg, x)["out"])
+        finally:
+            h.close()
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_device_status_clean_after_steps():
+    cfg = synth.get_config("tiny")
+    h = Harness(cfg)
+    try:
+        h.run(0, synth.router_logits(cfg, 0, 0), synth.activations(cfg, 0, 0))
+        assert h.moe.moe_device_status(h.ctx) == 0
+    finally:
+        h.close()
+
+
+@pytest.mark.slow
+def test_decode1_full_size_against_oracle():
+    """One-user decode step at full geometry (E=384, k=6, H=4096, I=2880,
+    T=7, hot 295 / cold 89): every routed row against the oracle."""
+    cfg = synth.get_config("decode1")
+    h = Harness(cfg)
+    try:
+        lg = synth.router_logits(cfg, 0, 0)
+        x = synth.activations(cfg, 0, 0)
+        res = h.run(0, lg, x)
+        ids_ref, w_ref = _check_routing(h, cfg, res, lg, cfg.T)
+        slots = np.arange(cfg.T * cfg.k, dtype=np.int32)
+        Y_ref = oracle.rows_for_slots(h.weights[0], ids_ref, x, slots).reshape(cfg.T, cfg.k, cfg.H)
+        assert_close_bf16(res["Y"], Y_ref, "Y decode1")
+        out_ref = oracle.finalize(Y_ref, w_ref)
+        assert_close_bf16(res["out"], out_ref, "out decode1")
+        assert np.array_equal(res["out"], oracle.finalize(res["Y"], res["w"]))
+        sp = h.split_lists(cfg.T)
+        assert sp[1]["n_picks"] > 0, "decode step should touch the cold bank"
+    finally:
+        h.close()
