@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--pool", type=int, default=32, help="distinct input batches cycled through")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of CPU-oracle work")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling-size variant: this many experts per layer (same expert geometry)")
+    ap.add_argument("--hot", type=int, default=0, help="hot-bank experts for --experts")
     return ap.parse_args()
 
 
@@ -222,6 +225,8 @@ def main():
     moe.build()
 
     cfg = synth.get_config(args.config)
+    if args.experts:
+        cfg = synth.get_config(args.config, E=args.experts, n_hot=args.hot or cfg.n_hot * args.experts // cfg.E)
     hbm_peak, tf_burst, tf_sust, peak_src = load_peaks()
     L = cfg.L
     ctx = moe.moe_create(L, cfg.E, cfg.k, cfg.H, cfg.I, cfg.T, device=local)
@@ -419,7 +424,9 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e2m1 weights, f16 tensor-core operands, f32 accumulate, bf16 rows",
             "data": "synthetic (seeded SplitMix64; Zipf-skewed routing)",
-            "config": {"workload": WORKLOADS[args.config], "layers": L, "tokens_per_step": T,
+            "config": {"workload": WORKLOADS[args.config] + (
+                           f" [profiling variant: {cfg.E} experts, {cfg.n_hot} hot]" if args.experts else ""),
+                       "layers": L, "tokens_per_step": T,
                        "l2": "flushed (512 MiB write) before every timed step", "cuda_graph": graph is not None,
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "us_per_layer_step": ms * 1e3 / L,

@@ -11,47 +11,55 @@
 //   largest element lies in [2^13, 2^14); the epilogue undoes the scale).
 //
 // Warp roles (192 threads):
-//   warp 4      producer: hot bank -> one bulk async copy (TMA) of each
-//               4352-byte (M-tile, K-chunk) weight block into a shared-memory
-//               ring; cold bank -> 16-byte cp.async reads of the mapped host
-//               bank (the host-link streaming path); token rows of the chunk
-//               into the canonical no-swizzle K-major layout.
+//   warp 4      producer.  Weights: hot bank -> one 1-D bulk async copy (TMA)
+//               of each 4352-byte (M-tile, K-chunk) block; cold bank ->
+//               16-byte cp.async reads of the mapped host bank (the host-link
+//               streaming path).  Token rows: 2-D tensor TMA boxes of 16 rows x
+//               64 f16 with 128-byte swizzle from the pick-ordered row array.
+//               All into a shared-memory ring, completion on one mbarrier per
+//               stage.
 //   warps 0-3   dequant: thread m owns weight row m = TMEM lane m; converts 64
 //               e2m1 codes with the hardware e2m1x2 -> f16x2 conversion,
-//               applies the e8m0 block scale (exact in f16), and stores the
-//               32 f16x2 columns to a double-buffered A operand in TMEM;
-//               then the epilogue (tcgen05.ld of D, SwiGLU or bf16 store).
-//   warp 5      TMEM allocation; lane 0 issues tcgen05.mma (A from TMEM,
-//               B from shared memory) and tcgen05.commit.
+//               applies the e8m0 block scale (exact in f16) and stores the 32
+//               f16x2 columns into a double-buffered A operand in TMEM; then
+//               the epilogue (tcgen05.ld of D, SwiGLU or bf16 row store).
+//   warp 5      TMEM allocation; lane 0 issues tcgen05.mma (A from TMEM, B
+//               from shared memory) and tcgen05.commit.
 //
 // The arithmetic of a pick depends only on its expert's weights, its token
 // row and the expert's token count (which fixes N), never on the bank, so the
 // hot and cold banks and any swap give bit-identical rows.
 //
 // Every mbarrier wait is bounded; on timeout the kernel sets the status word
-// to MOE_ETIMEOUT, drains its own copies in flight, frees TMEM and returns.
+// to MOE_ETIMEOUT, lets its own copies in flight land, frees TMEM and returns.
 #include "moe_internal.cuh"
 #include "sm103_ptx.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 namespace moe {
 
 namespace {
 
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kBoxRows = 16;                 // token rows per tensor-TMA box
+constexpr int kBoxBytes = kBoxRows * 128;    // 16 rows x 64 f16
 
 struct TcArgs {
     const uint8_t *bank;
     int64_t eb, part_off;
     int mt_count, kc;
     BankLists lists;
-    int b, k, H, I;
-    const __half *bsrc;     // phase 1: scaled x rows [T][H]; phase 2: scaled h rows [P][I]
-    int bsrc_ld;
-    const int32_t *bexp;    // phase 1: per token; phase 2: per slot
-    float *h_out;           // phase 1 output [P][I]
-    uint16_t *Y;            // phase 2 output [P][H]
+    int b, k, H, I, P;
+    const int32_t *bexp;    // [P] scale exponent of B row g
+    float *h_out;           // phase 1 output [P][I] by g
+    uint16_t *Y;            // phase 2 output [T*k][H] by slot
     int32_t *status;
+    int32_t *sched;         // work counter of this launch (zeroed before it)
 };
+
+constexpr int kQ = 4;       // unit queue depth (producer -> dequant / MMA roles)
 
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                          int32_t *status) {
@@ -94,36 +102,46 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t scale2, uint32
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[3]) : "r"(c3), "r"(scale2));
 }
 
+__device__ __forceinline__ int bank_offset(const BankLists &L, int b, int P) {
+    return b == 0 ? 0 : P - L.hdr[kHdrNPicks + 1];
+}
+
 template <int NMAX>
 struct TcCfg {
-    static constexpr int kStages = NMAX <= 16 ? 8 : (NMAX <= 64 ? 6 : 4);
-    static constexpr int kBStage = NMAX * 128;              // bytes of one B chunk
-    static constexpr uint32_t kLBO = NMAX * 16;             // core-matrix stride along K
+    static constexpr int kStages = NMAX <= 16 ? 8 : (NMAX <= 64 ? 5 : 4);
+    static constexpr int kBStage = NMAX * 128;              // bytes of one B chunk (NMAX rows x 128 B)
     static constexpr uint32_t kCols = NMAX <= 64 ? 128 : 512;
     static constexpr uint32_t kDCol = 64;                   // D after two 32-column A buffers
-    static constexpr int kBars = 2 * kStages + 6;
-    static constexpr size_t kSmem = (size_t)kStages * (kChunkBytes + kBStage) + kBars * 8 + 16;
+    static constexpr int kBars = 2 * kStages + 6 + 2 * kQ;
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * (kBStage + kChunkBytes) + kBars * 8 + 16 + 4 * kQ;
 };
 
 template <int NMAX, int PHASE, bool COLD>
-__global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
+__global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ CUtensorMap tmap, TcArgs args) {
     using C = TcCfg<NMAX>;
     constexpr int S = C::kStages;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + S * kChunkBytes;
-    uint64_t *bars = (uint64_t *)(sB + S * C::kBStage);
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte-swizzled B stages need 1024-byte alignment
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sB = smem;
+    uint8_t *sA = sB + S * C::kBStage;
+    uint64_t *bars = (uint64_t *)(sA + S * kChunkBytes);
     uint32_t *holder = (uint32_t *)(bars + C::kBars);
     volatile int *abort_flag = (volatile int *)(holder + 1);
+    volatile int *uq = (volatile int *)(holder + 2);   // [kQ] unit queue
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
-    // barrier indices
     const int FULL = 0, EMPTY = S, AREADY = 2 * S, AFREE = 2 * S + 2, ACCREADY = 2 * S + 4, ACCFREE = 2 * S + 5;
+    const int UQFULL = 2 * S + 6, UQEMPTY = 2 * S + 6 + kQ;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(bar(FULL + s), COLD ? 33 : 1);
             ptx::mbar_init(bar(EMPTY + s), 1);
+        }
+        for (int q = 0; q < kQ; ++q) {
+            ptx::mbar_init(bar(UQFULL + q), 1);
+            ptx::mbar_init(bar(UQEMPTY + q), 129);   // 128 dequant threads + the MMA thread
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(bar(AREADY + i), 128);
@@ -134,6 +152,7 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
+    if (warp == 4 && lane == 0) ptx::prefetch_tmap(&tmap);
     if (warp == 5) {
         ptx::tmem_alloc(ptx::smem_addr(holder), C::kCols);
         ptx::tmem_relinquish();
@@ -147,6 +166,7 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
     const int n_act = L.hdr[kHdrNAct + args.b];
     const int units = n_act * args.mt_count;
     const int kc = args.kc;
+    const int goff = bank_offset(L, args.b, args.P);
 
     if (warp < 4) {
         // ------------------------------------------------ dequant + epilogue
@@ -154,11 +174,23 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         uint32_t it = 0, j = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        for (uint32_t ui = 0; ok; ++ui) {
+            const int qs = ui % kQ;
+            if (!wait_warp(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status)) { ok = false; break; }
+            const int u = uq[qs];
+            ptx::mbar_arrive(bar(UQEMPTY + qs));
+            if (u < 0) break;
             const int a = u / args.mt_count, mt = u % args.mt_count;
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
+                // epilogue metadata for up to 32 columns, fetched before the
+                // K loop so its latency hides behind it
+                int my_slot = 0, my_exp = 0;
+                if (lane < nn && lane < 32) {
+                    my_slot = L.picks[p0 + n0 + lane];
+                    my_exp = args.bexp[goff + p0 + n0 + lane];
+                }
                 for (int c = 0; c < kc; ++c, ++it) {
                     const int st = it % S;
                     if (!wait_warp(bar(FULL + st), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
@@ -200,16 +232,22 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
                     for (int q = 0; q < 16; ++q) {
                         const int col = c0 + q;
                         if (col < nn) {   // warp-uniform
-                            const int slot = L.picks[p0 + n0 + col];
+                            int slot, e;
+                            if (col < 32) {
+                                slot = __shfl_sync(0xffffffffu, my_slot, col);
+                                e = __shfl_sync(0xffffffffu, my_exp, col);
+                            } else {
+                                slot = L.picks[p0 + n0 + col];
+                                e = args.bexp[goff + p0 + n0 + col];
+                            }
+                            const float d = ldexpf(__uint_as_float(v[q]), e);
                             if (PHASE == 1) {
-                                const float d = ldexpf(__uint_as_float(v[q]), args.bexp[slot / args.k]);
                                 const float o = __shfl_xor_sync(0xffffffffu, d, 16);
                                 if (l < 16) {
                                     const float hv = __fmul_rn(__fdiv_rn(d, 1.0f + expf(-d)), o);
-                                    args.h_out[(int64_t)slot * args.I + 64 * mt + 16 * w + l] = hv;
+                                    args.h_out[(int64_t)(goff + p0 + n0 + col) * args.I + 64 * mt + 16 * w + l] = hv;
                                 }
                             } else {
-                                const float d = ldexpf(__uint_as_float(v[q]), args.bexp[slot]);
                                 args.Y[(int64_t)slot * args.H + kMT * mt + m] =
                                     __bfloat16_as_ushort(__float2bfloat16_rn(d));
                             }
@@ -224,7 +262,23 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
         // ------------------------------------------------------------ producer
         uint32_t it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        for (uint32_t ui = 0; ok; ++ui) {
+            // take the next unit from the launch's work counter and publish it
+            const int qs = ui % kQ;
+            if (ui >= (uint32_t)kQ &&
+                !wait_warp(bar(UQEMPTY + qs), ((ui / kQ) - 1) & 1, abort_flag, args.status)) {
+                ok = false;
+                break;
+            }
+            int u = 0;
+            if (lane == 0) {
+                u = atomicAdd(args.sched, 1);
+                if (u >= units) u = -1;
+                uq[qs] = u;
+                ptx::mbar_arrive(bar(UQFULL + qs));
+            }
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (u < 0) break;
             const int a = u / args.mt_count, mt = u % args.mt_count;
             const int row = L.act_row[a];
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
@@ -232,7 +286,8 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
                                   (int64_t)mt * kc * kChunkBytes;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX) {
                 const int nn = min(NMAX, n - n0);
-                const int Nr = (nn + 15) & ~15;
+                const int nbox = (nn + kBoxRows - 1) / kBoxRows;
+                const int brow = goff + p0 + n0;
                 for (int c = 0; c < kc; ++c, ++it) {
                     const int st = it % S;
                     const uint32_t rnd = it / S;
@@ -240,31 +295,20 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
                         ok = false;
                         break;
                     }
-                    const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage);
-                    for (int idx = lane; idx < Nr * 8; idx += 32) {
-                        const int nr = idx >> 3, kb = idx & 7;
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (nr < nn) {
-                            const int slot = L.picks[p0 + n0 + nr];
-                            const int src = PHASE == 1 ? slot / args.k : slot;
-                            v = ptx::ld_nc_v4(args.bsrc + (int64_t)src * args.bsrc_ld + c * kKC + kb * 8);
-                        }
-                        ptx::st_shared_v4(b_addr + kb * C::kLBO + (nr >> 3) * 128 + (nr & 7) * 16, v);
-                    }
                     const uint32_t a_addr = ptx::smem_addr(sA + st * kChunkBytes);
+                    const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage);
                     const uint8_t *src_chunk = tile + (int64_t)c * kChunkBytes;
                     if (COLD) {
                         for (int i = lane; i < kChunkBytes / 16; i += 32) ptx::cp_async16(a_addr + i * 16, src_chunk + i * 16);
-                    }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (COLD) {
                         ptx::cp_async_arrive_noinc(bar(FULL + st));
-                        if (lane == 0) ptx::mbar_arrive(bar(FULL + st));
-                    } else if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(bar(FULL + st), kChunkBytes);
-                        ptx::bulk_g2s(a_addr, src_chunk, kChunkBytes, bar(FULL + st));
                     }
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(bar(FULL + st), (COLD ? 0u : (uint32_t)kChunkBytes) + nbox * kBoxBytes);
+                        if (!COLD) ptx::bulk_g2s(a_addr, src_chunk, kChunkBytes, bar(FULL + st));
+                        for (int q = 0; q < nbox; ++q)
+                            ptx::tma_load_2d(b_addr + q * kBoxBytes, &tmap, c * kKC, brow + q * kBoxRows, bar(FULL + st));
+                    }
+                    __syncwarp();
                 }
             }
         }
@@ -280,7 +324,12 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
         // ----------------------------------------------------------- MMA issue
         uint32_t it = 0, j = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        for (uint32_t ui = 0; ok; ++ui) {
+            const int qs = ui % kQ;
+            if (!wait_one(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status)) { ok = false; break; }
+            const int u = uq[qs];
+            ptx::mbar_arrive(bar(UQEMPTY + qs));
+            if (u < 0) break;
             const int a = u / args.mt_count;
             const int n = L.act_off[a + 1] - L.act_off[a];
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
@@ -293,11 +342,10 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
                     const int st = it % S, abuf = it & 1;
                     if (!wait_one(bar(AREADY + abuf), (it >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    ptx::fence_proxy_async_smem();
                     const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bd = ptx::smem_desc_noswizzle(b_addr + 2 * kk * C::kLBO, C::kLBO, 128);
+                        const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 32);
                         ptx::mma_f16_ts(tmem + C::kDCol, tmem + abuf * 32 + kk * 8, bd, idesc, (c | kk) != 0);
                     }
                     ptx::mma_commit(bar(EMPTY + st));
@@ -323,14 +371,28 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(TcArgs args) {
     }
 }
 
-// Per-token power-of-two scaling of x into f16: largest |x| -> [2^13, 2^14).
-__global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict__ x, int H,
-                                                     __half *__restrict__ xs, int32_t *__restrict__ xexp) {
+// Gather this bank's token rows in pick order, each scaled by a power of two
+// into f16 (largest |x| -> [2^13, 2^14)): row g = offset + p of xg.
+__global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict__ x, int H, int k, BankLists L,
+                                                     int b, int P, __half *__restrict__ xg,
+                                                     int32_t *__restrict__ xgexp, int32_t *sched) {
     __shared__ float red[8];
-    const int t = blockIdx.x;
-    const uint16_t *row = x + (int64_t)t * H;
+    const int p = blockIdx.x;
+    // reset the work counters of this bank's two GEMM launches (stream-ordered before them)
+    if (p == 0 && threadIdx.x < 2) sched[threadIdx.x] = 0;
+    if (p >= L.hdr[kHdrNPicks + b]) return;
+    const int g = bank_offset(L, b, P) + p;
+    const int t = L.picks[p] / k;
+    const uint4 *row = (const uint4 *)(x + (int64_t)t * H);
+    const int n8 = H / 8;
     float mx = 0.0f;
-    for (int h = threadIdx.x; h < H; h += blockDim.x) mx = fmaxf(mx, fabsf(__uint_as_float((uint32_t)row[h] << 16)));
+    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+        const uint4 v = row[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
+    }
     for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
     __syncthreads();
@@ -339,22 +401,37 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict_
     int e = 0;
     frexpf(mx, &e);
     const int c = mx > 0.0f ? e - 14 : 0;
-    for (int h = threadIdx.x; h < H; h += blockDim.x)
-        xs[(int64_t)t * H + h] = __float2half_rn(ldexpf(__uint_as_float((uint32_t)row[h] << 16), -c));
-    if (threadIdx.x == 0) xexp[t] = c;
+    uint4 *dst = (uint4 *)(xg + (int64_t)g * H);
+    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+        const uint4 v = row[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            __half2 h = __floats2half2_rn(ldexpf(__uint_as_float(w[q] << 16), -c),
+                                          ldexpf(__uint_as_float(w[q] & 0xFFFF0000u), -c));
+            o[q] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (threadIdx.x == 0) xgexp[g] = c;
 }
 
-// Per-pick power-of-two scaling of the gate/up output h into f16.
-__global__ void __launch_bounds__(256) prep_h_kernel(BankLists lists, int b, int I,
+// Scale this bank's gate/up rows h (fp32, row g) into f16 the same way.
+__global__ void __launch_bounds__(256) prep_h_kernel(BankLists L, int b, int P, int I,
                                                      const float *__restrict__ h32, __half *__restrict__ h16,
                                                      int32_t *__restrict__ hexp) {
     __shared__ float red[8];
     const int p = blockIdx.x;
-    if (p >= lists.hdr[kHdrNPicks + b]) return;
-    const int slot = lists.picks[p];
-    const float *row = h32 + (int64_t)slot * I;
+    if (p >= L.hdr[kHdrNPicks + b]) return;
+    const int g = bank_offset(L, b, P) + p;
+    const float4 *row = (const float4 *)(h32 + (int64_t)g * I);
+    const int n4 = I / 4;
     float mx = 0.0f;
-    for (int i = threadIdx.x; i < I; i += blockDim.x) mx = fmaxf(mx, fabsf(row[i]));
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = row[i];
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
     for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
     __syncthreads();
@@ -363,43 +440,94 @@ __global__ void __launch_bounds__(256) prep_h_kernel(BankLists lists, int b, int
     int e = 0;
     frexpf(mx, &e);
     const int c = mx > 0.0f ? e - 14 : 0;
-    for (int i = threadIdx.x; i < I; i += blockDim.x) h16[(int64_t)slot * I + i] = __float2half_rn(ldexpf(row[i], -c));
-    if (threadIdx.x == 0) hexp[slot] = c;
+    uint2 *dst = (uint2 *)(h16 + (int64_t)g * I);
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = row[i];
+        __half2 a = __floats2half2_rn(ldexpf(v.x, -c), ldexpf(v.y, -c));
+        __half2 bb = __floats2half2_rn(ldexpf(v.z, -c), ldexpf(v.w, -c));
+        dst[i] = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&bb));
+    }
+    if (threadIdx.x == 0) hexp[g] = c;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// Tensor map over a [rows][K] f16 array: boxes of 16 rows x 64 elements,
+// 128-byte swizzle, zero fill past the last row.
+int make_row_map(CUtensorMap *map, const void *base, int K, int rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kKC, (cuuint32_t)kBoxRows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
+    return MOE_OK;
 }
 
 template <int NMAX, int PHASE, bool COLD>
-int launch_one(moe_ctx *ctx, const TcArgs &args, int units_max, cudaStream_t s) {
+int launch_one(const CUtensorMap &map, const TcArgs &args, int blocks, cudaStream_t s) {
     using C = TcCfg<NMAX>;
     auto kern = ffn_tc_kernel<NMAX, PHASE, COLD>;
     MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem));
-    const int per_sm = NMAX <= 64 ? 4 : 1;   // TMEM: 128 columns per CTA, or 512
-    int blocks = std::min(units_max, ctx->sms * per_sm);
     if (blocks < 1) return MOE_OK;
-    kern<<<blocks, 192, C::kSmem, s>>>(args);
+    kern<<<blocks, 192, C::kSmem, s>>>(map, args);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
+// Grid of one GEMM launch.  Units are handed out dynamically, so the grid
+// only sets how many CTAs stream at once.  A cold-bank launch needs few CTAs
+// to keep the host link busy; when the layer also has a hot bank, the hot
+// launch leaves room on every SM for those, so both banks run concurrently.
 template <int NMAX>
-int launch_bank(moe_ctx *ctx, bool cold, TcArgs a1, TcArgs a2, int units1, int units2, BankLists lists, int b,
-                int T, int P, const WsLayout &lay, uint8_t *ws, const uint16_t *x, cudaStream_t s) {
+int grid_for(const moe_ctx *ctx, bool cold, bool shared, int units_max) {
+    const int per_sm = NMAX <= 16 ? 4 : (NMAX <= 64 ? 3 : 1);   // shared memory and TMEM both fit
+    const int cold_ctas = NMAX <= 64 ? 64 : 32;
+    int blocks;
+    if (cold) blocks = cold_ctas;
+    else if (!shared) blocks = ctx->sms * per_sm;
+    else if (per_sm > 1) blocks = ctx->sms * (per_sm - 1);
+    else blocks = ctx->sms - cold_ctas;
+    return std::max(1, std::min(units_max, blocks));
+}
+
+template <int NMAX>
+int launch_bank(moe_ctx *ctx, bool cold, bool shared, const TcArgs &a1, const TcArgs &a2, const CUtensorMap &m1,
+                const CUtensorMap &m2, int units1, int units2, const uint16_t *x, const WsLayout &lay, uint8_t *ws,
+                cudaStream_t s) {
     const Geom &g = ctx->g;
-    __half *xs16 = (__half *)(ws + lay.xs16) + (size_t)b * T * g.H;
-    int32_t *xexp = (int32_t *)(ws + lay.xexp) + (size_t)b * T;
-    prep_x_kernel<<<T, 256, 0, s>>>(x, g.H, xs16, xexp);
+    const int P = a1.P;
+    prep_x_kernel<<<P, 256, 0, s>>>(x, g.H, g.k, a1.lists, a1.b, P, (__half *)(ws + lay.xg16),
+                                    (int32_t *)(ws + lay.xgexp), a1.sched);
     MOE_LAUNCH_CHECK();
-    int r = cold ? launch_one<NMAX, 1, true>(ctx, a1, units1, s) : launch_one<NMAX, 1, false>(ctx, a1, units1, s);
+    const int b1 = grid_for<NMAX>(ctx, cold, shared, units1), b2 = grid_for<NMAX>(ctx, cold, shared, units2);
+    int r = cold ? launch_one<NMAX, 1, true>(m1, a1, b1, s) : launch_one<NMAX, 1, false>(m1, a1, b1, s);
     if (r) return r;
-    prep_h_kernel<<<P, 256, 0, s>>>(lists, b, g.I, (const float *)(ws + lay.h32), (__half *)(ws + lay.h16),
+    prep_h_kernel<<<P, 256, 0, s>>>(a1.lists, a1.b, P, g.I, (const float *)(ws + lay.h32), (__half *)(ws + lay.h16),
                                     (int32_t *)(ws + lay.hexp));
     MOE_LAUNCH_CHECK();
-    return cold ? launch_one<NMAX, 2, true>(ctx, a2, units2, s) : launch_one<NMAX, 2, false>(ctx, a2, units2, s);
+    return cold ? launch_one<NMAX, 2, true>(m2, a2, b2, s) : launch_one<NMAX, 2, false>(m2, a2, b2, s);
 }
 
 }  // namespace
 
 int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, int T, uint8_t *ws, uint16_t *Y,
-                  cudaStream_t s) {
+                  cudaStream_t s, bool shared) {
     const Geom &g = ctx->g;
     WsLayout lay = ws_layout(g, T);
     const int P = T * g.k;
@@ -408,6 +536,10 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, i
     lists.act_row = (const int32_t *)(ws + lay.act_row) + (size_t)b * P;
     lists.act_off = (const int32_t *)(ws + lay.act_off) + (size_t)b * (P + 1);
     lists.picks = (const int32_t *)(ws + lay.picks) + (size_t)b * P;
+
+    CUtensorMap m1, m2;
+    if (int r = make_row_map(&m1, ws + lay.xg16, g.H, P)) return r;
+    if (int r = make_row_map(&m2, ws + lay.h16, g.I, P)) return r;
 
     TcArgs a1{};
     a1.bank = bank;
@@ -420,29 +552,27 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, i
     a1.k = g.k;
     a1.H = g.H;
     a1.I = g.I;
-    a1.bsrc = (const __half *)(ws + lay.xs16) + (size_t)b * T * g.H;
-    a1.bsrc_ld = g.H;
-    a1.bexp = (const int32_t *)(ws + lay.xexp) + (size_t)b * T;
+    a1.P = P;
+    a1.bexp = (const int32_t *)(ws + lay.xgexp);
     a1.h_out = (float *)(ws + lay.h32);
     a1.status = ctx->status_dev;
+    a1.sched = (int32_t *)(ws + lay.hdr) + kHdrSched + 2 * b;
     TcArgs a2 = a1;
+    a2.sched = a1.sched + 1;
     a2.part_off = g.w2_off;
     a2.mt_count = g.mt2;
     a2.kc = g.kc2;
-    a2.bsrc = (const __half *)(ws + lay.h16);
-    a2.bsrc_ld = g.I;
     a2.bexp = (const int32_t *)(ws + lay.hexp);
     a2.h_out = nullptr;
     a2.Y = Y;
 
     const bool cold = b == MOE_BANK_COLD;
-    const int rows = P;   // active rows never exceed the picks
-    const int units1 = rows * g.mt13, units2 = rows * g.mt2;
+    const int units1 = P * g.mt13, units2 = P * g.mt2;   // active rows never exceed the picks
     // the token-tile width depends only on T, so an expert's arithmetic is
     // the same in either bank
-    if (T <= 16) return launch_bank<16>(ctx, cold, a1, a2, units1, units2, lists, b, T, P, lay, ws, x, s);
-    if (T <= 64) return launch_bank<64>(ctx, cold, a1, a2, units1, units2, lists, b, T, P, lay, ws, x, s);
-    return launch_bank<256>(ctx, cold, a1, a2, units1, units2, lists, b, T, P, lay, ws, x, s);
+    if (T <= 16) return launch_bank<16>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
+    if (T <= 64) return launch_bank<64>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
+    return launch_bank<256>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
 }
 
 }  // namespace moe

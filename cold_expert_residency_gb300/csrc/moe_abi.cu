@@ -322,7 +322,7 @@ int moe_expert_ffn_bank(moe_ctx *ctx, int layer, int bank, const uint16_t *x, in
     DeviceGuard guard(ctx->device);
     if (ctx->ffn_impl == MOE_FFN_SIMT)
         return launch_ffn_simt(ctx, base, bank, x, T, (uint8_t *)ws, Y, (cudaStream_t)stream);
-    return launch_ffn_tc(ctx, base, bank, x, T, (uint8_t *)ws, Y, (cudaStream_t)stream);
+    return launch_ffn_tc(ctx, base, bank, x, T, (uint8_t *)ws, Y, (cudaStream_t)stream, L.n_hot > 0 && L.n_cold > 0);
 }
 
 int moe_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_t *out, void *stream) {

@@ -65,11 +65,17 @@ inline Geom make_geom(const moe_geom &g) {
 // Workspace (caller-owned device memory) for a step of T tokens, P = T*k.
 // Every region starts on a 256-byte boundary.
 // ---------------------------------------------------------------------------
+// Rows of the FFN's intermediate arrays are indexed by the pick's global
+// position g: hot picks take g = p, cold picks g = P - n_cold + p (p = the
+// pick's index in its bank's list), so the two banks never share a row and
+// each expert's rows are contiguous.
 struct WsLayout {
-    size_t hdr, act_row, act_off, picks, epos, xs16, xexp, h32, h16, hexp, total;
+    size_t hdr, act_row, act_off, picks, epos, xg16, xgexp, h32, h16, hexp, total;
 };
 // header words
-enum { kHdrNPicks = 0, kHdrNAct = 2, kHdrWords = 64 };
+// kHdrSched + 2*bank + phase: work counters of the FFN kernels' dynamic
+// unit scheduler (zeroed by the bank's first FFN kernel).
+enum { kHdrNPicks = 0, kHdrNAct = 2, kHdrSched = 8, kHdrWords = 64 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -83,10 +89,10 @@ inline WsLayout ws_layout(const Geom &g, int T) {
     w.act_off = take(2 * (P + 1) * 4);        // [2][P+1]
     w.picks = take(2 * P * 4);                // [2][P]
     w.epos = take((size_t)g.E * 4);           // [E] start of expert e's picks in its bank list
-    w.xs16 = take(2 * (size_t)T * g.H * 2);   // [2 banks][T][H] f16, per-token scaled
-    w.xexp = take(2 * (size_t)T * 4);         // [2][T] int32 scale exponents
-    w.h32 = take(P * (size_t)g.I * 4);        // [P][I] fp32 gate/up output by slot
-    w.h16 = take(P * (size_t)g.I * 2);        // [P][I] f16, per-pick scaled
+    w.xg16 = take(P * (size_t)g.H * 2);       // [P][H] f16 token rows in pick order, per-row scaled
+    w.xgexp = take(P * 4);                    // [P] int32 scale exponents of those rows
+    w.h32 = take(P * (size_t)g.I * 4);        // [P][I] fp32 gate/up output (by g; by slot on CUDA cores)
+    w.h16 = take(P * (size_t)g.I * 2);        // [P][I] f16, per-row scaled, by g
     w.hexp = take(P * 4);                     // [P] int32
     w.total = off;
     return w;
@@ -153,8 +159,9 @@ int launch_route_split(moe_ctx *ctx, int layer, const float *logits, int T, int 
                        int32_t *ids, float *w, uint8_t *ws, cudaStream_t s);
 int launch_ffn_simt(moe_ctx *ctx, const uint8_t *bank, int bank_id, const uint16_t *x, int T,
                     uint8_t *ws, uint16_t *Y, cudaStream_t s);
+// shared: the layer has rows in both banks (their launches may overlap)
 int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int bank_id, const uint16_t *x, int T,
-                  uint8_t *ws, uint16_t *Y, cudaStream_t s);
+                  uint8_t *ws, uint16_t *Y, cudaStream_t s, bool shared);
 int launch_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_t *out,
                     cudaStream_t s);
 int launch_rowmap_write(int32_t *rowmap_dev, int32_t e0, int32_t v0, int32_t e1, int32_t v1,

@@ -44,6 +44,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
+// 2-D tiled tensor copy (TMA) global -> shared through a tensor map; the box
+// lands at dst with the map's swizzle, completing bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
 // 16-byte asynchronous copy global -> shared (L2 only).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -136,6 +147,20 @@ __device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t addr, uint32_t 
     d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
     d |= (uint64_t)1 << 46;   // version
     return d;                  // base offset 0, layout type 0 (no swizzle)
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, K-major: rows of 128
+// bytes, 8-row atoms of 1024 bytes (stride byte offset), leading offset
+// unused (encoded 1), layout type 2.  The start address may advance by the
+// K-step's byte offset inside the 128-byte row.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
 }
 
 // Instruction descriptor for kind::f16: f16 A and B, f32 accumulator,

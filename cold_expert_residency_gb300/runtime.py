@@ -40,7 +40,9 @@ class LayerStep:
     def __init__(self, ctx, E, k, H, T_max, device="cuda"):
         self.ctx = ctx
         self.buf = StepBuffers(ctx, E, k, H, T_max, device)
-        self.cold_stream = torch.cuda.Stream(device=device)
+        # high priority: the cold bank's few CTAs get SM slots first and keep
+        # the host link busy while the hot bank fills the rest of the GPU
+        self.cold_stream = torch.cuda.Stream(device=device, priority=-1)
         self.ev_routed = torch.cuda.Event()
         self.ev_cold = torch.cuda.Event()
 
