@@ -62,6 +62,8 @@ def lib():
         "moe_route_split_count": (i32, [P, i32, P, i32, i32, P, P, P, P]),
         "moe_read_split": (i32, [P, P, i32, i32, P, P, P, P, P, P]),
         "moe_expert_ffn_bank": (i32, [P, i32, i32, P, i32, P, P, P]),
+        "moe_expert_ffn_bank_static": (i32, [P, i32, i32, P, i32, P, P, P]),
+        "moe_static_scratch_bytes": (sz, []),
         "moe_finalize": (i32, [P, P, i32, i32, i32, P, P]),
         "moe_swap_rows": (i32, [P, i32, i32, P, P, P, P]),
         "moe_read_counts": (i32, [P, P, P]),
@@ -188,6 +190,17 @@ def moe_read_split(ctx, ws, T, k, bank, stream=None):
 def moe_expert_ffn_bank(ctx, layer, bank, x, T, ws, Y, stream=None):
     return _err("moe_expert_ffn_bank", lib().moe_expert_ffn_bank(
         ctx, layer, bank, _ptr(x), T, _ptr(ws), _ptr(Y), _stream(stream)))
+
+
+def moe_expert_ffn_bank_static(ctx, layer, bank, x, T, split_ws, Y, stream=None):
+    """Allocation-free FFN over one bank: scratch lives in the library's
+    static device area (see the C header)."""
+    return _err("moe_expert_ffn_bank_static", lib().moe_expert_ffn_bank_static(
+        ctx, layer, bank, _ptr(x), T, _ptr(split_ws), _ptr(Y), _stream(stream)))
+
+
+def moe_static_scratch_bytes():
+    return int(lib().moe_static_scratch_bytes())
 
 
 def moe_finalize(Y, w, T, k, H, out, stream=None):

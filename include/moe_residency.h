@@ -138,6 +138,28 @@ int moe_read_split(moe_ctx *ctx, const void *ws, int T, int bank, int32_t *n_act
 int moe_expert_ffn_bank(moe_ctx *ctx, int layer, int bank, const uint16_t *x, int T, void *ws,
                         uint16_t *Y, void *stream);
 
+/* Allocation-free variant of moe_expert_ffn_bank (async).  The write-ups
+ * have no counterpart: this serves callers that may not allocate device
+ * memory -- a plugin given a fixed memory budget by its host framework, or a
+ * serving loop that must not call cudaMalloc because it can synchronize the
+ * device and fail under memory pressure.  Instead of the FFN scratch part of
+ * a caller workspace it uses one library-owned area in a __device__ array of
+ * moe_static_scratch_bytes() (16 MiB) on every GPU that loads the library,
+ * held until the process exits.
+ *   split_ws: the caller's workspace after moe_route_split_count for this
+ *   step (only its pick lists are read).  x, T, Y as moe_expert_ffn_bank; Y
+ *   receives the same rows moe_expert_ffn_bank would write.
+ * Returns MOE_EINVAL if the step's scratch would exceed the area (about
+ * T*k*(2H + 6I) bytes).  The first call on a device looks up the area's
+ * device address; make that first call before any stream capture.  Every
+ * call shares the one area and leaves its contents behind: calls whose work
+ * overlaps on the GPU race, so run the two banks' calls one after the other
+ * on one stream.  Allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library call). */
+int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t *x, int T,
+                               const void *split_ws, uint16_t *Y, void *stream);
+size_t moe_static_scratch_bytes(void);
+
 /* Finalize (async).  "vLLM: Pin Hot Experts", Results: accumulate each
  * token's k bf16 expert rows in fp32 with fma in the original k order and
  * cast once:  out[t][c] = bf16(fma(w[t][k-1], Y[t][k-1][c], ... fma(w[t][0],
