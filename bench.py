@@ -244,6 +244,8 @@ def main():
 
     T, E, k, H = cfg.T, cfg.E, cfg.k, cfg.H
     npool = max(2, min(args.pool, args.steps + args.warmup))
+    if T > 256:
+        npool = min(npool, 4)     # large batches: a few distinct inputs suffice
     pool_lg, pool_x = make_pool(cfg, npool, L)
     dev = torch.device("cuda", local)
     d_lg = torch.stack([torch.from_numpy(np.stack(p)) for p in pool_lg]).to(dev)            # [n][L][T][E]
@@ -327,7 +329,7 @@ def main():
             run_step()
     main.synchronize()
 
-    step_ms, hot_ms, hot_bytes, cold_bytes, dh, dc = [], [], [], [], [], []
+    step_ms, hot_ms, hot_bytes, cold_bytes, dh, dc, hot_picks = [], [], [], [], [], [], []
     eb = moe.moe_expert_bytes(cfg.H, cfg.I)
     if dist:
         dist.barrier()
@@ -354,6 +356,7 @@ def main():
                 nc += c
                 if l == 0:
                     hot_bytes.append(a * eb)
+                    hot_picks.append(int((masks[l][ids] == 1).sum()))
             dh.append(nh)
             dc.append(nc)
     torch.cuda.synchronize()
@@ -392,11 +395,51 @@ def main():
         main.synchronize()
         e2e_ms.append(ev0.elapsed_time(ev1))
 
+    # breakdown: each bank alone (layer 0), graph-replayed like the step
+    breakdown = None
+    if graph is not None:
+        def part(hot, cold):
+            st = steps[0]
+            b = st.buf
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2, stream=main):
+                moe.moe_route_split_count(ctx, 0, b.logits, T, count_on, b.ids, b.w, b.ws_ptr, main)
+                if hot:
+                    moe.moe_expert_ffn_bank(ctx, 0, moe.MOE_BANK_HOT, b.x, T, b.ws_ptr, b.Y, main)
+                if cold:
+                    moe.moe_expert_ffn_bank(ctx, 0, moe.MOE_BANK_COLD, b.x, T, b.ws_ptr, b.Y, main)
+            ts = []
+            for i in range(min(args.steps, 20)):
+                load_inputs(i, main)
+                with torch.cuda.stream(main):
+                    flush.zero_()
+                    ev0.record(main)
+                    g2.replay()
+                    ev1.record(main)
+                main.synchronize()
+                ts.append(ev0.elapsed_time(ev1) * 1e3)
+            return float(np.mean(ts))
+        r_us = part(False, False)
+        breakdown = {"route_us": r_us, "hot_alone_us": part(True, False) - r_us,
+                     "cold_alone_us": part(False, True) - r_us, "note": "layer 0, each bank alone after routing"}
+
     ms = total_ms / args.steps
     tokens_per_step = T   # one layer-step of T tokens (all layers of the config)
     value = world * tokens_per_step * args.steps / (total_ms * 1e-3)
     hot_avg_ms = float(np.mean(hot_ms))
     hot_gbs = float(np.mean(hot_bytes)) / (hot_avg_ms * 1e-3) / 1e9
+    roofline = {"kernel": "hot-bank expert FFN (moe_expert_ffn_bank, layer 0)", "bound": "hbm",
+                "achieved": hot_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": hot_gbs / hbm_peak,
+                "peak_source": f"{peak_src} (burst copy)", "traffic": profiled_traffic(args.config),
+                "timing": hot_timing, "us_per_launch": hot_avg_ms * 1e3}
+    if T > 256:
+        # large batches are a dense contraction: 2 flops per weight element per pick
+        flops = float(np.mean(hot_picks)) * 2.0 * (3.0 * cfg.I * cfg.H)
+        tf = flops / (hot_avg_ms * 1e-3) / 1e12
+        roofline.update({"bound": "tensor", "achieved": tf, "peak": tf_burst, "unit": "TFLOP/s",
+                         "frac": tf / tf_burst, "flops_per_launch": flops,
+                         "peak_source": f"{peak_src} bf16 dense burst (f16 operands run at the same rate)",
+                         "hbm_gbs_achieved": hot_gbs})
     # bytes roofline of the step (the metric's definition)
     t_roof = [(a * eb) / (hbm_peak * 1e9) + (c * eb) / (link_gbs * 1e9) for a, c in zip(dh, dc)]
     t_roof_max = [max((a * eb) / (hbm_peak * 1e9), (c * eb) / (link_gbs * 1e9)) for a, c in zip(dh, dc)]
@@ -435,11 +478,8 @@ def main():
                                "distinct_hot": float(np.mean(dh)), "distinct_cold": float(np.mean(dc)),
                                "expert_bytes": eb, "hbm_gbs": hbm_peak, "hbm_peak_source": peak_src,
                                "link_gbs": link_gbs, "hbm_probe_gbs": hbm_probe_gbs},
-            "roofline": {"kernel": "hot-bank expert FFN (moe_expert_ffn_bank, layer 0)", "bound": "hbm",
-                         "achieved": hot_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": hot_gbs / hbm_peak,
-                         "peak_source": f"{peak_src} (burst copy)",
-                         "traffic": profiled_traffic(args.config), "timing": hot_timing,
-                         "us_per_launch": hot_avg_ms * 1e3},
+            "roofline": roofline,
+            "breakdown": breakdown,
             "cpu_baseline": cpu,
             "e2e": {"value": world * T * len(e2e_ms) / (sum(e2e_ms) * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

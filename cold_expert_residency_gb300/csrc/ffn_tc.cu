@@ -570,8 +570,10 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, i
     const int units1 = P * g.mt13, units2 = P * g.mt2;   // active rows never exceed the picks
     // the token-tile width depends only on T, so an expert's arithmetic is
     // the same in either bank
+    // (decode-sized steps use narrow tiles with several CTAs per SM; an expert
+    // with more tokens than the tile loops over token tiles)
     if (T <= 16) return launch_bank<16>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
-    if (T <= 64) return launch_bank<64>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
+    if (T <= 256) return launch_bank<64>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
     return launch_bank<256>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
 }
 

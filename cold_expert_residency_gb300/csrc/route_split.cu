@@ -146,8 +146,9 @@ __device__ __forceinline__ void warp_fill_expert(int e, int b, int pos, const in
     }
 }
 
-// Small steps (T <= 256, T*k <= 4096): route, count, scan and fill in one CTA.
-__global__ void __launch_bounds__(1024) route_split_small(
+// Small steps (T <= 32, T*k <= 4096): route, count, scan and fill in one
+// CTA of 8 warps.
+__global__ void __launch_bounds__(256) route_split_small(
     const float *__restrict__ logits, int T, int E, int k, const int32_t *__restrict__ rowmap,
     int n_hot, int n_cold, int32_t *counts, int32_t *__restrict__ ids, float *__restrict__ w, WsPtrs ws) {
     extern __shared__ int32_t sm[];
@@ -157,9 +158,9 @@ __global__ void __launch_bounds__(1024) route_split_small(
     int32_t *rmap = cnt + E;        // [E]
     int32_t *rowexp = rmap + E;     // [2][E]
     int32_t *epos = rowexp + 2 * E; // [E]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
 
-    for (int t = warp; t < T; t += 32) {
+    for (int t = warp; t < T; t += nwarps) {
         int id;
         float wv;
         warp_route_token(logits + (size_t)t * E, E, k, lane, &id, &wv);
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(1024) route_split_small(
     __syncthreads();
     if (warp < 2) warp_scan_bank(warp, warp == 0 ? n_hot : n_cold, E, rowexp, cnt, epos, ws, lane);
     __syncthreads();
-    for (int e = warp; e < E; e += 32) {
+    for (int e = warp; e < E; e += nwarps) {
         if (cnt[e] == 0) continue;
         int m = rmap[e];
         warp_fill_expert(e, m >= 0 ? 0 : 1, epos[e], s_ids, ws, lane);
@@ -258,9 +259,9 @@ int launch_route_split(moe_ctx *ctx, int layer, const float *logits, int T, int 
     }
     int32_t *counts = (count_on && T <= g.count_tmax) ? ctx->counts_dev + (size_t)layer * g.E : nullptr;
     const int P = ws.P;
-    if (T <= 256 && P <= 4096) {
+    if (T <= 32 && P <= 4096) {
         size_t smem = sizeof(int32_t) * ((size_t)P + 5 * (size_t)g.E);
-        route_split_small<<<1, 1024, smem, s>>>(logits, T, g.E, g.k, L.rowmap_dev, L.n_hot, L.n_cold,
+        route_split_small<<<1, 256, smem, s>>>(logits, T, g.E, g.k, L.rowmap_dev, L.n_hot, L.n_cold,
                                                 counts, ids, w, ws);
         MOE_LAUNCH_CHECK();
         return MOE_OK;
