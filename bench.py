@@ -170,7 +170,7 @@ def profiled_traffic(config):
             d = json.load(f)
         e = d.get(config)
         if e and e.get("source_sha") == source_sha():
-            return e.get("bytes_per_step")
+            return e.get("bytes_per_hot_expert")
     except Exception:
         pass
     return None
@@ -430,7 +430,10 @@ def main():
     hot_gbs = float(np.mean(hot_bytes)) / (hot_avg_ms * 1e-3) / 1e9
     roofline = {"kernel": "hot-bank expert FFN (moe_expert_ffn_bank, layer 0)", "bound": "hbm",
                 "achieved": hot_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": hot_gbs / hbm_peak,
-                "peak_source": f"{peak_src} (burst copy)", "traffic": profiled_traffic(args.config),
+                "peak_source": f"{peak_src} (burst copy)",
+                # ncu DRAM bytes per hot expert (profiles/traffic.json) x this run's mean hot experts
+                "traffic": (profiled_traffic(args.config) * float(np.mean(hot_bytes)) / eb
+                            if profiled_traffic(args.config) else None),
                 "timing": hot_timing, "us_per_launch": hot_avg_ms * 1e3}
     if T > 256:
         # large batches are a dense contraction: 2 flops per weight element per pick
