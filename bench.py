@@ -60,6 +60,7 @@ def parse():
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling-size variant: this many experts per layer (same expert geometry)")
     ap.add_argument("--hot", type=int, default=0, help="hot-bank experts for --experts")
+    ap.add_argument("--tokens", type=int, default=0, help="profiling-size variant: tokens per step")
     return ap.parse_args()
 
 
@@ -227,6 +228,9 @@ def main():
     cfg = synth.get_config(args.config)
     if args.experts:
         cfg = synth.get_config(args.config, E=args.experts, n_hot=args.hot or cfg.n_hot * args.experts // cfg.E)
+    if args.tokens:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, T=args.tokens)
     hbm_peak, tf_burst, tf_sust, peak_src = load_peaks()
     L = cfg.L
     ctx = moe.moe_create(L, cfg.E, cfg.k, cfg.H, cfg.I, cfg.T, device=local)
@@ -471,7 +475,8 @@ def main():
             "vs_baseline": None, "dtype": "e2m1 weights, f16 tensor-core operands, f32 accumulate, bf16 rows",
             "data": "synthetic (seeded SplitMix64; Zipf-skewed routing)",
             "config": {"workload": WORKLOADS[args.config] + (
-                           f" [profiling variant: {cfg.E} experts, {cfg.n_hot} hot]" if args.experts else ""),
+                           f" [profiling variant: {cfg.E} experts, {cfg.n_hot} hot, {cfg.T} tokens]"
+                           if (args.experts or args.tokens) else ""),
                        "layers": L, "tokens_per_step": T,
                        "l2": "flushed (512 MiB write) before every timed step", "cuda_graph": graph is not None,
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},

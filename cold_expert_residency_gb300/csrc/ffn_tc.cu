@@ -108,17 +108,27 @@ __device__ __forceinline__ int bank_offset(const BankLists &L, int b, int P) {
 
 template <int NMAX>
 struct TcCfg {
-    static constexpr int kStages = NMAX <= 16 ? 8 : (NMAX <= 64 ? 5 : 4);
+    static constexpr int kStages = NMAX <= 16 ? 8 : (NMAX <= 64 ? 5 : (NMAX <= 192 ? 7 : 4));
     static constexpr int kBStage = NMAX * 128;              // bytes of one B chunk (NMAX rows x 128 B)
-    static constexpr uint32_t kCols = NMAX <= 64 ? 128 : 512;
-    static constexpr uint32_t kDCol = 64;                   // D after two 32-column A buffers
-    static constexpr int kBars = 2 * kStages + 6 + 2 * kQ;
+    // Wide (prefill) tiles run one CTA per SM, so the chunks in flight come
+    // from inside the CTA: four groups of four dequant warps, group g taking
+    // the chunks c = g (mod 4) into its own TMEM A buffer.  Decode tiles run
+    // 3-4 CTAs per SM with one group and two A buffers each.
+    static constexpr int kDq = NMAX >= 128 ? 16 : 4;
+    static constexpr int kGroups = kDq / 4;
+    static constexpr int kABufs = kGroups > 2 ? kGroups : 2;
+    static constexpr uint32_t kDCol = kABufs * 32;          // D after the 32-column A buffers
+    static constexpr uint32_t kCols = kDCol + NMAX <= 128 ? 128 : (kDCol + NMAX <= 256 ? 256 : 512);
+    static constexpr int kThreads = 32 * (kDq + 2);
+    static constexpr int kBars = 2 * kStages + 2 * kABufs + 2 + 2 * kQ;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * (kBStage + kChunkBytes) + kBars * 8 + 16 + 4 * kQ;
 };
 
 template <int NMAX, int PHASE, bool COLD>
-__global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ CUtensorMap tmap, TcArgs args) {
+__global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                         TcArgs args) {
     using C = TcCfg<NMAX>;
+    constexpr int DQ = C::kDq, NA = C::kABufs;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled B stages need 1024-byte alignment
@@ -130,8 +140,10 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ 
     volatile int *abort_flag = (volatile int *)(holder + 1);
     volatile int *uq = (volatile int *)(holder + 2);   // [kQ] unit queue
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
-    const int FULL = 0, EMPTY = S, AREADY = 2 * S, AFREE = 2 * S + 2, ACCREADY = 2 * S + 4, ACCFREE = 2 * S + 5;
-    const int UQFULL = 2 * S + 6, UQEMPTY = 2 * S + 6 + kQ;
+    const int FULL = 0, EMPTY = S, AREADY = 2 * S, AFREE = 2 * S + NA, ACCREADY = 2 * S + 2 * NA,
+              ACCFREE = ACCREADY + 1;
+    const int UQFULL = ACCFREE + 1, UQEMPTY = UQFULL + kQ;
+    constexpr int kDqThreads = 32 * DQ;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
@@ -141,19 +153,19 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ 
         }
         for (int q = 0; q < kQ; ++q) {
             ptx::mbar_init(bar(UQFULL + q), 1);
-            ptx::mbar_init(bar(UQEMPTY + q), 129);   // 128 dequant threads + the MMA thread
+            ptx::mbar_init(bar(UQEMPTY + q), kDqThreads + 1);   // dequant threads + the MMA thread
         }
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(bar(AREADY + i), 128);
+        for (int i = 0; i < NA; ++i) {
+            ptx::mbar_init(bar(AREADY + i), 128);   // the four warps of the chunk's group
             ptx::mbar_init(bar(AFREE + i), 1);
         }
         ptx::mbar_init(bar(ACCREADY), 1);
-        ptx::mbar_init(bar(ACCFREE), 128);
+        ptx::mbar_init(bar(ACCFREE), kDqThreads);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 4 && lane == 0) ptx::prefetch_tmap(&tmap);
-    if (warp == 5) {
+    if (warp == DQ && lane == 0) ptx::prefetch_tmap(&tmap);
+    if (warp == DQ + 1) {
         ptx::tmem_alloc(ptx::smem_addr(holder), C::kCols);
         ptx::tmem_relinquish();
     }
@@ -168,10 +180,14 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ 
     const int kc = args.kc;
     const int goff = bank_offset(L, args.b, args.P);
 
-    if (warp < 4) {
+    if (warp < DQ) {
         // ------------------------------------------------ dequant + epilogue
-        const int m = tid;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        // warp w serves TMEM lane quarter w % 4 for the chunks of group w / 4,
+        // and that group's share of the D column blocks in the epilogue
+        constexpr int G = C::kGroups;
+        const int quarter = warp & 3, group = warp >> 2;
+        const int m = quarter * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         uint32_t it = 0, j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
@@ -192,9 +208,12 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ 
                     my_exp = args.bexp[goff + p0 + n0 + lane];
                 }
                 for (int c = 0; c < kc; ++c, ++it) {
+                    if (G > 1 && (int)(it % G) != group) continue;   // another group's chunk
                     const int st = it % S;
                     if (!wait_warp(bar(FULL + st), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
                     const uint8_t *a_st = sA + st * kChunkBytes;
+                    const int abuf = it % NA;
+                    const uint32_t ua = it / NA;
                     const uint4 q0 = *(const uint4 *)(a_st + m * 16);
                     const uint4 q1 = *(const uint4 *)(a_st + 2048 + m * 16);
                     const uint32_t sc = *(const uint16_t *)(a_st + kChunkQBytes + 2 * m);
@@ -208,8 +227,6 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ 
                     dequant_word(q1.y, s1, r + 20);
                     dequant_word(q1.z, s1, r + 24);
                     dequant_word(q1.w, s1, r + 28);
-                    const int abuf = it & 1;
-                    const uint32_t ua = it >> 1;
                     if (ua > 0 && !wait_warp(bar(AFREE + abuf), (ua - 1) & 1, abort_flag, args.status)) {
                         ok = false;
                         break;
@@ -222,9 +239,9 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ 
                 if (!ok) break;
                 if (!wait_warp(bar(ACCREADY), j & 1, abort_flag, args.status)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const int w = warp, l = lane;
+                const int w = quarter, l = lane;
                 const int Nr = (nn + 15) & ~15;
-                for (int c0 = 0; c0 < Nr; c0 += 16) {
+                for (int c0 = group * 16; c0 < Nr; c0 += 16 * G) {
                     uint32_t v[16];
                     ptx::tmem_ld16(tmem + lane_base + C::kDCol + c0, v);
                     ptx::tmem_wait_ld();
@@ -258,7 +275,7 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ 
                 ptx::mbar_arrive(bar(ACCFREE));
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == DQ) {
         // ------------------------------------------------------------ producer
         uint32_t it = 0;
         bool ok = true;
@@ -339,8 +356,8 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ 
                 if (j > 0 && !wait_one(bar(ACCFREE), (j - 1) & 1, abort_flag, args.status)) { ok = false; break; }
                 ptx::tc_fence_after();
                 for (int c = 0; c < kc; ++c, ++it) {
-                    const int st = it % S, abuf = it & 1;
-                    if (!wait_one(bar(AREADY + abuf), (it >> 1) & 1, abort_flag, args.status)) { ok = false; break; }
+                    const int st = it % S, abuf = it % NA;
+                    if (!wait_one(bar(AREADY + abuf), (it / NA) & 1, abort_flag, args.status)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage);
 #pragma unroll
@@ -359,13 +376,13 @@ __global__ void __launch_bounds__(192, 1) ffn_tc_kernel(const __grid_constant__ 
             // wait until the MMAs already issued have retired (bounded)
             const uint32_t last = it - 1;
             for (uint32_t t = 0; t < kWaitLimit; ++t)
-                if (ptx::mbar_try_wait(bar(AFREE + (last & 1)), (last >> 1) & 1)) break;
+                if (ptx::mbar_try_wait(bar(AFREE + (last % NA)), (last / NA) & 1)) break;
         }
     }
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == DQ + 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::kCols);
     }
@@ -485,7 +502,7 @@ int launch_one(const CUtensorMap &map, const TcArgs &args, int blocks, cudaStrea
     auto kern = ffn_tc_kernel<NMAX, PHASE, COLD>;
     MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem));
     if (blocks < 1) return MOE_OK;
-    kern<<<blocks, 192, C::kSmem, s>>>(map, args);
+    kern<<<blocks, C::kThreads, C::kSmem, s>>>(map, args);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
@@ -574,7 +591,9 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, i
     // with more tokens than the tile loops over token tiles)
     if (T <= 16) return launch_bank<16>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
     if (T <= 256) return launch_bank<64>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
-    return launch_bank<256>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
+    // prefill-sized steps: 192-wide token tiles (an expert's ~T*k/E tokens in one
+    // tile), one CTA per SM with a 7-stage ring
+    return launch_bank<192>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
 }
 
 }  // namespace moe

@@ -70,7 +70,7 @@ inline Geom make_geom(const moe_geom &g) {
 // pick's index in its bank's list), so the two banks never share a row and
 // each expert's rows are contiguous.
 struct WsLayout {
-    size_t hdr, act_row, act_off, picks, epos, xg16, xgexp, h32, h16, hexp, total;
+    size_t hdr, act_row, act_off, picks, epos, ecnt, xg16, xgexp, h32, h16, hexp, total;
 };
 // header words
 // kHdrSched + 2*bank + phase: work counters of the FFN kernels' dynamic
@@ -89,6 +89,7 @@ inline WsLayout ws_layout(const Geom &g, int T) {
     w.act_off = take(2 * (P + 1) * 4);        // [2][P+1]
     w.picks = take(2 * P * 4);                // [2][P]
     w.epos = take((size_t)g.E * 4);           // [E] start of expert e's picks in its bank list
+    w.ecnt = take((size_t)g.E * 4);           // [E] picks per expert (large-step routing path)
     w.xg16 = take(P * (size_t)g.H * 2);       // [P][H] f16 token rows in pick order, per-row scaled
     w.xgexp = take(P * 4);                    // [P] int32 scale exponents of those rows
     w.h32 = take(P * (size_t)g.I * 4);        // [P][I] fp32 gate/up output (by g; by slot on CUDA cores)

@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(256) route_split_small(
 // Large steps, stage 1: one warp per token.
 __global__ void __launch_bounds__(256) route_tokens(const float *__restrict__ logits, int T, int E, int k,
                                                    int32_t *counts, int32_t *__restrict__ ids,
-                                                   float *__restrict__ w) {
+                                                   float *__restrict__ w, int32_t *ecnt) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -204,11 +204,12 @@ __global__ void __launch_bounds__(256) route_tokens(const float *__restrict__ lo
         ids[t * k + lane] = id;
         w[t * k + lane] = wv;
         if (counts) red_relaxed_add(counts + id, 1);
+        red_relaxed_add(ecnt + id, 1);   // picks per expert for the split (order-free)
     }
 }
 
-// Large steps, stage 2: per-expert counts and the active-row scan (one CTA).
-__global__ void __launch_bounds__(1024) split_scan(const int32_t *__restrict__ ids, int E,
+// Large steps, stage 2: the active-row scan over the per-expert counts (one CTA).
+__global__ void __launch_bounds__(1024) split_scan(const int32_t *__restrict__ ecnt, int E,
                                                    const int32_t *__restrict__ rowmap, int n_hot,
                                                    int n_cold, WsPtrs ws) {
     extern __shared__ int32_t sm[];
@@ -216,14 +217,12 @@ __global__ void __launch_bounds__(1024) split_scan(const int32_t *__restrict__ i
     int32_t *rowexp = cnt + E;      // [2][E]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e < E; e += blockDim.x) {
-        cnt[e] = 0;
+        cnt[e] = ecnt[e];
         ws.epos[e] = -1;
         int m = rowmap[e];
         if (m >= 0) rowexp[m] = e;
         else rowexp[E + (-1 - m)] = e;
     }
-    __syncthreads();
-    for (int s = tid; s < ws.P; s += blockDim.x) atomicAdd(&cnt[ids[s]], 1);
     __syncthreads();
     if (warp < 2) warp_scan_bank(warp, warp == 0 ? n_hot : n_cold, E, rowexp, cnt, ws.epos, ws, lane);
 }
@@ -266,9 +265,11 @@ int launch_route_split(moe_ctx *ctx, int layer, const float *logits, int T, int 
         MOE_LAUNCH_CHECK();
         return MOE_OK;
     }
-    route_tokens<<<(T + 7) / 8, 256, 0, s>>>(logits, T, g.E, g.k, counts, ids, w);
+    int32_t *ecnt = (int32_t *)(ws_base + lay.ecnt);
+    MOE_CUDA_TRY(cudaMemsetAsync(ecnt, 0, sizeof(int32_t) * g.E, s));
+    route_tokens<<<(T + 7) / 8, 256, 0, s>>>(logits, T, g.E, g.k, counts, ids, w, ecnt);
     MOE_LAUNCH_CHECK();
-    split_scan<<<1, 1024, sizeof(int32_t) * 3 * (size_t)g.E, s>>>(ids, g.E, L.rowmap_dev, L.n_hot,
+    split_scan<<<1, 1024, sizeof(int32_t) * 3 * (size_t)g.E, s>>>(ecnt, g.E, L.rowmap_dev, L.n_hot,
                                                                   L.n_cold, ws);
     MOE_LAUNCH_CHECK();
     split_fill<<<(g.E + 7) / 8, 256, 0, s>>>(ids, g.E, L.rowmap_dev, ws);
