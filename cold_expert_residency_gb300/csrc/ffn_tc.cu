@@ -4,31 +4,37 @@
 // GEMM, SwiGLU, down GEMM) runs once per residency bank without finalize.
 // Here one launch per GEMM covers one bank:
 //
-//   unit = (active bank row = one expert, 128-row M-tile [, N-tile]);
+//   unit = (active bank row = one expert, 128-row M-tile [, token tile]);
 //   D[128 x N] = A[128 x K] * B[N x K]^T accumulated in TMEM (fp32), with
 //   A = the expert's MXFP4 weights dequantised exactly to f16 and
 //   B = the expert's token rows (f16, each row scaled by a power of two so its
 //   largest element lies in [2^13, 2^14); the epilogue undoes the scale).
 //
-// Warp roles (192 threads):
-//   warp 4      producer.  Weights: hot bank -> one 1-D bulk async copy (TMA)
-//               of each 4352-byte (M-tile, K-chunk) block; cold bank ->
-//               16-byte cp.async reads of the mapped host bank (the host-link
-//               streaming path).  Token rows: 2-D tensor TMA boxes of 16 rows x
-//               64 f16 with 128-byte swizzle from the pick-ordered row array.
-//               All into a shared-memory ring, completion on one mbarrier per
-//               stage.
-//   warps 0-3   dequant: thread m owns weight row m = TMEM lane m; converts 64
-//               e2m1 codes with the hardware e2m1x2 -> f16x2 conversion,
-//               applies the e8m0 block scale (exact in f16) and stores the 32
-//               f16x2 columns into a double-buffered A operand in TMEM; then
-//               the epilogue (tcgen05.ld of D, SwiGLU or bf16 row store).
-//   warp 5      TMEM allocation; lane 0 issues tcgen05.mma (A from TMEM, B
+// Warp roles:
+//   producer    Weights: hot bank -> one 1-D bulk async copy (TMA) of each
+//               4352-byte (M-tile, K-chunk) block; cold bank -> 16-byte
+//               cp.async reads of the mapped host bank (the host-link
+//               streaming path).  Token rows: 2-D tensor TMA boxes of 64 f16
+//               per row with 128-byte swizzle from the pick-ordered row
+//               array.  All into a shared-memory ring, completion on one
+//               mbarrier per stage.
+//   dequant     Thread m of a 4-warp group owns weight row m = TMEM lane m;
+//               it converts 64 e2m1 codes with the hardware e2m1x2 -> f16x2
+//               conversion, applies the e8m0 block scale (exact in f16) and
+//               stores the 32 f16x2 columns into the group's TMEM A buffer.
+//   epilogue    tcgen05.ld of D, the row's power of two undone, then SwiGLU
+//               (gate and up rows meet in lanes l and l^16) or the bf16 row.
+//   MMA         TMEM allocation; one lane issues tcgen05.mma (A from TMEM, B
 //               from shared memory) and tcgen05.commit.
+// Decode tiles (16 or 64 tokens): one dequant group that also runs the
+// epilogue, 3-4 CTAs per SM.  Prefill tiles (192 tokens): one CTA per SM with
+// four dequant groups (group g takes the chunks c = g mod 4, so four chunks
+// are in flight), four dedicated epilogue warps and a double-buffered
+// accumulator, so one tile's epilogue overlaps the next tile's MMAs.
 //
 // The arithmetic of a pick depends only on its expert's weights, its token
-// row and the expert's token count (which fixes N), never on the bank, so the
-// hot and cold banks and any swap give bit-identical rows.
+// row and the expert's token count (which fixes the tile), never on the bank,
+// so the hot and cold banks and any swap give bit-identical rows.
 //
 // Every mbarrier wait is bounded; on timeout the kernel sets the status word
 // to MOE_ETIMEOUT, lets its own copies in flight land, frees TMEM and returns.
@@ -43,8 +49,6 @@ namespace moe {
 namespace {
 
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr int kBoxRows = 16;                 // token rows per tensor-TMA box
-constexpr int kBoxBytes = kBoxRows * 128;    // 16 rows x 64 f16
 
 struct TcArgs {
     const uint8_t *bank;
@@ -59,7 +63,7 @@ struct TcArgs {
     int32_t *sched;         // work counter of this launch (zeroed before it)
 };
 
-constexpr int kQ = 4;       // unit queue depth (producer -> dequant / MMA roles)
+constexpr int kQ = 4;       // unit queue depth (producer -> the other roles)
 
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                          int32_t *status) {
@@ -108,28 +112,91 @@ __device__ __forceinline__ int bank_offset(const BankLists &L, int b, int P) {
 
 template <int NMAX>
 struct TcCfg {
-    static constexpr int kStages = NMAX <= 16 ? 8 : (NMAX <= 64 ? 5 : (NMAX <= 192 ? 7 : 4));
+    static constexpr int kStages = NMAX <= 16 ? 8 : (NMAX <= 64 ? 5 : 7);
     static constexpr int kBStage = NMAX * 128;              // bytes of one B chunk (NMAX rows x 128 B)
-    // Wide (prefill) tiles run one CTA per SM, so the chunks in flight come
-    // from inside the CTA: four groups of four dequant warps, group g taking
-    // the chunks c = g (mod 4) into its own TMEM A buffer.  Decode tiles run
-    // 3-4 CTAs per SM with one group and two A buffers each.
-    static constexpr int kDq = NMAX >= 128 ? 16 : 4;
-    static constexpr int kGroups = kDq / 4;
-    static constexpr int kABufs = kGroups > 2 ? kGroups : 2;
-    static constexpr uint32_t kDCol = kABufs * 32;          // D after the 32-column A buffers
-    static constexpr uint32_t kCols = kDCol + NMAX <= 128 ? 128 : (kDCol + NMAX <= 256 ? 256 : 512);
-    static constexpr int kThreads = 32 * (kDq + 2);
-    static constexpr int kBars = 2 * kStages + 2 * kABufs + 2 + 2 * kQ;
+    static constexpr bool kWide = NMAX >= 128;
+    static constexpr int kDq = kWide ? 16 : 4;              // dequant warps
+    static constexpr int kGroups = kDq / 4;                 // dequant groups (one TMEM lane set each)
+    static constexpr int kABufs = kGroups > 1 ? kGroups : (NMAX <= 16 ? 3 : 2);
+    static constexpr int kEpi = kWide ? 4 : 0;              // dedicated epilogue warps
+    static constexpr int kDBufs = kEpi ? 2 : 1;             // accumulators in TMEM
+    // token rows per tensor-TMA box: few large boxes for wide tiles (the TMA
+    // engine's cost is per box), 16-row boxes for the few tokens of decode
+    static constexpr int kBoxRows = kWide ? 64 : 16;
+    static constexpr int kBoxBytes = kBoxRows * 128;
+    static constexpr uint32_t kDCol = kABufs * 32;          // first D column (after the A buffers)
+    static constexpr uint32_t kColsUsed = kDCol + kDBufs * NMAX;
+    static constexpr uint32_t kCols = kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512);
+    static_assert(kColsUsed <= 512, "tile does not fit in tensor memory");
+    static constexpr int kProducer = kDq + kEpi;            // producer warp; the MMA warp follows
+    static constexpr int kThreads = 32 * (kDq + kEpi + 2);
+    static constexpr int kBars = 2 * kStages + 2 * kABufs + 2 * kDBufs + 2 * kQ;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * (kBStage + kChunkBytes) + kBars * 8 + 16 + 4 * kQ;
 };
+
+// Epilogue metadata of NBLK column blocks of 16: lane q of block i holds, for
+// column (blk0 + i*bstride)*16 + q, its slot and the exact power of two that
+// undoes its row's scaling (0 past the tile's last column).
+template <int NBLK>
+__device__ __forceinline__ void load_meta(const BankLists &L, const TcArgs &args, int blk0, int bstride, int nn,
+                                          int p, int g, int lane, int (&rs)[NBLK], float (&rsc)[NBLK]) {
+#pragma unroll
+    for (int i = 0; i < NBLK; ++i) {
+        const int col = (blk0 + i * bstride) * 16 + (lane & 15);
+        rs[i] = col < nn ? L.picks[p + col] : 0;
+        rsc[i] = col < nn ? ldexpf(1.0f, args.bexp[g + col]) : 0.0f;
+    }
+}
+
+// Drain NBLK column blocks of D (TMEM address dt = this warp's lane quarter,
+// first D column) into h rows (phase 1) or bf16 Y rows (phase 2).  All 16
+// columns of a block are computed together; only the stores are predicated.
+template <int PHASE, int NBLK>
+__device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, int blk0, int bstride, int nn, int g,
+                                              int mt, int quarter, int lane, const int (&rs)[NBLK],
+                                              const float (&rsc)[NBLK]) {
+    const int Nr = (nn + 15) & ~15;
+    const int m = quarter * 32 + lane;
+#pragma unroll
+    for (int i = 0; i < NBLK; ++i) {
+        const int c0 = (blk0 + i * bstride) * 16;
+        if (c0 >= Nr) break;   // warp-uniform
+        uint32_t v[16];
+        ptx::tmem_ld16(dt + c0, v);
+        ptx::tmem_wait_ld();
+        float d[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)   // undo the row's power of two (exact)
+            d[q] = __fmul_rn(__uint_as_float(v[q]), __shfl_sync(0xffffffffu, rsc[i], q));
+        if (PHASE == 1) {
+            float o[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) o[q] = __shfl_xor_sync(0xffffffffu, d[q], 16);
+            if (lane < 16) {
+                float *dst = args.h_out + (int64_t)(g + c0) * args.I + 64 * mt + 16 * quarter + lane;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    // silu(gate) * up with silu(z) = z / (1 + e^-z)
+                    const float hv = __fmul_rn(__fmul_rn(d[q], __frcp_rn(1.0f + __expf(-d[q]))), o[q]);
+                    if (c0 + q < nn) dst[(int64_t)q * args.I] = hv;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int slot = __shfl_sync(0xffffffffu, rs[i], q);
+                if (c0 + q < nn)
+                    args.Y[(int64_t)slot * args.H + kMT * mt + m] = __bfloat16_as_ushort(__float2bfloat16_rn(d[q]));
+            }
+        }
+    }
+}
 
 template <int NMAX, int PHASE, bool COLD>
 __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                          TcArgs args) {
     using C = TcCfg<NMAX>;
-    constexpr int DQ = C::kDq, NA = C::kABufs;
-    constexpr int S = C::kStages;
+    constexpr int DQ = C::kDq, NA = C::kABufs, DB = C::kDBufs, S = C::kStages, G = C::kGroups;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled B stages need 1024-byte alignment
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -141,9 +208,10 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
     volatile int *uq = (volatile int *)(holder + 2);   // [kQ] unit queue
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
     const int FULL = 0, EMPTY = S, AREADY = 2 * S, AFREE = 2 * S + NA, ACCREADY = 2 * S + 2 * NA,
-              ACCFREE = ACCREADY + 1;
-    const int UQFULL = ACCFREE + 1, UQEMPTY = UQFULL + kQ;
-    constexpr int kDqThreads = 32 * DQ;
+              ACCFREE = ACCREADY + DB, UQFULL = ACCFREE + DB, UQEMPTY = UQFULL + kQ;
+    constexpr int kEpiThreads = C::kEpi ? 32 * C::kEpi : 32 * DQ;   // threads that drain D
+    constexpr int kQueueReaders = 32 * DQ + 32 * C::kEpi + 1;       // + the MMA thread
+    constexpr int PROD = C::kProducer, MMAW = C::kProducer + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
@@ -153,19 +221,21 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
         }
         for (int q = 0; q < kQ; ++q) {
             ptx::mbar_init(bar(UQFULL + q), 1);
-            ptx::mbar_init(bar(UQEMPTY + q), kDqThreads + 1);   // dequant threads + the MMA thread
+            ptx::mbar_init(bar(UQEMPTY + q), kQueueReaders);
         }
         for (int i = 0; i < NA; ++i) {
             ptx::mbar_init(bar(AREADY + i), 128);   // the four warps of the chunk's group
             ptx::mbar_init(bar(AFREE + i), 1);
         }
-        ptx::mbar_init(bar(ACCREADY), 1);
-        ptx::mbar_init(bar(ACCFREE), kDqThreads);
+        for (int i = 0; i < DB; ++i) {
+            ptx::mbar_init(bar(ACCREADY + i), 1);
+            ptx::mbar_init(bar(ACCFREE + i), kEpiThreads);
+        }
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == DQ && lane == 0) ptx::prefetch_tmap(&tmap);
-    if (warp == DQ + 1) {
+    if (warp == PROD && lane == 0) ptx::prefetch_tmap(&tmap);
+    if (warp == MMAW) {
         ptx::tmem_alloc(ptx::smem_addr(holder), C::kCols);
         ptx::tmem_relinquish();
     }
@@ -180,33 +250,38 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
     const int kc = args.kc;
     const int goff = bank_offset(L, args.b, args.P);
 
+    // every role but the producer reads the unit sequence from the queue
+    auto take_unit = [&](uint32_t ui, bool warp_wide, bool &ok) -> int {
+        const int qs = ui % kQ;
+        const bool w = warp_wide ? wait_warp(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status)
+                                 : wait_one(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status);
+        if (!w) {
+            ok = false;
+            return -1;
+        }
+        const int u = uq[qs];
+        ptx::mbar_arrive(bar(UQEMPTY + qs));
+        return u;
+    };
+
     if (warp < DQ) {
-        // ------------------------------------------------ dequant + epilogue
-        // warp w serves TMEM lane quarter w % 4 for the chunks of group w / 4,
-        // and that group's share of the D column blocks in the epilogue
-        constexpr int G = C::kGroups;
+        // ------------------------------------------------ dequant (+ epilogue)
         const int quarter = warp & 3, group = warp >> 2;
         const int m = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        constexpr int NB = NMAX / 16 / G;   // this warp's D column blocks when it drains D
         uint32_t it = 0, j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
-            const int qs = ui % kQ;
-            if (!wait_warp(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status)) { ok = false; break; }
-            const int u = uq[qs];
-            ptx::mbar_arrive(bar(UQEMPTY + qs));
+            const int u = take_unit(ui, true, ok);
             if (u < 0) break;
             const int a = u / args.mt_count, mt = u % args.mt_count;
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
-                // epilogue metadata for up to 32 columns, fetched before the
-                // K loop so its latency hides behind it
-                int my_slot = 0, my_exp = 0;
-                if (lane < nn && lane < 32) {
-                    my_slot = L.picks[p0 + n0 + lane];
-                    my_exp = args.bexp[goff + p0 + n0 + lane];
-                }
+                int rs[NB];
+                float re[NB];
+                if (C::kEpi == 0) load_meta<NB>(L, args, group, G, nn, p0 + n0, goff + p0 + n0, lane, rs, re);
                 for (int c = 0; c < kc; ++c, ++it) {
                     if (G > 1 && (int)(it % G) != group) continue;   // another group's chunk
                     const int st = it % S;
@@ -237,45 +312,43 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                     ptx::mbar_arrive(bar(AREADY + abuf));
                 }
                 if (!ok) break;
-                if (!wait_warp(bar(ACCREADY), j & 1, abort_flag, args.status)) { ok = false; break; }
-                ptx::tc_fence_after();
-                const int w = quarter, l = lane;
-                const int Nr = (nn + 15) & ~15;
-                for (int c0 = group * 16; c0 < Nr; c0 += 16 * G) {
-                    uint32_t v[16];
-                    ptx::tmem_ld16(tmem + lane_base + C::kDCol + c0, v);
-                    ptx::tmem_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int col = c0 + q;
-                        if (col < nn) {   // warp-uniform
-                            int slot, e;
-                            if (col < 32) {
-                                slot = __shfl_sync(0xffffffffu, my_slot, col);
-                                e = __shfl_sync(0xffffffffu, my_exp, col);
-                            } else {
-                                slot = L.picks[p0 + n0 + col];
-                                e = args.bexp[goff + p0 + n0 + col];
-                            }
-                            const float d = ldexpf(__uint_as_float(v[q]), e);
-                            if (PHASE == 1) {
-                                const float o = __shfl_xor_sync(0xffffffffu, d, 16);
-                                if (l < 16) {
-                                    const float hv = __fmul_rn(__fdiv_rn(d, 1.0f + expf(-d)), o);
-                                    args.h_out[(int64_t)(goff + p0 + n0 + col) * args.I + 64 * mt + 16 * w + l] = hv;
-                                }
-                            } else {
-                                args.Y[(int64_t)slot * args.H + kMT * mt + m] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(d));
-                            }
-                        }
-                    }
+                if (C::kEpi == 0) {
+                    if (!wait_warp(bar(ACCREADY), j & 1, abort_flag, args.status)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    epilogue_cols<PHASE, NB>(args, tmem + lane_base + C::kDCol, group, G, nn, goff + p0 + n0, mt,
+                                             quarter, lane, rs, re);
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(bar(ACCFREE));
                 }
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(ACCFREE));
             }
         }
-    } else if (warp == DQ) {
+    } else if (C::kEpi && warp < DQ + C::kEpi) {
+        // -------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        constexpr int NB = NMAX / 16;
+        uint32_t j = 0;
+        bool ok = true;
+        for (uint32_t ui = 0; ok; ++ui) {
+            const int u = take_unit(ui, true, ok);
+            if (u < 0) break;
+            const int a = u / args.mt_count, mt = u % args.mt_count;
+            const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
+            for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
+                const int nn = min(NMAX, n - n0);
+                int rs[NB];
+                float re[NB];
+                load_meta<NB>(L, args, 0, 1, nn, p0 + n0, goff + p0 + n0, lane, rs, re);
+                const int db = j % DB;
+                if (!wait_warp(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status)) { ok = false; break; }
+                ptx::tc_fence_after();
+                epilogue_cols<PHASE, NB>(args, tmem + lane_base + C::kDCol + db * NMAX, 0, 1, nn, goff + p0 + n0,
+                                         mt, quarter, lane, rs, re);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(ACCFREE + db));
+            }
+        }
+    } else if (warp == PROD) {
         // ------------------------------------------------------------ producer
         uint32_t it = 0;
         bool ok = true;
@@ -303,7 +376,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                                   (int64_t)mt * kc * kChunkBytes;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX) {
                 const int nn = min(NMAX, n - n0);
-                const int nbox = (nn + kBoxRows - 1) / kBoxRows;
+                const int nbox = (nn + C::kBoxRows - 1) / C::kBoxRows;
                 const int brow = goff + p0 + n0;
                 for (int c = 0; c < kc; ++c, ++it) {
                     const int st = it % S;
@@ -320,10 +393,11 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                         ptx::cp_async_arrive_noinc(bar(FULL + st));
                     }
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(bar(FULL + st), (COLD ? 0u : (uint32_t)kChunkBytes) + nbox * kBoxBytes);
+                        ptx::mbar_arrive_expect_tx(bar(FULL + st), (COLD ? 0u : (uint32_t)kChunkBytes) + nbox * C::kBoxBytes);
                         if (!COLD) ptx::bulk_g2s(a_addr, src_chunk, kChunkBytes, bar(FULL + st));
                         for (int q = 0; q < nbox; ++q)
-                            ptx::tma_load_2d(b_addr + q * kBoxBytes, &tmap, c * kKC, brow + q * kBoxRows, bar(FULL + st));
+                            ptx::tma_load_2d(b_addr + q * C::kBoxBytes, &tmap, c * kKC, brow + q * C::kBoxRows,
+                                             bar(FULL + st));
                     }
                     __syncwarp();
                 }
@@ -337,15 +411,12 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                     if (ptx::mbar_try_wait(bar(FULL + i % S), (i / S) & 1)) break;
             }
         }
-    } else if (lane == 0) {
+    } else if (warp == MMAW && lane == 0) {
         // ----------------------------------------------------------- MMA issue
         uint32_t it = 0, j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
-            const int qs = ui % kQ;
-            if (!wait_one(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status)) { ok = false; break; }
-            const int u = uq[qs];
-            ptx::mbar_arrive(bar(UQEMPTY + qs));
+            const int u = take_unit(ui, false, ok);
             if (u < 0) break;
             const int a = u / args.mt_count;
             const int n = L.act_off[a + 1] - L.act_off[a];
@@ -353,8 +424,14 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                 const int nn = min(NMAX, n - n0);
                 const int Nr = (nn + 15) & ~15;
                 const uint32_t idesc = ptx::idesc_f16_f32(128, Nr);
-                if (j > 0 && !wait_one(bar(ACCFREE), (j - 1) & 1, abort_flag, args.status)) { ok = false; break; }
+                const int db = j % DB;
+                if (j >= (uint32_t)DB &&
+                    !wait_one(bar(ACCFREE + db), ((j / DB) - 1) & 1, abort_flag, args.status)) {
+                    ok = false;
+                    break;
+                }
                 ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem + C::kDCol + db * NMAX;
                 for (int c = 0; c < kc; ++c, ++it) {
                     const int st = it % S, abuf = it % NA;
                     if (!wait_one(bar(AREADY + abuf), (it / NA) & 1, abort_flag, args.status)) { ok = false; break; }
@@ -363,13 +440,13 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 32);
-                        ptx::mma_f16_ts(tmem + C::kDCol, tmem + abuf * 32 + kk * 8, bd, idesc, (c | kk) != 0);
+                        ptx::mma_f16_ts(d_tmem, tmem + abuf * 32 + kk * 8, bd, idesc, (c | kk) != 0);
                     }
                     ptx::mma_commit(bar(EMPTY + st));
                     ptx::mma_commit(bar(AFREE + abuf));
                 }
                 if (!ok) break;
-                ptx::mma_commit(bar(ACCREADY));
+                ptx::mma_commit(bar(ACCREADY + db));
             }
         }
         if (!ok && it > 0) {
@@ -382,7 +459,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == DQ + 1) {
+    if (warp == MMAW) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::kCols);
     }
@@ -480,14 +557,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Tensor map over a [rows][K] f16 array: boxes of 16 rows x 64 elements,
-// 128-byte swizzle, zero fill past the last row.
-int make_row_map(CUtensorMap *map, const void *base, int K, int rows) {
+// Tensor map over a [rows][K] f16 array: boxes of box_rows rows x 64
+// elements, 128-byte swizzle, zero fill past the last row.
+int make_row_map(CUtensorMap *map, const void *base, int K, int rows, int box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled unavailable");
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kKC, (cuuint32_t)kBoxRows};
+    cuuint32_t box[2] = {(cuuint32_t)kKC, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -524,11 +601,13 @@ int grid_for(const moe_ctx *ctx, bool cold, bool shared, int units_max) {
 }
 
 template <int NMAX>
-int launch_bank(moe_ctx *ctx, bool cold, bool shared, const TcArgs &a1, const TcArgs &a2, const CUtensorMap &m1,
-                const CUtensorMap &m2, int units1, int units2, const uint16_t *x, const WsLayout &lay, uint8_t *ws,
-                cudaStream_t s) {
+int launch_bank(moe_ctx *ctx, bool cold, bool shared, const TcArgs &a1, const TcArgs &a2, int units1, int units2,
+                const uint16_t *x, const WsLayout &lay, uint8_t *ws, cudaStream_t s) {
     const Geom &g = ctx->g;
     const int P = a1.P;
+    CUtensorMap m1, m2;
+    if (int r = make_row_map(&m1, ws + lay.xg16, g.H, P, TcCfg<NMAX>::kBoxRows)) return r;
+    if (int r = make_row_map(&m2, ws + lay.h16, g.I, P, TcCfg<NMAX>::kBoxRows)) return r;
     prep_x_kernel<<<P, 256, 0, s>>>(x, g.H, g.k, a1.lists, a1.b, P, (__half *)(ws + lay.xg16),
                                     (int32_t *)(ws + lay.xgexp), a1.sched);
     MOE_LAUNCH_CHECK();
@@ -553,10 +632,6 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, i
     lists.act_row = (const int32_t *)(ws + lay.act_row) + (size_t)b * P;
     lists.act_off = (const int32_t *)(ws + lay.act_off) + (size_t)b * (P + 1);
     lists.picks = (const int32_t *)(ws + lay.picks) + (size_t)b * P;
-
-    CUtensorMap m1, m2;
-    if (int r = make_row_map(&m1, ws + lay.xg16, g.H, P)) return r;
-    if (int r = make_row_map(&m2, ws + lay.h16, g.I, P)) return r;
 
     TcArgs a1{};
     a1.bank = bank;
@@ -585,15 +660,14 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, i
 
     const bool cold = b == MOE_BANK_COLD;
     const int units1 = P * g.mt13, units2 = P * g.mt2;   // active rows never exceed the picks
-    // the token-tile width depends only on T, so an expert's arithmetic is
-    // the same in either bank
-    // (decode-sized steps use narrow tiles with several CTAs per SM; an expert
-    // with more tokens than the tile loops over token tiles)
-    if (T <= 16) return launch_bank<16>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
-    if (T <= 256) return launch_bank<64>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
-    // prefill-sized steps: 192-wide token tiles (an expert's ~T*k/E tokens in one
-    // tile), one CTA per SM with a 7-stage ring
-    return launch_bank<192>(ctx, cold, shared, a1, a2, m1, m2, units1, units2, x, lay, ws, s);
+    // The token-tile width depends only on T, so an expert's arithmetic is
+    // the same in either bank.  Decode-sized steps use narrow tiles with
+    // several CTAs per SM (an expert with more tokens than the tile loops over
+    // token tiles); prefill-sized steps use 192-wide tiles (an expert's
+    // ~T*k/E tokens in one tile), one CTA per SM.
+    if (T <= 16) return launch_bank<16>(ctx, cold, shared, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= 256) return launch_bank<64>(ctx, cold, shared, a1, a2, units1, units2, x, lay, ws, s);
+    return launch_bank<192>(ctx, cold, shared, a1, a2, units1, units2, x, lay, ws, s);
 }
 
 }  // namespace moe
