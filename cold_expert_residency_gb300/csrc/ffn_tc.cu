@@ -157,13 +157,23 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
                                               const float (&rsc)[NBLK]) {
     const int Nr = (nn + 15) & ~15;
     const int m = quarter * 32 + lane;
+    uint32_t vv[32];
 #pragma unroll
     for (int i = 0; i < NBLK; ++i) {
         const int c0 = (blk0 + i * bstride) * 16;
         if (c0 >= Nr) break;   // warp-uniform
-        uint32_t v[16];
-        ptx::tmem_ld16(dt + c0, v);
-        ptx::tmem_wait_ld();
+        // contiguous column blocks are read 32 columns per TMEM load
+        const bool pair = bstride == 1 && (i & 1) == 0 && i + 1 < NBLK && c0 + 16 < Nr;
+        if ((i & 1) == 0 || bstride != 1) {
+            if (pair) {
+                ptx::tmem_ld32(dt + c0, vv);
+            } else {
+                uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&vv[0]);
+                ptx::tmem_ld16(dt + c0, lo);
+            }
+            ptx::tmem_wait_ld();
+        }
+        const uint32_t *v = vv + (bstride == 1 ? (i & 1) * 16 : 0);
         float d[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q)   // undo the row's power of two (exact)
