@@ -48,7 +48,8 @@ namespace moe {
 
 namespace {
 
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kWaitLimit = 1u << 22;        // polls of the teardown drains
+constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s bound of a pipeline wait
 
 struct TcArgs {
     const uint8_t *bank;
@@ -65,13 +66,22 @@ struct TcArgs {
 
 constexpr int kQ = 4;       // unit queue depth (producer -> the other roles)
 
+// Bounded mbarrier wait: gives up after kWaitNs of wall-clock time, raising
+// the CTA's abort flag and the launch status.  SUSP: each poll may suspend the
+// thread (up to 20 us) instead of returning at once -- used by the decode
+// tiles, whose 3-4 CTAs per SM otherwise spend issue slots polling.
+template <bool SUSP>
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                          int32_t *status) {
+    uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u) {
+        if (SUSP ? ptx::mbar_try_wait_suspend(bar, parity, 20000u) : ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & (SUSP ? 3u : 255u)) == 0u) {
             if (*abort_flag) return false;
-            if (i >= kWaitLimit) {
+            const uint64_t now = ptx::globaltimer_ns();
+            if (i == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitNs) {
                 *abort_flag = 1;
                 atomicCAS(status, 0, MOE_ETIMEOUT);
                 return false;
@@ -80,9 +90,10 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile
     }
 }
 
+template <bool SUSP>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           int32_t *status) {
-    bool ok = wait_one(bar, parity, abort_flag, status);
+    bool ok = wait_one<SUSP>(bar, parity, abort_flag, status);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -187,7 +198,7 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
                     // silu(gate) * up with silu(z) = z / (1 + e^-z)
-                    const float hv = __fmul_rn(__fmul_rn(d[q], __frcp_rn(1.0f + __expf(-d[q]))), o[q]);
+                    const float hv = __fmul_rn(__fdividef(d[q], 1.0f + __expf(-d[q])), o[q]);
                     if (c0 + q < nn) dst[(int64_t)q * args.I] = hv;
                 }
             }
@@ -222,6 +233,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
     constexpr int kEpiThreads = C::kEpi ? 32 * C::kEpi : 32 * DQ;   // threads that drain D
     constexpr int kQueueReaders = 32 * DQ + 32 * C::kEpi + 1;       // + the MMA thread
     constexpr int PROD = C::kProducer, MMAW = C::kProducer + 1;
+    constexpr bool SUSP = !C::kWide;   // suspend-hinted waits for the decode tiles
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
@@ -263,8 +275,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
     // every role but the producer reads the unit sequence from the queue
     auto take_unit = [&](uint32_t ui, bool warp_wide, bool &ok) -> int {
         const int qs = ui % kQ;
-        const bool w = warp_wide ? wait_warp(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status)
-                                 : wait_one(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status);
+        const bool w = warp_wide ? wait_warp<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status)
+                                 : wait_one<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status);
         if (!w) {
             ok = false;
             return -1;
@@ -279,7 +291,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
         const int quarter = warp & 3, group = warp >> 2;
         const int m = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        constexpr int NB = NMAX / 16 / G;   // this warp's D column blocks when it drains D
+        constexpr int NB = (NMAX / 16 + G - 1) / G;   // this warp's D column blocks when it drains D
         uint32_t it = 0, j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
@@ -295,7 +307,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                 for (int c = 0; c < kc; ++c, ++it) {
                     if (G > 1 && (int)(it % G) != group) continue;   // another group's chunk
                     const int st = it % S;
-                    if (!wait_warp(bar(FULL + st), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
+                    if (!wait_warp<SUSP>(bar(FULL + st), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
                     const uint8_t *a_st = sA + st * kChunkBytes;
                     const int abuf = it % NA;
                     const uint32_t ua = it / NA;
@@ -312,7 +324,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                     dequant_word(q1.y, s1, r + 20);
                     dequant_word(q1.z, s1, r + 24);
                     dequant_word(q1.w, s1, r + 28);
-                    if (ua > 0 && !wait_warp(bar(AFREE + abuf), (ua - 1) & 1, abort_flag, args.status)) {
+                    if (ua > 0 && !wait_warp<SUSP>(bar(AFREE + abuf), (ua - 1) & 1, abort_flag, args.status)) {
                         ok = false;
                         break;
                     }
@@ -323,7 +335,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                 }
                 if (!ok) break;
                 if (C::kEpi == 0) {
-                    if (!wait_warp(bar(ACCREADY), j & 1, abort_flag, args.status)) { ok = false; break; }
+                    if (!wait_warp<SUSP>(bar(ACCREADY), j & 1, abort_flag, args.status)) { ok = false; break; }
                     ptx::tc_fence_after();
                     epilogue_cols<PHASE, NB>(args, tmem + lane_base + C::kDCol, group, G, nn, goff + p0 + n0, mt,
                                              quarter, lane, rs, re);
@@ -350,7 +362,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                 float re[NB];
                 load_meta<NB>(L, args, 0, 1, nn, p0 + n0, goff + p0 + n0, lane, rs, re);
                 const int db = j % DB;
-                if (!wait_warp(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status)) { ok = false; break; }
+                if (!wait_warp<SUSP>(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status)) { ok = false; break; }
                 ptx::tc_fence_after();
                 epilogue_cols<PHASE, NB>(args, tmem + lane_base + C::kDCol + db * NMAX, 0, 1, nn, goff + p0 + n0,
                                          mt, quarter, lane, rs, re);
@@ -366,7 +378,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
             // take the next unit from the launch's work counter and publish it
             const int qs = ui % kQ;
             if (ui >= (uint32_t)kQ &&
-                !wait_warp(bar(UQEMPTY + qs), ((ui / kQ) - 1) & 1, abort_flag, args.status)) {
+                !wait_warp<SUSP>(bar(UQEMPTY + qs), ((ui / kQ) - 1) & 1, abort_flag, args.status)) {
                 ok = false;
                 break;
             }
@@ -391,7 +403,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                 for (int c = 0; c < kc; ++c, ++it) {
                     const int st = it % S;
                     const uint32_t rnd = it / S;
-                    if (rnd > 0 && !wait_warp(bar(EMPTY + st), (rnd - 1) & 1, abort_flag, args.status)) {
+                    if (rnd > 0 && !wait_warp<SUSP>(bar(EMPTY + st), (rnd - 1) & 1, abort_flag, args.status)) {
                         ok = false;
                         break;
                     }
@@ -436,7 +448,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                 const uint32_t idesc = ptx::idesc_f16_f32(128, Nr);
                 const int db = j % DB;
                 if (j >= (uint32_t)DB &&
-                    !wait_one(bar(ACCFREE + db), ((j / DB) - 1) & 1, abort_flag, args.status)) {
+                    !wait_one<SUSP>(bar(ACCFREE + db), ((j / DB) - 1) & 1, abort_flag, args.status)) {
                     ok = false;
                     break;
                 }
@@ -444,7 +456,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                 const uint32_t d_tmem = tmem + C::kDCol + db * NMAX;
                 for (int c = 0; c < kc; ++c, ++it) {
                     const int st = it % S, abuf = it % NA;
-                    if (!wait_one(bar(AREADY + abuf), (it / NA) & 1, abort_flag, args.status)) { ok = false; break; }
+                    if (!wait_one<SUSP>(bar(AREADY + abuf), (it / NA) & 1, abort_flag, args.status)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage);
 #pragma unroll
