@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(128) ffn_simt_kernel(const uint8_t *__restrict
 #pragma unroll
                         for (int ni = 0; ni < 8; ++ni) {
                             const int kk = hh * 32 + wi * 8 + ni;
-                            const float wv = e2m1_to_f32((wd[wi] >> (4 * ni)) & 15u) * sc[hh];
+                            const int sh = ni < 4 ? 8 * ni : 8 * (ni - 4) + 4;   // device nibble order
+                            const float wv = e2m1_to_f32((wd[wi] >> sh) & 15u) * sc[hh];
 #pragma unroll
                             for (int tn = 0; tn < kTok; ++tn)
                                 if (tn < nn) acc[tn] = __fmaf_rn(wv, sx[tn][kk], acc[tn]);

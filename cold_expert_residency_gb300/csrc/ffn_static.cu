@@ -80,7 +80,7 @@ int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t
     cudaStream_t s = (cudaStream_t)stream;
     if (!r) {
         // the pick lists are the front of the workspace (header, rows, offsets, picks, positions)
-        cudaError_t e = cudaMemcpyAsync(scratch, split_ws, lay.xg16, cudaMemcpyDeviceToDevice, s);
+        cudaError_t e = cudaMemcpyAsync(scratch, split_ws, lay.xq, cudaMemcpyDeviceToDevice, s);
         if (e != cudaSuccess) r = cuda_error(e, "copy pick lists into the static scratch");
     }
     if (!r) {

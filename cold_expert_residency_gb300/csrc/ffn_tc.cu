@@ -1,39 +1,46 @@
-// MXFP4 expert FFN on the 5th-generation tensor cores (tcgen05 + TMEM).
+// MXFP4 expert FFN on the 5th-generation tensor cores (tcgen05 + TMEM),
+// block-scaled.
 //
 // "vLLM: Pin Hot Experts", Results: the routed MXFP4 expert FFN (gate/up
 // GEMM, SwiGLU, down GEMM) runs once per residency bank without finalize.
 // Here one launch per GEMM covers one bank:
 //
 //   unit = (active bank row = one expert, 128-row M-tile [, token tile]);
-//   D[128 x N] = A[128 x K] * B[N x K]^T accumulated in TMEM (fp32), with
-//   A = the expert's MXFP4 weights dequantised exactly to f16 and
-//   B = the expert's token rows (f16, each row scaled by a power of two so its
-//   largest element lies in [2^13, 2^14); the epilogue undoes the scale).
+//   D[128 x N] = sum over 32-wide K blocks of (SFA * A) (SFB * B)^T, fp32 in
+//   TMEM, by tcgen05.mma kind::mxf8f6f4 with e8m0 block scales, where
+//   A = the expert's e2m1 weights with their own e8m0 scales (exact), and
+//   B = the expert's token rows (bf16 x, or the fp32 gate/up output h), each
+//       row scaled by a power of two so its largest |value| lies in (224, 448]
+//       and carried as two e4m3 pieces: q1 = e4m3(v), q2 = e4m3(16 (v - q1)).
+//       B's scales are constants (2^0 for q1, 2^-4 for q2); both pieces
+//       accumulate into the same D, so v is represented to about 2^-8 of
+//       itself; the epilogue undoes the row's power of two.
 //
 // Warp roles:
 //   producer    Weights: hot bank -> one 1-D bulk async copy (TMA) of each
 //               4352-byte (M-tile, K-chunk) block; cold bank -> 16-byte
 //               cp.async reads of the mapped host bank (the host-link
-//               streaming path).  Token rows: 2-D tensor TMA boxes of 64 f16
-//               per row with 128-byte swizzle from the pick-ordered row
-//               array.  All into a shared-memory ring, completion on one
-//               mbarrier per stage.
-//   dequant     Thread m of a 4-warp group owns weight row m = TMEM lane m;
-//               it converts 64 e2m1 codes with the hardware e2m1x2 -> f16x2
-//               conversion, applies the e8m0 block scale (exact in f16) and
-//               stores the 32 f16x2 columns into the group's TMEM A buffer.
+//               streaming path).  Token rows: 2-D tensor TMA boxes of 128
+//               bytes (the chunk's two e4m3 pieces) per row with 128-byte
+//               swizzle from the pick-ordered row array.  All into a
+//               shared-memory ring, completion on one mbarrier per stage.
+//   unpack      Thread m of a 4-warp group owns weight row m = TMEM lane m;
+//               per chunk it spreads its 64 e2m1 codes to one byte each
+//               (two masked shifts per 8 codes, thanks to the device nibble
+//               order) into the group's TMEM A slot, and its two e8m0 scale
+//               bytes into the slot's scale column.
 //   epilogue    tcgen05.ld of D, the row's power of two undone, then SwiGLU
 //               (gate and up rows meet in lanes l and l^16) or the bf16 row.
-//   MMA         TMEM allocation; one lane issues tcgen05.mma (A from TMEM, B
-//               from shared memory) and tcgen05.commit.
-// Decode tiles (16 or 64 tokens): one dequant group that also runs the
+//   MMA         TMEM allocation; one lane issues tcgen05.mma (A and the
+//               scales from TMEM, B from shared memory) and tcgen05.commit.
+// Decode tiles (16 or 64 tokens): one unpack group that also runs the
 // epilogue, 3-4 CTAs per SM.  Prefill tiles (192 tokens): one CTA per SM with
-// four dequant groups (group g takes the chunks c = g mod 4, so four chunks
-// are in flight), four dedicated epilogue warps and a double-buffered
-// accumulator, so one tile's epilogue overlaps the next tile's MMAs.
+// two unpack groups (group g takes the chunks c = g mod 2), four dedicated
+// epilogue warps and a double-buffered accumulator, so one tile's epilogue
+// overlaps the next tile's MMAs.
 //
 // The arithmetic of a pick depends only on its expert's weights, its token
-// row and the expert's token count (which fixes the tile), never on the bank,
+// row and the step's token count (which fixes the tile), never on the bank,
 // so the hot and cold banks and any swap give bit-identical rows.
 //
 // Every mbarrier wait is bounded; on timeout the kernel sets the status word
@@ -43,6 +50,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 
 namespace moe {
 
@@ -97,24 +105,11 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-// e8m0 byte (104..140, checked at bank init) -> the same power of two in f16.
-__device__ __forceinline__ uint32_t e8m0_f16x2(uint32_t s) {
-    uint32_t h = s >= 113u ? (s - 112u) << 10 : 1u << (s - 103u);
-    return h | (h << 16);
-}
-
-// 8 e2m1 codes (one 32-bit word, low nibble first) -> 4 f16x2, scaled.
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t scale2, uint32_t *o) {
-    uint32_t c0, c1, c2, c3;
-    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
-        : "=r"(c0), "=r"(c1), "=r"(c2), "=r"(c3)
-        : "r"(w));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[0]) : "r"(c0), "r"(scale2));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[1]) : "r"(c1), "r"(scale2));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2]) : "r"(c2), "r"(scale2));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[3]) : "r"(c3), "r"(scale2));
+// 8 e2m1 codes in the device nibble order (byte i: codes i and 4+i) -> two
+// TMEM columns of one code per byte, code in bits 5..2.
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    lo = (w << 2) & 0x3C3C3C3Cu;
+    hi = (w >> 2) & 0x3C3C3C3Cu;
 }
 
 __device__ __forceinline__ int bank_offset(const BankLists &L, int b, int P) {
@@ -123,25 +118,45 @@ __device__ __forceinline__ int bank_offset(const BankLists &L, int b, int P) {
 
 template <int NMAX>
 struct TcCfg {
-    static constexpr int kStages = NMAX <= 16 ? 8 : (NMAX <= 64 ? 5 : 7);
-    static constexpr int kBStage = NMAX * 128;              // bytes of one B chunk (NMAX rows x 128 B)
     static constexpr bool kWide = NMAX >= 128;
-    static constexpr int kDq = kWide ? 16 : 4;              // dequant warps
-    static constexpr int kGroups = kDq / 4;                 // dequant groups (one TMEM lane set each)
-    static constexpr int kABufs = kGroups > 1 ? kGroups : (NMAX <= 16 ? 3 : 2);
+    // 16-token tiles stack the two e4m3 pieces as token rows [0, Nr) and
+    // [Nr, 2 Nr) of one MMA (half the MMA instructions); wider tiles issue
+    // one MMA per piece.
+    static constexpr bool kStack = NMAX <= 16;
+    static constexpr int kStages = NMAX <= 16 ? 6 : (NMAX <= 64 ? 5 : 7);
+    static constexpr int kBStage = (kStack ? 2 : 1) * NMAX * 128;   // bytes of one B chunk (rows x 128 B)
+    static constexpr int kDq = kWide ? 8 : 4;               // unpack warps
+    static constexpr int kGroups = kDq / 4;                 // unpack groups (one TMEM lane set each)
+    static constexpr int kABufs = kWide ? 4 : (NMAX <= 16 ? 3 : 2);   // TMEM A slots
     static constexpr int kEpi = kWide ? 4 : 0;              // dedicated epilogue warps
     static constexpr int kDBufs = kEpi ? 2 : 1;             // accumulators in TMEM
     // token rows per tensor-TMA box: few large boxes for wide tiles (the TMA
     // engine's cost is per box), 16-row boxes for the few tokens of decode
     static constexpr int kBoxRows = kWide ? 64 : 16;
     static constexpr int kBoxBytes = kBoxRows * 128;
-    static constexpr uint32_t kDCol = kABufs * 32;          // first D column (after the A buffers)
-    static constexpr uint32_t kColsUsed = kDCol + kDBufs * NMAX;
+    // Tensor memory columns.  Slot s owns the 32-column block at
+    // kBlk + 32 s: its A scale columns at +0 (quarter q reads +q), its A
+    // codes (64 bytes = 16 columns) at +16; blocks 0 and 1 also hold the B
+    // scale columns of e4m3 piece 0 and 1 at +8 (one per 32 B rows; stacked
+    // tiles use block 0's for both pieces).  The accumulators (kDW columns
+    // each) take their own range.
+    static constexpr int kDW = (kStack ? 2 : 1) * NMAX;
+    static constexpr int kNCol = (kDW + 31) / 32;
+    static constexpr uint32_t kBlk = kWide ? kDBufs * NMAX : 0;
+    static constexpr uint32_t kDCol = kWide ? 0 : 32 * kABufs;
+    static constexpr uint32_t kSfaCol = kBlk;
+    static constexpr uint32_t kACol = kBlk + 16;
+    static constexpr uint32_t kSfbCol = kBlk + 8;
+    static constexpr uint32_t kSfbStride = 32;              // piece 1 in the next block
+    static constexpr uint32_t kColsUsed = kWide ? kBlk + 32 * kABufs : kDCol + kDBufs * kDW;
     static constexpr uint32_t kCols = kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512);
     static_assert(kColsUsed <= 512, "tile does not fit in tensor memory");
+    static_assert(kABufs >= 2 && kNCol <= 8, "B scale columns");
+    static_assert(NMAX % 16 == 0 && kBlk % 32 == 0 && kDCol % 32 == 0, "column alignment");
+    static constexpr int kPerSm = NMAX <= 16 ? 4 : (NMAX <= 64 ? 3 : 1);   // resident CTAs per SM
     static constexpr int kProducer = kDq + kEpi;            // producer warp; the MMA warp follows
     static constexpr int kThreads = 32 * (kDq + kEpi + 2);
-    static constexpr int kBars = 2 * kStages + 2 * kABufs + 2 * kDBufs + 2 * kQ;
+    static constexpr int kBars = 2 * kStages + kABufs + 2 * kDBufs + 2 * kQ;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * (kBStage + kChunkBytes) + kBars * 8 + 16 + 4 * kQ;
 };
 
@@ -162,7 +177,9 @@ __device__ __forceinline__ void load_meta(const BankLists &L, const TcArgs &args
 // Drain NBLK column blocks of D (TMEM address dt = this warp's lane quarter,
 // first D column) into h rows (phase 1) or bf16 Y rows (phase 2).  All 16
 // columns of a block are computed together; only the stores are predicated.
-template <int PHASE, int NBLK>
+// STACK: column n + Nr holds the second e4m3 piece's product (16x scaled),
+// so the token's value is D[n] + 2^-4 D[n + Nr].
+template <int PHASE, int NBLK, bool STACK>
 __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, int blk0, int bstride, int nn, int g,
                                               int mt, int quarter, int lane, const int (&rs)[NBLK],
                                               const float (&rsc)[NBLK]) {
@@ -173,22 +190,34 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
     for (int i = 0; i < NBLK; ++i) {
         const int c0 = (blk0 + i * bstride) * 16;
         if (c0 >= Nr) break;   // warp-uniform
-        // contiguous column blocks are read 32 columns per TMEM load
-        const bool pair = bstride == 1 && (i & 1) == 0 && i + 1 < NBLK && c0 + 16 < Nr;
-        if ((i & 1) == 0 || bstride != 1) {
-            if (pair) {
-                ptx::tmem_ld32(dt + c0, vv);
-            } else {
-                uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&vv[0]);
-                ptx::tmem_ld16(dt + c0, lo);
-            }
-            ptx::tmem_wait_ld();
-        }
-        const uint32_t *v = vv + (bstride == 1 ? (i & 1) * 16 : 0);
         float d[16];
+        if (STACK) {
+            uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&vv[0]);
+            uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&vv[16]);
+            ptx::tmem_ld16(dt + c0, lo);
+            ptx::tmem_ld16(dt + Nr + c0, hi);
+            ptx::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 16; ++q)   // undo the row's power of two (exact)
-            d[q] = __fmul_rn(__uint_as_float(v[q]), __shfl_sync(0xffffffffu, rsc[i], q));
+            for (int q = 0; q < 16; ++q)   // pieces combined, then the row's power of two undone (exact)
+                d[q] = __fmul_rn(__fmaf_rn(__uint_as_float(hi[q]), 0.0625f, __uint_as_float(lo[q])),
+                                 __shfl_sync(0xffffffffu, rsc[i], q));
+        } else {
+            // contiguous column blocks are read 32 columns per TMEM load
+            const bool pair = bstride == 1 && (i & 1) == 0 && i + 1 < NBLK && c0 + 16 < Nr;
+            if ((i & 1) == 0 || bstride != 1) {
+                if (pair) {
+                    ptx::tmem_ld32(dt + c0, vv);
+                } else {
+                    uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&vv[0]);
+                    ptx::tmem_ld16(dt + c0, lo);
+                }
+                ptx::tmem_wait_ld();
+            }
+            const uint32_t *v = vv + (bstride == 1 ? (i & 1) * 16 : 0);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)   // undo the row's power of two (exact)
+                d[q] = __fmul_rn(__uint_as_float(v[q]), __shfl_sync(0xffffffffu, rsc[i], q));
+        }
         if (PHASE == 1) {
             float o[16];
 #pragma unroll
@@ -214,7 +243,7 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
 }
 
 template <int NMAX, int PHASE, bool COLD>
-__global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const __grid_constant__ CUtensorMap tmap,
+__global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ffn_tc_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                          TcArgs args) {
     using C = TcCfg<NMAX>;
     constexpr int DQ = C::kDq, NA = C::kABufs, DB = C::kDBufs, S = C::kStages, G = C::kGroups;
@@ -228,8 +257,10 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
     volatile int *abort_flag = (volatile int *)(holder + 1);
     volatile int *uq = (volatile int *)(holder + 2);   // [kQ] unit queue
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
-    const int FULL = 0, EMPTY = S, AREADY = 2 * S, AFREE = 2 * S + NA, ACCREADY = 2 * S + 2 * NA,
-              ACCFREE = ACCREADY + DB, UQFULL = ACCFREE + DB, UQEMPTY = UQFULL + kQ;
+    // FULL: stage landed.  DONE: the chunk's MMAs completed (its stage and
+    // its A slot are free again).  AREADY: A slot written.
+    const int FULL = 0, DONE = S, AREADY = 2 * S, ACCREADY = 2 * S + NA, ACCFREE = ACCREADY + DB,
+              UQFULL = ACCFREE + DB, UQEMPTY = UQFULL + kQ;
     constexpr int kEpiThreads = C::kEpi ? 32 * C::kEpi : 32 * DQ;   // threads that drain D
     constexpr int kQueueReaders = 32 * DQ + 32 * C::kEpi + 1;       // + the MMA thread
     constexpr int PROD = C::kProducer, MMAW = C::kProducer + 1;
@@ -239,16 +270,13 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(bar(FULL + s), COLD ? 33 : 1);
-            ptx::mbar_init(bar(EMPTY + s), 1);
+            ptx::mbar_init(bar(DONE + s), 1);
         }
         for (int q = 0; q < kQ; ++q) {
             ptx::mbar_init(bar(UQFULL + q), 1);
             ptx::mbar_init(bar(UQEMPTY + q), kQueueReaders);
         }
-        for (int i = 0; i < NA; ++i) {
-            ptx::mbar_init(bar(AREADY + i), 128);   // the four warps of the chunk's group
-            ptx::mbar_init(bar(AFREE + i), 1);
-        }
+        for (int i = 0; i < NA; ++i) ptx::mbar_init(bar(AREADY + i), 128);   // the four warps of the chunk's group
         for (int i = 0; i < DB; ++i) {
             ptx::mbar_init(bar(ACCREADY + i), 1);
             ptx::mbar_init(bar(ACCFREE + i), kEpiThreads);
@@ -265,6 +293,18 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *holder;
+    if (warp < 4) {
+        // B scale columns, constant, in every lane quarter (each quarter
+        // reads its own): 2^0; wide tiles scale the second piece by 2^-4
+        // here, stacked tiles in the epilogue
+        const uint32_t lb = (uint32_t)(warp * 32) << 16;
+#pragma unroll
+        for (int j = 0; j < C::kNCol; ++j) {
+            ptx::tmem_st1(tmem + lb + C::kSfbCol + j, 0x7F7F7F7Fu);
+            if (!C::kStack) ptx::tmem_st1(tmem + lb + C::kSfbCol + C::kSfbStride + j, 0x7B7B7B7Bu);
+        }
+        ptx::tmem_wait_st();   // made visible to the MMA by the first A-slot handoff
+    }
 
     const BankLists &L = args.lists;
     const int n_act = L.hdr[kHdrNAct + args.b];
@@ -287,7 +327,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
     };
 
     if (warp < DQ) {
-        // ------------------------------------------------ dequant (+ epilogue)
+        // ------------------------------------------------- unpack (+ epilogue)
         const int quarter = warp & 3, group = warp >> 2;
         const int m = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -310,25 +350,27 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                     if (!wait_warp<SUSP>(bar(FULL + st), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
                     const uint8_t *a_st = sA + st * kChunkBytes;
                     const int abuf = it % NA;
-                    const uint32_t ua = it / NA;
                     const uint4 q0 = *(const uint4 *)(a_st + m * 16);
                     const uint4 q1 = *(const uint4 *)(a_st + 2048 + m * 16);
                     const uint32_t sc = *(const uint16_t *)(a_st + kChunkQBytes + 2 * m);
-                    const uint32_t s0 = e8m0_f16x2(sc & 0xFFu), s1 = e8m0_f16x2(sc >> 8);
-                    uint32_t r[32];
-                    dequant_word(q0.x, s0, r + 0);
-                    dequant_word(q0.y, s0, r + 4);
-                    dequant_word(q0.z, s0, r + 8);
-                    dequant_word(q0.w, s0, r + 12);
-                    dequant_word(q1.x, s1, r + 16);
-                    dequant_word(q1.y, s1, r + 20);
-                    dequant_word(q1.z, s1, r + 24);
-                    dequant_word(q1.w, s1, r + 28);
-                    if (ua > 0 && !wait_warp<SUSP>(bar(AFREE + abuf), (ua - 1) & 1, abort_flag, args.status)) {
+                    uint32_t r[16];
+                    unpack_word(q0.x, r[0], r[1]);
+                    unpack_word(q0.y, r[2], r[3]);
+                    unpack_word(q0.z, r[4], r[5]);
+                    unpack_word(q0.w, r[6], r[7]);
+                    unpack_word(q1.x, r[8], r[9]);
+                    unpack_word(q1.y, r[10], r[11]);
+                    unpack_word(q1.z, r[12], r[13]);
+                    unpack_word(q1.w, r[14], r[15]);
+                    // the slot's previous chunk (it - NA) must have been consumed
+                    if (it >= (uint32_t)NA && !wait_warp<SUSP>(bar(DONE + (it - NA) % S), ((it - NA) / S) & 1,
+                                                               abort_flag, args.status)) {
                         ok = false;
                         break;
                     }
-                    ptx::tmem_st32(tmem + lane_base + abuf * 32, r);
+                    ptx::tmem_st16(tmem + lane_base + C::kACol + abuf * 32, r);
+                    // the chunk's two K blocks' scales in bytes 0 and 1 of this quarter's column
+                    ptx::tmem_st1(tmem + lane_base + C::kSfaCol + abuf * 32 + quarter, sc);
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(bar(AREADY + abuf));
@@ -337,8 +379,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                 if (C::kEpi == 0) {
                     if (!wait_warp<SUSP>(bar(ACCREADY), j & 1, abort_flag, args.status)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    epilogue_cols<PHASE, NB>(args, tmem + lane_base + C::kDCol, group, G, nn, goff + p0 + n0, mt,
-                                             quarter, lane, rs, re);
+                    epilogue_cols<PHASE, NB, C::kStack>(args, tmem + lane_base + C::kDCol, group, G, nn,
+                                                        goff + p0 + n0, mt, quarter, lane, rs, re);
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(bar(ACCFREE));
                 }
@@ -364,8 +406,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                 const int db = j % DB;
                 if (!wait_warp<SUSP>(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status)) { ok = false; break; }
                 ptx::tc_fence_after();
-                epilogue_cols<PHASE, NB>(args, tmem + lane_base + C::kDCol + db * NMAX, 0, 1, nn, goff + p0 + n0,
-                                         mt, quarter, lane, rs, re);
+                epilogue_cols<PHASE, NB, C::kStack>(args, tmem + lane_base + C::kDCol + db * C::kDW, 0, 1, nn,
+                                                    goff + p0 + n0, mt, quarter, lane, rs, re);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(ACCFREE + db));
             }
@@ -403,7 +445,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                 for (int c = 0; c < kc; ++c, ++it) {
                     const int st = it % S;
                     const uint32_t rnd = it / S;
-                    if (rnd > 0 && !wait_warp<SUSP>(bar(EMPTY + st), (rnd - 1) & 1, abort_flag, args.status)) {
+                    if (rnd > 0 && !wait_warp<SUSP>(bar(DONE + st), (rnd - 1) & 1, abort_flag, args.status)) {
                         ok = false;
                         break;
                     }
@@ -415,11 +457,19 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                         ptx::cp_async_arrive_noinc(bar(FULL + st));
                     }
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(bar(FULL + st), (COLD ? 0u : (uint32_t)kChunkBytes) + nbox * C::kBoxBytes);
+                        ptx::mbar_arrive_expect_tx(bar(FULL + st), (COLD ? 0u : (uint32_t)kChunkBytes) +
+                                                                       (C::kStack ? 2 : 1) * nbox * C::kBoxBytes);
                         if (!COLD) ptx::bulk_g2s(a_addr, src_chunk, kChunkBytes, bar(FULL + st));
                         for (int q = 0; q < nbox; ++q)
-                            ptx::tma_load_2d(b_addr + q * C::kBoxBytes, &tmap, c * kKC, brow + q * C::kBoxRows,
+                            ptx::tma_load_2d(b_addr + q * C::kBoxBytes, &tmap, c * 128, brow + q * C::kBoxRows,
                                              bar(FULL + st));
+                        // stacked: the same rows again, 64 bytes further, so the
+                        // second piece starts each row (rows nbox*16 ...; the last
+                        // chunk's box reads past the row end: zero fill, unused)
+                        if (C::kStack)
+                            for (int q = 0; q < nbox; ++q)
+                                ptx::tma_load_2d(b_addr + (nbox + q) * C::kBoxBytes, &tmap, c * 128 + 64,
+                                                 brow + q * C::kBoxRows, bar(FULL + st));
                     }
                     __syncwarp();
                 }
@@ -445,7 +495,9 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
                 const int Nr = (nn + 15) & ~15;
-                const uint32_t idesc = ptx::idesc_f16_f32(128, Nr);
+                const int Nm = C::kStack ? 2 * Nr : Nr;                              // B rows of one MMA
+                const uint32_t idesc0 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 0, 0);   // K block 0 of the chunk
+                const uint32_t idesc1 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 1, 0);   // K block 1
                 const int db = j % DB;
                 if (j >= (uint32_t)DB &&
                     !wait_one<SUSP>(bar(ACCFREE + db), ((j / DB) - 1) & 1, abort_flag, args.status)) {
@@ -453,19 +505,24 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem + C::kDCol + db * NMAX;
+                const uint32_t d_tmem = tmem + C::kDCol + db * C::kDW;
                 for (int c = 0; c < kc; ++c, ++it) {
                     const int st = it % S, abuf = it % NA;
                     if (!wait_one<SUSP>(bar(AREADY + abuf), (it / NA) & 1, abort_flag, args.status)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage);
+                    const uint32_t a_tm = tmem + C::kACol + abuf * 32;
+                    const uint32_t sfa = tmem + C::kSfaCol + abuf * 32;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 32);
-                        ptx::mma_f16_ts(d_tmem, tmem + abuf * 32 + kk * 8, bd, idesc, (c | kk) != 0);
+                    for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+                        for (int pc = 0; pc < (C::kStack ? 1 : 2); ++pc) {   // e4m3 piece of B (wide tiles)
+                            const uint64_t bd = ptx::smem_desc_sw128(b_addr + pc * 64 + kk * 32);
+                            ptx::mma_mxf8f6f4_ts(d_tmem, a_tm + kk * 8, bd, kk ? idesc1 : idesc0, sfa,
+                                                 tmem + C::kSfbCol + pc * C::kSfbStride, (c | kk | pc) != 0);
+                        }
                     }
-                    ptx::mma_commit(bar(EMPTY + st));
-                    ptx::mma_commit(bar(AFREE + abuf));
+                    ptx::mma_commit(bar(DONE + st));
                 }
                 if (!ok) break;
                 ptx::mma_commit(bar(ACCREADY + db));
@@ -475,7 +532,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
             // wait until the MMAs already issued have retired (bounded)
             const uint32_t last = it - 1;
             for (uint32_t t = 0; t < kWaitLimit; ++t)
-                if (ptx::mbar_try_wait(bar(AFREE + (last % NA)), (last / NA) & 1)) break;
+                if (ptx::mbar_try_wait(bar(DONE + (last % S)), (last / S) & 1)) break;
         }
     }
 
@@ -487,10 +544,57 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1) ffn_tc_kernel(const 
     }
 }
 
-// Gather this bank's token rows in pick order, each scaled by a power of two
-// into f16 (largest |x| -> [2^13, 2^14)): row g = offset + p of xg.
+// Exponent e of a row whose largest |value| is mx: mx * 2^-e lies in
+// (224, 448], the top binade of e4m3 (largest finite 448 = 0.875 * 2^9).
+__device__ __forceinline__ int row_exponent(float mx) {
+    if (!(mx > 0.0f)) return 0;
+    int ex = 0;
+    const float f = frexpf(mx, &ex);   // mx = f * 2^ex, f in [0.5, 1)
+    return ex - 9 + (f > 0.875f ? 1 : 0);
+}
+
+// Eight scaled values -> the two e4m3 pieces (8 bytes each, value i in byte
+// i): q1 = e4m3(v), q2 = e4m3(16 (v - q1)); v - q1 is exact in fp32.
+__device__ __forceinline__ void split_e4m3x8(const float (&v)[8], uint2 &q1, uint2 &q2) {
+    uint32_t a[4], r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(v[2 * i], v[2 * i + 1]), __NV_SATFINITE,
+                                                               __NV_E4M3);
+        const float2 back = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3)));
+        const __nv_fp8x2_storage_t l = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fmul_rn(__fsub_rn(v[2 * i], back.x), 16.0f), __fmul_rn(__fsub_rn(v[2 * i + 1], back.y), 16.0f)),
+            __NV_SATFINITE, __NV_E4M3);
+        a[i] = h;
+        r[i] = l;
+    }
+    q1 = make_uint2(a[0] | (a[1] << 16), a[2] | (a[3] << 16));
+    q2 = make_uint2(r[0] | (r[1] << 16), r[2] | (r[3] << 16));
+}
+
+// Store values 8i..8i+7 of a row (K element 8i = chunk i/8, byte 8*(i%8)) as
+// the two pieces of that chunk's 128-byte record.
+__device__ __forceinline__ void store_pieces(uint8_t *row, int i, const float (&v)[8]) {
+    uint2 q1, q2;
+    split_e4m3x8(v, q1, q2);
+    uint8_t *rec = row + (i >> 3) * 128 + (i & 7) * 8;
+    *(uint2 *)rec = q1;
+    *(uint2 *)(rec + 64) = q2;
+}
+
+__device__ __forceinline__ float block_max(float mx, float *red) {
+    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = red[0];
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) mx = fmaxf(mx, red[i]);
+    return mx;
+}
+
+// Gather this bank's token rows in pick order (row g = offset + p of xq) as
+// two e4m3 pieces per 64-wide chunk, each row scaled by 2^-e (e in xgexp).
 __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict__ x, int H, int k, BankLists L,
-                                                     int b, int P, __half *__restrict__ xg,
+                                                     int b, int P, uint8_t *__restrict__ xq,
                                                      int32_t *__restrict__ xgexp, int32_t *sched) {
     __shared__ float red[8];
     const int p = blockIdx.x;
@@ -509,61 +613,46 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict_
         for (int q = 0; q < 4; ++q)
             mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
     }
-    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-    __syncthreads();
-    mx = red[0];
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) mx = fmaxf(mx, red[i]);
-    int e = 0;
-    frexpf(mx, &e);
-    const int c = mx > 0.0f ? e - 14 : 0;
-    uint4 *dst = (uint4 *)(xg + (int64_t)g * H);
+    const int e = row_exponent(block_max(mx, red));
+    uint8_t *dst = xq + (int64_t)g * H * 2;
     for (int i = threadIdx.x; i < n8; i += blockDim.x) {
         const uint4 v = row[i];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
+        float f[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            __half2 h = __floats2half2_rn(ldexpf(__uint_as_float(w[q] << 16), -c),
-                                          ldexpf(__uint_as_float(w[q] & 0xFFFF0000u), -c));
-            o[q] = *reinterpret_cast<uint32_t *>(&h);
+            f[2 * q] = ldexpf(__uint_as_float(w[q] << 16), -e);
+            f[2 * q + 1] = ldexpf(__uint_as_float(w[q] & 0xFFFF0000u), -e);
         }
-        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        store_pieces(dst, i, f);
     }
-    if (threadIdx.x == 0) xgexp[g] = c;
+    if (threadIdx.x == 0) xgexp[g] = e;
 }
 
-// Scale this bank's gate/up rows h (fp32, row g) into f16 the same way.
+// The same for this bank's gate/up rows h (fp32, row g).
 __global__ void __launch_bounds__(256) prep_h_kernel(BankLists L, int b, int P, int I,
-                                                     const float *__restrict__ h32, __half *__restrict__ h16,
+                                                     const float *__restrict__ h32, uint8_t *__restrict__ hq,
                                                      int32_t *__restrict__ hexp) {
     __shared__ float red[8];
     const int p = blockIdx.x;
     if (p >= L.hdr[kHdrNPicks + b]) return;
     const int g = bank_offset(L, b, P) + p;
     const float4 *row = (const float4 *)(h32 + (int64_t)g * I);
-    const int n4 = I / 4;
+    const int n8 = I / 8;
     float mx = 0.0f;
-    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    for (int i = threadIdx.x; i < 2 * n8; i += blockDim.x) {
         const float4 v = row[i];
         mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
-    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-    __syncthreads();
-    mx = red[0];
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) mx = fmaxf(mx, red[i]);
-    int e = 0;
-    frexpf(mx, &e);
-    const int c = mx > 0.0f ? e - 14 : 0;
-    uint2 *dst = (uint2 *)(h16 + (int64_t)g * I);
-    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-        const float4 v = row[i];
-        __half2 a = __floats2half2_rn(ldexpf(v.x, -c), ldexpf(v.y, -c));
-        __half2 bb = __floats2half2_rn(ldexpf(v.z, -c), ldexpf(v.w, -c));
-        dst[i] = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&bb));
+    const int e = row_exponent(block_max(mx, red));
+    uint8_t *dst = hq + (int64_t)g * I * 2;
+    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+        const float4 a = row[2 * i], c = row[2 * i + 1];
+        const float f[8] = {ldexpf(a.x, -e), ldexpf(a.y, -e), ldexpf(a.z, -e), ldexpf(a.w, -e),
+                            ldexpf(c.x, -e), ldexpf(c.y, -e), ldexpf(c.z, -e), ldexpf(c.w, -e)};
+        store_pieces(dst, i, f);
     }
-    if (threadIdx.x == 0) hexp[g] = c;
+    if (threadIdx.x == 0) hexp[g] = e;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -579,16 +668,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Tensor map over a [rows][K] f16 array: boxes of box_rows rows x 64
-// elements, 128-byte swizzle, zero fill past the last row.
+// Tensor map over the [rows][K/64][128 B] piece records of K-element rows:
+// boxes of box_rows rows x one 128-byte record, 128-byte swizzle, zero fill
+// past the last row.
 int make_row_map(CUtensorMap *map, const void *base, int K, int rows, int box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled unavailable");
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t dims[2] = {(cuuint64_t)K * 2, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kKC, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
@@ -612,7 +702,7 @@ int launch_one(const CUtensorMap &map, const TcArgs &args, int blocks, cudaStrea
 // launch leaves room on every SM for those, so both banks run concurrently.
 template <int NMAX>
 int grid_for(const moe_ctx *ctx, bool cold, bool shared, int units_max) {
-    const int per_sm = NMAX <= 16 ? 4 : (NMAX <= 64 ? 3 : 1);   // shared memory and TMEM both fit
+    const int per_sm = TcCfg<NMAX>::kPerSm;   // shared memory, registers and TMEM all fit
     const int cold_ctas = NMAX <= 64 ? 64 : 32;
     int blocks;
     if (cold) blocks = cold_ctas;
@@ -628,15 +718,15 @@ int launch_bank(moe_ctx *ctx, bool cold, bool shared, const TcArgs &a1, const Tc
     const Geom &g = ctx->g;
     const int P = a1.P;
     CUtensorMap m1, m2;
-    if (int r = make_row_map(&m1, ws + lay.xg16, g.H, P, TcCfg<NMAX>::kBoxRows)) return r;
-    if (int r = make_row_map(&m2, ws + lay.h16, g.I, P, TcCfg<NMAX>::kBoxRows)) return r;
-    prep_x_kernel<<<P, 256, 0, s>>>(x, g.H, g.k, a1.lists, a1.b, P, (__half *)(ws + lay.xg16),
+    if (int r = make_row_map(&m1, ws + lay.xq, g.H, P, TcCfg<NMAX>::kBoxRows)) return r;
+    if (int r = make_row_map(&m2, ws + lay.hq, g.I, P, TcCfg<NMAX>::kBoxRows)) return r;
+    prep_x_kernel<<<P, 256, 0, s>>>(x, g.H, g.k, a1.lists, a1.b, P, ws + lay.xq,
                                     (int32_t *)(ws + lay.xgexp), a1.sched);
     MOE_LAUNCH_CHECK();
     const int b1 = grid_for<NMAX>(ctx, cold, shared, units1), b2 = grid_for<NMAX>(ctx, cold, shared, units2);
     int r = cold ? launch_one<NMAX, 1, true>(m1, a1, b1, s) : launch_one<NMAX, 1, false>(m1, a1, b1, s);
     if (r) return r;
-    prep_h_kernel<<<P, 256, 0, s>>>(a1.lists, a1.b, P, g.I, (const float *)(ws + lay.h32), (__half *)(ws + lay.h16),
+    prep_h_kernel<<<P, 256, 0, s>>>(a1.lists, a1.b, P, g.I, (const float *)(ws + lay.h32), ws + lay.hq,
                                     (int32_t *)(ws + lay.hexp));
     MOE_LAUNCH_CHECK();
     return cold ? launch_one<NMAX, 2, true>(m2, a2, b2, s) : launch_one<NMAX, 2, false>(m2, a2, b2, s);

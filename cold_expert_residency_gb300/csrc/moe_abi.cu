@@ -42,6 +42,15 @@ static void parallel_for(int n, F f) {
     for (auto &th : pool) th.join();
 }
 
+// One MX block's 16 logical bytes (element 2i in the low nibble of byte i)
+// -> the device order of moe_internal.cuh (word j, byte i: elements 8j+i and
+// 8j+4+i).
+static void reorder_block(const uint8_t *q, uint8_t *o) {
+    auto code = [&](int e) { return (q[e >> 1] >> (4 * (e & 1))) & 0xF; };
+    for (int j = 0; j < 4; ++j)
+        for (int i = 0; i < 4; ++i) o[4 * j + i] = (uint8_t)(code(8 * j + i) | (code(8 * j + 4 + i) << 4));
+}
+
 // Logical MXFP4 expert -> tiled device layout (see moe_internal.cuh).
 // Returns false if a scale byte lies outside [104, 140].
 static bool repack_expert(const Geom &g, const uint8_t *w13_q, const uint8_t *w13_s,
@@ -55,8 +64,8 @@ static bool repack_expert(const Geom &g, const uint8_t *w13_q, const uint8_t *w1
                 int w = m / 32, l = m % 32;
                 int64_t row = (l < 16 ? 0 : I) + 64 * mt + 16 * w + (l % 16);
                 const uint8_t *q = w13_q + row * (H / 2) + c * 32;
-                std::memcpy(chunk + m * 16, q, 16);
-                std::memcpy(chunk + 2048 + m * 16, q + 16, 16);
+                reorder_block(q, chunk + m * 16);
+                reorder_block(q + 16, chunk + 2048 + m * 16);
                 const uint8_t *s = w13_s + row * (H / 32) + 2 * c;
                 chunk[kChunkQBytes + 2 * m] = s[0];
                 chunk[kChunkQBytes + 2 * m + 1] = s[1];
@@ -70,8 +79,8 @@ static bool repack_expert(const Geom &g, const uint8_t *w13_q, const uint8_t *w1
             for (int m = 0; m < kMT; ++m) {
                 int64_t row = (int64_t)kMT * mt + m;
                 const uint8_t *q = w2_q + row * (I / 2) + c * 32;
-                std::memcpy(chunk + m * 16, q, 16);
-                std::memcpy(chunk + 2048 + m * 16, q + 16, 16);
+                reorder_block(q, chunk + m * 16);
+                reorder_block(q + 16, chunk + 2048 + m * 16);
                 const uint8_t *s = w2_s + row * (I / 32) + 2 * c;
                 chunk[kChunkQBytes + 2 * m] = s[0];
                 chunk[kChunkQBytes + 2 * m + 1] = s[1];

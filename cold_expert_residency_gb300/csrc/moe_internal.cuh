@@ -25,6 +25,10 @@ namespace moe {
 //                                                  16 B, i.e. one MX block)
 //     [row m][2 scale bytes]                      (256 B: the row's two e8m0
 //                                                  scales of this chunk)
+// Inside a half, 32-bit word j (bytes 4j..4j+3) holds the block's elements
+// 8j..8j+7: byte i carries element 8j+i in its low nibble and element
+// 8j+4+i in its high nibble.  Two masked shifts of the word then give the
+// one-code-per-byte form the tensor cores read from tensor memory.
 // = 4352 bytes, exactly the logical bytes of those 128 x 64 elements.  Chunks
 // of a tile follow in K order, tiles in M order; the W13 tiles come first,
 // then the W2 tiles.  So the bank stores the same bytes the logical layout
@@ -70,7 +74,7 @@ inline Geom make_geom(const moe_geom &g) {
 // pick's index in its bank's list), so the two banks never share a row and
 // each expert's rows are contiguous.
 struct WsLayout {
-    size_t hdr, act_row, act_off, picks, epos, ecnt, xg16, xgexp, h32, h16, hexp, total;
+    size_t hdr, act_row, act_off, picks, epos, ecnt, xq, xgexp, h32, hq, hexp, total;
 };
 // header words
 // kHdrSched + 2*bank + phase: work counters of the FFN kernels' dynamic
@@ -90,10 +94,10 @@ inline WsLayout ws_layout(const Geom &g, int T) {
     w.picks = take(2 * P * 4);                // [2][P]
     w.epos = take((size_t)g.E * 4);           // [E] start of expert e's picks in its bank list
     w.ecnt = take((size_t)g.E * 4);           // [E] picks per expert (large-step routing path)
-    w.xg16 = take(P * (size_t)g.H * 2);       // [P][H] f16 token rows in pick order, per-row scaled
+    w.xq = take(P * (size_t)g.H * 2);         // [P][H/64][2][64] e4m3 token rows in pick order (two pieces)
     w.xgexp = take(P * 4);                    // [P] int32 scale exponents of those rows
     w.h32 = take(P * (size_t)g.I * 4);        // [P][I] fp32 gate/up output (by g; by slot on CUDA cores)
-    w.h16 = take(P * (size_t)g.I * 2);        // [P][I] f16, per-row scaled, by g
+    w.hq = take(P * (size_t)g.I * 2);         // [P][I/64][2][64] e4m3 h rows (two pieces), by g
     w.hexp = take(P * 4);                     // [P] int32
     w.total = off;
     return w;

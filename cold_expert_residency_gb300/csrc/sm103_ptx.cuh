@@ -135,6 +135,10 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
+// Warp-collective: lane i stores one 32-bit column of its TMEM lane.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Warp-collective: lane i loads 16 consecutive 32-bit columns of its TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -166,6 +170,25 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D[tmem] (+)= (A . SFA)[tmem] * (B . SFB)[smem desc]^T, kind::mxf8f6f4 with
+// one e8m0 scale per 32 K elements (scale_vec::1X), issued by one thread.
+// Tensor-memory operand forms on this target:
+//   A (e2m1)  row m = lane m; K element k in byte k of the row's columns
+//             (4 per column), the code in bits 5..2 of its byte.
+//   SFA       row m: lane m, column sfa + m/32, byte = the descriptor's
+//             A scale id.
+//   SFB       token n: column sfb + n/32, lane 32q + n%32 of every lane
+//             quarter q (the rows of quarter q read their own quarter),
+//             byte = the descriptor's B scale id.
+__device__ __forceinline__ void mma_mxf8f6f4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n}" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
 // Arrive on `bar` once all prior tcgen05 async ops of this thread complete.
@@ -208,6 +231,19 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
            | (0u << 7) | (0u << 10)        // A, B format: f16
            | ((uint32_t)(N >> 3) << 17)    // N / 8
            | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor for kind::mxf8f6f4 block_scale: e2m1 A, e4m3 B,
+// both K-major, f32 accumulator, e8m0 scales, M x N, with the byte of the
+// scale columns each operand reads.
+__host__ __device__ constexpr uint32_t idesc_mx_e2m1_e4m3(int M, int N, int sfa_id, int sfb_id) {
+    return ((uint32_t)sfb_id << 4)         // B scale byte
+           | (5u << 7)                     // A format: e2m1
+           | (0u << 10)                    // B format: e4m3
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | (1u << 23)                    // scale format: e8m0
+           | ((uint32_t)(M >> 4) << 24)    // M / 16
+           | ((uint32_t)sfa_id << 29);     // A scale byte
 }
 
 }  // namespace ptx
