@@ -17,10 +17,11 @@
 //       itself; the epilogue undoes the row's power of two.
 //
 // Warp roles:
-//   producer    Weights: hot bank -> one 1-D bulk async copy (TMA) of each
-//               4352-byte (M-tile, K-chunk) block; cold bank -> 16-byte
-//               cp.async reads of the mapped host bank (the host-link
-//               streaming path).  Token rows: 2-D tensor TMA boxes of 128
+//   producer    Weights: one 1-D bulk async copy (TMA) of each 4352-byte
+//               (M-tile, K-chunk) block, from HBM for the hot bank and from
+//               the mapped pinned host bank for the cold bank (the
+//               host-link streaming path: the copy engine of the SM reads
+//               the host memory in place).  Token rows: 2-D tensor TMA boxes of 128
 //               bytes (the chunk's two e4m3 pieces) per row with 128-byte
 //               swizzle from the pick-ordered row array.  All into a
 //               shared-memory ring, completion on one mbarrier per stage.
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(bar(FULL + s), COLD ? 33 : 1);
+            ptx::mbar_init(bar(FULL + s), 1);
             ptx::mbar_init(bar(DONE + s), 1);
         }
         for (int q = 0; q < kQ; ++q) {
@@ -452,14 +453,12 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                     const uint32_t a_addr = ptx::smem_addr(sA + st * kChunkBytes);
                     const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage);
                     const uint8_t *src_chunk = tile + (int64_t)c * kChunkBytes;
-                    if (COLD) {
-                        for (int i = lane; i < kChunkBytes / 16; i += 32) ptx::cp_async16(a_addr + i * 16, src_chunk + i * 16);
-                        ptx::cp_async_arrive_noinc(bar(FULL + st));
-                    }
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(bar(FULL + st), (COLD ? 0u : (uint32_t)kChunkBytes) +
-                                                                       (C::kStack ? 2 : 1) * nbox * C::kBoxBytes);
-                        if (!COLD) ptx::bulk_g2s(a_addr, src_chunk, kChunkBytes, bar(FULL + st));
+                        ptx::mbar_arrive_expect_tx(bar(FULL + st),
+                                                   (uint32_t)kChunkBytes + (C::kStack ? 2 : 1) * nbox * C::kBoxBytes);
+                        // one bulk copy per weight chunk, from HBM or, for the cold
+                        // bank, from the mapped host bank over the host link
+                        ptx::bulk_g2s(a_addr, src_chunk, kChunkBytes, bar(FULL + st));
                         for (int q = 0; q < nbox; ++q)
                             ptx::tma_load_2d(b_addr + q * C::kBoxBytes, &tmap, c * 128, brow + q * C::kBoxRows,
                                              bar(FULL + st));
@@ -697,13 +696,15 @@ int launch_one(const CUtensorMap &map, const TcArgs &args, int blocks, cudaStrea
 }
 
 // Grid of one GEMM launch.  Units are handed out dynamically, so the grid
-// only sets how many CTAs stream at once.  A cold-bank launch needs few CTAs
-// to keep the host link busy; when the layer also has a hot bank, the hot
-// launch leaves room on every SM for those, so both banks run concurrently.
+// only sets how many CTAs stream at once.  The host link needs a few MB in
+// flight, so a cold-bank launch of narrow tiles takes one CTA per SM; when
+// the layer also has a hot bank, the hot launch takes the SM's other slots,
+// so both banks run concurrently and every SM holds exactly kPerSm CTAs
+// whichever launch is placed first.
 template <int NMAX>
 int grid_for(const moe_ctx *ctx, bool cold, bool shared, int units_max) {
     const int per_sm = TcCfg<NMAX>::kPerSm;   // shared memory, registers and TMEM all fit
-    const int cold_ctas = NMAX <= 64 ? 64 : 32;
+    const int cold_ctas = per_sm > 1 ? ctx->sms : 32;
     int blocks;
     if (cold) blocks = cold_ctas;
     else if (!shared) blocks = ctx->sms * per_sm;
