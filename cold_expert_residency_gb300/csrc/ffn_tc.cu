@@ -69,6 +69,8 @@ struct TcArgs {
     const int32_t *bexp;    // [P] scale exponent of B row g
     float *h_out;           // phase 1 output [P][I] by g
     uint16_t *Y;            // phase 2 output [T*k][H] by slot
+    float *gu_out;          // split units, phase 1: [P][2I] gate/up sums by g (fp32, atomically added)
+    float *y_out;           // split units, phase 2: [T*k][H] sums by slot (fp32, atomically added)
     int32_t *status;
     int32_t *sched;         // work counter of this launch (zeroed before it)
 };
@@ -113,6 +115,18 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo, uint32_t &
     hi = (w >> 2) & 0x3C3C3C3Cu;
 }
 
+// Unit u -> active row a, M-tile mt and its K-chunk range [c0, c1) (one of
+// ks equal K parts).
+__device__ __forceinline__ void unit_pos(int u, int mt_count, int kc, int ks, int &a, int &mt, int &c0, int &c1) {
+    const int per = mt_count * ks;
+    a = u / per;
+    const int r = u - a * per;
+    mt = r / ks;
+    const int h = r - mt * ks;
+    c0 = h * kc / ks;
+    c1 = (h + 1) * kc / ks;
+}
+
 __device__ __forceinline__ int bank_offset(const BankLists &L, int b, int P) {
     return b == 0 ? 0 : P - L.hdr[kHdrNPicks + 1];
 }
@@ -155,6 +169,11 @@ struct TcCfg {
     static_assert(kABufs >= 2 && kNCol <= 8, "B scale columns");
     static_assert(NMAX % 16 == 0 && kBlk % 32 == 0 && kDCol % 32 == 0, "column alignment");
     static constexpr int kPerSm = NMAX <= 16 ? 4 : (NMAX <= 64 ? 3 : 1);   // resident CTAs per SM
+    // Narrow tiles split each (expert, M-tile) unit into two K halves: a
+    // decode step has only a few units per CTA, and halving them halves the
+    // tail of the launch.  Two partial sums added onto zero in either order
+    // give the same fp32 result, so the split stays deterministic.
+    static constexpr int kSplit = kWide ? 1 : 2;
     static constexpr int kProducer = kDq + kEpi;            // producer warp; the MMA warp follows
     static constexpr int kThreads = 32 * (kDq + kEpi + 2);
     static constexpr int kBars = 2 * kStages + kABufs + 2 * kDBufs + 2 * kQ;
@@ -180,7 +199,7 @@ __device__ __forceinline__ void load_meta(const BankLists &L, const TcArgs &args
 // columns of a block are computed together; only the stores are predicated.
 // STACK: column n + Nr holds the second e4m3 piece's product (16x scaled),
 // so the token's value is D[n] + 2^-4 D[n + Nr].
-template <int PHASE, int NBLK, bool STACK>
+template <int PHASE, int NBLK, bool STACK, int KS>
 __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, int blk0, int bstride, int nn, int g,
                                               int mt, int quarter, int lane, const int (&rs)[NBLK],
                                               const float (&rsc)[NBLK]) {
@@ -219,7 +238,24 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
             for (int q = 0; q < 16; ++q)   // undo the row's power of two (exact)
                 d[q] = __fmul_rn(__uint_as_float(v[q]), __shfl_sync(0xffffffffu, rsc[i], q));
         }
-        if (PHASE == 1) {
+        if (KS > 1) {
+            // partial sums of one K half: added into fp32 rows; SwiGLU and the
+            // bf16 rounding follow once both halves are in
+            if (PHASE == 1) {
+                // tile row m = W13 row (lane < 16 ? gate : up) of unit 64 mt + 16 quarter + lane % 16
+                float *dst = args.gu_out + (int64_t)(g + c0) * (2 * args.I) + (lane < 16 ? 0 : args.I) + 64 * mt +
+                             16 * quarter + (lane & 15);
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    if (c0 + q < nn) atomicAdd(dst + (int64_t)q * (2 * args.I), d[q]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int slot = __shfl_sync(0xffffffffu, rs[i], q);
+                    if (c0 + q < nn) atomicAdd(&args.y_out[(int64_t)slot * args.H + kMT * mt + m], d[q]);
+                }
+            }
+        } else if (PHASE == 1) {
             float o[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q) o[q] = __shfl_xor_sync(0xffffffffu, d[q], 16);
@@ -309,7 +345,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
 
     const BankLists &L = args.lists;
     const int n_act = L.hdr[kHdrNAct + args.b];
-    const int units = n_act * args.mt_count;
+    const int units = n_act * args.mt_count * C::kSplit;
     const int kc = args.kc;
     const int goff = bank_offset(L, args.b, args.P);
 
@@ -338,14 +374,15 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         for (uint32_t ui = 0; ok; ++ui) {
             const int u = take_unit(ui, true, ok);
             if (u < 0) break;
-            const int a = u / args.mt_count, mt = u % args.mt_count;
+            int a, mt, c0, c1;
+            unit_pos(u, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
                 int rs[NB];
                 float re[NB];
                 if (C::kEpi == 0) load_meta<NB>(L, args, group, G, nn, p0 + n0, goff + p0 + n0, lane, rs, re);
-                for (int c = 0; c < kc; ++c, ++it) {
+                for (int c = c0; c < c1; ++c, ++it) {
                     if (G > 1 && (int)(it % G) != group) continue;   // another group's chunk
                     const int st = it % S;
                     if (!wait_warp<SUSP>(bar(FULL + st), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
@@ -380,7 +417,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                 if (C::kEpi == 0) {
                     if (!wait_warp<SUSP>(bar(ACCREADY), j & 1, abort_flag, args.status)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    epilogue_cols<PHASE, NB, C::kStack>(args, tmem + lane_base + C::kDCol, group, G, nn,
+                    epilogue_cols<PHASE, NB, C::kStack, C::kSplit>(args, tmem + lane_base + C::kDCol, group, G, nn,
                                                         goff + p0 + n0, mt, quarter, lane, rs, re);
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(bar(ACCFREE));
@@ -397,7 +434,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         for (uint32_t ui = 0; ok; ++ui) {
             const int u = take_unit(ui, true, ok);
             if (u < 0) break;
-            const int a = u / args.mt_count, mt = u % args.mt_count;
+            int a, mt, c0, c1;
+            unit_pos(u, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
@@ -407,7 +445,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                 const int db = j % DB;
                 if (!wait_warp<SUSP>(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status)) { ok = false; break; }
                 ptx::tc_fence_after();
-                epilogue_cols<PHASE, NB, C::kStack>(args, tmem + lane_base + C::kDCol + db * C::kDW, 0, 1, nn,
+                epilogue_cols<PHASE, NB, C::kStack, C::kSplit>(args, tmem + lane_base + C::kDCol + db * C::kDW, 0, 1, nn,
                                                     goff + p0 + n0, mt, quarter, lane, rs, re);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(ACCFREE + db));
@@ -434,7 +472,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
             }
             u = __shfl_sync(0xffffffffu, u, 0);
             if (u < 0) break;
-            const int a = u / args.mt_count, mt = u % args.mt_count;
+            int a, mt, c0, c1;
+            unit_pos(u, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
             const int row = L.act_row[a];
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
             const uint8_t *tile = args.bank + (int64_t)row * args.eb + args.part_off +
@@ -443,7 +482,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                 const int nn = min(NMAX, n - n0);
                 const int nbox = (nn + C::kBoxRows - 1) / C::kBoxRows;
                 const int brow = goff + p0 + n0;
-                for (int c = 0; c < kc; ++c, ++it) {
+                for (int c = c0; c < c1; ++c, ++it) {
                     const int st = it % S;
                     const uint32_t rnd = it / S;
                     if (rnd > 0 && !wait_warp<SUSP>(bar(DONE + st), (rnd - 1) & 1, abort_flag, args.status)) {
@@ -489,7 +528,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         for (uint32_t ui = 0; ok; ++ui) {
             const int u = take_unit(ui, false, ok);
             if (u < 0) break;
-            const int a = u / args.mt_count;
+            int a, mt, c0, c1;
+            unit_pos(u, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
             const int n = L.act_off[a + 1] - L.act_off[a];
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
@@ -505,7 +545,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + C::kDCol + db * C::kDW;
-                for (int c = 0; c < kc; ++c, ++it) {
+                for (int c = c0; c < c1; ++c, ++it) {
                     const int st = it % S, abuf = it % NA;
                     if (!wait_one<SUSP>(bar(AREADY + abuf), (it / NA) & 1, abort_flag, args.status)) { ok = false; break; }
                     ptx::tc_fence_after();
@@ -518,7 +558,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                         for (int pc = 0; pc < (C::kStack ? 1 : 2); ++pc) {   // e4m3 piece of B (wide tiles)
                             const uint64_t bd = ptx::smem_desc_sw128(b_addr + pc * 64 + kk * 32);
                             ptx::mma_mxf8f6f4_ts(d_tmem, a_tm + kk * 8, bd, kk ? idesc1 : idesc0, sfa,
-                                                 tmem + C::kSfbCol + pc * C::kSfbStride, (c | kk | pc) != 0);
+                                                 tmem + C::kSfbCol + pc * C::kSfbStride, (c != c0) | kk | pc);
                         }
                     }
                     ptx::mma_commit(bar(DONE + st));
@@ -594,7 +634,8 @@ __device__ __forceinline__ float block_max(float mx, float *red) {
 // two e4m3 pieces per 64-wide chunk, each row scaled by 2^-e (e in xgexp).
 __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict__ x, int H, int k, BankLists L,
                                                      int b, int P, uint8_t *__restrict__ xq,
-                                                     int32_t *__restrict__ xgexp, int32_t *sched) {
+                                                     int32_t *__restrict__ xgexp, int32_t *sched,
+                                                     float *__restrict__ gu32, int I) {
     __shared__ float red[8];
     const int p = blockIdx.x;
     // reset the work counters of this bank's two GEMM launches (stream-ordered before them)
@@ -626,32 +667,79 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict_
         store_pieces(dst, i, f);
     }
     if (threadIdx.x == 0) xgexp[g] = e;
+    if (gu32) {   // split units: clear this pick's gate/up sums before the gate/up GEMM adds into them
+        float4 *z = (float4 *)(gu32 + (int64_t)g * 2 * I);
+        for (int i = threadIdx.x; i < I / 2; i += blockDim.x) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 }
 
-// The same for this bank's gate/up rows h (fp32, row g).
+// silu(gate) * up, silu(z) = z / (1 + e^-z)
+__device__ __forceinline__ float swiglu(float gate, float up) {
+    return __fmul_rn(__fdividef(gate, 1.0f + __expf(-gate)), up);
+}
+
+// Values 8i..8i+7 of row g of h: read from h32, or (split units) formed from
+// the row's gate/up sums.
+__device__ __forceinline__ void h_values(const float *h32, const float *gu32, int64_t g, int I, int i, float (&f)[8]) {
+    if (gu32) {
+        const float4 *gr = (const float4 *)(gu32 + g * 2 * I) + 2 * i, *ur = (const float4 *)(gu32 + g * 2 * I + I) + 2 * i;
+        const float4 g0 = gr[0], g1 = gr[1], u0 = ur[0], u1 = ur[1];
+        f[0] = swiglu(g0.x, u0.x); f[1] = swiglu(g0.y, u0.y); f[2] = swiglu(g0.z, u0.z); f[3] = swiglu(g0.w, u0.w);
+        f[4] = swiglu(g1.x, u1.x); f[5] = swiglu(g1.y, u1.y); f[6] = swiglu(g1.z, u1.z); f[7] = swiglu(g1.w, u1.w);
+    } else {
+        const float4 *row = (const float4 *)(h32 + g * I) + 2 * i;
+        const float4 a = row[0], c = row[1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = c.x; f[5] = c.y; f[6] = c.z; f[7] = c.w;
+    }
+}
+
+// The same for this bank's gate/up rows h (row g).  Split units: h is formed
+// here from the gate/up sums, and the pick's down-GEMM sum row is cleared.
 __global__ void __launch_bounds__(256) prep_h_kernel(BankLists L, int b, int P, int I,
-                                                     const float *__restrict__ h32, uint8_t *__restrict__ hq,
-                                                     int32_t *__restrict__ hexp) {
+                                                     const float *__restrict__ h32, const float *__restrict__ gu32,
+                                                     uint8_t *__restrict__ hq, int32_t *__restrict__ hexp,
+                                                     float *__restrict__ y32, int H) {
     __shared__ float red[8];
     const int p = blockIdx.x;
     if (p >= L.hdr[kHdrNPicks + b]) return;
     const int g = bank_offset(L, b, P) + p;
-    const float4 *row = (const float4 *)(h32 + (int64_t)g * I);
     const int n8 = I / 8;
     float mx = 0.0f;
-    for (int i = threadIdx.x; i < 2 * n8; i += blockDim.x) {
-        const float4 v = row[i];
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+        float f[8];
+        h_values(h32, gu32, g, I, i, f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(f[q]));
     }
     const int e = row_exponent(block_max(mx, red));
     uint8_t *dst = hq + (int64_t)g * I * 2;
     for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-        const float4 a = row[2 * i], c = row[2 * i + 1];
-        const float f[8] = {ldexpf(a.x, -e), ldexpf(a.y, -e), ldexpf(a.z, -e), ldexpf(a.w, -e),
-                            ldexpf(c.x, -e), ldexpf(c.y, -e), ldexpf(c.z, -e), ldexpf(c.w, -e)};
+        float f[8];
+        h_values(h32, gu32, g, I, i, f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) f[q] = ldexpf(f[q], -e);
         store_pieces(dst, i, f);
     }
     if (threadIdx.x == 0) hexp[g] = e;
+    if (y32) {
+        float4 *z = (float4 *)(y32 + (int64_t)L.picks[p] * H);
+        for (int i = threadIdx.x; i < H / 4; i += blockDim.x) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// Split units: this bank's down-GEMM sums (fp32, by slot) -> the bf16 rows of Y.
+__global__ void __launch_bounds__(256) round_y_kernel(BankLists L, int b, int H, const float *__restrict__ y32,
+                                                      uint16_t *__restrict__ Y) {
+    const int p = blockIdx.x;
+    if (p >= L.hdr[kHdrNPicks + b]) return;
+    const int64_t slot = L.picks[p];
+    const float4 *src = (const float4 *)(y32 + slot * H);
+    uint2 *dst = (uint2 *)(Y + slot * H);
+    for (int i = threadIdx.x; i < H / 4; i += blockDim.x) {
+        const float4 v = src[i];
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+        dst[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -722,15 +810,19 @@ int launch_bank(moe_ctx *ctx, bool cold, bool shared, const TcArgs &a1, const Tc
     if (int r = make_row_map(&m1, ws + lay.xq, g.H, P, TcCfg<NMAX>::kBoxRows)) return r;
     if (int r = make_row_map(&m2, ws + lay.hq, g.I, P, TcCfg<NMAX>::kBoxRows)) return r;
     prep_x_kernel<<<P, 256, 0, s>>>(x, g.H, g.k, a1.lists, a1.b, P, ws + lay.xq,
-                                    (int32_t *)(ws + lay.xgexp), a1.sched);
+                                    (int32_t *)(ws + lay.xgexp), a1.sched, a1.gu_out, g.I);
     MOE_LAUNCH_CHECK();
     const int b1 = grid_for<NMAX>(ctx, cold, shared, units1), b2 = grid_for<NMAX>(ctx, cold, shared, units2);
     int r = cold ? launch_one<NMAX, 1, true>(m1, a1, b1, s) : launch_one<NMAX, 1, false>(m1, a1, b1, s);
     if (r) return r;
-    prep_h_kernel<<<P, 256, 0, s>>>(a1.lists, a1.b, P, g.I, (const float *)(ws + lay.h32), ws + lay.hq,
-                                    (int32_t *)(ws + lay.hexp));
+    prep_h_kernel<<<P, 256, 0, s>>>(a1.lists, a1.b, P, g.I, (const float *)(ws + lay.h32), a1.gu_out, ws + lay.hq,
+                                    (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
     MOE_LAUNCH_CHECK();
-    return cold ? launch_one<NMAX, 2, true>(m2, a2, b2, s) : launch_one<NMAX, 2, false>(m2, a2, b2, s);
+    r = cold ? launch_one<NMAX, 2, true>(m2, a2, b2, s) : launch_one<NMAX, 2, false>(m2, a2, b2, s);
+    if (r || !a2.y_out) return r;
+    round_y_kernel<<<P, 256, 0, s>>>(a2.lists, a2.b, g.H, a2.y_out, a2.Y);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
 }
 
 }  // namespace
@@ -770,16 +862,22 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, i
     a2.bexp = (const int32_t *)(ws + lay.hexp);
     a2.h_out = nullptr;
     a2.Y = Y;
+    // narrow-tile steps: two K halves per unit, summed in fp32 rows
+    const bool split = split_k_steps(T);
+    a1.gu_out = split ? (float *)(ws + lay.gu32) : nullptr;
+    a1.y_out = nullptr;
+    a2.gu_out = nullptr;
+    a2.y_out = split ? (float *)(ws + lay.y32) : nullptr;
 
     const bool cold = b == MOE_BANK_COLD;
-    const int units1 = P * g.mt13, units2 = P * g.mt2;   // active rows never exceed the picks
+    const int units1 = 2 * P * g.mt13, units2 = 2 * P * g.mt2;   // active rows never exceed the picks
     // The token-tile width depends only on T, so an expert's arithmetic is
     // the same in either bank.  Decode-sized steps use narrow tiles with
     // several CTAs per SM (an expert with more tokens than the tile loops over
     // token tiles); prefill-sized steps use 192-wide tiles (an expert's
     // ~T*k/E tokens in one tile), one CTA per SM.
     if (T <= 16) return launch_bank<16>(ctx, cold, shared, a1, a2, units1, units2, x, lay, ws, s);
-    if (T <= 256) return launch_bank<64>(ctx, cold, shared, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= kNarrowMaxT) return launch_bank<64>(ctx, cold, shared, a1, a2, units1, units2, x, lay, ws, s);
     return launch_bank<192>(ctx, cold, shared, a1, a2, units1, units2, x, lay, ws, s);
 }
 

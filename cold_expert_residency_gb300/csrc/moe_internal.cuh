@@ -74,7 +74,7 @@ inline Geom make_geom(const moe_geom &g) {
 // pick's index in its bank's list), so the two banks never share a row and
 // each expert's rows are contiguous.
 struct WsLayout {
-    size_t hdr, act_row, act_off, picks, epos, ecnt, xq, xgexp, h32, hq, hexp, total;
+    size_t hdr, act_row, act_off, picks, epos, ecnt, xq, xgexp, h32, hq, hexp, gu32, y32, total;
 };
 // header words
 // kHdrSched + 2*bank + phase: work counters of the FFN kernels' dynamic
@@ -82,6 +82,11 @@ struct WsLayout {
 enum { kHdrNPicks = 0, kHdrNAct = 2, kHdrSched = 8, kHdrWords = 64 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Steps of at most this many tokens run the FFN with narrow token tiles and
+// two K halves per unit.
+constexpr int kNarrowMaxT = 256;
+inline bool split_k_steps(int T) { return T <= kNarrowMaxT; }
 
 inline WsLayout ws_layout(const Geom &g, int T) {
     WsLayout w;
@@ -99,6 +104,11 @@ inline WsLayout ws_layout(const Geom &g, int T) {
     w.h32 = take(P * (size_t)g.I * 4);        // [P][I] fp32 gate/up output (by g; by slot on CUDA cores)
     w.hq = take(P * (size_t)g.I * 2);         // [P][I/64][2][64] e4m3 h rows (two pieces), by g
     w.hexp = take(P * 4);                     // [P] int32
+    // Narrow-tile steps split each GEMM unit into two K halves whose partial
+    // sums meet in these fp32 rows (see the tensor-core FFN).
+    const size_t ks = split_k_steps(T) ? 1 : 0;
+    w.gu32 = take(ks * P * (size_t)g.I * 2 * 4); // [P][2I] gate/up sums before SwiGLU, by g
+    w.y32 = take(ks * P * (size_t)g.H * 4);     // [P][H] down-GEMM sums, by slot
     w.total = off;
     return w;
 }
