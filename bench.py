@@ -445,7 +445,9 @@ def main():
         tf = flops / (hot_avg_ms * 1e-3) / 1e12
         roofline.update({"bound": "tensor", "achieved": tf, "peak": tf_burst, "unit": "TFLOP/s",
                          "frac": tf / tf_burst, "flops_per_launch": flops,
-                         "peak_source": f"{peak_src} bf16 dense burst (f16 operands run at the same rate)",
+                         # rows carry bf16-class precision as two e4m3 pieces: two fp8-rate
+                         # MMAs per product, i.e. the tensor pipe's bf16 rate
+                         "peak_source": f"{peak_src} bf16 dense burst (two e4m3 pieces per row at the fp8 rate)",
                          "hbm_gbs_achieved": hot_gbs})
     # bytes roofline of the step (the metric's definition)
     t_roof = [(a * eb) / (hbm_peak * 1e9) + (c * eb) / (link_gbs * 1e9) for a, c in zip(dh, dc)]
@@ -472,7 +474,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "e2m1 weights, f16 tensor-core operands, f32 accumulate, bf16 rows",
+            "vs_baseline": None, "dtype": "e2m1 weights (e8m0 scales) x e4m3 rows (two pieces), block-scaled tensor cores, f32 accumulate, bf16 rows",
             "data": "synthetic (seeded SplitMix64; Zipf-skewed routing)",
             "config": {"workload": WORKLOADS[args.config] + (
                            f" [profiling variant: {cfg.E} experts, {cfg.n_hot} hot, {cfg.T} tokens]"

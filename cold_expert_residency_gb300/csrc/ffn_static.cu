@@ -1,7 +1,8 @@
 // Allocation-free variant of the expert-FFN entry point.
 //
-// moe_expert_ffn_bank keeps its intermediate rows (scaled token rows, the
-// gate/up output and its f16 copy, the scheduler counters) in a workspace the
+// moe_expert_ffn_bank keeps its intermediate rows (the token rows as e4m3
+// pieces, the gate/up output and its pieces, fp32 partial-sum rows of
+// decode-sized steps, the scheduler counters) in a workspace the
 // caller allocates.  Some callers cannot allocate device memory at all: a
 // plugin handed a fixed memory budget by its host framework, or a serving
 // loop that must not call cudaMalloc because the call can synchronize the

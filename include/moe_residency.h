@@ -150,7 +150,8 @@ int moe_expert_ffn_bank(moe_ctx *ctx, int layer, int bank, const uint16_t *x, in
  *   step (only its pick lists are read).  x, T, Y as moe_expert_ffn_bank; Y
  *   receives the same rows moe_expert_ffn_bank would write.
  * Returns MOE_EINVAL if the step's scratch would exceed the area (about
- * T*k*(2H + 6I) bytes).  The first call on a device looks up the area's
+ * T*k*(6H + 14I) bytes, fp32 partial-sum rows included: at H=4096, I=2880,
+ * k=6 steps of up to 43 tokens fit).  The first call on a device looks up the area's
  * device address; make that first call before any stream capture.  Every
  * call shares the one area and leaves its contents behind: calls whose work
  * overlaps on the GPU race, so run the two banks' calls one after the other
