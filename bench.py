@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--config", default="decode1", choices=sorted(WORKLOADS))
     ap.add_argument("--pool", type=int, default=32, help="distinct input batches cycled through")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--banks", default="streams", choices=["streams", "fused"],
+                    help="the two banks' FFN calls on two streams at once, or one call over both banks")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of CPU-oracle work")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling-size variant: this many experts per layer (same expert geometry)")
@@ -104,6 +106,13 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def wait_first(self, timeout=10.0):
+        """Wait until nvidia-smi has produced a sample: its start-up takes driver
+        locks that would otherwise stall the timed launches."""
+        t0 = time.time()
+        while self.proc and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
 
     def __exit__(self, *a):
         if self.proc:
@@ -276,16 +285,19 @@ def main():
             st = steps[l]
             b = st.buf
             moe.moe_route_split_count(ctx, l, b.logits, T, count_on, b.ids, b.w, b.ws_ptr, main)
-            st.ev_routed.record(main)
-            st.cold_stream.wait_event(st.ev_routed)
-            moe.moe_expert_ffn_bank(ctx, l, moe.MOE_BANK_COLD, b.x, T, b.ws_ptr, b.Y, st.cold_stream)
-            st.ev_cold.record(st.cold_stream)
             if timed_hot and l == 0:
                 ev_hot[0].record(main)
-            moe.moe_expert_ffn_bank(ctx, l, moe.MOE_BANK_HOT, b.x, T, b.ws_ptr, b.Y, main)
+            if args.banks == "fused":   # both banks' FFN, one launch per GEMM
+                moe.moe_expert_ffn_bank(ctx, l, moe.MOE_BANK_BOTH, b.x, T, b.ws_ptr, b.Y, main)
+            else:                       # the two banks' calls on two streams at once
+                st.ev_routed.record(main)
+                st.cold_stream.wait_event(st.ev_routed)
+                moe.moe_expert_ffn_bank(ctx, l, moe.MOE_BANK_COLD, b.x, T, b.ws_ptr, b.Y, st.cold_stream)
+                st.ev_cold.record(st.cold_stream)
+                moe.moe_expert_ffn_bank(ctx, l, moe.MOE_BANK_HOT, b.x, T, b.ws_ptr, b.Y, main)
+                main.wait_event(st.ev_cold)
             if timed_hot and l == 0:
                 ev_hot[1].record(main)
-            main.wait_event(st.ev_cold)
             moe.moe_finalize(b.Y, b.w, T, k, H, b.out, main)
 
     def load_inputs(i, stream):
@@ -325,6 +337,15 @@ def main():
 
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    # steady state: every pooled input batch once, untimed, so each expert a
+    # timed step routes to has been read before (the first read of a weight
+    # page sets up its address translation and runs far slower); every timed
+    # step still computes everything, after an L2 flush
+    for i in range(npool):
+        load_inputs(i, main)
+        with torch.cuda.stream(main):
+            run_step()
+    main.synchronize()
     for i in range(args.warmup):
         load_inputs(i, main)
         with torch.cuda.stream(main):
@@ -338,31 +359,38 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    ev_steps = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        clk.wait_first()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        # every timed step is enqueued back to back and the host synchronizes
+        # once, so a host-side stall cannot open a gap inside a step's events
         for i in range(args.steps):
             j = args.warmup + i
             load_inputs(j, main)
             with torch.cuda.stream(main):
                 flush.zero_()
-                ev0.record(main)
+                ev_steps[i][0].record(main)
                 run_step()
-                ev1.record(main)
-            main.synchronize()
-            step_ms.append(ev0.elapsed_time(ev1))
-            if hot_timing in ("in-graph events", "eager events"):
-                hot_ms.append(ev_hot[0].elapsed_time(ev_hot[1]))
-            nh = nc = 0
-            for l in range(L):
-                lg = pool_lg[j % npool][l]
-                ids = np.argsort(-lg, axis=1, kind="stable")[:, :k]
-                a, c = distinct_experts(ids, masks[l])
-                nh += a
-                nc += c
-                if l == 0:
-                    hot_bytes.append(a * eb)
-                    hot_picks.append(int((masks[l][ids] == 1).sum()))
-            dh.append(nh)
-            dc.append(nc)
+                ev_steps[i][1].record(main)
+        main.synchronize()
+    for i in range(args.steps):
+        j = args.warmup + i
+        step_ms.append(ev_steps[i][0].elapsed_time(ev_steps[i][1]))
+        nh = nc = 0
+        for l in range(L):
+            lg = pool_lg[j % npool][l]
+            ids = np.argsort(-lg, axis=1, kind="stable")[:, :k]
+            a, c = distinct_experts(ids, masks[l])
+            nh += a
+            nc += c
+            if l == 0:
+                hot_bytes.append(a * eb)
+                hot_picks.append(int((masks[l][ids] == 1).sum()))
+        dh.append(nh)
+        dc.append(nc)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -372,7 +400,16 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
 
-    if not hot_ms:   # eager timing of the hot-bank FFN
+    # the step's FFN call (layer 0), one step at a time
+    if hot_timing in ("in-graph events", "eager events"):
+        for i in range(min(args.steps, 20)):
+            load_inputs(args.warmup + i, main)
+            with torch.cuda.stream(main):
+                flush.zero_()
+                run_step()
+            main.synchronize()
+            hot_ms.append(ev_hot[0].elapsed_time(ev_hot[1]))
+    if not hot_ms:   # eager timing of the FFN call
         for i in range(min(args.steps, 20)):
             load_inputs(i, main)
             with torch.cuda.stream(main):
@@ -380,6 +417,46 @@ def main():
                 enqueue(timed_hot=True)
             main.synchronize()
             hot_ms.append(ev_hot[0].elapsed_time(ev_hot[1]))
+    ffn_ms = hot_ms   # layer 0's FFN call over both banks, inside the step
+
+    def ffn_alone(bank):
+        """One FFN call over `bank` of layer 0 after routing, graph-replayed with
+        events around the call (in the graph when possible); returns the
+        times (ms) and the inputs' distinct hot-expert bytes."""
+        st = steps[0]
+        b = st.buf
+        ea = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] if in_graph_events else ev_hot
+        g2 = None
+        if use_graph and in_graph_events:
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2, stream=main):
+                moe.moe_route_split_count(ctx, 0, b.logits, T, count_on, b.ids, b.w, b.ws_ptr, main)
+                ea[0].record(main)
+                moe.moe_expert_ffn_bank(ctx, 0, bank, b.x, T, b.ws_ptr, b.Y, main)
+                ea[1].record(main)
+        ts, by = [], []
+        for i in range(min(args.steps, 20)):
+            load_inputs(i, main)
+            with torch.cuda.stream(main):
+                flush.zero_()
+                if g2 is not None:
+                    g2.replay()
+                else:
+                    moe.moe_route_split_count(ctx, 0, b.logits, T, count_on, b.ids, b.w, b.ws_ptr, main)
+                    ea[0].record(main)
+                    moe.moe_expert_ffn_bank(ctx, 0, bank, b.x, T, b.ws_ptr, b.Y, main)
+                    ea[1].record(main)
+            main.synchronize()
+            ts.append(ea[0].elapsed_time(ea[1]))
+            ids = np.argsort(-pool_lg[i % npool][0], axis=1, kind="stable")[:, :k]
+            by.append(distinct_experts(ids, masks[0])[0] * eb)
+        return ts, by
+
+    # the roofline's kernel: the hot-bank FFN call on its own (inside the step
+    # it shares its launches with the cold bank)
+    hot_ms, hot_bytes_alone = ffn_alone(moe.MOE_BANK_HOT)
+    hot_timing = ("in-graph events" if (use_graph and in_graph_events) else "eager events") + \
+        ", hot-bank call alone after routing"
 
     # e2e: host inputs -> device -> step -> host output, all inside the events
     e2e_ms = []
@@ -424,19 +501,21 @@ def main():
                 ts.append(ev0.elapsed_time(ev1) * 1e3)
             return float(np.mean(ts))
         r_us = part(False, False)
-        breakdown = {"route_us": r_us, "hot_alone_us": part(True, False) - r_us,
-                     "cold_alone_us": part(False, True) - r_us, "note": "layer 0, each bank alone after routing"}
+        breakdown = {"route_us": r_us, "hot_alone_us": float(np.mean(hot_ms)) * 1e3,
+                     "cold_alone_us": float(np.mean(ffn_alone(moe.MOE_BANK_COLD)[0])) * 1e3,
+                     "ffn_in_step_us": float(np.mean(ffn_ms)) * 1e3, "banks": args.banks,
+                     "note": "layer 0: each bank's FFN call alone after routing, and the step's both-bank FFN call"}
 
     ms = total_ms / args.steps
     tokens_per_step = T   # one layer-step of T tokens (all layers of the config)
     value = world * tokens_per_step * args.steps / (total_ms * 1e-3)
     hot_avg_ms = float(np.mean(hot_ms))
-    hot_gbs = float(np.mean(hot_bytes)) / (hot_avg_ms * 1e-3) / 1e9
+    hot_gbs = float(np.mean(hot_bytes_alone)) / (hot_avg_ms * 1e-3) / 1e9
     roofline = {"kernel": "hot-bank expert FFN (moe_expert_ffn_bank, layer 0)", "bound": "hbm",
                 "achieved": hot_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": hot_gbs / hbm_peak,
                 "peak_source": f"{peak_src} (burst copy)",
                 # ncu DRAM bytes per hot expert (profiles/traffic.json) x this run's mean hot experts
-                "traffic": (profiled_traffic(args.config) * float(np.mean(hot_bytes)) / eb
+                "traffic": (profiled_traffic(args.config) * float(np.mean(hot_bytes_alone)) / eb
                             if profiled_traffic(args.config) else None),
                 "timing": hot_timing, "us_per_launch": hot_avg_ms * 1e3}
     if T > 256:
@@ -481,6 +560,7 @@ def main():
                            if (args.experts or args.tokens) else ""),
                        "layers": L, "tokens_per_step": T,
                        "l2": "flushed (512 MiB write) before every timed step", "cuda_graph": graph is not None,
+                       "ffn_calls": "one call over both banks" if args.banks == "fused" else "hot and cold bank calls on two streams",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "us_per_layer_step": ms * 1e3 / L,
             "bytes_roofline": {"frac_sum": frac, "frac_max": frac_max,

@@ -19,7 +19,7 @@ import numpy as np
 from ._build import LIB as _LIB_PATH, build  # noqa: F401
 
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTALE, MOE_ETIMEOUT, MOE_ESTATE = 0, -1, -2, -3, -4, -5, -6
-MOE_BANK_HOT, MOE_BANK_COLD = 0, 1
+MOE_BANK_HOT, MOE_BANK_COLD, MOE_BANK_BOTH = 0, 1, 2
 MOE_FFN_TCGEN05, MOE_FFN_SIMT = 0, 1
 
 _lib = None

@@ -59,7 +59,8 @@ int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t
     if (!ctx) return set_error(MOE_EINVAL, "null context");
     if (layer < 0 || layer >= ctx->g.L) return set_error(MOE_EINVAL, "layer out of range");
     if (!ctx->layers[layer].init) return set_error(MOE_ESTATE, "layer has no banks (call moe_init_banks first)");
-    if (bank != MOE_BANK_HOT && bank != MOE_BANK_COLD) return set_error(MOE_EINVAL, "bank must be 0 or 1");
+    if (bank != MOE_BANK_HOT && bank != MOE_BANK_COLD && bank != MOE_BANK_BOTH)
+        return set_error(MOE_EINVAL, "bank must be 0, 1 or 2");
     if (T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "T out of range");
     if (!split_ws || (uintptr_t)split_ws % 256) return set_error(MOE_EINVAL, "split workspace must be non-null and 256-byte aligned");
     if (T > 0 && (!x || !Y)) return set_error(MOE_EINVAL, "null pointer");
@@ -69,8 +70,8 @@ int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t
         return set_error(MOE_EINVAL, "step needs " + std::to_string(lay.total) + " bytes of FFN scratch; the static area holds " +
                                          std::to_string(kStaticScratchBytes));
     Layer &L = ctx->layers[layer];
-    const uint8_t *base = bank == MOE_BANK_HOT ? L.hot : L.cold_dev;
-    const int rows = bank == MOE_BANK_HOT ? L.n_hot : L.n_cold;
+    if (bank == MOE_BANK_BOTH && (L.n_hot == 0 || L.n_cold == 0)) bank = L.n_hot ? MOE_BANK_HOT : MOE_BANK_COLD;
+    const int rows = bank == MOE_BANK_HOT ? L.n_hot : (bank == MOE_BANK_COLD ? L.n_cold : L.n_hot + L.n_cold);
     if (T == 0 || rows == 0) return MOE_OK;
 
     int prev = -1;
@@ -85,8 +86,13 @@ int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t
         if (e != cudaSuccess) r = cuda_error(e, "copy pick lists into the static scratch");
     }
     if (!r) {
-        if (ctx->ffn_impl == MOE_FFN_SIMT) r = launch_ffn_simt(ctx, base, bank, x, T, scratch, Y, s);
-        else r = launch_ffn_tc(ctx, base, bank, x, T, scratch, Y, s, L.n_hot > 0 && L.n_cold > 0);
+        if (ctx->ffn_impl == MOE_FFN_SIMT) {
+            for (int bk = 0; bk < 2 && !r; ++bk)
+                if (bank == MOE_BANK_BOTH || bank == bk)
+                    r = launch_ffn_simt(ctx, bk == MOE_BANK_HOT ? L.hot : L.cold_dev, bk, x, T, scratch, Y, s);
+        } else {
+            r = launch_ffn_tc(ctx, L.hot, L.cold_dev, bank, x, T, scratch, Y, s, L.n_hot > 0 && L.n_cold > 0);
+        }
     }
     if (prev >= 0 && prev != ctx->device) cudaSetDevice(prev);
     return r;

@@ -61,18 +61,20 @@ constexpr uint32_t kWaitLimit = 1u << 22;        // polls of the teardown drains
 constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s bound of a pipeline wait
 
 struct TcArgs {
-    const uint8_t *bank;
+    const uint8_t *bank[2];  // device-visible base of the hot (HBM) and cold (mapped host) bank
     int64_t eb, part_off;
     int mt_count, kc;
-    BankLists lists;
-    int b, k, H, I, P;
+    BankLists lists[2];      // both banks' split lists
+    int b;                   // the bank this launch covers, or -1: both banks in one launch
+    int k, H, I, P;
     const int32_t *bexp;    // [P] scale exponent of B row g
     float *h_out;           // phase 1 output [P][I] by g
     uint16_t *Y;            // phase 2 output [T*k][H] by slot
     float *gu_out;          // split units, phase 1: [P][2I] gate/up sums by g (fp32, atomically added)
     float *y_out;           // split units, phase 2: [T*k][H] sums by slot (fp32, atomically added)
     int32_t *status;
-    int32_t *sched;         // work counter of this launch (zeroed before it)
+    int32_t *sched;         // [2 banks][2 phases] work counters (zeroed before the launch)
+    int32_t *claim;         // both banks: [SM] first-CTA claims (zeroed before the launch)
 };
 
 constexpr int kQ = 4;       // unit queue depth (producer -> the other roles)
@@ -279,7 +281,9 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
     }
 }
 
-template <int NMAX, int PHASE, bool COLD>
+// BANKS names the launch (0 hot bank, 1 cold bank, 2 both banks); the code
+// is the same, every unit carries its bank.
+template <int NMAX, int PHASE, int BANKS>
 __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ffn_tc_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                          TcArgs args) {
     using C = TcCfg<NMAX>;
@@ -304,6 +308,19 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
     constexpr bool SUSP = !C::kWide;   // suspend-hinted waits for the decode tiles
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (BANKS == 1) {
+        // A cold-bank launch keeps one host-link streamer per SM: a CTA placed
+        // on an SM that already holds one leaves at once (two streamers on one
+        // SM slow the hot-bank CTAs beside them).
+        __shared__ int extra;
+        if (tid == 0) {
+            uint32_t smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            extra = atomicAdd(&args.claim[smid & 1023u], 1) > 0;
+        }
+        __syncthreads();
+        if (extra) return;
+    }
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(bar(FULL + s), 1);
@@ -343,13 +360,11 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         ptx::tmem_wait_st();   // made visible to the MMA by the first A-slot handoff
     }
 
-    const BankLists &L = args.lists;
-    const int n_act = L.hdr[kHdrNAct + args.b];
-    const int units = n_act * args.mt_count * C::kSplit;
     const int kc = args.kc;
-    const int goff = bank_offset(L, args.b, args.P);
+    auto units_of = [&](int bk) { return args.lists[0].hdr[kHdrNAct + bk] * args.mt_count * C::kSplit; };
 
-    // every role but the producer reads the unit sequence from the queue
+    // every role but the producer reads the unit sequence from the queue:
+    // entry 2u + bank (unit u of that bank), or -1 at the end
     auto take_unit = [&](uint32_t ui, bool warp_wide, bool &ok) -> int {
         const int qs = ui % kQ;
         const bool w = warp_wide ? wait_warp<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status)
@@ -372,10 +387,13 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         uint32_t it = 0, j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
-            const int u = take_unit(ui, true, ok);
-            if (u < 0) break;
+            const int e = take_unit(ui, true, ok);
+            if (e < 0) break;
+            const int bk = e & 1;
+            const BankLists &L = args.lists[bk];
+            const int goff = bank_offset(L, bk, args.P);
             int a, mt, c0, c1;
-            unit_pos(u, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
+            unit_pos(e >> 1, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
@@ -432,10 +450,13 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         uint32_t j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
-            const int u = take_unit(ui, true, ok);
-            if (u < 0) break;
+            const int e = take_unit(ui, true, ok);
+            if (e < 0) break;
+            const int bk = e & 1;
+            const BankLists &L = args.lists[bk];
+            const int goff = bank_offset(L, bk, args.P);
             int a, mt, c0, c1;
-            unit_pos(u, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
+            unit_pos(e >> 1, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
@@ -453,6 +474,20 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         }
     } else if (warp == PROD) {
         // ------------------------------------------------------------ producer
+        // A launch over both banks prefers, in the first CTA that reaches each
+        // SM, the cold bank's units (one host-link streamer per SM) and in the
+        // others the hot bank's; each turns to the other bank's queue once
+        // its own is empty.
+        int pref = args.b;
+        if (args.b < 0) {
+            if (lane == 0) {
+                uint32_t smid;
+                asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+                pref = atomicAdd(&args.claim[smid & 1023u], 1) == 0 ? MOE_BANK_COLD : MOE_BANK_HOT;
+            }
+            pref = __shfl_sync(0xffffffffu, pref, 0);
+        }
+        bool dry_pref = false, dry_other = args.b >= 0;   // lane 0's view of the queues
         uint32_t it = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
@@ -463,20 +498,31 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                 ok = false;
                 break;
             }
-            int u = 0;
+            int e = -1;
             if (lane == 0) {
-                u = atomicAdd(args.sched, 1);
-                if (u >= units) u = -1;
-                uq[qs] = u;
+                if (!dry_pref) {
+                    const int u = atomicAdd(&args.sched[2 * pref + PHASE - 1], 1);
+                    if (u < units_of(pref)) e = 2 * u + pref;
+                    else dry_pref = true;
+                }
+                if (e < 0 && !dry_other) {
+                    const int u = atomicAdd(&args.sched[2 * (1 - pref) + PHASE - 1], 1);
+                    if (u < units_of(1 - pref)) e = 2 * u + (1 - pref);
+                    else dry_other = true;
+                }
+                uq[qs] = e;
                 ptx::mbar_arrive(bar(UQFULL + qs));
             }
-            u = __shfl_sync(0xffffffffu, u, 0);
-            if (u < 0) break;
+            e = __shfl_sync(0xffffffffu, e, 0);
+            if (e < 0) break;
+            const int bk = e & 1;
+            const BankLists &L = args.lists[bk];
+            const int goff = bank_offset(L, bk, args.P);
             int a, mt, c0, c1;
-            unit_pos(u, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
+            unit_pos(e >> 1, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
             const int row = L.act_row[a];
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
-            const uint8_t *tile = args.bank + (int64_t)row * args.eb + args.part_off +
+            const uint8_t *tile = args.bank[bk] + (int64_t)row * args.eb + args.part_off +
                                   (int64_t)mt * kc * kChunkBytes;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX) {
                 const int nn = min(NMAX, n - n0);
@@ -526,10 +572,11 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         uint32_t it = 0, j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
-            const int u = take_unit(ui, false, ok);
-            if (u < 0) break;
+            const int e = take_unit(ui, false, ok);
+            if (e < 0) break;
+            const BankLists &L = args.lists[e & 1];
             int a, mt, c0, c1;
-            unit_pos(u, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
+            unit_pos(e >> 1, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
             const int n = L.act_off[a + 1] - L.act_off[a];
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
@@ -630,16 +677,23 @@ __device__ __forceinline__ float block_max(float mx, float *red) {
     return mx;
 }
 
-// Gather this bank's token rows in pick order (row g = offset + p of xq) as
+// Gather the bank's token rows in pick order (row g = offset + p of xq) as
 // two e4m3 pieces per 64-wide chunk, each row scaled by 2^-e (e in xgexp).
-__global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict__ x, int H, int k, BankLists L,
-                                                     int b, int P, uint8_t *__restrict__ xq,
-                                                     int32_t *__restrict__ xgexp, int32_t *sched,
+// b0 >= 0: that bank; b0 < 0: both banks, bank = blockIdx.y.
+__global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict__ x, int H, int k, BankLists L0,
+                                                     BankLists L1, int b0, int P, uint8_t *__restrict__ xq,
+                                                     int32_t *__restrict__ xgexp, int32_t *sched, int32_t *claim,
                                                      float *__restrict__ gu32, int I) {
     __shared__ float red[8];
-    const int p = blockIdx.x;
-    // reset the work counters of this bank's two GEMM launches (stream-ordered before them)
-    if (p == 0 && threadIdx.x < 2) sched[threadIdx.x] = 0;
+    const int p = blockIdx.x, b = b0 >= 0 ? b0 : (int)blockIdx.y;
+    const BankLists &L = b ? L1 : L0;
+    if (p == 0 && blockIdx.y == 0) {
+        // reset the work counters (and SM claims) of this call's GEMM launches,
+        // stream-ordered before them; a one-bank call leaves the other bank's alone
+        if (threadIdx.x < 4 && (b0 < 0 || (int)threadIdx.x / 2 == b0)) sched[threadIdx.x] = 0;
+        if (claim)
+            for (int i = threadIdx.x; i < 1024; i += blockDim.x) claim[i] = 0;
+    }
     if (p >= L.hdr[kHdrNPicks + b]) return;
     const int g = bank_offset(L, b, P) + p;
     const int t = L.picks[p] / k;
@@ -695,12 +749,15 @@ __device__ __forceinline__ void h_values(const float *h32, const float *gu32, in
 
 // The same for this bank's gate/up rows h (row g).  Split units: h is formed
 // here from the gate/up sums, and the pick's down-GEMM sum row is cleared.
-__global__ void __launch_bounds__(256) prep_h_kernel(BankLists L, int b, int P, int I,
+__global__ void __launch_bounds__(256) prep_h_kernel(BankLists L0, BankLists L1, int b0, int P, int I,
                                                      const float *__restrict__ h32, const float *__restrict__ gu32,
                                                      uint8_t *__restrict__ hq, int32_t *__restrict__ hexp,
-                                                     float *__restrict__ y32, int H) {
+                                                     float *__restrict__ y32, int H, int32_t *claim) {
     __shared__ float red[8];
-    const int p = blockIdx.x;
+    const int p = blockIdx.x, b = b0 >= 0 ? b0 : (int)blockIdx.y;
+    const BankLists &L = b ? L1 : L0;
+    if (claim && p == 0 && blockIdx.y == 0)   // SM claims of the down GEMM's launch
+        for (int i = threadIdx.x; i < 1024; i += blockDim.x) claim[i] = 0;
     if (p >= L.hdr[kHdrNPicks + b]) return;
     const int g = bank_offset(L, b, P) + p;
     const int n8 = I / 8;
@@ -728,9 +785,10 @@ __global__ void __launch_bounds__(256) prep_h_kernel(BankLists L, int b, int P, 
 }
 
 // Split units: this bank's down-GEMM sums (fp32, by slot) -> the bf16 rows of Y.
-__global__ void __launch_bounds__(256) round_y_kernel(BankLists L, int b, int H, const float *__restrict__ y32,
-                                                      uint16_t *__restrict__ Y) {
-    const int p = blockIdx.x;
+__global__ void __launch_bounds__(256) round_y_kernel(BankLists L0, BankLists L1, int b0, int H,
+                                                      const float *__restrict__ y32, uint16_t *__restrict__ Y) {
+    const int p = blockIdx.x, b = b0 >= 0 ? b0 : (int)blockIdx.y;
+    const BankLists &L = b ? L1 : L0;
     if (p >= L.hdr[kHdrNPicks + b]) return;
     const int64_t slot = L.picks[p];
     const float4 *src = (const float4 *)(y32 + slot * H);
@@ -772,10 +830,10 @@ int make_row_map(CUtensorMap *map, const void *base, int K, int rows, int box_ro
     return MOE_OK;
 }
 
-template <int NMAX, int PHASE, bool COLD>
+template <int NMAX, int PHASE, int BANKS>
 int launch_one(const CUtensorMap &map, const TcArgs &args, int blocks, cudaStream_t s) {
     using C = TcCfg<NMAX>;
-    auto kern = ffn_tc_kernel<NMAX, PHASE, COLD>;
+    auto kern = ffn_tc_kernel<NMAX, PHASE, BANKS>;
     MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem));
     if (blocks < 1) return MOE_OK;
     kern<<<blocks, C::kThreads, C::kSmem, s>>>(map, args);
@@ -784,68 +842,78 @@ int launch_one(const CUtensorMap &map, const TcArgs &args, int blocks, cudaStrea
 }
 
 // Grid of one GEMM launch.  Units are handed out dynamically, so the grid
-// only sets how many CTAs stream at once.  The host link needs a few MB in
-// flight, so a cold-bank launch of narrow tiles takes one CTA per SM; when
-// the layer also has a hot bank, the hot launch takes the SM's other slots,
-// so both banks run concurrently and every SM holds exactly kPerSm CTAs
-// whichever launch is placed first.
+// only sets how many CTAs stream at once.  A launch over both banks fills
+// every SM with kPerSm CTAs.  One-bank launches: the host link needs a few
+// MB in flight, so a cold-bank launch of narrow tiles takes one CTA per SM;
+// when the layer also has a hot bank, the hot launch takes the SM's other
+// slots, so two concurrent one-bank launches fit.
 template <int NMAX>
-int grid_for(const moe_ctx *ctx, bool cold, bool shared, int units_max) {
+int grid_for(const moe_ctx *ctx, int b, bool shared, int units_max) {
     const int per_sm = TcCfg<NMAX>::kPerSm;   // shared memory, registers and TMEM all fit
     const int cold_ctas = per_sm > 1 ? ctx->sms : 32;
     int blocks;
-    if (cold) blocks = cold_ctas;
+    if (b < 0) blocks = ctx->sms * per_sm;
+    else if (b == MOE_BANK_COLD) blocks = cold_ctas;
     else if (!shared) blocks = ctx->sms * per_sm;
     else if (per_sm > 1) blocks = ctx->sms * (per_sm - 1);
     else blocks = ctx->sms - cold_ctas;
     return std::max(1, std::min(units_max, blocks));
 }
 
+template <int NMAX, int PHASE>
+int launch_gemm(const CUtensorMap &map, const TcArgs &a, int blocks, cudaStream_t s) {
+    if (a.b < 0) return launch_one<NMAX, PHASE, 2>(map, a, blocks, s);
+    if (a.b == MOE_BANK_COLD) return launch_one<NMAX, PHASE, 1>(map, a, blocks, s);
+    return launch_one<NMAX, PHASE, 0>(map, a, blocks, s);
+}
+
 template <int NMAX>
-int launch_bank(moe_ctx *ctx, bool cold, bool shared, const TcArgs &a1, const TcArgs &a2, int units1, int units2,
+int launch_bank(moe_ctx *ctx, bool shared, const TcArgs &a1, const TcArgs &a2, int units1, int units2,
                 const uint16_t *x, const WsLayout &lay, uint8_t *ws, cudaStream_t s) {
     const Geom &g = ctx->g;
     const int P = a1.P;
+    const dim3 grid_p(P, a1.b < 0 ? 2 : 1);   // one block per pick (of each bank)
     CUtensorMap m1, m2;
     if (int r = make_row_map(&m1, ws + lay.xq, g.H, P, TcCfg<NMAX>::kBoxRows)) return r;
     if (int r = make_row_map(&m2, ws + lay.hq, g.I, P, TcCfg<NMAX>::kBoxRows)) return r;
-    prep_x_kernel<<<P, 256, 0, s>>>(x, g.H, g.k, a1.lists, a1.b, P, ws + lay.xq,
-                                    (int32_t *)(ws + lay.xgexp), a1.sched, a1.gu_out, g.I);
+    prep_x_kernel<<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
+                                         (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
     MOE_LAUNCH_CHECK();
-    const int b1 = grid_for<NMAX>(ctx, cold, shared, units1), b2 = grid_for<NMAX>(ctx, cold, shared, units2);
-    int r = cold ? launch_one<NMAX, 1, true>(m1, a1, b1, s) : launch_one<NMAX, 1, false>(m1, a1, b1, s);
-    if (r) return r;
-    prep_h_kernel<<<P, 256, 0, s>>>(a1.lists, a1.b, P, g.I, (const float *)(ws + lay.h32), a1.gu_out, ws + lay.hq,
-                                    (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
+    const int b1 = grid_for<NMAX>(ctx, a1.b, shared, units1), b2 = grid_for<NMAX>(ctx, a1.b, shared, units2);
+    if (int r = launch_gemm<NMAX, 1>(m1, a1, b1, s)) return r;
+    prep_h_kernel<<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
+                                         a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H, a1.claim);
     MOE_LAUNCH_CHECK();
-    r = cold ? launch_one<NMAX, 2, true>(m2, a2, b2, s) : launch_one<NMAX, 2, false>(m2, a2, b2, s);
-    if (r || !a2.y_out) return r;
-    round_y_kernel<<<P, 256, 0, s>>>(a2.lists, a2.b, g.H, a2.y_out, a2.Y);
+    if (int r = launch_gemm<NMAX, 2>(m2, a2, b2, s)) return r;
+    if (!a2.y_out) return MOE_OK;
+    round_y_kernel<<<grid_p, 256, 0, s>>>(a2.lists[0], a2.lists[1], a2.b, g.H, a2.y_out, a2.Y);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
 }  // namespace
 
-int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, int T, uint8_t *ws, uint16_t *Y,
-                  cudaStream_t s, bool shared) {
+int launch_ffn_tc(moe_ctx *ctx, const uint8_t *hot, const uint8_t *cold, int b, const uint16_t *x, int T,
+                  uint8_t *ws, uint16_t *Y, cudaStream_t s, bool shared) {
     const Geom &g = ctx->g;
     WsLayout lay = ws_layout(g, T);
     const int P = T * g.k;
-    BankLists lists;
-    lists.hdr = (const int32_t *)(ws + lay.hdr);
-    lists.act_row = (const int32_t *)(ws + lay.act_row) + (size_t)b * P;
-    lists.act_off = (const int32_t *)(ws + lay.act_off) + (size_t)b * (P + 1);
-    lists.picks = (const int32_t *)(ws + lay.picks) + (size_t)b * P;
 
     TcArgs a1{};
-    a1.bank = bank;
+    a1.bank[MOE_BANK_HOT] = hot;
+    a1.bank[MOE_BANK_COLD] = cold;
+    for (int bk = 0; bk < 2; ++bk) {
+        BankLists &L = a1.lists[bk];
+        L.hdr = (const int32_t *)(ws + lay.hdr);
+        L.act_row = (const int32_t *)(ws + lay.act_row) + (size_t)bk * P;
+        L.act_off = (const int32_t *)(ws + lay.act_off) + (size_t)bk * (P + 1);
+        L.picks = (const int32_t *)(ws + lay.picks) + (size_t)bk * P;
+    }
     a1.eb = g.eb;
     a1.part_off = 0;
     a1.mt_count = g.mt13;
     a1.kc = g.kc13;
-    a1.lists = lists;
-    a1.b = b;
+    a1.b = b == MOE_BANK_BOTH ? -1 : b;
     a1.k = g.k;
     a1.H = g.H;
     a1.I = g.I;
@@ -853,9 +921,11 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, i
     a1.bexp = (const int32_t *)(ws + lay.xgexp);
     a1.h_out = (float *)(ws + lay.h32);
     a1.status = ctx->status_dev;
-    a1.sched = (int32_t *)(ws + lay.hdr) + kHdrSched + 2 * b;
+    a1.sched = (int32_t *)(ws + lay.hdr) + kHdrSched;
+    // SM claims: a launch over both banks, or a cold-bank launch (one each;
+    // the hot bank's concurrent launches never read them)
+    a1.claim = (a1.b < 0 || a1.b == MOE_BANK_COLD) ? (int32_t *)(ws + lay.claim) : nullptr;
     TcArgs a2 = a1;
-    a2.sched = a1.sched + 1;
     a2.part_off = g.w2_off;
     a2.mt_count = g.mt2;
     a2.kc = g.kc2;
@@ -869,16 +939,15 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x, i
     a2.gu_out = nullptr;
     a2.y_out = split ? (float *)(ws + lay.y32) : nullptr;
 
-    const bool cold = b == MOE_BANK_COLD;
-    const int units1 = 2 * P * g.mt13, units2 = 2 * P * g.mt2;   // active rows never exceed the picks
+    const int units1 = 4 * P * g.mt13, units2 = 4 * P * g.mt2;   // bound: active rows never exceed the picks
     // The token-tile width depends only on T, so an expert's arithmetic is
     // the same in either bank.  Decode-sized steps use narrow tiles with
     // several CTAs per SM (an expert with more tokens than the tile loops over
     // token tiles); prefill-sized steps use 192-wide tiles (an expert's
     // ~T*k/E tokens in one tile), one CTA per SM.
-    if (T <= 16) return launch_bank<16>(ctx, cold, shared, a1, a2, units1, units2, x, lay, ws, s);
-    if (T <= kNarrowMaxT) return launch_bank<64>(ctx, cold, shared, a1, a2, units1, units2, x, lay, ws, s);
-    return launch_bank<192>(ctx, cold, shared, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= 16) return launch_bank<16>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= kNarrowMaxT) return launch_bank<64>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
+    return launch_bank<192>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
 }
 
 }  // namespace moe

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <sys/mman.h>
 #include <thread>
 
 namespace moe {
@@ -40,6 +41,19 @@ static void parallel_for(int n, F f) {
             for (int i = next.fetch_add(1); i < n; i = next.fetch_add(1)) f(i);
         });
     for (auto &th : pool) th.join();
+}
+
+// The first GPU read of a page of mapped host memory sets up its address
+// translation, which is far slower than the reads that follow it.  Touching
+// every 4 KB of a cold bank once at placement takes that cost out of the
+// layer-steps (a decode step would otherwise pay it for each cold expert the
+// first time a token routes to it).
+__global__ void touch_host_bank_kernel(const uint8_t *__restrict__ p, size_t bytes, uint32_t *sink) {
+    uint32_t acc = 0;
+    for (size_t off = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4096; off < bytes;
+         off += (size_t)gridDim.x * blockDim.x * 4096)
+        acc ^= *(const volatile uint32_t *)(p + off);
+    if (acc == 0x9E3779B9u && sink) *sink = acc;   // keeps the reads; almost never taken
 }
 
 // One MX block's 16 logical bytes (element 2i in the low nibble of byte i)
@@ -91,9 +105,48 @@ static bool repack_expert(const Geom &g, const uint8_t *w13_q, const uint8_t *w1
     return ok;
 }
 
+// Pinned, device-mapped host memory for a cold bank.  The GPU reaches host
+// memory through the host's page tables, and a bank of 64 KB pages needs
+// tens of thousands of translations: more than the GPU keeps, so steps that
+// route to rarely used cold experts stall on translation misses.  Large
+// banks therefore go into an anonymous mapping aligned to 512 MB with huge
+// pages requested (best effort), pinned with cudaHostRegister; anything that
+// fails falls back to cudaHostAlloc.
+static cudaError_t alloc_cold_bank(size_t bytes, moe::Layer &L) {
+    constexpr size_t kAlign = 512ull << 20;
+    if (bytes >= (256ull << 20)) {
+        const size_t span = (bytes + kAlign - 1) / kAlign * kAlign;
+        void *m = mmap(nullptr, span + kAlign, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE,
+                       -1, 0);
+        if (m != MAP_FAILED) {
+            uint8_t *a = (uint8_t *)(((uintptr_t)m + kAlign - 1) & ~(uintptr_t)(kAlign - 1));
+            madvise(a, span, MADV_HUGEPAGE);
+            if (cudaHostRegister(a, span, cudaHostRegisterMapped | cudaHostRegisterPortable) == cudaSuccess) {
+                if (cudaHostGetDevicePointer((void **)&L.cold_dev, a, 0) == cudaSuccess) {
+                    L.cold_host = a;
+                    L.cold_map = m;
+                    L.cold_map_bytes = span + kAlign;
+                    return cudaSuccess;
+                }
+                cudaHostUnregister(a);
+            }
+            cudaGetLastError();   // the fallback below reports its own errors
+            munmap(m, span + kAlign);
+        }
+    }
+    cudaError_t e = cudaHostAlloc(&L.cold_host, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer((void **)&L.cold_dev, L.cold_host, 0);
+    return e;
+}
+
 static void free_layer(moe::Layer &L) {
     if (L.hot) cudaFree(L.hot);
-    if (L.cold_host) cudaFreeHost(L.cold_host);
+    if (L.cold_map) {
+        cudaHostUnregister(L.cold_host);
+        munmap(L.cold_map, L.cold_map_bytes);
+    } else if (L.cold_host) {
+        cudaFreeHost(L.cold_host);
+    }
     if (L.rowmap_dev) cudaFree(L.rowmap_dev);
     L = moe::Layer();
 }
@@ -224,8 +277,7 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
     std::atomic<bool> scales_ok{true};
     if (nl.n_hot) e = cudaMalloc(&nl.hot, (size_t)nl.n_hot * g.eb);
     if (e == cudaSuccess && nl.n_cold) {
-        e = cudaHostAlloc(&nl.cold_host, (size_t)nl.n_cold * g.eb, cudaHostAllocMapped | cudaHostAllocPortable);
-        if (e == cudaSuccess) e = cudaHostGetDevicePointer((void **)&nl.cold_dev, nl.cold_host, 0);
+        e = alloc_cold_bank((size_t)nl.n_cold * g.eb, nl);
     }
     if (e == cudaSuccess) e = cudaMalloc(&nl.rowmap_dev, sizeof(int32_t) * g.E);
     if (e == cudaSuccess)
@@ -253,6 +305,11 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
             if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         }
         if (pin) cudaFreeHost(pin);
+    }
+    if (e == cudaSuccess && nl.n_cold) {
+        touch_host_bank_kernel<<<4 * ctx->sms, 256, 0, s>>>(nl.cold_dev, (size_t)nl.n_cold * g.eb, nullptr);
+        e = cudaGetLastError();
+        if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
@@ -319,19 +376,28 @@ int moe_read_split(moe_ctx *ctx, const void *ws, int T, int bank, int32_t *n_act
 int moe_expert_ffn_bank(moe_ctx *ctx, int layer, int bank, const uint16_t *x, int T, void *ws,
                         uint16_t *Y, void *stream) {
     if (int r = check_layer(ctx, layer, true)) return r;
-    if (bank != MOE_BANK_HOT && bank != MOE_BANK_COLD) return set_error(MOE_EINVAL, "bank must be 0 or 1");
+    if (bank != MOE_BANK_HOT && bank != MOE_BANK_COLD && bank != MOE_BANK_BOTH)
+        return set_error(MOE_EINVAL, "bank must be 0, 1 or 2");
     if (T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "T out of range");
     if (!ws || (uintptr_t)ws % 256) return set_error(MOE_EINVAL, "workspace must be non-null and 256-byte aligned");
     if (T > 0 && (!x || !Y)) return set_error(MOE_EINVAL, "null pointer");
     if (((uintptr_t)x | (uintptr_t)Y) % 16) return set_error(MOE_EINVAL, "x and Y must be 16-byte aligned");
     Layer &L = ctx->layers[layer];
-    const uint8_t *base = bank == MOE_BANK_HOT ? L.hot : L.cold_dev;
-    int rows = bank == MOE_BANK_HOT ? L.n_hot : L.n_cold;
+    // a both-bank call over a layer with one empty bank is a one-bank call
+    if (bank == MOE_BANK_BOTH && (L.n_hot == 0 || L.n_cold == 0)) bank = L.n_hot ? MOE_BANK_HOT : MOE_BANK_COLD;
+    const int rows = bank == MOE_BANK_HOT ? L.n_hot : (bank == MOE_BANK_COLD ? L.n_cold : L.n_hot + L.n_cold);
     if (T == 0 || rows == 0) return MOE_OK;
     DeviceGuard guard(ctx->device);
-    if (ctx->ffn_impl == MOE_FFN_SIMT)
-        return launch_ffn_simt(ctx, base, bank, x, T, (uint8_t *)ws, Y, (cudaStream_t)stream);
-    return launch_ffn_tc(ctx, base, bank, x, T, (uint8_t *)ws, Y, (cudaStream_t)stream, L.n_hot > 0 && L.n_cold > 0);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (ctx->ffn_impl == MOE_FFN_SIMT) {
+        for (int bk = 0; bk < 2; ++bk) {
+            if (bank != MOE_BANK_BOTH && bank != bk) continue;
+            const uint8_t *base = bk == MOE_BANK_HOT ? L.hot : L.cold_dev;
+            if (int r = launch_ffn_simt(ctx, base, bk, x, T, (uint8_t *)ws, Y, s)) return r;
+        }
+        return MOE_OK;
+    }
+    return launch_ffn_tc(ctx, L.hot, L.cold_dev, bank, x, T, (uint8_t *)ws, Y, s, L.n_hot > 0 && L.n_cold > 0);
 }
 
 int moe_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_t *out, void *stream) {

@@ -74,7 +74,7 @@ inline Geom make_geom(const moe_geom &g) {
 // pick's index in its bank's list), so the two banks never share a row and
 // each expert's rows are contiguous.
 struct WsLayout {
-    size_t hdr, act_row, act_off, picks, epos, ecnt, xq, xgexp, h32, hq, hexp, gu32, y32, total;
+    size_t hdr, act_row, act_off, picks, epos, ecnt, xq, xgexp, h32, hq, hexp, gu32, y32, claim, total;
 };
 // header words
 // kHdrSched + 2*bank + phase: work counters of the FFN kernels' dynamic
@@ -109,6 +109,7 @@ inline WsLayout ws_layout(const Geom &g, int T) {
     const size_t ks = split_k_steps(T) ? 1 : 0;
     w.gu32 = take(ks * P * (size_t)g.I * 2 * 4); // [P][2I] gate/up sums before SwiGLU, by g
     w.y32 = take(ks * P * (size_t)g.H * 4);     // [P][H] down-GEMM sums, by slot
+    w.claim = take(1024 * 4);                   // [SM] first-CTA claims of a launch over both banks
     w.total = off;
     return w;
 }
@@ -130,6 +131,8 @@ struct Layer {
     uint8_t *hot = nullptr;        // device: n_hot * eb
     uint8_t *cold_host = nullptr;  // pinned host: n_cold * eb
     uint8_t *cold_dev = nullptr;   // device view of cold_host
+    void *cold_map = nullptr;      // the huge-page mapping holding cold_host (null: cudaHostAlloc)
+    size_t cold_map_bytes = 0;
     int32_t *rowmap_dev = nullptr; // device int32[E]
     std::vector<int32_t> rowmap;   // CPU copy
 };
@@ -174,8 +177,11 @@ int launch_route_split(moe_ctx *ctx, int layer, const float *logits, int T, int 
                        int32_t *ids, float *w, uint8_t *ws, cudaStream_t s);
 int launch_ffn_simt(moe_ctx *ctx, const uint8_t *bank, int bank_id, const uint16_t *x, int T,
                     uint8_t *ws, uint16_t *Y, cudaStream_t s);
-// shared: the layer has rows in both banks (their launches may overlap)
-int launch_ffn_tc(moe_ctx *ctx, const uint8_t *bank, int bank_id, const uint16_t *x, int T,
+// bank_id: MOE_BANK_HOT, MOE_BANK_COLD, or MOE_BANK_BOTH (one launch per GEMM
+// over both banks); hot/cold: the banks' device-visible bases (null if
+// unused); shared: the layer has rows in both banks (one-bank launches may
+// overlap)
+int launch_ffn_tc(moe_ctx *ctx, const uint8_t *hot, const uint8_t *cold, int bank_id, const uint16_t *x, int T,
                   uint8_t *ws, uint16_t *Y, cudaStream_t s, bool shared);
 int launch_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_t *out,
                     cudaStream_t s);

@@ -6,13 +6,15 @@ One layer-step ("vLLM: Pin Hot Experts", Results):
                                       and on a second stream, joined by events)
     finalize                         (moe_finalize, main stream)
 The hot bank streams HBM and the cold bank streams the host link, so the two
-run concurrently.  PyTorch provides the device buffers and streams.
+run concurrently.  One call with MOE_BANK_BOTH (one launch per GEMM over both
+banks) and the two calls one after the other give bit-identical rows.
+PyTorch provides the device buffers and streams.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (MOE_BANK_COLD, MOE_BANK_HOT, moe_expert_ffn_bank, moe_finalize,
+from . import (MOE_BANK_BOTH, MOE_BANK_COLD, MOE_BANK_HOT, moe_expert_ffn_bank, moe_finalize,
                moe_route_split_count, moe_workspace_bytes)
 
 
@@ -46,14 +48,17 @@ class LayerStep:
         self.ev_routed = torch.cuda.Event()
         self.ev_cold = torch.cuda.Event()
 
-    def run(self, layer, T, count_on=True, stream=None, split=True):
+    def run(self, layer, T, count_on=True, stream=None, split=True, fused=False):
         """Enqueue one layer-step of T tokens from buf.logits / buf.x into
-        buf.out (and buf.ids, buf.w, buf.Y).  ``split=False`` runs both banks
-        on the main stream one after the other."""
+        buf.out (and buf.ids, buf.w, buf.Y).  By default the two banks' calls
+        run on two streams at once; ``split=False`` runs them one after the
+        other on the main stream, ``fused=True`` as one call over both banks."""
         b = self.buf
         main = stream if stream is not None else torch.cuda.current_stream()
         moe_route_split_count(self.ctx, layer, b.logits, T, count_on, b.ids, b.w, b.ws_ptr, main)
-        if split:
+        if fused:
+            moe_expert_ffn_bank(self.ctx, layer, MOE_BANK_BOTH, b.x, T, b.ws_ptr, b.Y, main)
+        elif split:
             self.ev_routed.record(main)
             self.cold_stream.wait_event(self.ev_routed)
             moe_expert_ffn_bank(self.ctx, layer, MOE_BANK_COLD, b.x, T, b.ws_ptr, b.Y, self.cold_stream)

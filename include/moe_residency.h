@@ -52,7 +52,7 @@ enum {
     MOE_ESTATE = -6     /* call out of order (e.g. layer has no banks yet)   */
 };
 
-enum { MOE_BANK_HOT = 0, MOE_BANK_COLD = 1 };
+enum { MOE_BANK_HOT = 0, MOE_BANK_COLD = 1, MOE_BANK_BOTH = 2 };
 
 /* FFN kernel implementation: tensor cores (tcgen05 + TMEM, default) or a
  * CUDA-core kernel kept for cross-checking. */
@@ -134,6 +134,13 @@ int moe_read_split(moe_ctx *ctx, const void *ws, int T, int bank, int32_t *n_act
  * Rows of the other bank are not touched, so the two banks' calls may run on
  * two streams at once (each uses its own part of ws).  A bank with no picks
  * is a no-op on the device.
+ *   bank: MOE_BANK_HOT, MOE_BANK_COLD, or MOE_BANK_BOTH.  MOE_BANK_BOTH runs
+ *   both banks' FFNs in one launch per GEMM: the first CTA on each SM takes
+ *   cold-bank work first (keeping the host link streaming from every SM),
+ *   the others hot-bank work, and each turns to the other bank when its own
+ *   runs out.  The rows equal those of the two one-bank calls bit for bit.
+ *   Do not run a MOE_BANK_BOTH call concurrently with a one-bank call on the
+ *   same workspace.
  *   x: device bf16 [T][H];  Y: device bf16 [T][k][H] out;  ws as routed. */
 int moe_expert_ffn_bank(moe_ctx *ctx, int layer, int bank, const uint16_t *x, int T, void *ws,
                         uint16_t *Y, void *stream);

@@ -73,9 +73,9 @@ class Harness:
         b.x[:T].copy_(torch.from_numpy(np.ascontiguousarray(x).view(np.int16)))
         return T
 
-    def run(self, layer, logits, x, count_on=True, split=True):
+    def run(self, layer, logits, x, count_on=True, split=True, fused=True):
         T = self.load(logits, x)
-        self.step.run(layer, T, count_on=count_on, split=split)
+        self.step.run(layer, T, count_on=count_on, split=split, fused=fused)
         torch.cuda.synchronize()
         b = self.step.buf
         return dict(ids=b.ids[:T].cpu().numpy(), w=b.w[:T].cpu().numpy(),

@@ -73,11 +73,13 @@ def test_split_equals_unsplit_bitwise(impl):
         for step in range(3):
             lg = synth.router_logits(cfg, 0, step)
             x = synth.activations(cfg, 0, step)
-            a = split.run(0, lg, x)
+            a = split.run(0, lg, x)                            # one call over both banks
             b = unsplit.run(0, lg, x)
-            c = split.run(0, lg, x, split=False)
+            c = split.run(0, lg, x, fused=False, split=False)  # one bank after the other
+            d = split.run(0, lg, x, fused=False)               # the two banks on two streams
             assert np.array_equal(a["Y"], b["Y"]) and np.array_equal(a["out"], b["out"])
-            assert np.array_equal(a["out"], c["out"])
+            for r in (c, d):
+                assert np.array_equal(a["Y"], r["Y"]) and np.array_equal(a["out"], r["out"])
     finally:
         split.close()
         unsplit.close()
