@@ -140,7 +140,7 @@ struct TcCfg {
     // [Nr, 2 Nr) of one MMA (half the MMA instructions); wider tiles issue
     // one MMA per piece.
     static constexpr bool kStack = NMAX <= 16;
-    static constexpr int kStages = NMAX <= 16 ? 6 : (NMAX <= 64 ? 5 : 7);
+    static constexpr int kStages = NMAX <= 8 ? 8 : (NMAX <= 16 ? 6 : (NMAX <= 64 ? 5 : 7));
     static constexpr int kBStage = (kStack ? 2 : 1) * NMAX * 128;   // bytes of one B chunk (rows x 128 B)
     static constexpr int kDq = kWide ? 8 : 4;               // unpack warps
     static constexpr int kGroups = kDq / 4;                 // unpack groups (one TMEM lane set each)
@@ -149,8 +149,11 @@ struct TcCfg {
     static constexpr int kDBufs = kEpi ? 2 : 1;             // accumulators in TMEM
     // token rows per tensor-TMA box: few large boxes for wide tiles (the TMA
     // engine's cost is per box), 16-row boxes for the few tokens of decode
-    static constexpr int kBoxRows = kWide ? 64 : 16;
+    static constexpr int kBoxRows = kWide ? 64 : (NMAX <= 8 ? 8 : 16);
     static constexpr int kBoxBytes = kBoxRows * 128;
+    // token rows of one piece are padded to a multiple of kRowQ (8-token tiles:
+    // pieces at rows [0, 8) and [8, 16) of an N = 16 MMA)
+    static constexpr int kRowQ = kStack ? kBoxRows : 16;
     // Tensor memory columns.  Slot s owns the 32-column block at
     // kBlk + 32 s: its A scale columns at +0 (quarter q reads +q), its A
     // codes (64 bytes = 16 columns) at +16; blocks 0 and 1 also hold the B
@@ -169,7 +172,7 @@ struct TcCfg {
     static constexpr uint32_t kCols = kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512);
     static_assert(kColsUsed <= 512, "tile does not fit in tensor memory");
     static_assert(kABufs >= 2 && kNCol <= 8, "B scale columns");
-    static_assert(NMAX % 16 == 0 && kBlk % 32 == 0 && kDCol % 32 == 0, "column alignment");
+    static_assert(NMAX % 8 == 0 && kDW % 16 == 0 && kBlk % 32 == 0 && kDCol % 32 == 0, "column alignment");
     static constexpr int kPerSm = NMAX <= 16 ? 4 : (NMAX <= 64 ? 3 : 1);   // resident CTAs per SM
     // Narrow tiles split each (expert, M-tile) unit into two K halves: a
     // decode step has only a few units per CTA, and halving them halves the
@@ -201,11 +204,11 @@ __device__ __forceinline__ void load_meta(const BankLists &L, const TcArgs &args
 // columns of a block are computed together; only the stores are predicated.
 // STACK: column n + Nr holds the second e4m3 piece's product (16x scaled),
 // so the token's value is D[n] + 2^-4 D[n + Nr].
-template <int PHASE, int NBLK, bool STACK, int KS>
+template <int PHASE, int NBLK, bool STACK, int KS, int RQ>
 __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, int blk0, int bstride, int nn, int g,
                                               int mt, int quarter, int lane, const int (&rs)[NBLK],
                                               const float (&rsc)[NBLK]) {
-    const int Nr = (nn + 15) & ~15;
+    const int Nr = (nn + RQ - 1) / RQ * RQ;
     const int m = quarter * 32 + lane;
     uint32_t vv[32];
 #pragma unroll
@@ -213,7 +216,17 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
         const int c0 = (blk0 + i * bstride) * 16;
         if (c0 >= Nr) break;   // warp-uniform
         float d[16];
-        if (STACK) {
+        if (STACK && RQ == 8) {
+            // 8-token tile: one load of the 16 columns, pieces at q and 8 + q
+            uint32_t (&v)[16] = *reinterpret_cast<uint32_t(*)[16]>(&vv[0]);
+            ptx::tmem_ld16(dt, v);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                d[q] = q < 8 ? __fmul_rn(__fmaf_rn(__uint_as_float(v[8 + (q & 7)]), 0.0625f, __uint_as_float(v[q & 7])),
+                                         __shfl_sync(0xffffffffu, rsc[i], q))
+                             : 0.0f;
+        } else if (STACK) {
             uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&vv[0]);
             uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&vv[16]);
             ptx::tmem_ld16(dt + c0, lo);
@@ -383,7 +396,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         const int quarter = warp & 3, group = warp >> 2;
         const int m = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        constexpr int NB = (NMAX / 16 + G - 1) / G;   // this warp's D column blocks when it drains D
+        constexpr int NB = ((NMAX + 15) / 16 + G - 1) / G;   // this warp's D column blocks when it drains D
         uint32_t it = 0, j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
@@ -435,7 +448,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                 if (C::kEpi == 0) {
                     if (!wait_warp<SUSP>(bar(ACCREADY), j & 1, abort_flag, args.status)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    epilogue_cols<PHASE, NB, C::kStack, C::kSplit>(args, tmem + lane_base + C::kDCol, group, G, nn,
+                    epilogue_cols<PHASE, NB, C::kStack, C::kSplit, C::kRowQ>(args, tmem + lane_base + C::kDCol, group, G, nn,
                                                         goff + p0 + n0, mt, quarter, lane, rs, re);
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(bar(ACCFREE));
@@ -446,7 +459,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         // -------------------------------------------------------- epilogue
         const int quarter = warp & 3;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        constexpr int NB = NMAX / 16;
+        constexpr int NB = (NMAX + 15) / 16;
         uint32_t j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
@@ -466,7 +479,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                 const int db = j % DB;
                 if (!wait_warp<SUSP>(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status)) { ok = false; break; }
                 ptx::tc_fence_after();
-                epilogue_cols<PHASE, NB, C::kStack, C::kSplit>(args, tmem + lane_base + C::kDCol + db * C::kDW, 0, 1, nn,
+                epilogue_cols<PHASE, NB, C::kStack, C::kSplit, C::kRowQ>(args, tmem + lane_base + C::kDCol + db * C::kDW, 0, 1, nn,
                                                     goff + p0 + n0, mt, quarter, lane, rs, re);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(ACCFREE + db));
@@ -580,7 +593,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
             const int n = L.act_off[a + 1] - L.act_off[a];
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
-                const int Nr = (nn + 15) & ~15;
+                const int Nr = (nn + C::kRowQ - 1) / C::kRowQ * C::kRowQ;
                 const int Nm = C::kStack ? 2 * Nr : Nr;                              // B rows of one MMA
                 const uint32_t idesc0 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 0, 0);   // K block 0 of the chunk
                 const uint32_t idesc1 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 1, 0);   // K block 1
@@ -945,6 +958,7 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *hot, const uint8_t *cold, int b, 
     // several CTAs per SM (an expert with more tokens than the tile loops over
     // token tiles); prefill-sized steps use 192-wide tiles (an expert's
     // ~T*k/E tokens in one tile), one CTA per SM.
+    if (T <= 8) return launch_bank<8>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
     if (T <= 16) return launch_bank<16>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
     if (T <= kNarrowMaxT) return launch_bank<64>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
     return launch_bank<192>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
