@@ -3,8 +3,8 @@
 // Same work decomposition and device layout as the tensor-core kernel: a unit
 // is (active bank row, 128-row M-tile); thread m of the 128-thread block owns
 // tile row m, reads its 32 packed bytes and two e8m0 scales per 64-wide
-// K-chunk, dequantises them exactly to fp32 and accumulates up to 8 tokens
-// with fp32 fma in K order.  Phase 1 (gate/up) writes h = silu(g) * u in fp32
+// K-chunk (two K blocks of the chunk's group), dequantises them exactly to
+// fp32 and accumulates up to 8 tokens with fp32 fma in K order.  Phase 1 (gate/up) writes h = silu(g) * u in fp32
 // per slot; phase 2 (down) writes the bf16 expert row into Y.
 #include "moe_internal.cuh"
 
@@ -22,8 +22,7 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
 
 template <int PHASE>
 __global__ void __launch_bounds__(128) ffn_simt_kernel(const uint8_t *__restrict__ bank, int64_t eb,
-                                                       int64_t part_off, int mt_count, int kc,
-                                                       BankLists lists, int b, int k, int H, int I,
+                                                       PartLayout part, BankLists lists, int b, int k, int H, int I,
                                                        const uint16_t *__restrict__ x,
                                                        const float *__restrict__ h_in,
                                                        float *__restrict__ h_out,
@@ -31,12 +30,13 @@ __global__ void __launch_bounds__(128) ffn_simt_kernel(const uint8_t *__restrict
     __shared__ float sx[kTok][kKC];
     const int m = threadIdx.x;
     const int n_act = lists.hdr[kHdrNAct + b];
+    const int mt_count = part.tiles, kc = part.kchunks;
     const int units = n_act * mt_count;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const int a = u / mt_count, mt = u % mt_count;
         const int row = lists.act_row[a];
         const int p0 = lists.act_off[a], n = lists.act_off[a + 1] - p0;
-        const uint8_t *tile = bank + (int64_t)row * eb + part_off + (int64_t)mt * kc * kChunkBytes;
+        const uint8_t *expert = bank + (int64_t)row * eb;
         for (int ng = 0; ng < n; ng += kTok) {
             const int nn = min(kTok, n - ng);
             float acc[kTok];
@@ -53,10 +53,13 @@ __global__ void __launch_bounds__(128) ffn_simt_kernel(const uint8_t *__restrict
                     sx[tn][kk] = v;
                 }
                 __syncthreads();
-                const uint8_t *chunk = tile + (int64_t)c * kChunkBytes;
-                const uint4 q[2] = {*(const uint4 *)(chunk + m * 16), *(const uint4 *)(chunk + 2048 + m * 16)};
-                const float sc[2] = {ldexpf(1.0f, (int)chunk[kChunkQBytes + 2 * m] - 127),
-                                     ldexpf(1.0f, (int)chunk[kChunkQBytes + 2 * m + 1] - 127)};
+                int slot, tidx, kb0, nkb;
+                part.group(mt, c >> 1, slot, tidx, kb0, nkb);
+                const uint8_t *grp = expert + part.group_off(slot, tidx);
+                const int kb = kb0 + 2 * (c & 1);   // the chunk's first K block in its group
+                const uint4 q[2] = {*(const uint4 *)(grp + m * 64 + kb * 16), *(const uint4 *)(grp + m * 64 + kb * 16 + 16)};
+                const uint8_t *sa = grp + kGroupQBytes + (m % 32) * 16 + 4 * (m / 32) + kb;
+                const float sc[2] = {ldexpf(1.0f, (int)sa[0] - 127), ldexpf(1.0f, (int)sa[1] - 127)};
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const uint32_t wd[4] = {q[hh].x, q[hh].y, q[hh].z, q[hh].w};
@@ -65,7 +68,7 @@ __global__ void __launch_bounds__(128) ffn_simt_kernel(const uint8_t *__restrict
 #pragma unroll
                         for (int ni = 0; ni < 8; ++ni) {
                             const int kk = hh * 32 + wi * 8 + ni;
-                            const int sh = ni < 4 ? 8 * ni : 8 * (ni - 4) + 4;   // device nibble order
+                            const int sh = 4 * ni;   // element 2i in the low nibble of byte i
                             const float wv = e2m1_to_f32((wd[wi] >> sh) & 15u) * sc[hh];
 #pragma unroll
                             for (int tn = 0; tn < kTok; ++tn)
@@ -111,11 +114,11 @@ int launch_ffn_simt(moe_ctx *ctx, const uint8_t *bank, int b, const uint16_t *x,
     float *h32 = (float *)(ws + lay.h32);
     const int max_rows = P;   // active rows never exceed the picks
     int blocks1 = (int)std::min<long long>((long long)max_rows * g.mt13, (long long)ctx->sms * 8);
-    ffn_simt_kernel<1><<<blocks1, 128, 0, s>>>(bank, g.eb, 0, g.mt13, g.kc13, lists, b, g.k, g.H, g.I, x,
+    ffn_simt_kernel<1><<<blocks1, 128, 0, s>>>(bank, g.eb, g.w13, lists, b, g.k, g.H, g.I, x,
                                                nullptr, h32, nullptr);
     MOE_LAUNCH_CHECK();
     int blocks2 = (int)std::min<long long>((long long)max_rows * g.mt2, (long long)ctx->sms * 8);
-    ffn_simt_kernel<2><<<blocks2, 128, 0, s>>>(bank, g.eb, g.w2_off, g.mt2, g.kc2, lists, b, g.k, g.H, g.I,
+    ffn_simt_kernel<2><<<blocks2, 128, 0, s>>>(bank, g.eb, g.w2, lists, b, g.k, g.H, g.I,
                                                nullptr, h32, nullptr, Y);
     MOE_LAUNCH_CHECK();
     return MOE_OK;

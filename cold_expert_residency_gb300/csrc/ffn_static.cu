@@ -91,7 +91,7 @@ int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t
                 if (bank == MOE_BANK_BOTH || bank == bk)
                     r = launch_ffn_simt(ctx, bk == MOE_BANK_HOT ? L.hot : L.cold_dev, bk, x, T, scratch, Y, s);
         } else {
-            r = launch_ffn_tc(ctx, L.hot, L.cold_dev, bank, x, T, scratch, Y, s, L.n_hot > 0 && L.n_cold > 0);
+            r = launch_ffn_tc(ctx, L, bank, x, T, scratch, Y, s);
         }
     }
     if (prev >= 0 && prev != ctx->device) cudaSetDevice(prev);

@@ -1,44 +1,44 @@
 // MXFP4 expert FFN on the 5th-generation tensor cores (tcgen05 + TMEM),
-// block-scaled.
+// block-scaled, with the weights moved only by the tensor memory accelerator.
 //
 // "vLLM: Pin Hot Experts", Results: the routed MXFP4 expert FFN (gate/up
 // GEMM, SwiGLU, down GEMM) runs once per residency bank without finalize.
-// Here one launch per GEMM covers one bank:
+// Here one launch per GEMM covers one bank (or both):
 //
-//   unit = (active bank row = one expert, 128-row M-tile [, token tile]);
+//   unit = (active bank row = one expert, 128-row M-tile [, K half]);
 //   D[128 x N] = sum over 32-wide K blocks of (SFA * A) (SFB * B)^T, fp32 in
 //   TMEM, by tcgen05.mma kind::mxf8f6f4 with e8m0 block scales, where
-//   A = the expert's e2m1 weights with their own e8m0 scales (exact), and
-//   B = the expert's token rows (bf16 x, or the fp32 gate/up output h), each
+//   A = the expert's e2m1 weights with their own e8m0 scales (exact), read
+//       by the tensor cores from shared memory, and
+//   B = the expert's token rows (bf16 x, or the gate/up output h), each
 //       row scaled by a power of two so its largest |value| lies in (224, 448]
 //       and carried as two e4m3 pieces: q1 = e4m3(v), q2 = e4m3(16 (v - q1)).
 //       B's scales are constants (2^0 for q1, 2^-4 for q2); both pieces
 //       accumulate into the same D, so v is represented to about 2^-8 of
 //       itself; the epilogue undoes the row's power of two.
 //
-// Warp roles:
-//   producer    Weights: one 1-D bulk async copy (TMA) of each 4352-byte
-//               (M-tile, K-chunk) block, from HBM for the hot bank and from
-//               the mapped pinned host bank for the cold bank (the
-//               host-link streaming path: the copy engine of the SM reads
-//               the host memory in place).  Token rows: 2-D tensor TMA boxes of 128
-//               bytes (the chunk's two e4m3 pieces) per row with 128-byte
-//               swizzle from the pick-ordered row array.  All into a
-//               shared-memory ring, completion on one mbarrier per stage.
-//   unpack      Thread m of a 4-warp group owns weight row m = TMEM lane m;
-//               per chunk it spreads its 64 e2m1 codes to one byte each
-//               (two masked shifts per 8 codes, thanks to the device nibble
-//               order) into the group's TMEM A slot, and its two e8m0 scale
-//               bytes into the slot's scale column.
-//   epilogue    tcgen05.ld of D, the row's power of two undone, then SwiGLU
-//               (gate and up rows meet in lanes l and l^16) or the bf16 row.
-//   MMA         TMEM allocation; one lane issues tcgen05.mma (A and the
-//               scales from TMEM, B from shared memory) and tcgen05.commit.
-// Decode tiles (16 or 64 tokens): one unpack group that also runs the
-// epilogue, 3-4 CTAs per SM.  Prefill tiles (192 tokens): one CTA per SM with
-// two unpack groups (group g takes the chunks c = g mod 2), four dedicated
-// epilogue warps and a double-buffered accumulator, so one tile's epilogue
-// overlaps the next tile's MMAs.
+// No SM instruction touches a weight byte.  Warp roles:
+//   producer  Per K group of 128: one tensor-TMA box of the padded 4-bit
+//             type (the group's 8 KB code block becomes 16 KB of shared
+//             memory in the layout the MMA reads, 128-byte swizzle), one bulk
+//             copy of its 512-byte scale atom, and one box of the tile's
+//             token rows (4-D tensor TMA, both e4m3 pieces of both 64-wide
+//             chunks, 64-byte swizzle, from the pick-ordered row array); from
+//             HBM for the hot bank, over the host link from the mapped pinned
+//             host bank for the cold bank.  All into a ring of stages with one
+//             mbarrier each; one thread issues them.
+//   MMA       One thread: tcgen05.cp of the stage's scale atom into its
+//             tensor-memory scale slot, the group's MMAs (four K blocks, two
+//             for a half group), tcgen05.commit to free the stage; after a
+//             token tile's last group, a commit hands its accumulator over.
+//   epilogue  Four warps (thread m = accumulator row m): tcgen05.ld of D, the
+//             row's power of two undone, then SwiGLU (gate and up rows meet
+//             in lanes l and l^16), the bf16 row, or fp32 partial sums of a
+//             K half.  Two accumulators, so a tile's epilogue overlaps the
+//             next tile's MMAs.
+// Decode tiles (8, 16 or 32 tokens) run 1-3 CTAs per SM, prefill tiles (192
+// tokens) one; the ring's depth is set per launch from the shared memory
+// that the SM's CTAs leave.
 //
 // The arithmetic of a pick depends only on its expert's weights, its token
 // row and the step's token count (which fixes the tile), never on the bank,
@@ -49,7 +49,6 @@
 #include "moe_internal.cuh"
 #include "sm103_ptx.cuh"
 
-#include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp8.h>
 
@@ -62,27 +61,30 @@ constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s bound of a pipeline wait
 
 struct TcArgs {
     const uint8_t *bank[2];  // device-visible base of the hot (HBM) and cold (mapped host) bank
-    int64_t eb, part_off;
-    int mt_count, kc;
+    int64_t eb;              // bytes per expert
+    PartLayout part;         // this GEMM's part of an expert (W13 or W2)
+    int ks;                  // K parts per (expert, M-tile) unit
+    int S;                   // stages of the shared-memory ring (2 .. kMaxStages)
     BankLists lists[2];      // both banks' split lists
     int b;                   // the bank this launch covers, or -1: both banks in one launch
     int k, H, I, P;
     const int32_t *bexp;    // [P] scale exponent of B row g
     float *h_out;           // phase 1 output [P][I] by g
     uint16_t *Y;            // phase 2 output [T*k][H] by slot
-    float *gu_out;          // split units, phase 1: [P][2I] gate/up sums by g (fp32, atomically added)
-    float *y_out;           // split units, phase 2: [T*k][H] sums by slot (fp32, atomically added)
+    float *gu_out;          // narrow tiles, phase 1: [P][2I] gate/up sums by g (fp32, atomically added)
+    float *y_out;           // narrow tiles, phase 2: [T*k][H] sums by slot (fp32, atomically added)
     int32_t *status;
     int32_t *sched;         // [2 banks][2 phases] work counters (zeroed before the launch)
-    int32_t *claim;         // both banks: [SM] first-CTA claims (zeroed before the launch)
+    int32_t *claim;         // [SM] first-CTA claims (zeroed before the launch)
 };
 
 constexpr int kQ = 4;       // unit queue depth (producer -> the other roles)
+constexpr int kMaxStages = 8;
 
 // Bounded mbarrier wait: gives up after kWaitNs of wall-clock time, raising
 // the CTA's abort flag and the launch status.  SUSP: each poll may suspend the
 // thread (up to 20 us) instead of returning at once -- used by the decode
-// tiles, whose 3-4 CTAs per SM otherwise spend issue slots polling.
+// tiles, whose CTAs share an SM.
 template <bool SUSP>
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                          int32_t *status) {
@@ -110,23 +112,16 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-// 8 e2m1 codes in the device nibble order (byte i: codes i and 4+i) -> two
-// TMEM columns of one code per byte, code in bits 5..2.
-__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    lo = (w << 2) & 0x3C3C3C3Cu;
-    hi = (w >> 2) & 0x3C3C3C3Cu;
-}
-
-// Unit u -> active row a, M-tile mt and its K-chunk range [c0, c1) (one of
-// ks equal K parts).
-__device__ __forceinline__ void unit_pos(int u, int mt_count, int kc, int ks, int &a, int &mt, int &c0, int &c1) {
+// Unit u -> active row a, M-tile mt and its K-step range [s0, s1) (one of ks
+// equal parts of the tile's ns K groups).
+__device__ __forceinline__ void unit_pos(int u, int mt_count, int ns, int ks, int &a, int &mt, int &s0, int &s1) {
     const int per = mt_count * ks;
     a = u / per;
     const int r = u - a * per;
     mt = r / ks;
     const int h = r - mt * ks;
-    c0 = h * kc / ks;
-    c1 = (h + 1) * kc / ks;
+    s0 = h * ns / ks;
+    s1 = (h + 1) * ns / ks;
 }
 
 __device__ __forceinline__ int bank_offset(const BankLists &L, int b, int P) {
@@ -136,53 +131,52 @@ __device__ __forceinline__ int bank_offset(const BankLists &L, int b, int P) {
 template <int NMAX>
 struct TcCfg {
     static constexpr bool kWide = NMAX >= 128;
-    // 16-token tiles stack the two e4m3 pieces as token rows [0, Nr) and
-    // [Nr, 2 Nr) of one MMA (half the MMA instructions); wider tiles issue
-    // one MMA per piece.
+    // Tiles of up to 16 tokens stack the two e4m3 pieces as token rows
+    // [0, Nr) and [Nr, 2 Nr) of one MMA (half the MMA instructions); wider
+    // tiles issue one MMA per piece.
     static constexpr bool kStack = NMAX <= 16;
-    static constexpr int kStages = NMAX <= 8 ? 8 : (NMAX <= 16 ? 6 : (NMAX <= 64 ? 5 : 7));
-    static constexpr int kBStage = (kStack ? 2 : 1) * NMAX * 128;   // bytes of one B chunk (rows x 128 B)
-    static constexpr int kDq = kWide ? 8 : 4;               // unpack warps
-    static constexpr int kGroups = kDq / 4;                 // unpack groups (one TMEM lane set each)
-    static constexpr int kABufs = kWide ? 4 : (NMAX <= 16 ? 3 : 2);   // TMEM A slots
-    static constexpr int kEpi = kWide ? 4 : 0;              // dedicated epilogue warps
-    static constexpr int kDBufs = kEpi ? 2 : 1;             // accumulators in TMEM
-    // token rows per tensor-TMA box: few large boxes for wide tiles (the TMA
-    // engine's cost is per box), 16-row boxes for the few tokens of decode
-    static constexpr int kBoxRows = kWide ? 64 : (NMAX <= 8 ? 8 : 16);
-    static constexpr int kBoxBytes = kBoxRows * 128;
-    // token rows of one piece are padded to a multiple of kRowQ (8-token tiles:
-    // pieces at rows [0, 8) and [8, 16) of an N = 16 MMA)
-    static constexpr int kRowQ = kStack ? kBoxRows : 16;
-    // Tensor memory columns.  Slot s owns the 32-column block at
-    // kBlk + 32 s: its A scale columns at +0 (quarter q reads +q), its A
-    // codes (64 bytes = 16 columns) at +16; blocks 0 and 1 also hold the B
-    // scale columns of e4m3 piece 0 and 1 at +8 (one per 32 B rows; stacked
-    // tiles use block 0's for both pieces).  The accumulators (kDW columns
-    // each) take their own range.
-    static constexpr int kDW = (kStack ? 2 : 1) * NMAX;
-    static constexpr int kNCol = (kDW + 31) / 32;
-    static constexpr uint32_t kBlk = kWide ? kDBufs * NMAX : 0;
-    static constexpr uint32_t kDCol = kWide ? 0 : 32 * kABufs;
-    static constexpr uint32_t kSfaCol = kBlk;
-    static constexpr uint32_t kACol = kBlk + 16;
-    static constexpr uint32_t kSfbCol = kBlk + 8;
-    static constexpr uint32_t kSfbStride = 32;              // piece 1 in the next block
-    static constexpr uint32_t kColsUsed = kWide ? kBlk + 32 * kABufs : kDCol + kDBufs * kDW;
-    static constexpr uint32_t kCols = kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512);
+    // One 4-D tensor-TMA box per stage brings the tile's token rows: both
+    // e4m3 pieces of both 64-wide chunks, as [chunk][piece][NMAX rows][64 B]
+    // with 64-byte swizzle (rows past the tile's tokens are loaded and unused).
+    static constexpr int kBChunk = 2 * NMAX * 64;           // one chunk: both pieces
+    static constexpr int kBStage = 2 * kBChunk;
+    // token rows of one piece are padded to a multiple of kRowQ (stacked
+    // tiles: the whole tile, so piece 1 starts at row NMAX)
+    static constexpr int kRowQ = kStack ? NMAX : 16;
+    static constexpr int kAStage = 2 * kGroupQBytes;                // padded code block: 16 KB
+    // One stage holds a group's 8.5 KB of weights as 16.5 KB of padded codes
+    // and scales, plus the token rows; the host sizes the ring per launch
+    // from the SM's shared memory and the CTAs that share it.
+    static constexpr int kStageBytes = kAStage + kBStage + kSfAtomBytes;
+    static constexpr int kDBufs = 2;                        // accumulators in TMEM
+    static constexpr int kDW = (kStack ? 2 : 1) * NMAX;     // columns of one accumulator
+    static constexpr int kNCol = (kDW + 31) / 32;           // B scale columns of one piece
+    // A scale slots in TMEM, reused round-robin: the MMA thread refills slot
+    // it % kNsf after the MMAs of iteration it - kNsf have completed.
+    static constexpr int kNsf = kWide ? 3 : 2;
+    // Tensor memory columns: slot i's A scales at 32 i (four columns written
+    // by tcgen05.cp); slot 0's block also holds the B scale columns of piece
+    // 0 at +8 and of piece 1 at +16 (stacked tiles use piece 0's for both);
+    // then the accumulators.
+    static constexpr uint32_t kSfbCol = 8;
+    static constexpr uint32_t kSfbStride = 8;
+    static constexpr uint32_t kDCol = 32 * kNsf;
+    static constexpr uint32_t kColsUsed = kDCol + kDBufs * kDW;
+    static constexpr uint32_t kCols = kColsUsed <= 64 ? 64 : (kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512));
+    static constexpr int kPerSmMax = 512 / kCols;           // CTAs per SM that tensor memory admits
     static_assert(kColsUsed <= 512, "tile does not fit in tensor memory");
-    static_assert(kABufs >= 2 && kNCol <= 8, "B scale columns");
-    static_assert(NMAX % 8 == 0 && kDW % 16 == 0 && kBlk % 32 == 0 && kDCol % 32 == 0, "column alignment");
-    static constexpr int kPerSm = NMAX <= 16 ? 4 : (NMAX <= 64 ? 3 : 1);   // resident CTAs per SM
+    static_assert(kNCol <= 8 && kSfbCol + kSfbStride + kNCol <= 32, "B scale columns");
+    static_assert(NMAX % 8 == 0 && NMAX <= 256 && kDW % 16 == 0 && kDCol % 32 == 0, "tile alignment");
     // Narrow tiles split each (expert, M-tile) unit into two K halves: a
     // decode step has only a few units per CTA, and halving them halves the
     // tail of the launch.  Two partial sums added onto zero in either order
     // give the same fp32 result, so the split stays deterministic.
     static constexpr int kSplit = kWide ? 1 : 2;
-    static constexpr int kProducer = kDq + kEpi;            // producer warp; the MMA warp follows
-    static constexpr int kThreads = 32 * (kDq + kEpi + 2);
-    static constexpr int kBars = 2 * kStages + kABufs + 2 * kDBufs + 2 * kQ;
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * (kBStage + kChunkBytes) + kBars * 8 + 16 + 4 * kQ;
+    static constexpr int kProducer = 4, kMmaWarp = 5;
+    static constexpr int kThreads = 192;
+    static constexpr int kBars = 2 * kMaxStages + 2 * kDBufs + 2 * kQ;
+    static constexpr size_t kFixedSmem = 1024 + kBars * 8 + 16 + 4 * kQ;   // alignment slack, barriers, queue
+    static size_t smem_bytes(int S) { return kFixedSmem + (size_t)S * kStageBytes; }
 };
 
 // Epilogue metadata of NBLK column blocks of 16: lane q of block i holds, for
@@ -295,30 +289,32 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
 }
 
 // BANKS names the launch (0 hot bank, 1 cold bank, 2 both banks); the code
-// is the same, every unit carries its bank.
+// is the same, every unit carries its bank.  tmA0 / tmA1: the hot and cold
+// bank's code-block maps of this GEMM's part; tmB: the token-row records.
 template <int NMAX, int PHASE, int BANKS>
-__global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ffn_tc_kernel(const __grid_constant__ CUtensorMap tmap,
-                                                                         TcArgs args) {
+__global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kWide ? 1 : 3)
+    ffn_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0,
+                  const __grid_constant__ CUtensorMap tmA1, TcArgs args) {
     using C = TcCfg<NMAX>;
-    constexpr int DQ = C::kDq, NA = C::kABufs, DB = C::kDBufs, S = C::kStages, G = C::kGroups;
+    constexpr int DB = C::kDBufs, NSF = C::kNsf;
+    const int S = args.S;
     extern __shared__ uint8_t smem_raw[];
-    // 128-byte-swizzled B stages need 1024-byte alignment
+    // 128-byte-swizzled stages need 1024-byte alignment
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint8_t *sB = smem;
-    uint8_t *sA = sB + S * C::kBStage;
-    uint64_t *bars = (uint64_t *)(sA + S * kChunkBytes);
+    uint8_t *sA = smem;                          // [S][16 KB] padded code blocks
+    uint8_t *sB = sA + S * C::kAStage;           // [S][2 chunks][2 pieces][NMAX rows][64 B] token rows
+    uint8_t *sSF = sB + S * C::kBStage;          // [S][512] scale atoms
+    uint64_t *bars = (uint64_t *)(sSF + S * kSfAtomBytes);
     uint32_t *holder = (uint32_t *)(bars + C::kBars);
     volatile int *abort_flag = (volatile int *)(holder + 1);
     volatile int *uq = (volatile int *)(holder + 2);   // [kQ] unit queue
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
-    // FULL: stage landed.  DONE: the chunk's MMAs completed (its stage and
-    // its A slot are free again).  AREADY: A slot written.
-    const int FULL = 0, DONE = S, AREADY = 2 * S, ACCREADY = 2 * S + NA, ACCFREE = ACCREADY + DB,
-              UQFULL = ACCFREE + DB, UQEMPTY = UQFULL + kQ;
-    constexpr int kEpiThreads = C::kEpi ? 32 * C::kEpi : 32 * DQ;   // threads that drain D
-    constexpr int kQueueReaders = 32 * DQ + 32 * C::kEpi + 1;       // + the MMA thread
-    constexpr int PROD = C::kProducer, MMAW = C::kProducer + 1;
-    constexpr bool SUSP = !C::kWide;   // suspend-hinted waits for the decode tiles
+    // FULL: stage landed.  DONE: the stage's MMAs completed (stage and scale
+    // slot free again).  ACCREADY / ACCFREE: accumulator handover.
+    const int FULL = 0, DONE = kMaxStages, ACCREADY = 2 * kMaxStages, ACCFREE = ACCREADY + DB, UQFULL = ACCFREE + DB,
+              UQEMPTY = UQFULL + kQ;
+    constexpr int kQueueReaders = 128 + 1;   // the epilogue warps and the MMA thread
+    constexpr bool SUSP = !C::kWide;         // suspend-hinted waits for the decode tiles
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (BANKS == 1) {
@@ -343,16 +339,19 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
             ptx::mbar_init(bar(UQFULL + q), 1);
             ptx::mbar_init(bar(UQEMPTY + q), kQueueReaders);
         }
-        for (int i = 0; i < NA; ++i) ptx::mbar_init(bar(AREADY + i), 128);   // the four warps of the chunk's group
         for (int i = 0; i < DB; ++i) {
             ptx::mbar_init(bar(ACCREADY + i), 1);
-            ptx::mbar_init(bar(ACCFREE + i), kEpiThreads);
+            ptx::mbar_init(bar(ACCFREE + i), 128);
         }
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == PROD && lane == 0) ptx::prefetch_tmap(&tmap);
-    if (warp == MMAW) {
+    if (warp == C::kProducer && lane == 0) {
+        ptx::prefetch_tmap(&tmB);
+        ptx::prefetch_tmap(&tmA0);
+        ptx::prefetch_tmap(&tmA1);
+    }
+    if (warp == C::kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_addr(holder), C::kCols);
         ptx::tmem_relinquish();
     }
@@ -370,11 +369,15 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
             ptx::tmem_st1(tmem + lb + C::kSfbCol + j, 0x7F7F7F7Fu);
             if (!C::kStack) ptx::tmem_st1(tmem + lb + C::kSfbCol + C::kSfbStride + j, 0x7B7B7B7Bu);
         }
-        ptx::tmem_wait_st();   // made visible to the MMA by the first A-slot handoff
+        ptx::tmem_wait_st();
     }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
 
-    const int kc = args.kc;
-    auto units_of = [&](int bk) { return args.lists[0].hdr[kHdrNAct + bk] * args.mt_count * C::kSplit; };
+    const PartLayout &part = args.part;
+    const int ns = part.steps();
+    auto units_of = [&](int bk) { return args.lists[0].hdr[kHdrNAct + bk] * part.tiles * args.ks; };
 
     // every role but the producer reads the unit sequence from the queue:
     // entry 2u + bank (unit u of that bank), or -1 at the end
@@ -391,73 +394,9 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         return u;
     };
 
-    if (warp < DQ) {
-        // ------------------------------------------------- unpack (+ epilogue)
-        const int quarter = warp & 3, group = warp >> 2;
-        const int m = quarter * 32 + lane;
-        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        constexpr int NB = ((NMAX + 15) / 16 + G - 1) / G;   // this warp's D column blocks when it drains D
-        uint32_t it = 0, j = 0;
-        bool ok = true;
-        for (uint32_t ui = 0; ok; ++ui) {
-            const int e = take_unit(ui, true, ok);
-            if (e < 0) break;
-            const int bk = e & 1;
-            const BankLists &L = args.lists[bk];
-            const int goff = bank_offset(L, bk, args.P);
-            int a, mt, c0, c1;
-            unit_pos(e >> 1, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
-            const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
-            for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
-                const int nn = min(NMAX, n - n0);
-                int rs[NB];
-                float re[NB];
-                if (C::kEpi == 0) load_meta<NB>(L, args, group, G, nn, p0 + n0, goff + p0 + n0, lane, rs, re);
-                for (int c = c0; c < c1; ++c, ++it) {
-                    if (G > 1 && (int)(it % G) != group) continue;   // another group's chunk
-                    const int st = it % S;
-                    if (!wait_warp<SUSP>(bar(FULL + st), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
-                    const uint8_t *a_st = sA + st * kChunkBytes;
-                    const int abuf = it % NA;
-                    const uint4 q0 = *(const uint4 *)(a_st + m * 16);
-                    const uint4 q1 = *(const uint4 *)(a_st + 2048 + m * 16);
-                    const uint32_t sc = *(const uint16_t *)(a_st + kChunkQBytes + 2 * m);
-                    uint32_t r[16];
-                    unpack_word(q0.x, r[0], r[1]);
-                    unpack_word(q0.y, r[2], r[3]);
-                    unpack_word(q0.z, r[4], r[5]);
-                    unpack_word(q0.w, r[6], r[7]);
-                    unpack_word(q1.x, r[8], r[9]);
-                    unpack_word(q1.y, r[10], r[11]);
-                    unpack_word(q1.z, r[12], r[13]);
-                    unpack_word(q1.w, r[14], r[15]);
-                    // the slot's previous chunk (it - NA) must have been consumed
-                    if (it >= (uint32_t)NA && !wait_warp<SUSP>(bar(DONE + (it - NA) % S), ((it - NA) / S) & 1,
-                                                               abort_flag, args.status)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tmem_st16(tmem + lane_base + C::kACol + abuf * 32, r);
-                    // the chunk's two K blocks' scales in bytes 0 and 1 of this quarter's column
-                    ptx::tmem_st1(tmem + lane_base + C::kSfaCol + abuf * 32 + quarter, sc);
-                    ptx::tmem_wait_st();
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(bar(AREADY + abuf));
-                }
-                if (!ok) break;
-                if (C::kEpi == 0) {
-                    if (!wait_warp<SUSP>(bar(ACCREADY), j & 1, abort_flag, args.status)) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    epilogue_cols<PHASE, NB, C::kStack, C::kSplit, C::kRowQ>(args, tmem + lane_base + C::kDCol, group, G, nn,
-                                                        goff + p0 + n0, mt, quarter, lane, rs, re);
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(bar(ACCFREE));
-                }
-            }
-        }
-    } else if (C::kEpi && warp < DQ + C::kEpi) {
+    if (warp < 4) {
         // -------------------------------------------------------- epilogue
-        const int quarter = warp & 3;
+        const int quarter = warp;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         constexpr int NB = (NMAX + 15) / 16;
         uint32_t j = 0;
@@ -468,8 +407,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
             const int bk = e & 1;
             const BankLists &L = args.lists[bk];
             const int goff = bank_offset(L, bk, args.P);
-            int a, mt, c0, c1;
-            unit_pos(e >> 1, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
+            int a, mt, s0, s1;
+            unit_pos(e >> 1, part.tiles, ns, args.ks, a, mt, s0, s1);
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
@@ -479,13 +418,13 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                 const int db = j % DB;
                 if (!wait_warp<SUSP>(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status)) { ok = false; break; }
                 ptx::tc_fence_after();
-                epilogue_cols<PHASE, NB, C::kStack, C::kSplit, C::kRowQ>(args, tmem + lane_base + C::kDCol + db * C::kDW, 0, 1, nn,
-                                                    goff + p0 + n0, mt, quarter, lane, rs, re);
+                epilogue_cols<PHASE, NB, C::kStack, C::kSplit, C::kRowQ>(args, tmem + lane_base + C::kDCol + db * C::kDW, 0, 1,
+                                                                        nn, goff + p0 + n0, mt, quarter, lane, rs, re);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(ACCFREE + db));
             }
         }
-    } else if (warp == PROD) {
+    } else if (warp == C::kProducer && lane == 0) {
         // ------------------------------------------------------------ producer
         // A launch over both banks prefers, in the first CTA that reaches each
         // SM, the cold bank's units (one host-link streamer per SM) and in the
@@ -493,94 +432,75 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
         // its own is empty.
         int pref = args.b;
         if (args.b < 0) {
-            if (lane == 0) {
-                uint32_t smid;
-                asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-                pref = atomicAdd(&args.claim[smid & 1023u], 1) == 0 ? MOE_BANK_COLD : MOE_BANK_HOT;
-            }
-            pref = __shfl_sync(0xffffffffu, pref, 0);
+            uint32_t smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            pref = atomicAdd(&args.claim[smid & 1023u], 1) == 0 ? MOE_BANK_COLD : MOE_BANK_HOT;
         }
-        bool dry_pref = false, dry_other = args.b >= 0;   // lane 0's view of the queues
+        bool dry_pref = false, dry_other = args.b >= 0;
         uint32_t it = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
             // take the next unit from the launch's work counter and publish it
             const int qs = ui % kQ;
             if (ui >= (uint32_t)kQ &&
-                !wait_warp<SUSP>(bar(UQEMPTY + qs), ((ui / kQ) - 1) & 1, abort_flag, args.status)) {
+                !wait_one<SUSP>(bar(UQEMPTY + qs), ((ui / kQ) - 1) & 1, abort_flag, args.status)) {
                 ok = false;
                 break;
             }
             int e = -1;
-            if (lane == 0) {
-                if (!dry_pref) {
-                    const int u = atomicAdd(&args.sched[2 * pref + PHASE - 1], 1);
-                    if (u < units_of(pref)) e = 2 * u + pref;
-                    else dry_pref = true;
-                }
-                if (e < 0 && !dry_other) {
-                    const int u = atomicAdd(&args.sched[2 * (1 - pref) + PHASE - 1], 1);
-                    if (u < units_of(1 - pref)) e = 2 * u + (1 - pref);
-                    else dry_other = true;
-                }
-                uq[qs] = e;
-                ptx::mbar_arrive(bar(UQFULL + qs));
+            if (!dry_pref) {
+                const int u = atomicAdd(&args.sched[2 * pref + PHASE - 1], 1);
+                if (u < units_of(pref)) e = 2 * u + pref;
+                else dry_pref = true;
             }
-            e = __shfl_sync(0xffffffffu, e, 0);
+            if (e < 0 && !dry_other) {
+                const int u = atomicAdd(&args.sched[2 * (1 - pref) + PHASE - 1], 1);
+                if (u < units_of(1 - pref)) e = 2 * u + (1 - pref);
+                else dry_other = true;
+            }
+            uq[qs] = e;
+            ptx::mbar_arrive(bar(UQFULL + qs));
             if (e < 0) break;
             const int bk = e & 1;
             const BankLists &L = args.lists[bk];
             const int goff = bank_offset(L, bk, args.P);
-            int a, mt, c0, c1;
-            unit_pos(e >> 1, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
+            int a, mt, s0, s1;
+            unit_pos(e >> 1, part.tiles, ns, args.ks, a, mt, s0, s1);
             const int row = L.act_row[a];
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
-            const uint8_t *tile = args.bank[bk] + (int64_t)row * args.eb + args.part_off +
-                                  (int64_t)mt * kc * kChunkBytes;
+            const CUtensorMap *tmA = bk ? &tmA1 : &tmA0;
+            const uint8_t *expert = args.bank[bk] + (int64_t)row * args.eb;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX) {
-                const int nn = min(NMAX, n - n0);
-                const int nbox = (nn + C::kBoxRows - 1) / C::kBoxRows;
                 const int brow = goff + p0 + n0;
-                for (int c = c0; c < c1; ++c, ++it) {
+                for (int s = s0; s < s1; ++s, ++it) {
                     const int st = it % S;
                     const uint32_t rnd = it / S;
-                    if (rnd > 0 && !wait_warp<SUSP>(bar(DONE + st), (rnd - 1) & 1, abort_flag, args.status)) {
+                    if (rnd > 0 && !wait_one<SUSP>(bar(DONE + st), (rnd - 1) & 1, abort_flag, args.status)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t a_addr = ptx::smem_addr(sA + st * kChunkBytes);
-                    const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage);
-                    const uint8_t *src_chunk = tile + (int64_t)c * kChunkBytes;
-                    if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(bar(FULL + st),
-                                                   (uint32_t)kChunkBytes + (C::kStack ? 2 : 1) * nbox * C::kBoxBytes);
-                        // one bulk copy per weight chunk, from HBM or, for the cold
-                        // bank, from the mapped host bank over the host link
-                        ptx::bulk_g2s(a_addr, src_chunk, kChunkBytes, bar(FULL + st));
-                        for (int q = 0; q < nbox; ++q)
-                            ptx::tma_load_2d(b_addr + q * C::kBoxBytes, &tmap, c * 128, brow + q * C::kBoxRows,
-                                             bar(FULL + st));
-                        // stacked: the same rows again, 64 bytes further, so the
-                        // second piece starts each row (rows nbox*16 ...; the last
-                        // chunk's box reads past the row end: zero fill, unused)
-                        if (C::kStack)
-                            for (int q = 0; q < nbox; ++q)
-                                ptx::tma_load_2d(b_addr + (nbox + q) * C::kBoxBytes, &tmap, c * 128 + 64,
-                                                 brow + q * C::kBoxRows, bar(FULL + st));
-                    }
-                    __syncwarp();
+                    int slot, tidx, kb0, nkb;
+                    part.group(mt, s, slot, tidx, kb0, nkb);
+                    // the code block counts its packed (global) bytes; the token-row
+                    // box counts in full (a half group's second chunk is past the
+                    // rows' end: zero fill, unused)
+                    ptx::mbar_arrive_expect_tx(bar(FULL + st), (uint32_t)(kGroupQBytes + kSfAtomBytes + C::kBStage));
+                    ptx::tma_load_5d(ptx::smem_addr(sA + st * C::kAStage), tmA, 0, 0, slot, tidx, row, bar(FULL + st));
+                    ptx::bulk_g2s(ptx::smem_addr(sSF + st * kSfAtomBytes), expert + part.group_off(slot, tidx) + kGroupQBytes,
+                                  kSfAtomBytes, bar(FULL + st));
+                    ptx::tma_load_4d(ptx::smem_addr(sB + st * C::kBStage), &tmB, 0, brow, 0, 2 * s, bar(FULL + st));
                 }
             }
         }
         if (!ok) {
-            // let the copies this warp issued land before the CTA goes away
+            // let the copies this thread issued land before the CTA goes away
             const uint32_t first = it > (uint32_t)S ? it - S : 0u;
             for (uint32_t i = first; i < it; ++i) {
                 for (uint32_t t = 0; t < kWaitLimit; ++t)
                     if (ptx::mbar_try_wait(bar(FULL + i % S), (i / S) & 1)) break;
             }
         }
-    } else if (warp == MMAW && lane == 0) {
+    } else if (warp == C::kMmaWarp && lane == 0) {
         // ----------------------------------------------------------- MMA issue
         uint32_t it = 0, j = 0;
         bool ok = true;
@@ -588,15 +508,14 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
             const int e = take_unit(ui, false, ok);
             if (e < 0) break;
             const BankLists &L = args.lists[e & 1];
-            int a, mt, c0, c1;
-            unit_pos(e >> 1, args.mt_count, kc, C::kSplit, a, mt, c0, c1);
+            int a, mt, s0, s1;
+            unit_pos(e >> 1, part.tiles, ns, args.ks, a, mt, s0, s1);
             const int n = L.act_off[a + 1] - L.act_off[a];
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
                 const int Nr = (nn + C::kRowQ - 1) / C::kRowQ * C::kRowQ;
-                const int Nm = C::kStack ? 2 * Nr : Nr;                              // B rows of one MMA
-                const uint32_t idesc0 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 0, 0);   // K block 0 of the chunk
-                const uint32_t idesc1 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 1, 0);   // K block 1
+                const int Nm = C::kStack ? 2 * Nr : Nr;   // B rows of one MMA
+                const uint32_t idesc0 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 0, 0);   // | (K block << 29): A scale byte
                 const int db = j % DB;
                 if (j >= (uint32_t)DB &&
                     !wait_one<SUSP>(bar(ACCFREE + db), ((j / DB) - 1) & 1, abort_flag, args.status)) {
@@ -605,20 +524,34 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + C::kDCol + db * C::kDW;
-                for (int c = c0; c < c1; ++c, ++it) {
-                    const int st = it % S, abuf = it % NA;
-                    if (!wait_one<SUSP>(bar(AREADY + abuf), (it / NA) & 1, abort_flag, args.status)) { ok = false; break; }
+                for (int s = s0; s < s1; ++s, ++it) {
+                    const int st = it % S;
+                    if (!wait_one<SUSP>(bar(FULL + st), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage);
-                    const uint32_t a_tm = tmem + C::kACol + abuf * 32;
-                    const uint32_t sfa = tmem + C::kSfaCol + abuf * 32;
+                    int slot, tidx, kb0, nkb;
+                    part.group(mt, s, slot, tidx, kb0, nkb);
+                    // the group's scales -> slot it % NSF, once the MMAs of iteration
+                    // it - NSF (the slot's last reader) have completed
+                    if (it >= (uint32_t)NSF) {
+                        const uint32_t prev = it - NSF;
+                        if (!wait_one<SUSP>(bar(DONE + prev % S), (prev / S) & 1, abort_flag, args.status)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    const uint32_t sfa = tmem + 32u * (it % NSF);
+                    ptx::tmem_cp_32x128b_warpx4(sfa, ptx::smem_desc_noswizzle(ptx::smem_addr(sSF + st * kSfAtomBytes), 128, 128));
+                    const uint32_t a_addr = ptx::smem_addr(sA + st * C::kAStage);
+                    for (int i = 0; i < nkb; ++i) {
+                        const int kb = kb0 + i;   // K block of the group (A bytes kb*32.., scale byte kb)
+                        const uint64_t ad = ptx::smem_desc_sw128(a_addr + kb * 32);
+                        // this tile's chunk i/2 of the group, its K block i%2
+                        const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage + (i >> 1) * C::kBChunk) + (i & 1) * 32;
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-                        for (int pc = 0; pc < (C::kStack ? 1 : 2); ++pc) {   // e4m3 piece of B (wide tiles)
-                            const uint64_t bd = ptx::smem_desc_sw128(b_addr + pc * 64 + kk * 32);
-                            ptx::mma_mxf8f6f4_ts(d_tmem, a_tm + kk * 8, bd, kk ? idesc1 : idesc0, sfa,
-                                                 tmem + C::kSfbCol + pc * C::kSfbStride, (c != c0) | kk | pc);
+                        for (int pc = 0; pc < (C::kStack ? 1 : 2); ++pc) {   // e4m3 piece of B (unstacked tiles)
+                            const uint64_t bd = ptx::smem_desc_sw64(b_addr + pc * NMAX * 64);
+                            ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29), sfa, tmem + C::kSfbCol + pc * C::kSfbStride,
+                                                 (s != s0) | i | pc);
                         }
                     }
                     ptx::mma_commit(bar(DONE + st));
@@ -637,7 +570,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kPerSm) ff
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == MMAW) {
+    if (warp == C::kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::kCols);
     }
@@ -826,78 +759,118 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Tensor map over the [rows][K/64][128 B] piece records of K-element rows:
-// boxes of box_rows rows x one 128-byte record, 128-byte swizzle, zero fill
-// past the last row.
-int make_row_map(CUtensorMap *map, const void *base, int K, int rows, int box_rows) {
+// Tensor map over the [rows][K/64][2 pieces][64 B] records of K-element
+// rows, viewed as (byte, row, piece, chunk): a box of box_rows rows x both
+// pieces x two chunks lands as [chunk][piece][row][64 B], 64-byte swizzle,
+// zero fill past the last row or chunk.
+int make_piece_map(CUtensorMap *map, const void *base, int K, int rows, int box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled unavailable");
-    cuuint64_t dims[2] = {(cuuint64_t)K * 2, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    cuuint64_t dims[4] = {64, (cuuint64_t)rows, 2, (cuuint64_t)K / 64};
+    cuuint64_t strides[3] = {(cuuint64_t)K * 2, 64, 128};
+    cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, 2, 2};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
     return MOE_OK;
 }
 
 template <int NMAX, int PHASE, int BANKS>
-int launch_one(const CUtensorMap &map, const TcArgs &args, int blocks, cudaStream_t s) {
+int launch_one(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap &mA1, const TcArgs &args, int blocks,
+               cudaStream_t s) {
     using C = TcCfg<NMAX>;
     auto kern = ffn_tc_kernel<NMAX, PHASE, BANKS>;
-    MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem));
+    const size_t smem = C::smem_bytes(args.S);
+    MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     if (blocks < 1) return MOE_OK;
-    kern<<<blocks, C::kThreads, C::kSmem, s>>>(map, args);
+    kern<<<blocks, C::kThreads, smem, s>>>(mB, mA0, mA1, args);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
-// Grid of one GEMM launch.  Units are handed out dynamically, so the grid
-// only sets how many CTAs stream at once.  A launch over both banks fills
-// every SM with kPerSm CTAs.  One-bank launches: the host link needs a few
-// MB in flight, so a cold-bank launch of narrow tiles takes one CTA per SM;
-// when the layer also has a hot bank, the hot launch takes the SM's other
-// slots, so two concurrent one-bank launches fit.
+constexpr size_t kSmSmem = 228u * 1024u;   // shared memory of one SM
+constexpr size_t kCtaReserve = 1024;       // reserved by the system per resident CTA
+
+struct LaunchPlan {
+    int blocks, S;
+};
+
+// Grid and ring depth of one GEMM launch.  Units are handed out dynamically,
+// so the grid only sets how many CTAs stream at once, and the ring is as deep
+// as the SM's shared memory allows for the CTAs that share it:
+//   - a cold-bank launch of narrow tiles: one CTA per SM with a short ring
+//     (the host link needs only a few KB in flight per SM);
+//   - a hot-bank launch: two CTAs per SM, sharing what the cold CTA leaves
+//     when the layer has both banks (the two launches run side by side);
+//   - a launch over both banks: three CTAs per SM;
+//   - prefill tiles: one CTA per SM (32 SMs' worth for a cold bank).
 template <int NMAX>
-int grid_for(const moe_ctx *ctx, int b, bool shared, int units_max) {
-    const int per_sm = TcCfg<NMAX>::kPerSm;   // shared memory, registers and TMEM all fit
-    const int cold_ctas = per_sm > 1 ? ctx->sms : 32;
-    int blocks;
-    if (b < 0) blocks = ctx->sms * per_sm;
-    else if (b == MOE_BANK_COLD) blocks = cold_ctas;
-    else if (!shared) blocks = ctx->sms * per_sm;
-    else if (per_sm > 1) blocks = ctx->sms * (per_sm - 1);
-    else blocks = ctx->sms - cold_ctas;
-    return std::max(1, std::min(units_max, blocks));
+LaunchPlan plan_for(const moe_ctx *ctx, int b, bool shared, int units_max) {
+    using C = TcCfg<NMAX>;
+    auto fit = [](size_t budget, int ctas) {
+        const long per = (long)(budget / ctas) - (long)kCtaReserve - (long)C::kFixedSmem;
+        return std::max(C::kNsf, std::min(kMaxStages, (int)(per / C::kStageBytes)));
+    };
+    const int cold_S = std::max(2, C::kNsf);
+    const size_t cold_bytes = kCtaReserve + C::smem_bytes(cold_S);
+    LaunchPlan p;
+    if (C::kWide) {
+        const int cold_ctas = 32;
+        p.S = fit(kSmSmem, 1);
+        if (b < 0 || !shared) p.blocks = ctx->sms;
+        else p.blocks = b == MOE_BANK_COLD ? cold_ctas : ctx->sms - cold_ctas;
+    } else if (b < 0) {
+        p.blocks = 3 * ctx->sms;
+        p.S = fit(kSmSmem, 3);
+    } else if (b == MOE_BANK_COLD) {
+        p.blocks = ctx->sms;
+        p.S = cold_S;
+    } else {
+        p.blocks = 2 * ctx->sms;
+        p.S = fit(shared ? kSmSmem - cold_bytes : kSmSmem, 2);
+        // beside a cold bank, a third hot CTA must not fit on an SM (it would
+        // take the cold streamer's place there)
+        while (shared && p.S < kMaxStages && 3 * (kCtaReserve + C::smem_bytes(p.S)) <= kSmSmem) ++p.S;
+    }
+    static_assert(C::kWide || C::kPerSmMax >= 3, "narrow tiles run up to three CTAs per SM");
+    p.blocks = std::max(1, std::min(units_max, p.blocks));
+    return p;
 }
 
 template <int NMAX, int PHASE>
-int launch_gemm(const CUtensorMap &map, const TcArgs &a, int blocks, cudaStream_t s) {
-    if (a.b < 0) return launch_one<NMAX, PHASE, 2>(map, a, blocks, s);
-    if (a.b == MOE_BANK_COLD) return launch_one<NMAX, PHASE, 1>(map, a, blocks, s);
-    return launch_one<NMAX, PHASE, 0>(map, a, blocks, s);
+int launch_gemm(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap &mA1, const TcArgs &a, int blocks,
+                cudaStream_t s) {
+    if (a.b < 0) return launch_one<NMAX, PHASE, 2>(mB, mA0, mA1, a, blocks, s);
+    if (a.b == MOE_BANK_COLD) return launch_one<NMAX, PHASE, 1>(mB, mA0, mA1, a, blocks, s);
+    return launch_one<NMAX, PHASE, 0>(mB, mA0, mA1, a, blocks, s);
 }
 
 template <int NMAX>
-int launch_bank(moe_ctx *ctx, bool shared, const TcArgs &a1, const TcArgs &a2, int units1, int units2,
+int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs a2, int units1, int units2,
                 const uint16_t *x, const WsLayout &lay, uint8_t *ws, cudaStream_t s) {
     const Geom &g = ctx->g;
     const int P = a1.P;
+    // K parts per unit: two halves for narrow tiles, unless the tile has a
+    // single K group
+    a1.ks = std::min(TcCfg<NMAX>::kSplit, a1.part.steps());
+    a2.ks = std::min(TcCfg<NMAX>::kSplit, a2.part.steps());
+    const LaunchPlan p1 = plan_for<NMAX>(ctx, a1.b, shared, units1), p2 = plan_for<NMAX>(ctx, a1.b, shared, units2);
+    a1.S = p1.S;
+    a2.S = p2.S;
     const dim3 grid_p(P, a1.b < 0 ? 2 : 1);   // one block per pick (of each bank)
     CUtensorMap m1, m2;
-    if (int r = make_row_map(&m1, ws + lay.xq, g.H, P, TcCfg<NMAX>::kBoxRows)) return r;
-    if (int r = make_row_map(&m2, ws + lay.hq, g.I, P, TcCfg<NMAX>::kBoxRows)) return r;
+    if (int r = make_piece_map(&m1, ws + lay.xq, g.H, P, NMAX)) return r;
+    if (int r = make_piece_map(&m2, ws + lay.hq, g.I, P, NMAX)) return r;
     prep_x_kernel<<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
                                          (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
     MOE_LAUNCH_CHECK();
-    const int b1 = grid_for<NMAX>(ctx, a1.b, shared, units1), b2 = grid_for<NMAX>(ctx, a1.b, shared, units2);
-    if (int r = launch_gemm<NMAX, 1>(m1, a1, b1, s)) return r;
+    if (int r = launch_gemm<NMAX, 1>(m1, layer.wmap[0][0], layer.wmap[1][0], a1, p1.blocks, s)) return r;
     prep_h_kernel<<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
                                          a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H, a1.claim);
     MOE_LAUNCH_CHECK();
-    if (int r = launch_gemm<NMAX, 2>(m2, a2, b2, s)) return r;
+    if (int r = launch_gemm<NMAX, 2>(m2, layer.wmap[0][1], layer.wmap[1][1], a2, p2.blocks, s)) return r;
     if (!a2.y_out) return MOE_OK;
     round_y_kernel<<<grid_p, 256, 0, s>>>(a2.lists[0], a2.lists[1], a2.b, g.H, a2.y_out, a2.Y);
     MOE_LAUNCH_CHECK();
@@ -906,15 +879,35 @@ int launch_bank(moe_ctx *ctx, bool shared, const TcArgs &a1, const TcArgs &a2, i
 
 }  // namespace
 
-int launch_ffn_tc(moe_ctx *ctx, const uint8_t *hot, const uint8_t *cold, int b, const uint16_t *x, int T,
-                  uint8_t *ws, uint16_t *Y, cudaStream_t s, bool shared) {
+int make_weight_map(CUtensorMap *map, const uint8_t *bank, const Geom &g, const PartLayout &part, int rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled unavailable");
+    // (code, row, slot, tile index, expert): 128 4-bit codes of a row, the
+    // block's 128 rows of 64 bytes, the groups of a tile (or tile pair), the
+    // tiles, the bank's experts
+    cuuint64_t dims[5] = {(cuuint64_t)kKG, (cuuint64_t)kMT, (cuuint64_t)part.slots(), (cuuint64_t)part.tile_index_count(),
+                          (cuuint64_t)rows};
+    cuuint64_t strides[4] = {(cuuint64_t)kKG / 2, (cuuint64_t)kGroupBytes, (cuuint64_t)part.tile_stride, (cuuint64_t)g.eb};
+    cuuint32_t box[5] = {(cuuint32_t)kKG, (cuuint32_t)kMT, 1, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 5, const_cast<uint8_t *>(bank + part.off), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled (weights) failed: " + std::to_string((int)r));
+    return MOE_OK;
+}
+
+int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int b, const uint16_t *x, int T, uint8_t *ws, uint16_t *Y,
+                  cudaStream_t s) {
     const Geom &g = ctx->g;
     WsLayout lay = ws_layout(g, T);
     const int P = T * g.k;
+    const bool shared = layer.n_hot > 0 && layer.n_cold > 0;
 
     TcArgs a1{};
-    a1.bank[MOE_BANK_HOT] = hot;
-    a1.bank[MOE_BANK_COLD] = cold;
+    a1.bank[MOE_BANK_HOT] = layer.hot;
+    a1.bank[MOE_BANK_COLD] = layer.cold_dev;
     for (int bk = 0; bk < 2; ++bk) {
         BankLists &L = a1.lists[bk];
         L.hdr = (const int32_t *)(ws + lay.hdr);
@@ -923,9 +916,7 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *hot, const uint8_t *cold, int b, 
         L.picks = (const int32_t *)(ws + lay.picks) + (size_t)bk * P;
     }
     a1.eb = g.eb;
-    a1.part_off = 0;
-    a1.mt_count = g.mt13;
-    a1.kc = g.kc13;
+    a1.part = g.w13;
     a1.b = b == MOE_BANK_BOTH ? -1 : b;
     a1.k = g.k;
     a1.H = g.H;
@@ -939,13 +930,11 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *hot, const uint8_t *cold, int b, 
     // the hot bank's concurrent launches never read them)
     a1.claim = (a1.b < 0 || a1.b == MOE_BANK_COLD) ? (int32_t *)(ws + lay.claim) : nullptr;
     TcArgs a2 = a1;
-    a2.part_off = g.w2_off;
-    a2.mt_count = g.mt2;
-    a2.kc = g.kc2;
+    a2.part = g.w2;
     a2.bexp = (const int32_t *)(ws + lay.hexp);
     a2.h_out = nullptr;
     a2.Y = Y;
-    // narrow-tile steps: two K halves per unit, summed in fp32 rows
+    // narrow-tile steps: K parts per unit, summed in fp32 rows
     const bool split = split_k_steps(T);
     a1.gu_out = split ? (float *)(ws + lay.gu32) : nullptr;
     a1.y_out = nullptr;
@@ -954,14 +943,14 @@ int launch_ffn_tc(moe_ctx *ctx, const uint8_t *hot, const uint8_t *cold, int b, 
 
     const int units1 = 4 * P * g.mt13, units2 = 4 * P * g.mt2;   // bound: active rows never exceed the picks
     // The token-tile width depends only on T, so an expert's arithmetic is
-    // the same in either bank.  Decode-sized steps use narrow tiles with
-    // several CTAs per SM (an expert with more tokens than the tile loops over
-    // token tiles); prefill-sized steps use 192-wide tiles (an expert's
-    // ~T*k/E tokens in one tile), one CTA per SM.
-    if (T <= 8) return launch_bank<8>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
-    if (T <= 16) return launch_bank<16>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
-    if (T <= kNarrowMaxT) return launch_bank<64>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
-    return launch_bank<192>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
+    // the same in either bank.  Decode-sized steps use narrow tiles (8, 16 or
+    // 32 tokens) with several CTAs per SM (an expert with more tokens than the
+    // tile loops over token tiles); prefill-sized steps use 192-wide tiles (an
+    // expert's ~T*k/E tokens in one tile), one CTA per SM.
+    if (T <= 8) return launch_bank<8>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= 16) return launch_bank<16>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= kNarrowMaxT) return launch_bank<32>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
+    return launch_bank<192>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
 }
 
 }  // namespace moe

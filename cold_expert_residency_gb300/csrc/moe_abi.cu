@@ -56,52 +56,42 @@ __global__ void touch_host_bank_kernel(const uint8_t *__restrict__ p, size_t byt
     if (acc == 0x9E3779B9u && sink) *sink = acc;   // keeps the reads; almost never taken
 }
 
-// One MX block's 16 logical bytes (element 2i in the low nibble of byte i)
-// -> the device order of moe_internal.cuh (word j, byte i: elements 8j+i and
-// 8j+4+i).
-static void reorder_block(const uint8_t *q, uint8_t *o) {
-    auto code = [&](int e) { return (q[e >> 1] >> (4 * (e & 1))) & 0xF; };
-    for (int j = 0; j < 4; ++j)
-        for (int i = 0; i < 4; ++i) o[4 * j + i] = (uint8_t)(code(8 * j + i) | (code(8 * j + 4 + i) << 4));
+// Logical MXFP4 expert -> tiled device layout (see moe_internal.cuh).
+// q: [rows][K/2] codes, sc: [rows][K/32] e8m0 scales of one part; row_of(mt,
+// m) names the logical row held by tile row m.  Every byte of the part is
+// written.  Returns false if a scale byte lies outside [104, 140].
+template <class RowOf>
+static bool repack_part(const PartLayout &part, int K, const uint8_t *q, const uint8_t *sc, RowOf row_of, uint8_t *dst) {
+    bool ok = true;
+    for (int mt = 0; mt < part.tiles; ++mt) {
+        for (int s = 0; s < part.steps(); ++s) {
+            int slot, tidx, kb0, nkb;
+            part.group(mt, s, slot, tidx, kb0, nkb);
+            uint8_t *grp = dst + part.group_off(slot, tidx);
+            for (int m = 0; m < kMT; ++m) {
+                const int64_t row = row_of(mt, m);
+                for (int i = 0; i < nkb; ++i) {
+                    const int kb = kb0 + i, blk = 4 * s + i;   // the group's K block, the row's 32-element block
+                    std::memcpy(grp + m * 64 + kb * 16, q + row * (K / 2) + blk * 16, 16);
+                    const uint8_t e = sc[row * (K / 32) + blk];
+                    grp[kGroupQBytes + (m % 32) * 16 + 4 * (m / 32) + kb] = e;
+                    ok &= e >= 104 && e <= 140;
+                }
+            }
+        }
+    }
+    return ok;
 }
 
-// Logical MXFP4 expert -> tiled device layout (see moe_internal.cuh).
-// Returns false if a scale byte lies outside [104, 140].
 static bool repack_expert(const Geom &g, const uint8_t *w13_q, const uint8_t *w13_s,
                           const uint8_t *w2_q, const uint8_t *w2_s, uint8_t *dst) {
-    const int H = g.H, I = g.I;
-    bool ok = true;
-    for (int mt = 0; mt < g.mt13; ++mt) {
-        for (int c = 0; c < g.kc13; ++c) {
-            uint8_t *chunk = dst + ((int64_t)mt * g.kc13 + c) * kChunkBytes;
-            for (int m = 0; m < kMT; ++m) {
-                int w = m / 32, l = m % 32;
-                int64_t row = (l < 16 ? 0 : I) + 64 * mt + 16 * w + (l % 16);
-                const uint8_t *q = w13_q + row * (H / 2) + c * 32;
-                reorder_block(q, chunk + m * 16);
-                reorder_block(q + 16, chunk + 2048 + m * 16);
-                const uint8_t *s = w13_s + row * (H / 32) + 2 * c;
-                chunk[kChunkQBytes + 2 * m] = s[0];
-                chunk[kChunkQBytes + 2 * m + 1] = s[1];
-                ok &= s[0] >= 104 && s[0] <= 140 && s[1] >= 104 && s[1] <= 140;
-            }
-        }
-    }
-    for (int mt = 0; mt < g.mt2; ++mt) {
-        for (int c = 0; c < g.kc2; ++c) {
-            uint8_t *chunk = dst + g.w2_off + ((int64_t)mt * g.kc2 + c) * kChunkBytes;
-            for (int m = 0; m < kMT; ++m) {
-                int64_t row = (int64_t)kMT * mt + m;
-                const uint8_t *q = w2_q + row * (I / 2) + c * 32;
-                reorder_block(q, chunk + m * 16);
-                reorder_block(q + 16, chunk + 2048 + m * 16);
-                const uint8_t *s = w2_s + row * (I / 32) + 2 * c;
-                chunk[kChunkQBytes + 2 * m] = s[0];
-                chunk[kChunkQBytes + 2 * m + 1] = s[1];
-                ok &= s[0] >= 104 && s[0] <= 140 && s[1] >= 104 && s[1] <= 140;
-            }
-        }
-    }
+    const int I = g.I;
+    std::memset(dst, 0, (size_t)g.eb);
+    bool ok = repack_part(g.w13, g.H, w13_q, w13_s, [&](int mt, int m) {
+        const int w = m / 32, l = m % 32;
+        return (int64_t)(l < 16 ? 0 : I) + 64 * mt + 16 * w + (l % 16);
+    }, dst);
+    ok &= repack_part(g.w2, g.I, w2_q, w2_s, [&](int mt, int m) { return (int64_t)kMT * mt + m; }, dst);
     return ok;
 }
 
@@ -195,9 +185,10 @@ int moe_create(const moe_geom *geom, int device, moe_ctx **out) {
     const moe_geom &g = *geom;
     if (g.layers < 1 || g.experts < 2 || g.experts > 1024 || g.top_k < 1 || g.top_k > 16 ||
         g.top_k > g.experts || g.hidden < 128 || g.hidden % 128 || g.inter < 64 || g.inter % 64 ||
+        (g.hidden % 256 && g.inter % 128) ||
         g.max_tokens < 1 || g.count_tmax < 0)
         return set_error(MOE_EINVAL, "invalid geometry (need E in 2..1024, k in 1..min(16,E), "
-                                     "H % 128 == 0, I % 64 == 0, T_max >= 1)");
+                                     "H % 128 == 0, I % 64 == 0, H % 256 == 0 or I % 128 == 0, T_max >= 1)");
     if ((int64_t)g.max_tokens * g.top_k > (1 << 24))
         return set_error(MOE_EINVAL, "max_tokens * top_k too large");
     int ndev = 0;
@@ -321,6 +312,20 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
         free_layer(nl);
         return set_error(MOE_EINVAL, "e8m0 scale byte outside [104, 140]");
     }
+    // tensor maps of each bank's code blocks, fixed for the banks' lifetime
+    // (swaps move rows, never the banks)
+    std::memset(nl.wmap, 0, sizeof(nl.wmap));
+    for (int bk = 0; bk < 2; ++bk) {
+        const int rows = bk == MOE_BANK_HOT ? nl.n_hot : nl.n_cold;
+        const uint8_t *base = bk == MOE_BANK_HOT ? nl.hot : nl.cold_dev;
+        if (!rows) continue;
+        int r = make_weight_map(&nl.wmap[bk][0], base, g, g.w13, rows);
+        if (r == MOE_OK) r = make_weight_map(&nl.wmap[bk][1], base, g, g.w2, rows);
+        if (r != MOE_OK) {
+            free_layer(nl);
+            return r;
+        }
+    }
     nl.rowmap = std::move(rowmap);
     nl.init = true;
     L = std::move(nl);
@@ -397,7 +402,7 @@ int moe_expert_ffn_bank(moe_ctx *ctx, int layer, int bank, const uint16_t *x, in
         }
         return MOE_OK;
     }
-    return launch_ffn_tc(ctx, L.hot, L.cold_dev, bank, x, T, (uint8_t *)ws, Y, s, L.n_hot > 0 && L.n_cold > 0);
+    return launch_ffn_tc(ctx, L, bank, x, T, (uint8_t *)ws, Y, s);
 }
 
 int moe_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_t *out, void *stream) {

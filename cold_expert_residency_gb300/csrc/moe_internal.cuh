@@ -3,6 +3,7 @@
 // launch helpers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -19,49 +20,92 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Device layout of one expert ("tiled MXFP4")
 //
-// Both GEMMs of an expert are cut into M-tiles of 128 weight rows and K-chunks
-// of 64 elements.  One (M-tile, K-chunk) is stored contiguously as
-//     [half h = 0,1][row m = 0..127][16 bytes]   (4096 B: 32 e2m1 codes per
-//                                                  16 B, i.e. one MX block)
-//     [row m][2 scale bytes]                      (256 B: the row's two e8m0
-//                                                  scales of this chunk)
-// Inside a half, 32-bit word j (bytes 4j..4j+3) holds the block's elements
-// 8j..8j+7: byte i carries element 8j+i in its low nibble and element
-// 8j+4+i in its high nibble.  Two masked shifts of the word then give the
-// one-code-per-byte form the tensor cores read from tensor memory.
-// = 4352 bytes, exactly the logical bytes of those 128 x 64 elements.  Chunks
-// of a tile follow in K order, tiles in M order; the W13 tiles come first,
-// then the W2 tiles.  So the bank stores the same bytes the logical layout
-// holds (18,800,640 per expert at H=4096, I=2880), permuted so that a warp's
-// 16-byte loads are contiguous and one tile's chunk is one bulk copy.
+// Both GEMMs of an expert are cut into M-tiles of 128 weight rows and K-groups
+// of 128 elements.  One (M-tile, K-group) is stored contiguously as
+//     [row m = 0..127][64 bytes]    (8192 B: the row's 128 e2m1 codes, element
+//                                    2i in the low nibble of byte i, as in
+//                                    the logical MXFP4 rows)
+//     [512-byte scale atom]          (the e8m0 scale of row m and 32-element K
+//                                    block kb at byte (m%32)*16 + 4*(m/32) + kb)
+// = 8704 bytes.  The code block is what one tensor-TMA box of the padded 4-bit
+// type moves into shared memory in the layout the tensor cores read; the
+// scale atom is what one tensor-memory copy (32 lanes x 16 bytes, repeated in
+// all four lane quarters) puts where the block-scaled MMA reads A's scales.
 //
 // W13 M-tile mt covers gate units i = 64*mt .. 64*mt+63 and their up rows:
 // tile row m = 32*w + l (w = m/32, l = m%32) holds W13 row
 //     (l < 16 ? 0 : I) + 64*mt + 16*w + (l % 16),
 // so within a warp lane l (gate) and lane l^16 (up) hold the same unit.
 // W2 M-tile mt row m holds W2 row 128*mt + m.
+//
+// A part (W13 or W2) is a sequence of tile slots: tile t's groups in K order.
+// W2's K (= I) may end in half a group (I % 128 == 64).  Then M-tiles 2p and
+// 2p+1 are stored as a pair: tile 2p's full groups, tile 2p+1's full groups,
+// and one shared group whose K blocks 0-1 hold tile 2p's last 64 columns and
+// blocks 2-3 tile 2p+1's.  Either way an expert holds exactly its logical
+// MXFP4 bytes (18,800,640 at H=4096, I=2880), permuted.
 // ---------------------------------------------------------------------------
-constexpr int kKC = 64;                       // K elements per chunk
+constexpr int kKC = 64;                       // K elements per chunk (one token-row record)
+constexpr int kKG = 128;                      // K elements per group
 constexpr int kMT = 128;                      // weight rows per M-tile
-constexpr int kChunkQBytes = kMT * kKC / 2;   // 4096
-constexpr int kChunkBytes = kChunkQBytes + kMT * 2;  // 4352
+constexpr int kGroupQBytes = kMT * kKG / 2;   // 8192
+constexpr int kSfAtomBytes = 512;
+constexpr int kGroupBytes = kGroupQBytes + kSfAtomBytes;   // 8704
+
+struct PartLayout {
+    int64_t off;           // byte offset of the part in an expert
+    int64_t tile_stride;   // bytes per tile index (a tile, or a pair of tiles)
+    int tiles;             // M-tiles
+    int gfull;             // full K groups per tile
+    int paired;            // 1: the last K group is half, shared by tiles 2p and 2p+1
+    int kchunks;           // K / 64
+    __host__ __device__ int steps() const { return gfull + paired; }
+    __host__ __device__ int tile_index_count() const { return paired ? tiles / 2 : tiles; }
+    __host__ __device__ int slots() const { return paired ? 2 * gfull + 1 : gfull; }
+    // K step s of tile mt: its group's slot and tile index, and the first and
+    // number of the group's 32-wide K blocks that belong to this tile
+    __host__ __device__ void group(int mt, int s, int &slot, int &tidx, int &kb0, int &nkb) const {
+        if (!paired) {
+            slot = s; tidx = mt; kb0 = 0; nkb = 4;
+        } else {
+            tidx = mt >> 1;
+            if (s < gfull) { slot = (mt & 1) * gfull + s; kb0 = 0; nkb = 4; }
+            else { slot = 2 * gfull; kb0 = 2 * (mt & 1); nkb = 2; }
+        }
+    }
+    __host__ __device__ int64_t group_off(int slot, int tidx) const {
+        return off + (int64_t)tidx * tile_stride + (int64_t)slot * kGroupBytes;
+    }
+};
 
 struct Geom {
     int L, E, k, H, I, count_tmax, Tmax;
     int64_t eb;                // bytes per expert
-    int mt13, kc13;            // W13: M-tiles (I/64) and K-chunks (H/64)
-    int mt2, kc2;              // W2:  M-tiles (H/128) and K-chunks (I/64)
-    int64_t w2_off;            // byte offset of the W2 tiles in an expert
+    PartLayout w13, w2;
+    int mt13, mt2;             // M-tiles of W13 (I/64) and W2 (H/128)
+    int64_t w2_off;            // byte offset of the W2 part in an expert
 };
 
 inline Geom make_geom(const moe_geom &g) {
     Geom o;
     o.L = g.layers; o.E = g.experts; o.k = g.top_k; o.H = g.hidden; o.I = g.inter;
     o.count_tmax = g.count_tmax; o.Tmax = g.max_tokens;
-    o.mt13 = g.inter / 64; o.kc13 = g.hidden / kKC;
-    o.mt2 = g.hidden / kMT; o.kc2 = g.inter / kKC;
-    o.w2_off = (int64_t)o.mt13 * o.kc13 * kChunkBytes;
-    o.eb = o.w2_off + (int64_t)o.mt2 * o.kc2 * kChunkBytes;
+    o.mt13 = g.inter / 64;
+    o.mt2 = g.hidden / kMT;
+    o.w13.off = 0;
+    o.w13.tiles = o.mt13;
+    o.w13.gfull = g.hidden / kKG;
+    o.w13.paired = 0;
+    o.w13.kchunks = g.hidden / kKC;
+    o.w13.tile_stride = (int64_t)o.w13.gfull * kGroupBytes;
+    o.w2_off = (int64_t)o.mt13 * o.w13.tile_stride;
+    o.w2.off = o.w2_off;
+    o.w2.tiles = o.mt2;
+    o.w2.gfull = g.inter / kKG;
+    o.w2.paired = (g.inter / kKC) % 2;
+    o.w2.kchunks = g.inter / kKC;
+    o.w2.tile_stride = (int64_t)o.w2.slots() * kGroupBytes;
+    o.eb = o.w2_off + (int64_t)o.w2.tile_index_count() * o.w2.tile_stride;
     return o;
 }
 
@@ -134,6 +178,9 @@ struct Layer {
     void *cold_map = nullptr;      // the huge-page mapping holding cold_host (null: cudaHostAlloc)
     size_t cold_map_bytes = 0;
     int32_t *rowmap_dev = nullptr; // device int32[E]
+    // tensor maps of the weight code blocks: [bank][part] (part 0 = W13,
+    // 1 = W2); valid where the bank has rows
+    CUtensorMap wmap[2][2];
     std::vector<int32_t> rowmap;   // CPU copy
 };
 
@@ -178,11 +225,14 @@ int launch_route_split(moe_ctx *ctx, int layer, const float *logits, int T, int 
 int launch_ffn_simt(moe_ctx *ctx, const uint8_t *bank, int bank_id, const uint16_t *x, int T,
                     uint8_t *ws, uint16_t *Y, cudaStream_t s);
 // bank_id: MOE_BANK_HOT, MOE_BANK_COLD, or MOE_BANK_BOTH (one launch per GEMM
-// over both banks); hot/cold: the banks' device-visible bases (null if
-// unused); shared: the layer has rows in both banks (one-bank launches may
-// overlap)
-int launch_ffn_tc(moe_ctx *ctx, const uint8_t *hot, const uint8_t *cold, int bank_id, const uint16_t *x, int T,
-                  uint8_t *ws, uint16_t *Y, cudaStream_t s, bool shared);
+// over both banks); a layer with rows in both banks sizes one-bank launches so
+// that the two banks' launches can run side by side
+int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int bank_id, const uint16_t *x, int T, uint8_t *ws,
+                  uint16_t *Y, cudaStream_t s);
+// Tensor map over one part's code blocks in a bank of `rows` experts at `bank`
+// (device-visible address; 16U4_ALIGN16B boxes of 128 x 128 codes, 128-byte
+// swizzle).
+int make_weight_map(CUtensorMap *map, const uint8_t *bank, const Geom &g, const PartLayout &part, int rows);
 int launch_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_t *out,
                     cudaStream_t s);
 int launch_rowmap_write(int32_t *rowmap_dev, int32_t e0, int32_t v0, int32_t e1, int32_t v1,

@@ -64,7 +64,8 @@ typedef struct moe_geom {
     int32_t layers;      /* L: MoE layers managed by this context            */
     int32_t experts;     /* E: routed experts per layer (<= 1024)             */
     int32_t top_k;       /* k: experts per token (1..16)                      */
-    int32_t hidden;      /* H: model width, a multiple of 128                 */
+    int32_t hidden;      /* H: model width, a multiple of 128 (of 256 unless
+                            I is a multiple of 128)                         */
     int32_t inter;       /* I: expert intermediate width, a multiple of 64    */
     int32_t count_tmax;  /* count only steps with T <= count_tmax (256)       */
     int32_t max_tokens;  /* T_max: largest T any call will pass               */
@@ -95,8 +96,8 @@ int moe_set_ffn_impl(moe_ctx *ctx, int impl);
  * Inputs are HOST pointers to all E experts stacked ([E][...] each, logical
  * layout above); the library repacks them into its tiled device layout and
  * does not keep the pointers.  Re-initialising a layer frees its old banks.
- * Scale bytes must lie in [104, 140] (the range the FFN's f16 operand holds
- * exactly); other values return MOE_EINVAL.  Synchronous. */
+ * Scale bytes must lie in [104, 140] (scales 2^-23 .. 2^13); other values
+ * return MOE_EINVAL.  Synchronous. */
 int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t *w13_s,
                    const uint8_t *w2_q, const uint8_t *w2_s, const uint8_t *is_hot,
                    void *stream);

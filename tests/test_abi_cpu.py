@@ -33,7 +33,8 @@ def test_expert_bytes(lib):
 
 def test_bad_geometry_is_rejected(lib):
     bad = [dict(layers=0), dict(experts=1), dict(top_k=0), dict(top_k=17), dict(hidden=100),
-           dict(inter=96), dict(max_tokens=0), dict(experts=2000)]
+           dict(inter=96), dict(max_tokens=0), dict(experts=2000),
+           dict(hidden=384, inter=192)]   # W2 tiles odd in number and K ending in half a group
     base = dict(layers=1, experts=16, top_k=2, hidden=256, inter=128, max_tokens=8)
     for b in bad:
         kw = dict(base, **b)

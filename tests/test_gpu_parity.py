@@ -199,6 +199,30 @@ def test_token_counts_and_ragged_tiles(T):
         h.close()
 
 
+@pytest.mark.parametrize("T,impl", [(3, 0), (3, 1), (12, 0), (40, 0), (300, 0)])
+def test_half_group_geometry(T, impl):
+    """I = 192: the down GEMM's K ends in half a 128-wide K group, which
+    M-tiles 2p and 2p+1 share in the device layout.  Every tile width against
+    the oracle, and the split banks bit-identical to an all-HBM placement."""
+    cfg = synth.get_config("tiny", I=192, T=T)
+    w = synth.layer_weights(cfg, 0)
+    h = Harness(cfg, weights={0: w}, impl=impl)
+    ref = Harness(cfg, weights={0: w}, masks={0: np.ones(cfg.E, np.uint8)}, impl=impl)
+    try:
+        lg = synth.router_logits(cfg, 0, 5, T=T)
+        x = synth.activations(cfg, 0, 5, T=T)
+        res = h.run(0, lg, x)
+        _check_routing(h, cfg, res, lg, T)
+        _, _, Y_ref, out_ref = oracle.layer_step(h.weights[0], lg, x, cfg.k)
+        assert_close_bf16(res["Y"], Y_ref, f"Y T={T}")
+        assert_close_bf16(res["out"], out_ref, f"out T={T}")
+        r2 = ref.run(0, lg, x)
+        assert np.array_equal(res["Y"], r2["Y"]) and np.array_equal(res["out"], r2["out"])
+    finally:
+        h.close()
+        ref.close()
+
+
 def test_all_cold_and_all_hot_banks():
     cfg = synth.get_config("tiny")
     w = synth.layer_weights(cfg, 0)
