@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--config", default="decode1", choices=sorted(WORKLOADS))
     ap.add_argument("--pool", type=int, default=32, help="distinct input batches cycled through")
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--banks", default="streams", choices=["streams", "fused"],
+    ap.add_argument("--banks", default="fused", choices=["streams", "fused"],
                     help="the two banks' FFN calls on two streams at once, or one call over both banks")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of CPU-oracle work")
     ap.add_argument("--experts", type=int, default=0,

@@ -576,6 +576,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kWide ? 1 
     }
 }
 
+#include "ffn_tc_decode.cuh"
+
 // Exponent e of a row whose largest |value| is mx: mx * 2^-e lies in
 // (224, 448], the top binade of e4m3 (largest finite 448 = 0.875 * 2^9).
 __device__ __forceinline__ int row_exponent(float mx) {
@@ -605,10 +607,18 @@ __device__ __forceinline__ void split_e4m3x8(const float (&v)[8], uint2 &q1, uin
 }
 
 // Store values 8i..8i+7 of a row (K element 8i = chunk i/8, byte 8*(i%8)) as
-// the two pieces of that chunk's 128-byte record.
+// the two pieces of that chunk's 128-byte record.  PERM: in the order
+// 0,2,4,6,1,3,5,7 -- the K order in which the decode-tile kernel spreads an
+// expert's codes into tensor memory.
+template <bool PERM>
 __device__ __forceinline__ void store_pieces(uint8_t *row, int i, const float (&v)[8]) {
     uint2 q1, q2;
-    split_e4m3x8(v, q1, q2);
+    if (PERM) {
+        const float w[8] = {v[0], v[2], v[4], v[6], v[1], v[3], v[5], v[7]};
+        split_e4m3x8(w, q1, q2);
+    } else {
+        split_e4m3x8(v, q1, q2);
+    }
     uint8_t *rec = row + (i >> 3) * 128 + (i & 7) * 8;
     *(uint2 *)rec = q1;
     *(uint2 *)(rec + 64) = q2;
@@ -625,7 +635,9 @@ __device__ __forceinline__ float block_max(float mx, float *red) {
 
 // Gather the bank's token rows in pick order (row g = offset + p of xq) as
 // two e4m3 pieces per 64-wide chunk, each row scaled by 2^-e (e in xgexp).
-// b0 >= 0: that bank; b0 < 0: both banks, bank = blockIdx.y.
+// b0 >= 0: that bank; b0 < 0: both banks, bank = blockIdx.y.  PERM: decode
+// tiles' K order (see store_pieces).
+template <bool PERM>
 __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict__ x, int H, int k, BankLists L0,
                                                      BankLists L1, int b0, int P, uint8_t *__restrict__ xq,
                                                      int32_t *__restrict__ xgexp, int32_t *sched, int32_t *claim,
@@ -664,7 +676,7 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict_
             f[2 * q] = ldexpf(__uint_as_float(w[q] << 16), -e);
             f[2 * q + 1] = ldexpf(__uint_as_float(w[q] & 0xFFFF0000u), -e);
         }
-        store_pieces(dst, i, f);
+        store_pieces<PERM>(dst, i, f);
     }
     if (threadIdx.x == 0) xgexp[g] = e;
     if (gu32) {   // split units: clear this pick's gate/up sums before the gate/up GEMM adds into them
@@ -695,6 +707,7 @@ __device__ __forceinline__ void h_values(const float *h32, const float *gu32, in
 
 // The same for this bank's gate/up rows h (row g).  Split units: h is formed
 // here from the gate/up sums, and the pick's down-GEMM sum row is cleared.
+template <bool PERM>
 __global__ void __launch_bounds__(256) prep_h_kernel(BankLists L0, BankLists L1, int b0, int P, int I,
                                                      const float *__restrict__ h32, const float *__restrict__ gu32,
                                                      uint8_t *__restrict__ hq, int32_t *__restrict__ hexp,
@@ -721,7 +734,7 @@ __global__ void __launch_bounds__(256) prep_h_kernel(BankLists L0, BankLists L1,
         h_values(h32, gu32, g, I, i, f);
 #pragma unroll
         for (int q = 0; q < 8; ++q) f[q] = ldexpf(f[q], -e);
-        store_pieces(dst, i, f);
+        store_pieces<PERM>(dst, i, f);
     }
     if (threadIdx.x == 0) hexp[g] = e;
     if (y32) {
@@ -863,15 +876,72 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
     CUtensorMap m1, m2;
     if (int r = make_piece_map(&m1, ws + lay.xq, g.H, P, NMAX)) return r;
     if (int r = make_piece_map(&m2, ws + lay.hq, g.I, P, NMAX)) return r;
-    prep_x_kernel<<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
+    prep_x_kernel<false><<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
                                          (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
     MOE_LAUNCH_CHECK();
     if (int r = launch_gemm<NMAX, 1>(m1, layer.wmap[0][0], layer.wmap[1][0], a1, p1.blocks, s)) return r;
-    prep_h_kernel<<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
+    prep_h_kernel<false><<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
                                          a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H, a1.claim);
     MOE_LAUNCH_CHECK();
     if (int r = launch_gemm<NMAX, 2>(m2, layer.wmap[0][1], layer.wmap[1][1], a2, p2.blocks, s)) return r;
     if (!a2.y_out) return MOE_OK;
+    round_y_kernel<<<grid_p, 256, 0, s>>>(a2.lists[0], a2.lists[1], a2.b, g.H, a2.y_out, a2.Y);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+template <int NMAX, int PHASE, int BANKS>
+int launch_decode_one(const CUtensorMap &mB, const TcArgs &args, int blocks, cudaStream_t s) {
+    using C = DecCfg<NMAX>;
+    auto kern = ffn_tc_decode_kernel<NMAX, PHASE, BANKS>;
+    MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem));
+    if (blocks < 1) return MOE_OK;
+    kern<<<blocks, C::kThreads, C::kSmem, s>>>(mB, args);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+template <int NMAX, int PHASE>
+int launch_decode_gemm(const CUtensorMap &mB, const TcArgs &a, int blocks, cudaStream_t s) {
+    if (a.b < 0) return launch_decode_one<NMAX, PHASE, 2>(mB, a, blocks, s);
+    if (a.b == MOE_BANK_COLD) return launch_decode_one<NMAX, PHASE, 1>(mB, a, blocks, s);
+    return launch_decode_one<NMAX, PHASE, 0>(mB, a, blocks, s);
+}
+
+// Grid of a decode-tile GEMM launch: kPerSm CTAs per SM fill the SM; a
+// cold-bank launch takes one per SM (the host link needs a few MB in flight
+// GPU-wide) and, beside it, a hot-bank launch the SM's other slots, so the
+// two banks' launches run side by side.
+template <int NMAX>
+int decode_blocks(const moe_ctx *ctx, int b, bool shared, int units_max) {
+    const int per_sm = DecCfg<NMAX>::kPerSm;
+    int blocks;
+    if (b < 0 || (b == MOE_BANK_HOT && !shared)) blocks = ctx->sms * per_sm;
+    else if (b == MOE_BANK_COLD) blocks = ctx->sms;
+    else blocks = ctx->sms * (per_sm - 1);
+    return std::max(1, std::min(units_max, blocks));
+}
+
+template <int NMAX>
+int launch_bank_decode(moe_ctx *ctx, bool shared, TcArgs a1, TcArgs a2, int units1, int units2, const uint16_t *x,
+                       const WsLayout &lay, uint8_t *ws, cudaStream_t s) {
+    const Geom &g = ctx->g;
+    const int P = a1.P;
+    a1.ks = std::min(DecCfg<NMAX>::kSplit, a1.part.steps());
+    a2.ks = std::min(DecCfg<NMAX>::kSplit, a2.part.steps());
+    const dim3 grid_p(P, a1.b < 0 ? 2 : 1);   // one block per pick (of each bank)
+    CUtensorMap m1, m2;
+    if (int r = make_piece_map(&m1, ws + lay.xq, g.H, P, NMAX)) return r;
+    if (int r = make_piece_map(&m2, ws + lay.hq, g.I, P, NMAX)) return r;
+    prep_x_kernel<true><<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
+                                               (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
+    MOE_LAUNCH_CHECK();
+    if (int r = launch_decode_gemm<NMAX, 1>(m1, a1, decode_blocks<NMAX>(ctx, a1.b, shared, units1), s)) return r;
+    prep_h_kernel<true><<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
+                                               a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H,
+                                               a1.claim);
+    MOE_LAUNCH_CHECK();
+    if (int r = launch_decode_gemm<NMAX, 2>(m2, a2, decode_blocks<NMAX>(ctx, a1.b, shared, units2), s)) return r;
     round_y_kernel<<<grid_p, 256, 0, s>>>(a2.lists[0], a2.lists[1], a2.b, g.H, a2.y_out, a2.Y);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
@@ -944,12 +1014,13 @@ int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int b, const uint16_t *x, in
     const int units1 = 4 * P * g.mt13, units2 = 4 * P * g.mt2;   // bound: active rows never exceed the picks
     // The token-tile width depends only on T, so an expert's arithmetic is
     // the same in either bank.  Decode-sized steps use narrow tiles (8, 16 or
-    // 32 tokens) with several CTAs per SM (an expert with more tokens than the
-    // tile loops over token tiles); prefill-sized steps use 192-wide tiles (an
-    // expert's ~T*k/E tokens in one tile), one CTA per SM.
-    if (T <= 8) return launch_bank<8>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
-    if (T <= 16) return launch_bank<16>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
-    if (T <= kNarrowMaxT) return launch_bank<32>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
+    // 32 tokens; an expert with more tokens loops over token tiles) in the
+    // decode-tile kernel, which keeps more weight bytes in flight per SM;
+    // prefill-sized steps use 192-wide tiles (an expert's ~T*k/E tokens in
+    // one tile) in the shared-memory-A kernel, one CTA per SM.
+    if (T <= 8) return launch_bank_decode<8>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= 16) return launch_bank_decode<16>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= kNarrowMaxT) return launch_bank_decode<32>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
     return launch_bank<192>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
 }
 

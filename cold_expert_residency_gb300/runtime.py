@@ -48,11 +48,13 @@ class LayerStep:
         self.ev_routed = torch.cuda.Event()
         self.ev_cold = torch.cuda.Event()
 
-    def run(self, layer, T, count_on=True, stream=None, split=True, fused=False):
+    def run(self, layer, T, count_on=True, stream=None, split=True, fused=True):
         """Enqueue one layer-step of T tokens from buf.logits / buf.x into
-        buf.out (and buf.ids, buf.w, buf.Y).  By default the two banks' calls
-        run on two streams at once; ``split=False`` runs them one after the
-        other on the main stream, ``fused=True`` as one call over both banks."""
+        buf.out (and buf.ids, buf.w, buf.Y).  By default one FFN call covers
+        both banks (its launches stream the cold bank from one CTA per SM
+        and the hot bank from the others); ``fused=False`` runs the two banks'
+        calls on two streams at once, and with ``split=False`` one after the
+        other on the main stream."""
         b = self.buf
         main = stream if stream is not None else torch.cuda.current_stream()
         moe_route_split_count(self.ctx, layer, b.logits, T, count_on, b.ids, b.w, b.ws_ptr, main)
