@@ -164,10 +164,12 @@ def make_pool(cfg, n, layers):
 
 
 def source_sha():
+    """Hash of the FFN kernels' sources (a stored profile is used only while
+    they are unchanged)."""
     h = hashlib.sha256()
-    p = os.path.join(ROOT, "cold_expert_residency_gb300", "csrc", "ffn_tc.cu")
-    with open(p, "rb") as f:
-        h.update(f.read())
+    for name in ("ffn_tc.cu", "ffn_tc_decode.cuh"):
+        with open(os.path.join(ROOT, "cold_expert_residency_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
