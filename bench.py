@@ -3,7 +3,8 @@
 
 One step = one layer-step of the whole hot path over one batch of synthetic
 inputs: route + split + count, the hot-bank and cold-bank MXFP4 expert FFN
-(two streams), and the finalize.  Default workload: the one-user decode step
+(one call over both banks; ``--banks streams``: two calls on two streams),
+and the finalize.  Default workload: the one-user decode step
 (1 layer, 384 experts, top-6, H=4096, I=2880, 7 tokens, Zipf-skewed routing,
 295 experts in HBM and 89 in pinned host memory).
 
