@@ -108,7 +108,9 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile
 template <bool SUSP>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           int32_t *status) {
-    bool ok = wait_one<SUSP>(bar, parity, abort_flag, status);
+    // the warps that spread the weights mostly find their phase complete: a
+    // non-blocking check costs less than a suspend-hinted wait
+    bool ok = (SUSP && ptx::mbar_test_wait(bar, parity)) || wait_one<SUSP>(bar, parity, abort_flag, status);
     return __all_sync(0xffffffffu, ok);
 }
 
