@@ -648,11 +648,11 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict_
     const int p = blockIdx.x, b = b0 >= 0 ? b0 : (int)blockIdx.y;
     const BankLists &L = b ? L1 : L0;
     if (p == 0 && blockIdx.y == 0) {
-        // reset the work counters (and SM claims) of this call's GEMM launches,
+        // reset the work counters (and both GEMMs' SM claims) of this call's launches,
         // stream-ordered before them; a one-bank call leaves the other bank's alone
         if (threadIdx.x < 4 && (b0 < 0 || (int)threadIdx.x / 2 == b0)) sched[threadIdx.x] = 0;
         if (claim)
-            for (int i = threadIdx.x; i < 1024; i += blockDim.x) claim[i] = 0;
+            for (int i = threadIdx.x; i < 2 * 1024; i += blockDim.x) claim[i] = 0;
     }
     if (p >= L.hdr[kHdrNPicks + b]) return;
     const int g = bank_offset(L, b, P) + p;
@@ -713,12 +713,15 @@ template <bool PERM>
 __global__ void __launch_bounds__(256) prep_h_kernel(BankLists L0, BankLists L1, int b0, int P, int I,
                                                      const float *__restrict__ h32, const float *__restrict__ gu32,
                                                      uint8_t *__restrict__ hq, int32_t *__restrict__ hexp,
-                                                     float *__restrict__ y32, int H, int32_t *claim) {
+                                                     float *__restrict__ y32, int H) {
     __shared__ float red[8];
     const int p = blockIdx.x, b = b0 >= 0 ? b0 : (int)blockIdx.y;
     const BankLists &L = b ? L1 : L0;
-    if (claim && p == 0 && blockIdx.y == 0)   // SM claims of the down GEMM's launch
-        for (int i = threadIdx.x; i < 1024; i += blockDim.x) claim[i] = 0;
+    // Launched as a programmatic dependent of the gate/up GEMM: wait for its
+    // sums, and let the down GEMM launch at once (it streams weights, and
+    // waits for these rows before it reads them).
+    ptx::gdc_wait();
+    ptx::gdc_launch_dependents();
     if (p >= L.hdr[kHdrNPicks + b]) return;
     const int g = bank_offset(L, b, P) + p;
     const int n8 = I / 8;
@@ -883,7 +886,7 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
     MOE_LAUNCH_CHECK();
     if (int r = launch_gemm<NMAX, 1>(m1, layer.wmap[0][0], layer.wmap[1][0], a1, p1.blocks, s)) return r;
     prep_h_kernel<false><<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
-                                         a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H, a1.claim);
+                                         a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
     MOE_LAUNCH_CHECK();
     if (int r = launch_gemm<NMAX, 2>(m2, layer.wmap[0][1], layer.wmap[1][1], a2, p2.blocks, s)) return r;
     if (!a2.y_out) return MOE_OK;
@@ -892,22 +895,53 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
     return MOE_OK;
 }
 
+// Launch `kern` on `s` as a programmatic dependent of the kernel before it:
+// it may start once every block of that kernel has started or finished, and
+// synchronizes with it through griddepcontrol.wait.
+template <class T>
+struct same_type {
+    using type = T;
+};
+
+template <typename... KArgs>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             typename same_type<KArgs>::type... args) {
+    void *pargs[] = {(void *)&args...};   // each argument in the kernel's own parameter type
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, (const void *)kern, pargs);
+}
+
 template <int NMAX, int PHASE, int BANKS>
-int launch_decode_one(const CUtensorMap &mB, const TcArgs &args, int blocks, cudaStream_t s) {
+int launch_decode_one(const CUtensorMap &mB, const TcArgs &args, int blocks, bool dependent, cudaStream_t s) {
     using C = DecCfg<NMAX>;
     auto kern = ffn_tc_decode_kernel<NMAX, PHASE, BANKS>;
     MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem));
     if (blocks < 1) return MOE_OK;
-    kern<<<blocks, C::kThreads, C::kSmem, s>>>(mB, args);
+    if (PHASE == 2 && dependent) {
+        // the down GEMM depends on prep_h programmatically: it claims units
+        // and streams weights before prep_h's rows exist
+        MOE_CUDA_TRY(launch_dependent(kern, dim3(blocks), dim3(C::kThreads), C::kSmem, s, mB, args));
+    } else {
+        kern<<<blocks, C::kThreads, C::kSmem, s>>>(mB, args);
+    }
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
 template <int NMAX, int PHASE>
-int launch_decode_gemm(const CUtensorMap &mB, const TcArgs &a, int blocks, cudaStream_t s) {
-    if (a.b < 0) return launch_decode_one<NMAX, PHASE, 2>(mB, a, blocks, s);
-    if (a.b == MOE_BANK_COLD) return launch_decode_one<NMAX, PHASE, 1>(mB, a, blocks, s);
-    return launch_decode_one<NMAX, PHASE, 0>(mB, a, blocks, s);
+int launch_decode_gemm(const CUtensorMap &mB, const TcArgs &a, int blocks, bool dependent, cudaStream_t s) {
+    if (a.b < 0) return launch_decode_one<NMAX, PHASE, 2>(mB, a, blocks, dependent, s);
+    if (a.b == MOE_BANK_COLD) return launch_decode_one<NMAX, PHASE, 1>(mB, a, blocks, dependent, s);
+    return launch_decode_one<NMAX, PHASE, 0>(mB, a, blocks, dependent, s);
 }
 
 // Grid of a decode-tile GEMM launch: kPerSm CTAs per SM fill the SM; a
@@ -925,8 +959,8 @@ int decode_blocks(const moe_ctx *ctx, int b, bool shared, int units_max) {
 }
 
 template <int NMAX>
-int launch_bank_decode(moe_ctx *ctx, bool shared, TcArgs a1, TcArgs a2, int units1, int units2, const uint16_t *x,
-                       const WsLayout &lay, uint8_t *ws, cudaStream_t s) {
+int launch_bank_decode(moe_ctx *ctx, bool shared, bool cold_rows, TcArgs a1, TcArgs a2, int units1, int units2,
+                       const uint16_t *x, const WsLayout &lay, uint8_t *ws, cudaStream_t s) {
     const Geom &g = ctx->g;
     const int P = a1.P;
     a1.ks = std::min(DecCfg<NMAX>::kSplit, a1.part.steps());
@@ -938,12 +972,21 @@ int launch_bank_decode(moe_ctx *ctx, bool shared, TcArgs a1, TcArgs a2, int unit
     prep_x_kernel<true><<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
                                                (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
     MOE_LAUNCH_CHECK();
-    if (int r = launch_decode_gemm<NMAX, 1>(m1, a1, decode_blocks<NMAX>(ctx, a1.b, shared, units1), s)) return r;
-    prep_h_kernel<true><<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
-                                               a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H,
-                                               a1.claim);
+    if (int r = launch_decode_gemm<NMAX, 1>(m1, a1, decode_blocks<NMAX>(ctx, a1.b, shared, units1), false, s)) return r;
+    // A call that streams the cold bank chains prep_h and the down GEMM to
+    // the gate/up GEMM as programmatic dependents, so the host link restarts
+    // before prep_h ends; an HBM-only call measured faster without.
+    const bool dependent = a1.b != MOE_BANK_HOT && cold_rows;
+    if (dependent) {
+        MOE_CUDA_TRY(launch_dependent(prep_h_kernel<true>, grid_p, dim3(256), 0, s, a1.lists[0], a1.lists[1], a1.b, P,
+                                      g.I, (const float *)(ws + lay.h32), (const float *)a1.gu_out, ws + lay.hq,
+                                      (int32_t *)(ws + lay.hexp), a2.y_out, g.H));
+    } else {
+        prep_h_kernel<true><<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
+                                                   a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
+    }
     MOE_LAUNCH_CHECK();
-    if (int r = launch_decode_gemm<NMAX, 2>(m2, a2, decode_blocks<NMAX>(ctx, a1.b, shared, units2), s)) return r;
+    if (int r = launch_decode_gemm<NMAX, 2>(m2, a2, decode_blocks<NMAX>(ctx, a1.b, shared, units2), dependent, s)) return r;
     round_y_kernel<<<grid_p, 256, 0, s>>>(a2.lists[0], a2.lists[1], a2.b, g.H, a2.y_out, a2.Y);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
@@ -1002,6 +1045,7 @@ int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int b, const uint16_t *x, in
     // the hot bank's concurrent launches never read them)
     a1.claim = (a1.b < 0 || a1.b == MOE_BANK_COLD) ? (int32_t *)(ws + lay.claim) : nullptr;
     TcArgs a2 = a1;
+    a2.claim = a1.claim ? a1.claim + 1024 : nullptr;   // the down GEMM's own claims
     a2.part = g.w2;
     a2.bexp = (const int32_t *)(ws + lay.hexp);
     a2.h_out = nullptr;
@@ -1020,9 +1064,10 @@ int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int b, const uint16_t *x, in
     // decode-tile kernel, which keeps more weight bytes in flight per SM;
     // prefill-sized steps use 192-wide tiles (an expert's ~T*k/E tokens in
     // one tile) in the shared-memory-A kernel, one CTA per SM.
-    if (T <= 8) return launch_bank_decode<8>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
-    if (T <= 16) return launch_bank_decode<16>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
-    if (T <= kNarrowMaxT) return launch_bank_decode<32>(ctx, shared, a1, a2, units1, units2, x, lay, ws, s);
+    const bool cold_rows = layer.n_cold > 0;
+    if (T <= 8) return launch_bank_decode<8>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= 16) return launch_bank_decode<16>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= kNarrowMaxT) return launch_bank_decode<32>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
     return launch_bank<192>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
 }
 

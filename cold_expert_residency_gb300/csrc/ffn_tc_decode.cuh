@@ -162,6 +162,9 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
         for (uint32_t ui = 0; ok; ++ui) {
             const int e = take_unit(ui, true, ok);
             if (e < 0) break;
+            // the down GEMM reads prep_h's row exponents and adds into the rows
+            // it cleared: wait for it (once)
+            if (PHASE == 2 && ui == 0) ptx::gdc_wait();
             const int bk = e & 1;
             const BankLists &L = args.lists[bk];
             const int goff = bank_offset(L, bk, args.P);
@@ -231,6 +234,18 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
         bool dry_pref = false, dry_other = args.b >= 0;
         uint32_t it = 0;
         bool ok = true;
+        // The down GEMM's token rows are prep_h's output: the ring's first round
+        // of weight copies goes out at once, its token-row boxes once prep_h
+        // has finished (before any stage is reused, and at the end).
+        bool rows_ready = PHASE == 1;
+        int def_brow[S], def_s[S], ndef = 0;
+        auto release_rows = [&]() {
+            if (rows_ready) return;
+            ptx::gdc_wait();
+            rows_ready = true;
+            for (int i = 0; i < ndef; ++i)
+                ptx::tma_load_4d(ptx::smem_addr(sB + i * C::kBStage), &tmB, 0, def_brow[i], 0, 2 * def_s[i], bar(FULL + i));
+        };
         for (uint32_t ui = 0; ok; ++ui) {
             const int qs = ui % kQ;
             if (ui >= (uint32_t)kQ &&
@@ -265,6 +280,7 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
                 for (int s = s0; s < s1; ++s, ++it) {
                     const int st = it % S;
                     const uint32_t rnd = it / S;
+                    if (rnd > 0) release_rows();
                     if (rnd > 0 && !wait_one<SUSP>(bar(DONEG + st), (rnd - 1) & 1, abort_flag, args.status)) {
                         ok = false;
                         break;
@@ -276,10 +292,17 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
                     ptx::mbar_arrive_expect_tx(bar(FULL + st), (uint32_t)(kGroupBytes + C::kBStage));
                     ptx::bulk_g2s(ptx::smem_addr(sA + st * kGroupBytes), expert + part.group_off(slot, tidx), kGroupBytes,
                                   bar(FULL + st));
-                    ptx::tma_load_4d(ptx::smem_addr(sB + st * C::kBStage), &tmB, 0, brow, 0, 2 * s, bar(FULL + st));
+                    if (rows_ready) {
+                        ptx::tma_load_4d(ptx::smem_addr(sB + st * C::kBStage), &tmB, 0, brow, 0, 2 * s, bar(FULL + st));
+                    } else {   // first round: stage st == ndef
+                        def_brow[ndef] = brow;
+                        def_s[ndef] = s;
+                        ++ndef;
+                    }
                 }
             }
         }
+        release_rows();
         if (!ok) {
             // let the copies this thread issued land before the CTA goes away
             const uint32_t first = it > (uint32_t)S ? it - S : 0u;

@@ -153,7 +153,7 @@ inline WsLayout ws_layout(const Geom &g, int T) {
     const size_t ks = split_k_steps(T) ? 1 : 0;
     w.gu32 = take(ks * P * (size_t)g.I * 2 * 4); // [P][2I] gate/up sums before SwiGLU, by g
     w.y32 = take(ks * P * (size_t)g.H * 4);     // [P][H] down-GEMM sums, by slot
-    w.claim = take(1024 * 4);                   // [SM] first-CTA claims of a launch over both banks
+    w.claim = take(2 * 1024 * 4);               // [GEMM][SM] first-CTA claims of a launch over both banks
     w.total = off;
     return w;
 }

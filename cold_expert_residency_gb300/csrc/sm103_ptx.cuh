@@ -58,6 +58,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Programmatic dependent launch: block until the grids this one depends on
+// have completed and their memory is visible (returns at once in a grid
+// launched without such a dependency).
+__device__ __forceinline__ void gdc_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the grids that depend on this one start launching.
+__device__ __forceinline__ void gdc_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Nanosecond wall clock of the device (the globaltimer special register).
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
