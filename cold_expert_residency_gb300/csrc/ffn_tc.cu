@@ -1,11 +1,15 @@
 // MXFP4 expert FFN on the 5th-generation tensor cores (tcgen05 + TMEM),
-// block-scaled, with the weights moved only by the tensor memory accelerator.
+// block-scaled.  This file holds the prefill-tile kernel, whose weights are
+// moved only by the tensor memory accelerator, the row kernels around the
+// GEMMs, and the launch code; decode tiles run the kernel in
+// ffn_tc_decode.cuh (included below).
 //
 // "vLLM: Pin Hot Experts", Results: the routed MXFP4 expert FFN (gate/up
 // GEMM, SwiGLU, down GEMM) runs once per residency bank without finalize.
 // Here one launch per GEMM covers one bank (or both):
 //
-//   unit = (active bank row = one expert, 128-row M-tile [, K half]);
+//   unit = (active bank row = one expert, 128-row M-tile [, K half for decode
+//          tiles]);
 //   D[128 x N] = sum over 32-wide K blocks of (SFA * A) (SFB * B)^T, fp32 in
 //   TMEM, by tcgen05.mma kind::mxf8f6f4 with e8m0 block scales, where
 //   A = the expert's e2m1 weights with their own e8m0 scales (exact), read
@@ -33,12 +37,10 @@
 //             token tile's last group, a commit hands its accumulator over.
 //   epilogue  Four warps (thread m = accumulator row m): tcgen05.ld of D, the
 //             row's power of two undone, then SwiGLU (gate and up rows meet
-//             in lanes l and l^16), the bf16 row, or fp32 partial sums of a
-//             K half.  Two accumulators, so a tile's epilogue overlaps the
-//             next tile's MMAs.
-// Decode tiles (8, 16 or 32 tokens) run 1-3 CTAs per SM, prefill tiles (192
-// tokens) one; the ring's depth is set per launch from the shared memory
-// that the SM's CTAs leave.
+//             in lanes l and l^16) or the bf16 row.  Two accumulators, so a
+//             tile's epilogue overlaps the next tile's MMAs.
+// Prefill tiles (192 tokens) run one CTA per SM; the ring's depth is set per
+// launch from the SM's shared memory.
 //
 // The arithmetic of a pick depends only on its expert's weights, its token
 // row and the step's token count (which fixes the tile), never on the bank,
@@ -132,48 +134,38 @@ __device__ __forceinline__ int bank_offset(const BankLists &L, int b, int P) {
 
 template <int NMAX>
 struct TcCfg {
-    static constexpr bool kWide = NMAX >= 128;
-    // Tiles of up to 16 tokens stack the two e4m3 pieces as token rows
-    // [0, Nr) and [Nr, 2 Nr) of one MMA (half the MMA instructions); wider
-    // tiles issue one MMA per piece.
-    static constexpr bool kStack = NMAX <= 16;
+    // This kernel runs the prefill tiles; decode tiles run ffn_tc_decode_kernel.
+    static_assert(NMAX >= 128 && NMAX <= 256 && NMAX % 16 == 0, "prefill tile");
+    static constexpr bool kWide = true;
+    static constexpr bool kStack = false;                   // one MMA per e4m3 piece
     // One 4-D tensor-TMA box per stage brings the tile's token rows: both
     // e4m3 pieces of both 64-wide chunks, as [chunk][piece][NMAX rows][64 B]
     // with 64-byte swizzle (rows past the tile's tokens are loaded and unused).
     static constexpr int kBChunk = 2 * NMAX * 64;           // one chunk: both pieces
     static constexpr int kBStage = 2 * kBChunk;
-    // token rows of one piece are padded to a multiple of kRowQ (stacked
-    // tiles: the whole tile, so piece 1 starts at row NMAX)
-    static constexpr int kRowQ = kStack ? NMAX : 16;
-    static constexpr int kAStage = 2 * kGroupQBytes;                // padded code block: 16 KB
+    static constexpr int kRowQ = 16;                        // token rows of a piece, padded to 16
+    static constexpr int kAStage = 2 * kGroupQBytes;        // padded code block: 16 KB
     // One stage holds a group's 8.5 KB of weights as 16.5 KB of padded codes
     // and scales, plus the token rows; the host sizes the ring per launch
-    // from the SM's shared memory and the CTAs that share it.
+    // from the SM's shared memory.
     static constexpr int kStageBytes = kAStage + kBStage + kSfAtomBytes;
     static constexpr int kDBufs = 2;                        // accumulators in TMEM
-    static constexpr int kDW = (kStack ? 2 : 1) * NMAX;     // columns of one accumulator
+    static constexpr int kDW = NMAX;                        // columns of one accumulator
     static constexpr int kNCol = (kDW + 31) / 32;           // B scale columns of one piece
     // A scale slots in TMEM, reused round-robin: the MMA thread refills slot
     // it % kNsf after the MMAs of iteration it - kNsf have completed.
-    static constexpr int kNsf = kWide ? 3 : 2;
+    static constexpr int kNsf = 3;
     // Tensor memory columns: slot i's A scales at 32 i (four columns written
     // by tcgen05.cp); slot 0's block also holds the B scale columns of piece
-    // 0 at +8 and of piece 1 at +16 (stacked tiles use piece 0's for both);
-    // then the accumulators.
+    // 0 at +8 and of piece 1 at +16; then the accumulators.
     static constexpr uint32_t kSfbCol = 8;
     static constexpr uint32_t kSfbStride = 8;
     static constexpr uint32_t kDCol = 32 * kNsf;
     static constexpr uint32_t kColsUsed = kDCol + kDBufs * kDW;
-    static constexpr uint32_t kCols = kColsUsed <= 64 ? 64 : (kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512));
-    static constexpr int kPerSmMax = 512 / kCols;           // CTAs per SM that tensor memory admits
-    static_assert(kColsUsed <= 512, "tile does not fit in tensor memory");
+    static constexpr uint32_t kCols = 512;                  // one CTA per SM
+    static_assert(kColsUsed <= kCols, "tile does not fit in tensor memory");
     static_assert(kNCol <= 8 && kSfbCol + kSfbStride + kNCol <= 32, "B scale columns");
-    static_assert(NMAX % 8 == 0 && NMAX <= 256 && kDW % 16 == 0 && kDCol % 32 == 0, "tile alignment");
-    // Narrow tiles split each (expert, M-tile) unit into two K halves: a
-    // decode step has only a few units per CTA, and halving them halves the
-    // tail of the launch.  Two partial sums added onto zero in either order
-    // give the same fp32 result, so the split stays deterministic.
-    static constexpr int kSplit = kWide ? 1 : 2;
+    static constexpr int kSplit = 1;                        // whole-K units
     static constexpr int kProducer = 4, kMmaWarp = 5;
     static constexpr int kThreads = 192;
     static constexpr int kBars = 2 * kMaxStages + 2 * kDBufs + 2 * kQ;
@@ -294,7 +286,7 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
 // is the same, every unit carries its bank.  tmA0 / tmA1: the hot and cold
 // bank's code-block maps of this GEMM's part; tmB: the token-row records.
 template <int NMAX, int PHASE, int BANKS>
-__global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kWide ? 1 : 3)
+__global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0,
                   const __grid_constant__ CUtensorMap tmA1, TcArgs args) {
     using C = TcCfg<NMAX>;
@@ -316,7 +308,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, TcCfg<NMAX>::kWide ? 1 
     const int FULL = 0, DONE = kMaxStages, ACCREADY = 2 * kMaxStages, ACCFREE = ACCREADY + DB, UQFULL = ACCFREE + DB,
               UQEMPTY = UQFULL + kQ;
     constexpr int kQueueReaders = 128 + 1;   // the epilogue warps and the MMA thread
-    constexpr bool SUSP = !C::kWide;         // suspend-hinted waits for the decode tiles
+    constexpr bool SUSP = false;             // one CTA per SM: plain polling
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (BANKS == 1) {
@@ -815,44 +807,19 @@ struct LaunchPlan {
     int blocks, S;
 };
 
-// Grid and ring depth of one GEMM launch.  Units are handed out dynamically,
-// so the grid only sets how many CTAs stream at once, and the ring is as deep
-// as the SM's shared memory allows for the CTAs that share it:
-//   - a cold-bank launch of narrow tiles: one CTA per SM with a short ring
-//     (the host link needs only a few KB in flight per SM);
-//   - a hot-bank launch: two CTAs per SM, sharing what the cold CTA leaves
-//     when the layer has both banks (the two launches run side by side);
-//   - a launch over both banks: three CTAs per SM;
-//   - prefill tiles: one CTA per SM (32 SMs' worth for a cold bank).
+// Grid and ring depth of one prefill GEMM launch: one CTA per SM (32 SMs'
+// worth for a cold bank when the layer has both banks, so the two banks'
+// launches run side by side), and a ring as deep as the SM's shared memory
+// allows.
 template <int NMAX>
 LaunchPlan plan_for(const moe_ctx *ctx, int b, bool shared, int units_max) {
     using C = TcCfg<NMAX>;
-    auto fit = [](size_t budget, int ctas) {
-        const long per = (long)(budget / ctas) - (long)kCtaReserve - (long)C::kFixedSmem;
-        return std::max(C::kNsf, std::min(kMaxStages, (int)(per / C::kStageBytes)));
-    };
-    const int cold_S = std::max(2, C::kNsf);
-    const size_t cold_bytes = kCtaReserve + C::smem_bytes(cold_S);
+    const long per = (long)kSmSmem - (long)kCtaReserve - (long)C::kFixedSmem;
     LaunchPlan p;
-    if (C::kWide) {
-        const int cold_ctas = 32;
-        p.S = fit(kSmSmem, 1);
-        if (b < 0 || !shared) p.blocks = ctx->sms;
-        else p.blocks = b == MOE_BANK_COLD ? cold_ctas : ctx->sms - cold_ctas;
-    } else if (b < 0) {
-        p.blocks = 3 * ctx->sms;
-        p.S = fit(kSmSmem, 3);
-    } else if (b == MOE_BANK_COLD) {
-        p.blocks = ctx->sms;
-        p.S = cold_S;
-    } else {
-        p.blocks = 2 * ctx->sms;
-        p.S = fit(shared ? kSmSmem - cold_bytes : kSmSmem, 2);
-        // beside a cold bank, a third hot CTA must not fit on an SM (it would
-        // take the cold streamer's place there)
-        while (shared && p.S < kMaxStages && 3 * (kCtaReserve + C::smem_bytes(p.S)) <= kSmSmem) ++p.S;
-    }
-    static_assert(C::kWide || C::kPerSmMax >= 3, "narrow tiles run up to three CTAs per SM");
+    p.S = std::max(C::kNsf, std::min(kMaxStages, (int)(per / C::kStageBytes)));
+    const int cold_ctas = 32;
+    if (b < 0 || !shared) p.blocks = ctx->sms;
+    else p.blocks = b == MOE_BANK_COLD ? cold_ctas : ctx->sms - cold_ctas;
     p.blocks = std::max(1, std::min(units_max, p.blocks));
     return p;
 }

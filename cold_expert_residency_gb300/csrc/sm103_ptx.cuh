@@ -1,5 +1,6 @@
-// Thin inline-PTX wrappers for sm_103a: mbarriers, bulk async copies (TMA),
-// cp.async, proxy fences and the tcgen05 tensor-core / tensor-memory ops.
+// Thin inline-PTX wrappers for sm_103a: mbarriers, programmatic dependent
+// launch, bulk and tensor async copies (TMA) and the tcgen05 tensor-core /
+// tensor-memory ops.
 // Written from the PTX ISA's instruction descriptions.
 #pragma once
 #include <cstdint>
@@ -80,18 +81,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
-// 2-D tiled tensor copy (TMA) global -> shared through a tensor map; the box
-// lands at dst with the map's swizzle, completing bytes on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-// Bulk prefetch of `bytes` (a multiple of 16) of global memory into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 // 5-D tiled tensor copy global -> shared (coordinates innermost first).
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, int c0, int c1, int c2, int c3, int c4,
                                             uint32_t bar) {
@@ -112,29 +101,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int 
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
-// 16-byte asynchronous copy global -> shared (L2 only).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// Arrive on `bar` when all of this thread's prior cp.async copies complete;
-// the arrival counts toward the barrier's expected count.
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
 
 // ---- tcgen05 / tensor memory ----------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t holder_smem, uint32_t ncols) {
@@ -153,18 +119,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// Warp-collective: lane i stores 32 consecutive 32-bit columns of TMEM lane
-// (quarter base + i) starting at column taddr.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
@@ -202,15 +156,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16, issued by one thread.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 // D[tmem] (+)= (A . SFA)[tmem] * (B . SFB)[smem desc]^T, kind::mxf8f6f4 with
 // one e8m0 scale per 32 K elements (scale_vec::1X), issued by one thread.
 // Tensor-memory operand forms on this target:
@@ -292,14 +237,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t addr) {
     return d;
 }
 
-// Instruction descriptor for kind::f16: f16 A and B, f32 accumulator,
-// both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
-    return (1u << 4)                       // D format: f32
-           | (0u << 7) | (0u << 10)        // A, B format: f16
-           | ((uint32_t)(N >> 3) << 17)    // N / 8
-           | ((uint32_t)(M >> 4) << 24);   // M / 16
-}
 
 // Instruction descriptor for kind::mxf8f6f4 block_scale: e2m1 A, e4m3 B,
 // both K-major, f32 accumulator, e8m0 scales, M x N, with the byte of the
