@@ -54,6 +54,7 @@ def lib():
     sig = {
         "moe_last_error": (C.c_char_p, []),
         "moe_expert_bytes": (i64, [C.c_int32, C.c_int32]),
+        "moe_pack_expert": (i32, [C.c_int32, C.c_int32, P, P, P, P, P]),
         "moe_create": (i32, [C.POINTER(moe_geom), i32, C.POINTER(P)]),
         "moe_destroy": (i32, [P]),
         "moe_set_ffn_impl": (i32, [P, i32]),
@@ -141,6 +142,16 @@ def _err(fn, rc):
 
 def moe_expert_bytes(hidden, inter):
     return int(lib().moe_expert_bytes(hidden, inter))
+
+
+def moe_pack_expert(hidden, inter, w13_q, w13_s, w2_q, w2_s):
+    """One expert's logical MXFP4 arrays (host numpy uint8) -> the bytes of
+    its bank row (numpy uint8 [moe_expert_bytes(hidden, inter)])."""
+    import numpy as np
+    arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (w13_q, w13_s, w2_q, w2_s)]
+    out = np.empty(moe_expert_bytes(hidden, inter), np.uint8)
+    _err("moe_pack_expert", lib().moe_pack_expert(hidden, inter, *[a.ctypes.data for a in arrs], out.ctypes.data))
+    return out
 
 
 def moe_create(layers, experts, top_k, hidden, inter, max_tokens, count_tmax=256, device=0):

@@ -179,6 +179,25 @@ int64_t moe_expert_bytes(int32_t hidden, int32_t inter) {
     return n / 2 + n / 32;
 }
 
+int moe_pack_expert(int32_t hidden, int32_t inter, const uint8_t *w13_q, const uint8_t *w13_s,
+                    const uint8_t *w2_q, const uint8_t *w2_s, uint8_t *out) {
+    if (!w13_q || !w13_s || !w2_q || !w2_s || !out) return set_error(MOE_EINVAL, "null argument");
+    if (hidden < 128 || hidden % 128 || inter < 64 || inter % 64 || (hidden % 256 && inter % 128))
+        return set_error(MOE_EINVAL, "invalid geometry (need H % 128 == 0, I % 64 == 0, "
+                                     "H % 256 == 0 or I % 128 == 0)");
+    moe_geom mg{};
+    mg.layers = 1;
+    mg.experts = 2;
+    mg.top_k = 1;
+    mg.hidden = hidden;
+    mg.inter = inter;
+    mg.max_tokens = 1;
+    const Geom g = make_geom(mg);
+    if (!repack_expert(g, w13_q, w13_s, w2_q, w2_s, out))
+        return set_error(MOE_EINVAL, "e8m0 scale byte outside [104, 140]");
+    return MOE_OK;
+}
+
 int moe_create(const moe_geom *geom, int device, moe_ctx **out) {
     if (!geom || !out) return set_error(MOE_EINVAL, "null argument");
     *out = nullptr;

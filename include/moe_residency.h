@@ -78,6 +78,23 @@ const char *moe_last_error(void);
  * ("vLLM: Pin Hot Experts": 17.93 MiB per MXFP4 expert). */
 int64_t moe_expert_bytes(int32_t hidden, int32_t inter);
 
+/* Pack one expert, given in the logical MXFP4 layout above, into the bytes of
+ * a bank row (what moe_init_banks places and moe_read_bank_row returns).
+ * Host memory only; no device is touched.  out: moe_expert_bytes(hidden,
+ * inter) bytes.  The row is the W13 part, then the W2 part.  Each part is a
+ * sequence of 8704-byte blocks, one per (128-row M-tile, 128-wide K group):
+ * the tile's 128 rows of 64 code bytes in the logical nibble order, then a
+ * 512-byte scale atom holding the scale of tile row m and 32-wide K block kb
+ * at byte (m%32)*16 + 4*(m/32) + kb.  W13 tile mt row 32w+l holds W13 row
+ * (l<16 ? 0 : I) + 64mt + 16w + l%16; W2 tile mt row m holds W2 row 128mt+m.
+ * A tile's blocks follow in K order, tiles in order.  When I % 128 == 64, W2
+ * tiles 2p and 2p+1 are stored as a pair: 2p's full groups, then 2p+1's, then
+ * one shared group whose K blocks 0-1 are 2p's last 64 columns and whose
+ * blocks 2-3 are 2p+1's.  The geometry must satisfy moe_create's rules for
+ * H and I, and the scale bytes moe_init_banks' range; otherwise MOE_EINVAL. */
+int moe_pack_expert(int32_t hidden, int32_t inter, const uint8_t *w13_q, const uint8_t *w13_s,
+                    const uint8_t *w2_q, const uint8_t *w2_s, uint8_t *out);
+
 /* Create a context on CUDA device `device`: validates the geometry and
  * allocates the [L x E] int32 usage table (zeroed) and one HBM staging row
  * for swaps.  *out receives the context. */
