@@ -79,6 +79,7 @@ def lib():
         "moe_policy_create": (i32, [i32, C.c_double, C.c_double, C.c_double, C.c_double, i32, P, C.POINTER(P)]),
         "moe_policy_destroy": (i32, [P]),
         "moe_policy_read": (i32, [P, P, P, P, P]),
+        "moe_plan_restore": (i32, [i32, P, P, i32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -277,6 +278,20 @@ def moe_device_status(ctx):
 
 def moe_kernel_launches():
     return int(lib().moe_kernel_launches())
+
+
+def moe_plan_restore(row_map, target, max_pairs):
+    """Swap pairs (promote, demote) that bring row_map's hot set back to
+    target's, at most max_pairs of them (moe_plan_restore ABI)."""
+    rm = np.ascontiguousarray(row_map, dtype=np.int32)
+    tg = np.ascontiguousarray(target, dtype=np.int32)
+    if rm.shape != tg.shape:
+        raise ValueError("row_map and target differ in length")
+    pro = np.zeros(max(int(max_pairs), 1), np.int32)
+    dem = np.zeros(max(int(max_pairs), 1), np.int32)
+    n = _err("moe_plan_restore", lib().moe_plan_restore(rm.size, _ptr(rm), _ptr(tg), int(max_pairs),
+                                                        _ptr(pro), _ptr(dem)))
+    return pro[:n].copy(), dem[:n].copy()
 
 
 class moe_policy:

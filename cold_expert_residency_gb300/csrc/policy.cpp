@@ -7,13 +7,25 @@
 // hysteresis, minimum average 8, <= 8 swaps per step).  The average is an
 // exponentially weighted mean of the per-read pick counts, normalised by the
 // decayed weight sum so that it is unbiased from the first read.
+//
+// The same section's runtime control can queue a restore to the boot-time
+// map; its round-trip check restores the boot-time hot set by swaps.  The
+// restore planner gives those swaps for any saved map.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <new>
+#include <string>
 #include <vector>
 
 #include "../../include/moe_residency.h"
+
+// The library's thread-local error message (moe_abi.cu); the header that
+// declares it also carries CUDA types, which this host-only file does without.
+namespace moe {
+int set_error(int code, const std::string &msg);
+}
+using moe::set_error;
 
 struct moe_policy {
     int E;
@@ -29,9 +41,9 @@ extern "C" {
 int moe_policy_create(int experts, double read_every, double half_life, double hysteresis, double min_avg,
                       int max_pairs, const int32_t *counts_now, moe_policy **out) {
     if (!out || experts < 1 || !(read_every > 0) || !(half_life > 0) || !(hysteresis >= 1.0) || max_pairs < 0)
-        return MOE_EINVAL;
+        return set_error(MOE_EINVAL, "invalid policy parameter");
     moe_policy *p = new (std::nothrow) moe_policy();
-    if (!p) return MOE_ENOMEM;
+    if (!p) return set_error(MOE_ENOMEM, "out of host memory");
     p->E = experts;
     p->decay = std::pow(0.5, read_every / half_life);
     p->hysteresis = hysteresis;
@@ -52,7 +64,7 @@ int moe_policy_destroy(moe_policy *p) {
 
 int moe_policy_read(moe_policy *p, const int32_t *counts, const int32_t *row_map, int32_t *promote,
                     int32_t *demote) {
-    if (!p || !counts || !row_map || !promote || !demote) return MOE_EINVAL;
+    if (!p || !counts || !row_map || !promote || !demote) return set_error(MOE_EINVAL, "null argument");
     const int E = p->E;
     for (int e = 0; e < E; ++e) {
         const uint32_t now = (uint32_t)counts[e];
@@ -80,6 +92,25 @@ int moe_policy_read(moe_policy *p, const int32_t *counts, const int32_t *row_map
         if (!(avg[cold[n]] > p->hysteresis * avg[hot[n]])) break;
         promote[n] = cold[n];
         demote[n] = hot[n];
+    }
+    return n;
+}
+
+int moe_plan_restore(int experts, const int32_t *row_map, const int32_t *target, int max_pairs,
+                     int32_t *promote, int32_t *demote) {
+    if (experts < 1 || !row_map || !target || max_pairs < 0 || ((!promote || !demote) && max_pairs > 0))
+        return set_error(MOE_EINVAL, "invalid argument");
+    std::vector<int> in, out;       // experts to bring into HBM, experts to move out
+    for (int e = 0; e < experts; ++e) {
+        const bool hot = row_map[e] >= 0, want = target[e] >= 0;
+        if (hot != want) (want ? in : out).push_back(e);
+    }
+    if (in.size() != out.size())    // swaps never change the hot bank's size
+        return set_error(MOE_EINVAL, "the two maps hold different numbers of hot experts");
+    const int n = std::min((int)in.size(), max_pairs);
+    for (int i = 0; i < n; ++i) {
+        promote[i] = in[i];
+        demote[i] = out[i];
     }
     return n;
 }

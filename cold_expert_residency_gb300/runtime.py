@@ -15,7 +15,7 @@ from __future__ import annotations
 import torch
 
 from . import (MOE_BANK_BOTH, MOE_BANK_COLD, MOE_BANK_HOT, moe_expert_ffn_bank, moe_finalize,
-               moe_route_split_count, moe_workspace_bytes)
+               moe_get_rowmap, moe_plan_restore, moe_route_split_count, moe_swap_rows, moe_workspace_bytes)
 
 
 class StepBuffers:
@@ -71,3 +71,17 @@ class LayerStep:
             moe_expert_ffn_bank(self.ctx, layer, MOE_BANK_HOT, b.x, T, b.ws_ptr, b.Y, main)
             moe_expert_ffn_bank(self.ctx, layer, MOE_BANK_COLD, b.x, T, b.ws_ptr, b.Y, main)
         moe_finalize(b.Y, b.w, T, b.k, b.H, b.out, main)
+
+
+def restore_placement(ctx, layer, saved, budget=8, stream=None):
+    """Between steps: queue at most ``budget`` swaps that move the layer's
+    hot set toward the saved row map's (one saved by moe_get_rowmap, e.g. at
+    boot).  Returns the number of swaps applied; 0 once the hot set is
+    restored.  "We Built the Counter", section 2: restore to the boot-time
+    map, at most 8 swaps per step."""
+    row_map = moe_get_rowmap(ctx, layer, len(saved))
+    promote, demote = moe_plan_restore(row_map, saved, budget)
+    if promote.size == 0:
+        return 0
+    n, _ = moe_swap_rows(ctx, layer, promote, demote, stream)
+    return n

@@ -257,6 +257,24 @@ int moe_policy_destroy(moe_policy *p);
 int moe_policy_read(moe_policy *p, const int32_t *counts, const int32_t *row_map,
                     int32_t *promote, int32_t *demote);
 
+/* ---- restore a saved placement (host, between steps) ----
+ * "We Built the Counter", section 2: the runtime control can queue a restore
+ * to the boot-time map, and the round-trip check restores the boot-time hot
+ * set by swaps with the output unchanged.  A map is saved with
+ * moe_get_rowmap.  moe_plan_restore gives the swaps that bring row_map's hot
+ * set back to target's: the experts cold in row_map and hot in target, in
+ * ascending id, are promoted, the i-th against the i-th expert hot in row_map
+ * and cold in target (ascending id).  Only the hot SET is restored; the row an
+ * expert takes inside a bank changes no output.  At most max_pairs pairs are
+ * written (call again after applying them with moe_swap_rows to continue;
+ * a step budget of 8 swaps keeps the restore off the step's critical path).
+ * row_map, target: host int32 [experts] (negative = cold); promote, demote:
+ * host int32 [max_pairs] out.  Returns the pair count (0 = restored), or
+ * MOE_EINVAL when the maps hold different numbers of hot experts or an
+ * argument is invalid. */
+int moe_plan_restore(int experts, const int32_t *row_map, const int32_t *target, int max_pairs,
+                     int32_t *promote, int32_t *demote);
+
 #ifdef __cplusplus
 }
 #endif

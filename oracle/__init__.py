@@ -61,6 +61,7 @@ def _load():
             "orc_layer_step": (None, [P, P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P, P, P, i32, i32]),
             "orc_rows_for_slots": (None, [P, P, P, P, i32, i32, i32, P, P, P, i32, P]),
             "orc_swap": (i32, [P, i32, i32, P, P, P]),
+            "orc_plan_restore": (i32, [P, P, i32, i32, P, P]),
             "orc_policy_init": (None, [P, i32, P, P, P]),
             "orc_policy_read": (i32, [P, P, P, f64, f64, f64, f64, i32, P, P]),
             "orc_expert_bytes": (i64, [i32, i32]),
@@ -237,6 +238,21 @@ def swap(row_map: np.ndarray, promote, demote):
     applied = np.zeros(promote.size, np.int32)
     _load().orc_swap(_p(row_map), row_map.size, promote.size, _p(promote), _p(demote), _p(applied))
     return applied
+
+
+def plan_restore(row_map, target, max_pairs: int):
+    """Swap pairs that bring ``row_map``'s hot set back to ``target``'s
+    (see moe_oracle.h).  Returns (promote, demote) int32 arrays, or None when
+    the two maps hold different numbers of hot experts."""
+    rm = _c(row_map, np.int32)
+    tg = _c(target, np.int32)
+    assert rm.size == tg.size
+    pro = np.zeros(max(rm.size, 1), np.int32)
+    dem = np.zeros(max(rm.size, 1), np.int32)
+    n = _load().orc_plan_restore(_p(rm), _p(tg), rm.size, int(max_pairs), _p(pro), _p(dem))
+    if n < 0:
+        return None
+    return pro[:n].copy(), dem[:n].copy()
 
 
 class _Policy(C.Structure):

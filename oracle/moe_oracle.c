@@ -321,6 +321,26 @@ int orc_swap(int32_t *row_map, int E, int n, const int32_t *promote, const int32
     return done;
 }
 
+/* ----------------------------------------------------------------- restore */
+
+int orc_plan_restore(const int32_t *row_map, const int32_t *target, int E, int max_pairs,
+                     int32_t *promote, int32_t *demote) {
+    int hot_now = 0, hot_target = 0;
+    for (int e = 0; e < E; ++e) {
+        hot_now += row_map[e] >= 0;
+        hot_target += target[e] >= 0;
+    }
+    if (hot_now != hot_target) return -1;
+    /* the i-th expert to come in pairs with the i-th expert to go out */
+    int n_in = 0, n_out = 0;
+    for (int e = 0; e < E; ++e) {
+        int was_hot = row_map[e] >= 0, want_hot = target[e] >= 0;
+        if (!was_hot && want_hot && n_in < max_pairs) promote[n_in++] = e;
+        if (was_hot && !want_hot && n_out < max_pairs) demote[n_out++] = e;
+    }
+    return n_in < n_out ? n_in : n_out;
+}
+
 /* ------------------------------------------------------------------ policy */
 
 void orc_policy_init(orc_policy_t *p, int E, uint32_t *last, double *acc, const int32_t *counts) {

@@ -121,6 +121,18 @@ void orc_rows_for_slots(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_
 int orc_swap(int32_t *row_map, int E, int n, const int32_t *promote, const int32_t *demote,
              int32_t *applied);
 
+/* ---- restore to a saved placement ----
+ * "We Built the Counter", section 2 (runtime control: queue a restore to the
+ * boot-time map) and the round-trip check (the boot-time hot set is restored
+ * by swaps and the output is unchanged).  Reading: a restore brings back the
+ * saved HOT SET; which row of a bank an expert occupies changes no output.
+ * Pairs: the experts cold in row_map and hot in target (ascending id) are
+ * promoted, each against the next expert hot in row_map and cold in target
+ * (ascending id); at most max_pairs pairs.  Returns the pair count, or -1
+ * when the two maps have different hot counts. */
+int orc_plan_restore(const int32_t *row_map, const int32_t *target, int E, int max_pairs,
+                     int32_t *promote, int32_t *demote);
+
 /* ---- adaptive policy (host side, between steps) ----
  * State per layer: the last counts read, an exponentially decaying sum of the
  * per-read pick deltas and the matching decaying sum of weights.  At a read:

@@ -1,6 +1,7 @@
 """The C ABI without a GPU: the library builds for sm_103a and loads, every
 symbol include/moe_residency.h declares is exported, argument validation
-fails cleanly, and the native host policy takes the oracle's decisions."""
+fails cleanly, and the native host policy and restore planner take the
+oracle's decisions."""
 import ctypes as C
 
 import numpy as np
@@ -83,3 +84,28 @@ def test_policy_counts_wrap_as_uint32(lib):
     now = (np.array([2**31 - 5 + 2, 2**31 - 5 + 40], np.int64) & 0xFFFFFFFF).astype(np.uint32).view(np.int32)
     assert [x.tolist() for x in nat.read(now, rm)] == [[1], [0]]
     assert [x.tolist() for x in ref.read(now, rm)] == [[1], [0]]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_native_restore_plan_matches_oracle(lib, seed):
+    rng = np.random.default_rng(seed)
+    E = 384
+    mask = np.zeros(E, np.uint8)
+    mask[rng.permutation(E)[:295]] = 1
+    saved, _, _ = oracle.initial_rowmap(mask)
+    rm = saved.copy()
+    for _ in range(40):
+        hot, cold = np.flatnonzero(rm >= 0), np.flatnonzero(rm < 0)
+        oracle.swap(rm, [rng.choice(cold)], [rng.choice(hot)])
+    for budget in (0, 1, 8, E):
+        a = oracle.plan_restore(rm, saved, budget)
+        b = moe.moe_plan_restore(rm, saved, budget)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), budget
+
+
+def test_native_restore_plan_rejects_a_different_hot_count(lib):
+    now, _, _ = oracle.initial_rowmap(np.array([1, 0, 0], np.uint8))
+    other, _, _ = oracle.initial_rowmap(np.array([1, 1, 0], np.uint8))
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_plan_restore(now, other, 4)
+    assert ei.value.code == moe.MOE_EINVAL and "hot experts" in str(ei.value)

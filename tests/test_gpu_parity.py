@@ -159,6 +159,56 @@ def test_swaps_bit_identical_and_negative_control(impl):
         ref.close()
 
 
+@pytest.mark.parametrize("impl", IMPLS)
+def test_restore_round_trip_is_lossless(impl):
+    """Wander away from the boot placement with swaps, restore its hot set in
+    budgets of three swaps, then check every expert's bank row byte for byte
+    against its packing and the output against the all-HBM layer."""
+    from cold_expert_residency_gb300.runtime import restore_placement
+    cfg = synth.get_config("tiny")
+    w = synth.layer_weights(cfg, 0)
+    h = Harness(cfg, weights={0: w}, impl=impl)
+    ref = Harness(cfg, weights={0: w}, masks={0: np.ones(cfg.E, np.uint8)}, impl=impl)
+    try:
+        lg = synth.router_logits(cfg, 0, 1)
+        x = synth.activations(cfg, 0, 1)
+        base = ref.run(0, lg, x)
+        boot = h.moe.moe_get_rowmap(h.ctx, 0, cfg.E).copy()
+        rng = np.random.default_rng(5)
+        rm = boot.copy()
+        for _ in range(3):       # three adaptation rounds of up to four swaps each
+            pro = rng.permutation(np.flatnonzero(rm < 0))[:4]
+            dem = rng.permutation(np.flatnonzero(rm >= 0))[:pro.size]
+            n, applied = h.moe.moe_swap_rows(h.ctx, 0, pro, dem)
+            assert applied.tolist() == oracle.swap(rm, pro, dem).tolist()
+            assert np.array_equal(h.run(0, lg, x)["out"], base["out"])
+        away = int(np.count_nonzero((rm >= 0) & (boot < 0)))
+        assert away > 0
+        total, calls = 0, 0
+        while True:
+            n = restore_placement(h.ctx, 0, boot, budget=3)
+            if n == 0:
+                break
+            total += n
+            calls += 1
+            assert np.array_equal(h.run(0, lg, x)["out"], base["out"])
+        assert total == away and calls == -(-away // 3)
+        rm = h.moe.moe_get_rowmap(h.ctx, 0, cfg.E)
+        assert np.array_equal(rm >= 0, boot >= 0)
+        assert np.array_equal(h.moe.moe_read_rowmap_device(h.ctx, 0, cfg.E), rm)
+        eb = h.moe.moe_expert_bytes(cfg.H, cfg.I)
+        for e in range(cfg.E):
+            bank, row = (0, rm[e]) if rm[e] >= 0 else (1, -1 - rm[e])
+            got = h.moe.moe_read_bank_row(h.ctx, 0, bank, int(row), eb)
+            want = h.moe.moe_pack_expert(cfg.H, cfg.I, *(a[e] for a in w))
+            assert np.array_equal(got, want), e
+        r = h.run(0, lg, x)
+        assert np.array_equal(r["out"], base["out"]) and np.array_equal(r["Y"], base["Y"])
+    finally:
+        h.close()
+        ref.close()
+
+
 def test_counts_only_for_small_steps_and_when_on():
     cfg = synth.get_config("tiny")
     h = Harness(cfg, T_max=300)

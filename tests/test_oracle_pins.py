@@ -396,3 +396,52 @@ def test_policy_hysteresis_boundary_is_strict():
     pol3 = oracle.Policy(E, read_every=1, half_life=1e9, hysteresis=1.5, min_avg=8, max_pairs=4)
     pro, _ = pol3.read(np.array([0, 7], np.int32), rm)        # below minimum average
     assert pro.size == 0
+
+
+# ------------------------------------------------------------------ restore
+
+def test_restore_plan_hand_example():
+    # now hot {0, 1, 3, 6}; saved hot {1, 2, 3, 4}: 2 and 4 come in, 0 and 6 go out
+    now, _, _ = oracle.initial_rowmap(np.array([1, 1, 0, 1, 0, 0, 1], np.uint8))
+    saved, _, _ = oracle.initial_rowmap(np.array([0, 1, 1, 1, 1, 0, 0], np.uint8))
+    pro, dem = oracle.plan_restore(now, saved, 8)
+    assert pro.tolist() == [2, 4] and dem.tolist() == [0, 6]
+    pro, dem = oracle.plan_restore(now, saved, 1)
+    assert pro.tolist() == [2] and dem.tolist() == [0]
+    assert [a.tolist() for a in oracle.plan_restore(now, now, 8)] == [[], []]
+    bigger, _, _ = oracle.initial_rowmap(np.array([1, 1, 1, 1, 1, 0, 0], np.uint8))
+    assert oracle.plan_restore(now, bigger, 8) is None        # hot counts differ
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_restore_reaches_the_saved_hot_set_in_the_fewest_swaps(seed):
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(2, 200))
+    n_hot = int(rng.integers(1, E))
+    saved_mask = np.zeros(E, np.uint8)
+    saved_mask[rng.permutation(E)[:n_hot]] = 1
+    saved, _, _ = oracle.initial_rowmap(saved_mask)
+    rm = saved.copy()
+    # wander away with random valid swaps
+    for _ in range(int(rng.integers(0, 3 * E))):
+        hot, cold = np.flatnonzero(rm >= 0), np.flatnonzero(rm < 0)
+        oracle.swap(rm, [rng.choice(cold)], [rng.choice(hot)])
+    # each swap moves one expert in and one out, so no plan can be shorter
+    # than the number of experts hot now and cold in the saved map
+    need = int(np.count_nonzero((rm >= 0) & (saved < 0)))
+    budget = int(rng.integers(1, 9))
+    rounds, total = 0, 0
+    while True:
+        pro, dem = oracle.plan_restore(rm, saved, budget)
+        if pro.size == 0:
+            break
+        assert pro.size <= budget
+        assert np.all(rm[pro] < 0) and np.all(saved[pro] >= 0)
+        assert np.all(rm[dem] >= 0) and np.all(saved[dem] < 0)
+        assert oracle.swap(rm, pro, dem).tolist() == [1] * pro.size
+        rounds += 1
+        total += pro.size
+    assert total == need and rounds == -(-need // budget)
+    assert np.array_equal(rm >= 0, saved >= 0)
+    hot_rows = sorted(rm[rm >= 0].tolist())
+    assert hot_rows == list(range(n_hot))                   # still a bijection onto the bank rows
