@@ -504,10 +504,33 @@ def main():
                 ts.append(ev0.elapsed_time(ev1) * 1e3)
             return float(np.mean(ts))
         r_us = part(False, False)
-        breakdown = {"route_us": r_us, "hot_alone_us": float(np.mean(hot_ms)) * 1e3,
+
+        def router_alone():
+            """The router GEMM that would produce layer 0's logits from its
+            hidden states (the workload supplies logits, so it is outside the
+            step), graph-replayed after an L2 flush."""
+            wr = torch.from_numpy(synth.router_weights(cfg, 0).view(np.int16)).to(dev)
+            br = torch.from_numpy(synth.router_bias(cfg, 0)).to(dev)
+            rl = torch.empty((T, E), dtype=torch.float32, device=dev)
+            g3 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g3, stream=main):
+                moe.moe_router_logits(ctx, steps[0].buf.x, wr, br, T, E, H, rl, main)
+            ts = []
+            for i in range(min(args.steps, 20)):
+                load_inputs(i, main)
+                with torch.cuda.stream(main):
+                    flush.zero_()
+                    ev0.record(main)
+                    g3.replay()
+                    ev1.record(main)
+                main.synchronize()
+                ts.append(ev0.elapsed_time(ev1) * 1e3)
+            return float(np.mean(ts))
+        breakdown = {"route_us": r_us, "router_gemm_us": router_alone(), "hot_alone_us": float(np.mean(hot_ms)) * 1e3,
                      "cold_alone_us": float(np.mean(ffn_alone(moe.MOE_BANK_COLD)[0])) * 1e3,
                      "ffn_in_step_us": float(np.mean(ffn_ms)) * 1e3, "banks": args.banks,
-                     "note": "layer 0: each bank's FFN call alone after routing, and the step's both-bank FFN call"}
+                     "note": "layer 0: each bank's FFN call alone after routing, and the step's both-bank FFN call; "
+                             "the router GEMM (hidden states -> logits) alone, outside the step"}
 
     ms = total_ms / args.steps
     tokens_per_step = T   # one layer-step of T tokens (all layers of the config)

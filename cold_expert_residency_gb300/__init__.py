@@ -66,6 +66,7 @@ def lib():
         "moe_expert_ffn_bank_static": (i32, [P, i32, i32, P, i32, P, P, P]),
         "moe_static_scratch_bytes": (sz, []),
         "moe_finalize": (i32, [P, P, i32, i32, i32, P, P]),
+        "moe_router_logits": (i32, [P, P, P, P, i32, i32, i32, P, P]),
         "moe_swap_rows": (i32, [P, i32, i32, P, P, P, P]),
         "moe_read_counts": (i32, [P, P, P]),
         "moe_reset_counts": (i32, [P, P]),
@@ -217,6 +218,11 @@ def moe_static_scratch_bytes():
 
 def moe_finalize(Y, w, T, k, H, out, stream=None):
     return _err("moe_finalize", lib().moe_finalize(_ptr(Y), _ptr(w), T, k, H, _ptr(out), _stream(stream)))
+
+
+def moe_router_logits(ctx, x, w_router, bias, T, E, H, logits, stream=None):
+    return _err("moe_router_logits", lib().moe_router_logits(ctx, _ptr(x), _ptr(w_router), _ptr(bias), T, E, H,
+                                                             _ptr(logits), _stream(stream)))
 
 
 def moe_swap_rows(ctx, layer, promote, demote, stream=None):

@@ -432,6 +432,19 @@ int moe_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_
     return launch_finalize(Y, w, T, k, H, out, (cudaStream_t)stream);
 }
 
+int moe_router_logits(moe_ctx *ctx, const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int E,
+                      int H, float *logits, void *stream) {
+    if (!ctx) return set_error(MOE_EINVAL, "null context");
+    if (T < 0 || E < 1 || E > (1 << 20) || H < 8 || H % 8)
+        return set_error(MOE_EINVAL, "bad router shape (H % 8 == 0, 1 <= E <= 2^20)");
+    if (T == 0) return MOE_OK;
+    if (!x || !w_router || !logits) return set_error(MOE_EINVAL, "null pointer");
+    if (((uintptr_t)x | (uintptr_t)w_router) % 16 || (uintptr_t)logits % 4 || (uintptr_t)bias % 4)
+        return set_error(MOE_EINVAL, "x and w_router must be 16-byte aligned, logits and bias 4-byte aligned");
+    DeviceGuard guard(ctx->device);
+    return launch_router(x, w_router, bias, T, E, H, logits, ctx->status_dev, ctx->sms, (cudaStream_t)stream);
+}
+
 int moe_swap_rows(moe_ctx *ctx, int layer, int n, const int32_t *promote, const int32_t *demote,
                   int32_t *applied, void *stream) {
     if (int r = check_layer(ctx, layer, true)) return r;

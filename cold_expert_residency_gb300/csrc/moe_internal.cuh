@@ -235,6 +235,8 @@ int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int bank_id, const uint16_t 
 int make_weight_map(CUtensorMap *map, const uint8_t *bank, const Geom &g, const PartLayout &part, int rows);
 int launch_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_t *out,
                     cudaStream_t s);
+int launch_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int E, int H,
+                  float *logits, int32_t *status, int sms, cudaStream_t s);
 int launch_rowmap_write(int32_t *rowmap_dev, int32_t e0, int32_t v0, int32_t e1, int32_t v1,
                         cudaStream_t s);
 int launch_probe_read(const uint8_t *src, size_t bytes, uint64_t *sink, int blocks,

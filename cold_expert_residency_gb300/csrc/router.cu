@@ -1,0 +1,329 @@
+// Router GEMM: the step that produces the routing logits from the layer's
+// hidden states.
+//
+// "vLLM: Pin Hot Experts", Where the experts live today: every MoE layer's
+// router scores all experts for every token and keeps its top-6, whichever
+// bank the experts sit in.  Here the scores are
+//     logits[t][e] = bias[e] + sum_h x[t][h] * w_router[e][h]
+// with bf16 hidden states and router weights, exact products, fp32 sums and
+// fp32 logits written where the routing kernel reads them.
+//
+// Two kernels:
+//  * up to 32 tokens (decode): CUDA cores.  One CTA per (expert, group of 8
+//    tokens); its 8 warps split K, so every lane has at most a couple of
+//    16-byte weight loads in flight and the 3 MB of router weights (E = 384,
+//    H = 4096) stream from HBM across the whole GPU.  Each lane sums its
+//    columns in order, a butterfly adds the 32 lanes, the 8 warps' sums are
+//    added in warp order, then the bias.
+//  * more tokens: a dense bf16 GEMM on the tensor cores (tcgen05.mma
+//    kind::f16, fp32 accumulator in tensor memory).  One CTA per (128-token
+//    tile, BN-expert tile); one thread issues TMA loads of 64-wide K slices of
+//    both operands (128-byte swizzle) into a ring of stages, one thread
+//    issues the MMAs, four warps read the accumulator back and add the bias.
+//    Tokens and experts past the ends are zero-filled by the TMA and never
+//    stored.  At 8192 tokens the GEMM is 25.8 GFLOP.
+//
+// Every mbarrier wait is bounded; on timeout the kernel sets the status word
+// to MOE_ETIMEOUT, lets its own copies and MMAs in flight finish, frees its
+// tensor memory and returns.
+#include "moe_internal.cuh"
+#include "sm103_ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace moe {
+
+namespace {
+
+// ---------------------------------------------------------------- CUDA cores
+
+constexpr int kTok = 8;      // tokens per CTA
+constexpr int kKWarps = 8;   // warps splitting K
+
+__device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
+    const uint32_t p[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        f[2 * q] = __uint_as_float(p[q] << 16);
+        f[2 * q + 1] = __uint_as_float(p[q] & 0xFFFF0000u);
+    }
+}
+
+__global__ void __launch_bounds__(32 * kKWarps) router_simt_kernel(const uint4 *__restrict__ x,
+                                                                   const uint4 *__restrict__ w,
+                                                                   const float *__restrict__ bias, int T, int E,
+                                                                   int H8, float *__restrict__ logits) {
+    __shared__ float part[kKWarps][kTok];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int e = blockIdx.x;
+    const int t0 = blockIdx.y * kTok;
+    const int nt = min(kTok, T - t0);            // >= 1: the grid covers T exactly
+    const uint4 *wr = w + (size_t)e * H8;
+    const uint4 *xr = x + (size_t)t0 * H8;
+    float acc[kTok];
+#pragma unroll
+    for (int j = 0; j < kTok; ++j) acc[j] = 0.0f;
+    for (int c = warp * 32 + lane; c < H8; c += 32 * kKWarps) {
+        float wf[8];
+        bf16x8(__ldg(wr + c), wf);
+#pragma unroll
+        for (int j = 0; j < kTok; ++j) {
+            if (j < nt) {
+                float xf[8];
+                bf16x8(__ldg(xr + (size_t)j * H8 + c), xf);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[j] = __fmaf_rn(xf[q], wf[q], acc[j]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kTok; ++j) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
+        if (lane == 0) part[warp][j] = acc[j];
+    }
+    __syncthreads();
+    if (threadIdx.x < nt) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kKWarps; ++q) sum += part[q][threadIdx.x];
+        logits[(size_t)(t0 + threadIdx.x) * E + e] = sum + (bias ? __ldg(bias + e) : 0.0f);
+    }
+}
+
+// -------------------------------------------------------------- tensor cores
+
+constexpr int kBM = 128;                 // tokens per tile (MMA M)
+constexpr int kBK = 64;                  // K elements per stage (128 bytes of bf16: one swizzle row)
+constexpr int kAStage = kBM * kBK * 2;   // 16 KB
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint32_t kDrainPolls = 1u << 22;
+
+template <int BN>
+struct RouterCfg {
+    static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "MMA N");
+    static constexpr int kStages = BN >= 128 ? 5 : 8;
+    static constexpr int kBStage = BN * kBK * 2;
+    static constexpr int kStage = kAStage + kBStage;
+    static constexpr uint32_t kCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;   // TMEM columns
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + (2 * kStages + 1) * 8 + 16;
+};
+
+// Bounded mbarrier wait (one thread): false once kWaitNs of wall-clock time
+// have passed or another role gave up.
+__device__ __forceinline__ bool rwait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int32_t *status) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0u) {
+            if (*abort_flag) return false;
+            const uint64_t now = ptx::globaltimer_ns();
+            if (i == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitNs) {
+                *abort_flag = 1;
+                atomicCAS(status, 0, MOE_ETIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                     const float *__restrict__ bias, int T, int E, int H, float *__restrict__ logits,
+                     int32_t *status) {
+    using C = RouterCfg<BN>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = (uint64_t *)(smem + (size_t)S * C::kStage);   // FULL[S], DONE[S], ACC
+    uint32_t *holder = (uint32_t *)(bars + 2 * S + 1);
+    volatile int *abort_flag = (volatile int *)(holder + 1);
+    auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
+    const int FULL = 0, DONE = S, ACC = 2 * S;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * BN;
+    const int nk = (H + kBK - 1) / kBK;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(bar(FULL + s), 1);
+            ptx::mbar_init(bar(DONE + s), 1);
+        }
+        ptx::mbar_init(bar(ACC), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 4 && lane == 0) {
+        ptx::prefetch_tmap(&tmX);
+        ptx::prefetch_tmap(&tmW);
+    }
+    if (warp == 5) {
+        ptx::tmem_alloc(ptx::smem_addr(holder), C::kCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *holder;
+
+    if (warp < 4) {
+        // ---------------------------------------------------------- epilogue
+        // thread 32 w + l reads accumulator row (token) m0 + 32 w + l
+        const bool ok = rwait(bar(ACC), 0, abort_flag, status);
+        if (__all_sync(0xFFFFFFFFu, ok)) {
+            ptx::tc_fence_after();
+            const int t = m0 + warp * 32 + lane;
+            float *row = logits + (size_t)t * E;
+            const bool vec = (E % 4) == 0 && ((uintptr_t)logits % 16) == 0;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
+                ptx::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, r);
+                ptx::tmem_wait_ld();
+                if (t < T) {
+                    const int e0 = n0 + c0;
+                    if (vec && e0 + 32 <= E) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            float4 v;
+                            v.x = __uint_as_float(r[i]) + (bias ? __ldg(bias + e0 + i) : 0.0f);
+                            v.y = __uint_as_float(r[i + 1]) + (bias ? __ldg(bias + e0 + i + 1) : 0.0f);
+                            v.z = __uint_as_float(r[i + 2]) + (bias ? __ldg(bias + e0 + i + 2) : 0.0f);
+                            v.w = __uint_as_float(r[i + 3]) + (bias ? __ldg(bias + e0 + i + 3) : 0.0f);
+                            *reinterpret_cast<float4 *>(row + e0 + i) = v;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (e0 + i < E) row[e0 + i] = __uint_as_float(r[i]) + (bias ? __ldg(bias + e0 + i) : 0.0f);
+                    }
+                }
+            }
+        }
+    } else if (warp == 4 && lane == 0) {
+        // ---------------------------------------------------------- producer
+        int it = 0;
+        bool ok = true;
+        for (; it < nk; ++it) {
+            const int st = it % S;
+            if (it >= S && !rwait(bar(DONE + st), ((it / S) - 1) & 1, abort_flag, status)) {
+                ok = false;
+                break;
+            }
+            uint8_t *a = smem + (size_t)st * C::kStage;
+            // out-of-range rows and columns are zero-filled and still counted
+            ptx::mbar_arrive_expect_tx(bar(FULL + st), (uint32_t)C::kStage);
+            ptx::tma_load_2d(ptx::smem_addr(a), &tmX, it * kBK, m0, bar(FULL + st));
+            ptx::tma_load_2d(ptx::smem_addr(a + kAStage), &tmW, it * kBK, n0, bar(FULL + st));
+        }
+        if (!ok) {
+            // let the copies this thread issued land before the CTA goes away
+            for (int i = it > S ? it - S : 0; i < it; ++i)
+                for (uint32_t p = 0; p < kDrainPolls; ++p)
+                    if (ptx::mbar_try_wait(bar(FULL + i % S), (i / S) & 1)) break;
+        }
+    } else if (warp == 5 && lane == 0) {
+        // --------------------------------------------------------- MMA issue
+        constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, BN);
+        int it = 0;
+        bool ok = true;
+        for (; it < nk; ++it) {
+            const int st = it % S;
+            if (!rwait(bar(FULL + st), (it / S) & 1, abort_flag, status)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a_addr = ptx::smem_addr(smem + (size_t)st * C::kStage);
+            const uint32_t b_addr = a_addr + kAStage;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)   // 16 bf16 = 32 bytes per MMA
+                ptx::mma_f16_ss(tmem, ptx::smem_desc_sw128(a_addr + kk * 32), ptx::smem_desc_sw128(b_addr + kk * 32),
+                                idesc, (it | kk) != 0);
+            ptx::mma_commit(bar(DONE + st));
+        }
+        if (ok) {
+            ptx::mma_commit(bar(ACC));
+        } else if (it > 0) {
+            // wait until the MMAs already issued have retired (bounded)
+            const int last = it - 1;
+            for (uint32_t p = 0; p < kDrainPolls; ++p)
+                if (ptx::mbar_try_wait(bar(DONE + last % S), (last / S) & 1)) break;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::kCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// Row-major bf16 [rows][H] as (column, row) boxes of 64 columns x box_rows
+// rows, 128-byte swizzle, zero fill outside.
+int bf16_rows_map(CUtensorMap *map, const uint16_t *base, int rows, int H, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled (router) failed: " + std::to_string((int)r));
+    return MOE_OK;
+}
+
+template <int BN>
+int launch_router_tc(const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int E, int H,
+                     float *logits, int32_t *status, cudaStream_t s) {
+    using C = RouterCfg<BN>;
+    CUtensorMap tmX, tmW;
+    if (int r = bf16_rows_map(&tmX, x, T, H, kBM)) return r;
+    if (int r = bf16_rows_map(&tmW, w_router, E, H, BN)) return r;
+    auto kern = router_tc_kernel<BN>;
+    MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem));
+    const dim3 grid((T + kBM - 1) / kBM, (E + BN - 1) / BN);
+    kern<<<grid, 192, C::kSmem, s>>>(tmX, tmW, bias, T, E, H, logits, status);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+}  // namespace
+
+int launch_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int E, int H,
+                  float *logits, int32_t *status, int sms, cudaStream_t s) {
+    if (T <= 32) {
+        const dim3 grid(E, (T + kTok - 1) / kTok);
+        router_simt_kernel<<<grid, 32 * kKWarps, 0, s>>>((const uint4 *)x, (const uint4 *)w_router, bias, T, E, H / 8,
+                                                         logits);
+        MOE_LAUNCH_CHECK();
+        return MOE_OK;
+    }
+    // wide expert tiles once they alone fill half the SMs; narrow ones
+    // spread a few token tiles over more CTAs
+    const int mtiles = (T + kBM - 1) / kBM;
+    if (2 * mtiles * ((E + 191) / 192) >= sms)
+        return launch_router_tc<192>(x, w_router, bias, T, E, H, logits, status, s);
+    return launch_router_tc<32>(x, w_router, bias, T, E, H, logits, status, s);
+}
+
+}  // namespace moe

@@ -90,6 +90,14 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, int 
         "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
         : "memory");
 }
+// 2-D tiled tensor copy global -> shared (coordinates innermost first).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
 // 4-D tiled tensor copy global -> shared (coordinates innermost first).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int c0, int c1, int c2, int c3, uint32_t bar) {
     asm volatile(
@@ -186,6 +194,16 @@ __device__ __forceinline__ void mma_mxf8f6f4_ss(uint32_t d_tmem, uint64_t a_desc
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (A and B both bf16
+// here), fp32 accumulator, issued by one thread.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Shared -> tensor memory copy of a 32-row x 16-byte matrix (smem
 // descriptor) into lanes 0-31 of four columns from taddr, repeated in all
 // four lane quarters.  Ordered with the same thread's later tcgen05.mma.
@@ -249,6 +267,16 @@ __host__ __device__ constexpr uint32_t idesc_mx_e2m1_e4m3(int M, int N, int sfa_
            | (1u << 23)                    // scale format: e8m0
            | ((uint32_t)(M >> 4) << 24)    // M / 16
            | ((uint32_t)sfa_id << 29);     // A scale byte
+}
+
+// Instruction descriptor for kind::f16: bf16 A and B, both K-major, f32
+// accumulator, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                       // accumulator format: f32
+           | (1u << 7)                     // A format: bf16
+           | (1u << 10)                    // B format: bf16
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
 }  // namespace ptx

@@ -1,6 +1,7 @@
 """Layer-step orchestration over the C ABI (streams and buffers only).
 
 One layer-step ("vLLM: Pin Hot Experts", Results):
+    [router GEMM                     (moe_router_logits, optional)]
     route + split + count            (moe_route_split_count, main stream)
     hot-bank FFN   || cold-bank FFN  (moe_expert_ffn_bank on the main stream
                                       and on a second stream, joined by events)
@@ -15,7 +16,8 @@ from __future__ import annotations
 import torch
 
 from . import (MOE_BANK_BOTH, MOE_BANK_COLD, MOE_BANK_HOT, moe_expert_ffn_bank, moe_finalize,
-               moe_get_rowmap, moe_plan_restore, moe_route_split_count, moe_swap_rows, moe_workspace_bytes)
+               moe_get_rowmap, moe_plan_restore, moe_route_split_count, moe_router_logits, moe_swap_rows,
+               moe_workspace_bytes)
 
 
 class StepBuffers:
@@ -48,15 +50,20 @@ class LayerStep:
         self.ev_routed = torch.cuda.Event()
         self.ev_cold = torch.cuda.Event()
 
-    def run(self, layer, T, count_on=True, stream=None, split=True, fused=True):
+    def run(self, layer, T, count_on=True, stream=None, split=True, fused=True, router=None):
         """Enqueue one layer-step of T tokens from buf.logits / buf.x into
         buf.out (and buf.ids, buf.w, buf.Y).  By default one FFN call covers
         both banks (its launches stream the cold bank from one CTA per SM
         and the hot bank from the others); ``fused=False`` runs the two banks'
         calls on two streams at once, and with ``split=False`` one after the
-        other on the main stream."""
+        other on the main stream.  ``router=(w_router, bias)`` (device bf16
+        [E][H] and fp32 [E] or None) first computes buf.logits from buf.x by
+        the router GEMM."""
         b = self.buf
         main = stream if stream is not None else torch.cuda.current_stream()
+        if router is not None:
+            w_router, bias = router
+            moe_router_logits(self.ctx, b.x, w_router, bias, T, b.E, b.H, b.logits, main)
         moe_route_split_count(self.ctx, layer, b.logits, T, count_on, b.ids, b.w, b.ws_ptr, main)
         if fused:
             moe_expert_ffn_bank(self.ctx, layer, MOE_BANK_BOTH, b.x, T, b.ws_ptr, b.Y, main)

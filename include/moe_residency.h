@@ -186,6 +186,22 @@ int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t
                                const void *split_ws, uint16_t *Y, void *stream);
 size_t moe_static_scratch_bytes(void);
 
+/* Router GEMM (async): the logits the routing call reads.  "vLLM: Pin Hot
+ * Experts", Where the experts live today: each MoE layer's router scores all
+ * experts for every token, whatever bank they sit in.
+ *   logits[t][e] = bias[e] + sum_h x[t][h] * w_router[e][h]
+ * x: device bf16 [T][H] (16-byte aligned); w_router: device bf16 [E][H]
+ * (16-byte aligned); bias: device fp32 [E] or NULL (zero); logits: device
+ * fp32 [T][E] out.  Exact products, fp32 sums: up to 32 tokens on the CUDA
+ * cores (in a fixed order), beyond that on the tensor cores (kind::f16, fp32
+ * accumulator), so a logit may differ from the exactly rounded sum in its
+ * last bits.  H % 8 == 0, 1 <= E <= 2^20; T == 0 is a no-op.  The context
+ * gives the device and the status word a bounded wait sets on timeout
+ * (moe_device_status).  All other pointers are caller-owned.  MOE_EINVAL on
+ * a bad shape or a null or misaligned pointer. */
+int moe_router_logits(moe_ctx *ctx, const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int E,
+                      int H, float *logits, void *stream);
+
 /* Finalize (async).  "vLLM: Pin Hot Experts", Results: accumulate each
  * token's k bf16 expert rows in fp32 with fma in the original k order and
  * cast once:  out[t][c] = bf16(fma(w[t][k-1], Y[t][k-1][c], ... fma(w[t][0],

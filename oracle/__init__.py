@@ -52,6 +52,7 @@ def _load():
             "orc_dequant": (None, [P, P, i64, i64, P]),
             "orc_bf16_to_f32": (C.c_float, [C.c_uint16]),
             "orc_f32_to_bf16": (C.c_uint16, [C.c_float]),
+            "orc_router_logits": (None, [P, P, P, i32, i32, i32, P]),
             "orc_route": (None, [P, i32, i32, i32, P, P]),
             "orc_initial_rowmap": (None, [P, i32, P, P, P]),
             "orc_split": (None, [P, i32, P, i32, i32, P]),
@@ -112,6 +113,20 @@ def f32_to_bf16(f: float) -> int:
 
 
 # ----------------------------------------------------------------- routing
+
+def router_logits(x_bits: np.ndarray, w_router_bits: np.ndarray, bias=None) -> np.ndarray:
+    """x bf16 bits [T][H], router weight bf16 bits [E][H], bias fp32 [E] or
+    None -> logits float32 [T][E]."""
+    x = _c(x_bits, np.uint16)
+    w = _c(w_router_bits, np.uint16)
+    T, H = x.shape
+    E = w.shape[0]
+    assert w.shape[1] == H
+    b = None if bias is None else _c(bias, np.float32)
+    out = np.empty((T, E), np.float32)
+    _load().orc_router_logits(_p(x), _p(w), None if b is None else _p(b), T, E, H, _p(out))
+    return out
+
 
 def route(logits: np.ndarray, k: int):
     """-> ids int32 [T][k], w float32 [T][k]."""

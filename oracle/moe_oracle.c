@@ -74,6 +74,22 @@ uint16_t orc_f32_to_bf16(float f) {
     return (uint16_t)(u >> 16);
 }
 
+/* ------------------------------------------------------------------ router */
+
+void orc_router_logits(const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int E, int H,
+                       float *logits) {
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            double sum = bias ? (double)bias[e] : 0.0;
+            for (int h = 0; h < H; ++h)
+                sum += (double)orc_bf16_to_f32(x[(int64_t)t * H + h]) *
+                       (double)orc_bf16_to_f32(w_router[(int64_t)e * H + h]);
+            logits[(int64_t)t * E + e] = (float)sum;
+        }
+    }
+}
+
 /* ---------------------------------------------------------------- routing */
 
 /* a ranks before b: larger logit first, equal logits by lower expert id. */

@@ -52,6 +52,14 @@ void orc_dequant(const uint8_t *q, const uint8_t *s, int64_t rows, int64_t K, do
 float orc_bf16_to_f32(uint16_t b);
 uint16_t orc_f32_to_bf16(float f);             /* round to nearest even */
 
+/* ---- router (the step that produces the logits) ----
+ * "vLLM: Pin Hot Experts", Where the experts live today: the router scores
+ * every expert for every token.  logits[t][e] = fp32(bias[e] + sum_h
+ * x[t][h] * w_router[e][h]) with bf16 x and w_router widened exactly, the sum
+ * taken in double and rounded to fp32 once.  bias may be NULL (zero). */
+void orc_router_logits(const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int E, int H,
+                       float *logits);
+
 /* ---- routing: top-k over fp32 logits, softmax over the k picks ----
  * ids[t][j]: the j-th largest logit of token t (ties: lower expert id first);
  * w[t][j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k picks, in fp32,

@@ -23,6 +23,8 @@ Workloads (the write-ups' decode and prefill shapes; see ``CONFIGS``)
 * logits: fp32(N(0,1) + bias_e), with bias_e = beta * ln p_rank(e) for a
   Zipf(s) popularity law over a seeded per-layer ranking of the experts
   (the write-ups measure the top-25% of experts taking ~71% of decode picks).
+* router weights (for the router GEMM that produces logits from hidden
+  states): bf16(N(0,1)/sqrt(H)) [E][H], with the same per-expert bias.
 * hot bank: the ``n_hot`` experts with the best Zipf rank; cold bank: the rest.
 """
 from __future__ import annotations
@@ -36,7 +38,7 @@ import numpy as np
 
 __all__ = [
     "Config", "CONFIGS", "get_config", "stream_u64", "stream_bytes",
-    "expert_weights", "layer_weights", "activations", "router_logits",
+    "expert_weights", "layer_weights", "activations", "router_logits", "router_weights", "router_bias",
     "zipf_ranks", "zipf_bias", "hot_mask", "shifted_ranks", "spearman",
     "bf16_bits_to_f32", "expert_bytes",
 ]
@@ -297,18 +299,38 @@ def zipf_bias(cfg: Config, rank: np.ndarray) -> np.ndarray:
     return cfg.beta * np.log(p[rank - 1])
 
 
+def _step_bias(cfg: Config, layer: int, step: int, s: int) -> np.ndarray:
+    rank = zipf_ranks(cfg, layer, 0, s)
+    if cfg.shift_at >= 0 and step >= cfg.shift_at:
+        rank = shifted_ranks(cfg, layer, rank, s)
+    return zipf_bias(cfg, rank)
+
+
 def router_logits(cfg: Config, layer: int = 0, step: int = 0, T: int | None = None,
                   seed: int | None = None) -> np.ndarray:
     """fp32 logits [T][E] = N(0,1) + bias_e (bias from the layer's Zipf
     ranking, re-drawn at ``cfg.shift_at`` when set)."""
     s = cfg.seed if seed is None else seed
     T = cfg.T if T is None else T
-    rank = zipf_ranks(cfg, layer, 0, s)
-    if cfg.shift_at >= 0 and step >= cfg.shift_at:
-        rank = shifted_ranks(cfg, layer, rank, s)
-    bias = zipf_bias(cfg, rank)
+    bias = _step_bias(cfg, layer, step, s)
     z = _normal(_key(s, "logit", layer, step), T * cfg.E).reshape(T, cfg.E)
     return (z + bias[None, :]).astype(np.float32)
+
+
+def router_weights(cfg: Config, layer: int = 0, seed: int | None = None) -> np.ndarray:
+    """bf16(N(0,1) / sqrt(H)) router weights [E][H] as uint16 bit patterns.
+    With bf16(N(0,1)) activations each score is then about N(0,1), the same
+    law as ``router_logits`` before its bias."""
+    s = cfg.seed if seed is None else seed
+    z = _normal(_key(s, "router", layer), cfg.E * cfg.H) / math.sqrt(cfg.H)
+    return _f32_to_bf16_bits(z.astype(np.float32)).reshape(cfg.E, cfg.H)
+
+
+def router_bias(cfg: Config, layer: int = 0, step: int = 0, seed: int | None = None) -> np.ndarray:
+    """fp32 per-expert router bias [E]: the layer's Zipf bias (as in
+    ``router_logits``)."""
+    s = cfg.seed if seed is None else seed
+    return _step_bias(cfg, layer, step, s).astype(np.float32)
 
 
 def hot_mask(cfg: Config, layer: int, seed: int | None = None) -> np.ndarray:

@@ -118,6 +118,53 @@ def _route_case(T=64, E=48, k=6, seed=3):
     return lg, oracle.route(lg, k)
 
 
+# ------------------------------------------------------------------- router
+
+def _bf16_bits(a):
+    return synth._f32_to_bf16_bits(np.asarray(a, np.float32))
+
+
+def test_router_integer_case_is_exact():
+    # small integers are exact in bf16 and every partial sum is exact in
+    # fp32, so the logits are the integer matrix product; T != E catches a
+    # transposed operand, distinct values a wrong index
+    rng = np.random.default_rng(3)
+    T, E, H = 5, 7, 96
+    xi = rng.integers(-8, 9, size=(T, H))
+    wi = rng.integers(-8, 9, size=(E, H))
+    bi = rng.integers(-50, 51, size=E)
+    got = oracle.router_logits(_bf16_bits(xi), _bf16_bits(wi), bi.astype(np.float32))
+    assert np.array_equal(got.astype(np.int64), xi @ wi.T + bi[None, :])
+    got0 = oracle.router_logits(_bf16_bits(xi), _bf16_bits(wi), None)
+    assert np.array_equal(got0.astype(np.int64), xi @ wi.T)
+
+
+def test_router_one_hot_rows_pick_weight_columns():
+    E, H = 6, 40
+    w = synth.router_weights(synth.get_config("tiny", E=E, H=H), 0)
+    x = np.zeros((H, H), np.float32)
+    x[np.arange(H), np.arange(H)] = 1.0
+    b = np.linspace(-1, 1, E).astype(np.float32)
+    got = oracle.router_logits(_bf16_bits(x), w, b)
+    want = synth.bf16_bits_to_f32(w).T.astype(np.float64) + b[None, :].astype(np.float64)
+    assert np.array_equal(got, want.astype(np.float32))
+
+
+def test_router_rounds_the_exact_sum_once():
+    rng = np.random.default_rng(11)
+    T, E, H = 3, 4, 24
+    xb = _bf16_bits(rng.standard_normal((T, H)))
+    wb = _bf16_bits(rng.standard_normal((E, H)))
+    bias = rng.standard_normal(E).astype(np.float32)
+    got = oracle.router_logits(xb, wb, bias)
+    xf = [[Fraction(float(v)) for v in row] for row in synth.bf16_bits_to_f32(xb)]
+    wf = [[Fraction(float(v)) for v in row] for row in synth.bf16_bits_to_f32(wb)]
+    for t in range(T):
+        for e in range(E):
+            exact = Fraction(float(bias[e])) + sum(a * b for a, b in zip(xf[t], wf[e]))
+            assert Fraction(float(got[t, e])) == f32_round(exact), (t, e)
+
+
 def test_route_topk_matches_full_sort():
     lg, (ids, w) = _route_case()
     order = np.argsort(-lg, axis=1, kind="stable")[:, :6]      # stable: ties -> lower id
