@@ -8,9 +8,9 @@
 // exponentially weighted mean of the per-read pick counts, normalised by the
 // decayed weight sum so that it is unbiased from the first read.
 //
-// The same section's runtime control can queue a restore to the boot-time
-// map; its round-trip check restores the boot-time hot set by swaps.  The
-// restore planner gives those swaps for any saved map.
+// The same section lets an operator ask for the placement chosen at start-up
+// back, and checks that swapping back to it loses nothing.  The restore
+// planner gives those swaps for any saved placement.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>

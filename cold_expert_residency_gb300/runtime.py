@@ -84,8 +84,8 @@ def restore_placement(ctx, layer, saved, budget=8, stream=None):
     """Between steps: queue at most ``budget`` swaps that move the layer's
     hot set toward the saved row map's (one saved by moe_get_rowmap, e.g. at
     boot).  Returns the number of swaps applied; 0 once the hot set is
-    restored.  "We Built the Counter", section 2: restore to the boot-time
-    map, at most 8 swaps per step."""
+    restored.  "We Built the Counter", section 2: a return to the start-up
+    placement, at most 8 swaps per step."""
     row_map = moe_get_rowmap(ctx, layer, len(saved))
     promote, demote = moe_plan_restore(row_map, saved, budget)
     if promote.size == 0:

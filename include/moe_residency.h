@@ -274,9 +274,9 @@ int moe_policy_read(moe_policy *p, const int32_t *counts, const int32_t *row_map
                     int32_t *promote, int32_t *demote);
 
 /* ---- restore a saved placement (host, between steps) ----
- * "We Built the Counter", section 2: the runtime control can queue a restore
- * to the boot-time map, and the round-trip check restores the boot-time hot
- * set by swaps with the output unchanged.  A map is saved with
+ * "We Built the Counter", section 2: an operator may ask for the start-up
+ * placement back, and a round trip of swaps back to the start-up hot set
+ * leaves the output unchanged.  A map is saved with
  * moe_get_rowmap.  moe_plan_restore gives the swaps that bring row_map's hot
  * set back to target's: the experts cold in row_map and hot in target, in
  * ascending id, are promoted, the i-th against the i-th expert hot in row_map

@@ -130,9 +130,9 @@ int orc_swap(int32_t *row_map, int E, int n, const int32_t *promote, const int32
              int32_t *applied);
 
 /* ---- restore to a saved placement ----
- * "We Built the Counter", section 2 (runtime control: queue a restore to the
- * boot-time map) and the round-trip check (the boot-time hot set is restored
- * by swaps and the output is unchanged).  Reading: a restore brings back the
+ * "We Built the Counter", section 2: an operator may ask for the start-up
+ * placement back, and a round trip of swaps back to the start-up hot set
+ * leaves the output unchanged.  Reading: a restore brings back the
  * saved HOT SET; which row of a bank an expert occupies changes no output.
  * Pairs: the experts cold in row_map and hot in target (ascending id) are
  * promoted, each against the next expert hot in row_map and cold in target
