@@ -283,11 +283,12 @@ def main():
         ev_hot = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         in_graph_events = False
 
-    def enqueue(timed_hot=False):
+    def enqueue(timed_hot=False, count=None):
+        cnt = count_on if count is None else count
         for l in range(L):
             st = steps[l]
             b = st.buf
-            moe.moe_route_split_count(ctx, l, b.logits, T, count_on, b.ids, b.w, b.ws_ptr, main)
+            moe.moe_route_split_count(ctx, l, b.logits, T, cnt, b.ids, b.w, b.ws_ptr, main)
             if timed_hot and l == 0:
                 ev_hot[0].record(main)
             if args.banks == "fused":   # both banks' FFN, one launch per GEMM
@@ -482,12 +483,13 @@ def main():
     # breakdown: each bank alone (layer 0), graph-replayed like the step
     breakdown = None
     if graph is not None:
-        def part(hot, cold):
+        def part(hot, cold, count=None):
             st = steps[0]
             b = st.buf
             g2 = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g2, stream=main):
-                moe.moe_route_split_count(ctx, 0, b.logits, T, count_on, b.ids, b.w, b.ws_ptr, main)
+                moe.moe_route_split_count(ctx, 0, b.logits, T, count_on if count is None else count, b.ids, b.w,
+                                          b.ws_ptr, main)
                 if hot:
                     moe.moe_expert_ffn_bank(ctx, 0, moe.MOE_BANK_HOT, b.x, T, b.ws_ptr, b.Y, main)
                 if cold:
@@ -526,7 +528,33 @@ def main():
                 main.synchronize()
                 ts.append(ev0.elapsed_time(ev1) * 1e3)
             return float(np.mean(ts))
-        breakdown = {"route_us": r_us, "router_gemm_us": router_alone(), "hot_alone_us": float(np.mean(hot_ms)) * 1e3,
+        def whole_step(count):
+            """The whole step (all layers) with counting on or off, graph-replayed
+            after an L2 flush, alternating with the other setting."""
+            g4 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g4, stream=main):
+                enqueue(count=count)
+            return g4
+
+        counter_ab = None
+        if count_on:
+            g_on, g_off = whole_step(True), whole_step(False)
+            t_on, t_off = [], []
+            for i in range(min(args.steps, 20)):
+                for g4, ts in ((g_on, t_on), (g_off, t_off)):
+                    load_inputs(i, main)
+                    with torch.cuda.stream(main):
+                        flush.zero_()
+                        ev0.record(main)
+                        g4.replay()
+                        ev1.record(main)
+                    main.synchronize()
+                    ts.append(ev0.elapsed_time(ev1) * 1e3)
+            counter_ab = {"step_on_us": float(np.median(t_on)), "step_off_us": float(np.median(t_off)),
+                          "route_on_us": r_us, "route_off_us": part(False, False, count=False),
+                          "note": "medians over the same inputs, on and off alternating; the usage count is "
+                                  "also incremented by the on runs"}
+        breakdown = {"route_us": r_us, "router_gemm_us": router_alone(), "counter_ab": counter_ab, "hot_alone_us": float(np.mean(hot_ms)) * 1e3,
                      "cold_alone_us": float(np.mean(ffn_alone(moe.MOE_BANK_COLD)[0])) * 1e3,
                      "ffn_in_step_us": float(np.mean(ffn_ms)) * 1e3, "banks": args.banks,
                      "note": "layer 0: each bank's FFN call alone after routing, and the step's both-bank FFN call; "
@@ -589,6 +617,8 @@ def main():
                        "ffn_calls": "one call over both banks" if args.banks == "fused" else "hot and cold bank calls on two streams",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "us_per_layer_step": ms * 1e3 / L,
+            "step_us_pct": {q: float(np.percentile(step_ms, p)) * 1e3 for q, p in (("p10", 10), ("median", 50),
+                                                                               ("p90", 90))},
             "bytes_roofline": {"frac_sum": frac, "frac_max": frac_max,
                                "t_roof_us": float(np.mean(t_roof)) * 1e6, "t_step_us": ms * 1e3,
                                "distinct_hot": float(np.mean(dh)), "distinct_cold": float(np.mean(dc)),
