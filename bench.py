@@ -22,6 +22,7 @@ bounded sample of the same workload).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -65,6 +66,35 @@ def parse():
     ap.add_argument("--hot", type=int, default=0, help="hot-bank experts for --experts")
     ap.add_argument("--tokens", type=int, default=0, help="profiling-size variant: tokens per step")
     return ap.parse_args()
+
+
+def bench_config(args):
+    """The workload of a run: the named config, optionally narrowed to fewer
+    experts (``--experts``/``--hot``) or another token count (``--tokens``).
+    Both arms use it."""
+    cfg = synth.get_config(args.config)
+    if args.experts:
+        cfg = synth.get_config(args.config, E=args.experts, n_hot=args.hot or cfg.n_hot * args.experts // cfg.E)
+    if args.tokens:
+        cfg = dataclasses.replace(cfg, T=args.tokens)
+    return cfg
+
+
+def slowest_rank_ms(total_ms, dist=None, device="cpu"):
+    """The job's time: the largest of the ranks' own totals (one process per
+    GPU, each timing its steps with CUDA events)."""
+    if dist is None:
+        return float(total_ms)
+    import torch
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_step, steps, total_ms):
+    """Whole-job throughput: the tokens all ranks processed over the slowest
+    rank's time."""
+    return world * tokens_per_step * steps / (total_ms * 1e-3)
 
 
 def load_peaks():
@@ -194,9 +224,9 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    cfg = synth.get_config(args.config)
+    cfg = bench_config(args)
     if cfg.L != 1:
-        cfg = synth.get_config(args.config, L=1)
+        cfg = dataclasses.replace(cfg, L=1)
     weights = synth.layer_weights(cfg, 0)
     mask = synth.hot_mask(cfg, 0)
     n = max(1, min(args.steps + args.warmup, 64))
@@ -237,12 +267,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     moe.build()
 
-    cfg = synth.get_config(args.config)
-    if args.experts:
-        cfg = synth.get_config(args.config, E=args.experts, n_hot=args.hot or cfg.n_hot * args.experts // cfg.E)
-    if args.tokens:
-        import dataclasses
-        cfg = dataclasses.replace(cfg, T=args.tokens)
+    cfg = bench_config(args)
     hbm_peak, tf_burst, tf_sust, peak_src = load_peaks()
     L = cfg.L
     ctx = moe.moe_create(L, cfg.E, cfg.k, cfg.H, cfg.I, cfg.T, device=local)
@@ -398,11 +423,7 @@ def main():
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    total_ms = float(sum(step_ms))
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(sum(step_ms), dist, dev)
 
     # the step's FFN call (layer 0), one step at a time
     if hot_timing in ("in-graph events", "eager events"):
@@ -562,7 +583,8 @@ def main():
 
     ms = total_ms / args.steps
     tokens_per_step = T   # one layer-step of T tokens (all layers of the config)
-    value = world * tokens_per_step * args.steps / (total_ms * 1e-3)
+    value = job_tokens_per_s(world, tokens_per_step, args.steps, total_ms)
+    e2e_total_ms = slowest_rank_ms(sum(e2e_ms), dist, dev)
     hot_avg_ms = float(np.mean(hot_ms))
     hot_gbs = float(np.mean(hot_bytes_alone)) / (hot_avg_ms * 1e-3) / 1e9
     roofline = {"kernel": "hot-bank expert FFN (moe_expert_ffn_bank, layer 0)", "bound": "hbm",
@@ -590,7 +612,7 @@ def main():
 
     cpu = None
     if rank == 0:
-        cfg1 = cfg if cfg.L == 1 else synth.get_config(args.config, L=1)
+        cfg1 = cfg if cfg.L == 1 else dataclasses.replace(cfg, L=1)
         if args.config == "prefill":
             lgs = [synth.router_logits(cfg1, 0, s, T=64) for s in range(8)]
             xss = [synth.activations(cfg1, 0, s, T=64) for s in range(8)]
@@ -627,7 +649,7 @@ def main():
             "roofline": roofline,
             "breakdown": breakdown,
             "cpu_baseline": cpu,
-            "e2e": {"value": world * T * len(e2e_ms) / (sum(e2e_ms) * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": job_tokens_per_s(world, T, len(e2e_ms), e2e_total_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
