@@ -188,6 +188,22 @@ def cpu_oracle_steps(cfg, weights, mask, pool_lg, pool_x, budget_s):
     return tokens / t_used, steps, t_used, oracle.num_threads()
 
 
+def single_core_oracle(cfg, weights, mask, pool_lg, pool_x, budget_s):
+    """The same oracle layer-steps on one host thread, at least one whole
+    step (decode-sized workloads only; prefill needs every core).  Returns
+    the cpu_baseline sub-entry."""
+    import oracle
+    if pool_lg[0].shape[0] > 256:
+        return None
+    cores = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        tps, n, used, _ = cpu_oracle_steps(cfg, weights, mask, pool_lg, pool_x, budget_s)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": tps, "unit": "tokens/s", "cores": 1, "sample": f"{n} whole layer-steps, {used:.1f} s"}
+
+
 def make_pool(cfg, n, layers):
     lg = [[synth.router_logits(cfg, l, s) for l in range(layers)] for s in range(n)]
     xs = [[synth.activations(cfg, l, s) for l in range(layers)] for s in range(n)]
@@ -241,7 +257,8 @@ def run_reference(args):
         "steps": steps, "warmup": 0, "ms_per_step": used / steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": WORKLOADS[args.config] + ("" if T == cfg.T else f"; sampled at {T} tokens")},
-        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "single_core": single_core_oracle(cfg, weights, mask, lg, xs, max(1.0, budget / 4))},
         "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -67,6 +67,7 @@ def _load():
             "orc_policy_read": (i32, [P, P, P, f64, f64, f64, f64, i32, P, P]),
             "orc_expert_bytes": (i64, [i32, i32]),
             "orc_num_threads": (i32, []),
+            "orc_set_num_threads": (None, [i32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -304,3 +305,7 @@ def expert_bytes(H: int, I: int) -> int:
 
 def num_threads() -> int:
     return int(_load().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().orc_set_num_threads(int(n))

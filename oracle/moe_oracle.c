@@ -24,6 +24,14 @@ int orc_num_threads(void) {
 #endif
 }
 
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* OCP MX v1.0, FP4 E2M1: 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit.
  * Exponent field 0 is subnormal: value = 2^(1-1) * (0 + m/2).
  * Otherwise value = 2^(E-1) * (1 + m/2).  No Inf/NaN encodings. */

@@ -167,6 +167,7 @@ int orc_policy_read(orc_policy_t *p, const int32_t *counts, const int32_t *row_m
 int64_t orc_expert_bytes(int H, int I);
 
 int orc_num_threads(void);
+void orc_set_num_threads(int n);   /* threads of the OpenMP loops (n > 0) */
 
 #ifdef __cplusplus
 }

@@ -69,6 +69,7 @@ def test_reference_arm_under_torchrun_prints_once():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["single_core"]["cores"] == 1 and line["cpu_baseline"]["single_core"]["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
 
 
