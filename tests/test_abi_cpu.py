@@ -112,3 +112,37 @@ def test_native_restore_plan_rejects_a_different_hot_count(lib):
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_plan_restore(now, other, 4)
     assert ei.value.code == moe.MOE_EINVAL and "hot experts" in str(ei.value)
+
+
+def _declared_param_counts():
+    """Parameter count of every function the header declares, read from the
+    header text (comments stripped)."""
+    import os
+    import re
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_residency.h")
+    text = re.sub(r"/\*.*?\*/", "", open(hdr).read(), flags=re.S)
+    counts = {}
+    for m in re.finditer(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(moe_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", text, re.M):
+        params = m.group(2).strip()
+        counts[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return counts
+
+
+def test_binding_signatures_match_the_header(lib):
+    counts = _declared_param_counts()
+    assert set(counts) == set(moe.exported_symbols())
+    for name, n in counts.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name} has no ctypes signature"
+        assert len(fn.argtypes) == n, f"{name}: header has {n} parameters, binding {len(fn.argtypes)}"
+
+
+def test_restore_plan_argument_checks(lib):
+    rm = np.array([0, -1, 1, -2], np.int32)
+    tg = np.array([-1, 0, 1, -2], np.int32)
+    assert [a.tolist() for a in moe.moe_plan_restore(rm, tg, 0)] == [[], []]       # zero budget: no pairs
+    assert lib.moe_plan_restore(4, moe._ptr(rm), moe._ptr(tg), 2, None, None) == moe.MOE_EINVAL
+    assert lib.moe_plan_restore(0, moe._ptr(rm), moe._ptr(tg), 2, None, None) == moe.MOE_EINVAL
+    assert lib.moe_plan_restore(4, None, moe._ptr(tg), 0, None, None) == moe.MOE_EINVAL
+    pro, dem = moe.moe_plan_restore(rm, tg, 4)
+    assert pro.tolist() == [1] and dem.tolist() == [0]
