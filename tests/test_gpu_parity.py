@@ -288,6 +288,30 @@ def test_all_cold_and_all_hot_banks():
     assert np.array_equal(outs[0], outs[1])
 
 
+def test_empty_step_is_a_no_op():
+    """A step of zero tokens routes nothing, counts nothing, writes no row and
+    leaves the next step unchanged."""
+    cfg = synth.get_config("tiny")
+    h = Harness(cfg)
+    try:
+        lg = synth.router_logits(cfg, 0, 0)
+        x = synth.activations(cfg, 0, 0)
+        first = h.run(0, lg, x)
+        c1 = h.moe.moe_read_counts(h.ctx, 1, cfg.E)
+        empty = h.run(0, np.zeros((0, cfg.E), np.float32), np.zeros((0, cfg.H), np.uint16))
+        assert empty["ids"].shape == (0, cfg.k) and empty["out"].shape == (0, cfg.H)
+        assert np.array_equal(h.moe.moe_read_counts(h.ctx, 1, cfg.E), c1)
+        for b in range(2):
+            sp = h.moe.moe_read_split(h.ctx, h.step.buf.ws_ptr, 0, cfg.k, b)
+            assert sp["n_act"] == 0 and sp["n_picks"] == 0
+        again = h.run(0, lg, x)
+        assert np.array_equal(again["Y"], first["Y"]) and np.array_equal(again["out"], first["out"])
+        assert h.moe.moe_read_counts(h.ctx, 1, cfg.E).sum() == c1.sum() + cfg.T * cfg.k
+        assert h.moe.moe_device_status(h.ctx) == 0
+    finally:
+        h.close()
+
+
 def test_device_status_clean_after_steps():
     cfg = synth.get_config("tiny")
     h = Harness(cfg)
