@@ -1,0 +1,53 @@
+"""The bench's host-side helpers, on the CPU: the distinct-expert count behind
+the bytes roofline, the peaks it divides by, the profiled-traffic lookup and
+the workload table."""
+import json
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench                                # noqa: E402
+import synth                                # noqa: E402
+
+
+def test_distinct_experts_counts_each_expert_once_per_bank():
+    mask = np.array([1, 1, 0, 1, 0, 0], np.uint8)       # experts 0, 1, 3 hot; 2, 4, 5 cold
+    ids = np.array([[0, 2], [0, 4], [1, 2], [2, 0]])    # hot {0, 1}, cold {2, 4}
+    assert bench.distinct_experts(ids, mask) == (2, 2)
+    assert bench.distinct_experts(np.array([[3, 3]]), mask) == (1, 0)
+
+
+def test_bytes_roofline_terms_match_the_expert_size():
+    # the bench's per-expert bytes are the library's and the oracle's byte model
+    cfg = synth.get_config("decode1")
+    assert synth.expert_bytes(cfg.H, cfg.I) == 18_800_640
+
+
+def test_peaks_are_positive_and_labelled():
+    hbm, burst, sustained, src = bench.load_peaks()
+    assert hbm > 1000 and burst > 100 and 0 < sustained <= burst * 1.2
+    assert src in ("measured", "fallback")
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        assert src == "measured" and hbm == float(json.load(open(p))["hbm_gbs"])
+
+
+def test_profiled_traffic_only_for_the_profiled_source():
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["decode1"]
+    got = bench.profiled_traffic("decode1")
+    if rec["source_sha"] == bench.source_sha():
+        assert got == rec["bytes_per_hot_expert"]
+        # a hot expert's DRAM bytes within a few percent of its algorithmic bytes
+        assert 1.0 <= got / 18_800_640 <= 1.05
+    else:
+        assert got is None
+    assert bench.profiled_traffic("no-such-workload") is None
+
+
+def test_every_workload_is_a_generator_config():
+    for name in bench.WORKLOADS:
+        cfg = synth.get_config(name)
+        assert cfg.E == 384 and cfg.k == 6 and cfg.H == 4096 and cfg.I == 2880
