@@ -118,6 +118,33 @@ def _route_case(T=64, E=48, k=6, seed=3):
     return lg, oracle.route(lg, k)
 
 
+# --------------------------------------------------------------------- bf16
+
+def _f32(bits):
+    return float(np.array([bits], np.uint32).view(np.float32)[0])
+
+
+def test_bf16_rounding_hand_cases():
+    # bf16 keeps the top 16 bits of a binary32; hand-worked round-to-nearest-even
+    cases = [
+        (0x3F800000, 0x3F80),   # 1.0 exact
+        (0x3F808000, 0x3F80),   # 1 + 2^-8: halfway, even neighbour below
+        (0x3F818000, 0x3F82),   # 1 + 3*2^-8: halfway, even neighbour above
+        (0x3F808001, 0x3F81),   # just above halfway
+        (0x3F807FFF, 0x3F80),   # just below halfway
+        (0xBF808000, 0xBF80),   # sign does not change the tie rule
+        (0x7F7FFFFF, 0x7F80),   # largest binary32 rounds up to +inf
+        (0x00008000, 0x0000),   # tiny subnormal halfway: to even (zero)
+        (0x80000000, 0x8000),   # -0 stays -0
+    ]
+    for f_bits, want in cases:
+        assert oracle.f32_to_bf16(_f32(f_bits)) == want, hex(f_bits)
+    nan = oracle.f32_to_bf16(float("nan"))
+    assert (nan & 0x7F80) == 0x7F80 and (nan & 0x007F) != 0          # stays a NaN
+    for b in (0x0000, 0x3F80, 0xC2F7, 0x7F80, 0x0001):
+        assert np.array([oracle.bf16_to_f32(b)], np.float32).view(np.uint32)[0] == b << 16
+
+
 # ------------------------------------------------------------------- router
 
 def _bf16_bits(a):
