@@ -146,3 +146,22 @@ def test_restore_plan_argument_checks(lib):
     assert lib.moe_plan_restore(4, None, moe._ptr(tg), 0, None, None) == moe.MOE_EINVAL
     pro, dem = moe.moe_plan_restore(rm, tg, 4)
     assert pro.tolist() == [1] and dem.tolist() == [0]
+
+
+def test_policy_and_counter_defaults_are_the_printed_ones(lib):
+    import inspect
+    from conftest import load_golden
+    g = {r[0]: float(r[1]) for r in load_golden("policy_defaults.txt")}
+    for fn in (moe.moe_policy.__init__, oracle.Policy.__init__):
+        p = inspect.signature(fn).parameters
+        assert p["read_every"].default == g["read_every"]
+        assert p["half_life"].default == g["half_life"]
+        assert p["hysteresis"].default == g["hysteresis"]
+        assert p["min_avg"].default == g["min_avg"]
+        assert p["max_pairs"].default == g["max_pairs_per_read"]
+    assert inspect.signature(moe.moe_create).parameters["count_tmax"].default == g["count_tmax"]
+    # the restore helper's per-call budget is the per-step swap budget
+    from cold_expert_residency_gb300.runtime import restore_placement
+    assert inspect.signature(restore_placement).parameters["budget"].default == g["max_swaps_per_step"]
+    # the usage table: int32 per (layer, expert), 40 x 384 x 4 B = 61 KB (rounded down)
+    assert int(g["table_layers"] * g["table_experts"] * 4 / 1000) == g["table_kb"]
