@@ -56,9 +56,7 @@ size_t moe_static_scratch_bytes(void) { return kStaticScratchBytes; }
 
 int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t *x, int T, const void *split_ws,
                                uint16_t *Y, void *stream) {
-    if (!ctx) return set_error(MOE_EINVAL, "null context");
-    if (layer < 0 || layer >= ctx->g.L) return set_error(MOE_EINVAL, "layer out of range");
-    if (!ctx->layers[layer].init) return set_error(MOE_ESTATE, "layer has no banks (call moe_init_banks first)");
+    if (int r = check_layer(ctx, layer, true)) return r;
     if (bank != MOE_BANK_HOT && bank != MOE_BANK_COLD && bank != MOE_BANK_BOTH)
         return set_error(MOE_EINVAL, "bank must be 0, 1 or 2");
     if (T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "T out of range");
@@ -74,28 +72,21 @@ int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t
     const int rows = bank == MOE_BANK_HOT ? L.n_hot : (bank == MOE_BANK_COLD ? L.n_cold : L.n_hot + L.n_cold);
     if (T == 0 || rows == 0) return MOE_OK;
 
-    int prev = -1;
-    cudaGetDevice(&prev);
-    if (prev != ctx->device) cudaSetDevice(ctx->device);
+    DeviceGuard guard(ctx->device);
+    if (guard.status() != cudaSuccess) return cuda_error(guard.status(), "cudaSetDevice(context device)");
     uint8_t *scratch = nullptr;
-    int r = scratch_for_device(ctx->device, &scratch);
+    if (int r = scratch_for_device(ctx->device, &scratch)) return r;
     cudaStream_t s = (cudaStream_t)stream;
-    if (!r) {
-        // the pick lists are the front of the workspace (header, rows, offsets, picks, positions)
-        cudaError_t e = cudaMemcpyAsync(scratch, split_ws, lay.xq, cudaMemcpyDeviceToDevice, s);
-        if (e != cudaSuccess) r = cuda_error(e, "copy pick lists into the static scratch");
+    // the pick lists are the front of the workspace (header, rows, offsets, picks, positions)
+    MOE_CUDA_TRY(cudaMemcpyAsync(scratch, split_ws, lay.xq, cudaMemcpyDeviceToDevice, s));
+    if (ctx->ffn_impl == MOE_FFN_SIMT) {
+        for (int bk = 0; bk < 2; ++bk)
+            if (bank == MOE_BANK_BOTH || bank == bk)
+                if (int r = launch_ffn_simt(ctx, bk == MOE_BANK_HOT ? L.hot : L.cold_dev, bk, x, T, scratch, Y, s))
+                    return r;
+        return MOE_OK;
     }
-    if (!r) {
-        if (ctx->ffn_impl == MOE_FFN_SIMT) {
-            for (int bk = 0; bk < 2 && !r; ++bk)
-                if (bank == MOE_BANK_BOTH || bank == bk)
-                    r = launch_ffn_simt(ctx, bk == MOE_BANK_HOT ? L.hot : L.cold_dev, bk, x, T, scratch, Y, s);
-        } else {
-            r = launch_ffn_tc(ctx, L, bank, x, T, scratch, Y, s);
-        }
-    }
-    if (prev >= 0 && prev != ctx->device) cudaSetDevice(prev);
-    return r;
+    return launch_ffn_tc(ctx, L, bank, x, T, scratch, Y, s);
 }
 
 }  // extern "C"

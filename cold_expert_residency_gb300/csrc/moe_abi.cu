@@ -141,30 +141,18 @@ static void free_layer(moe::Layer &L) {
     L = moe::Layer();
 }
 
-static int check_ctx(const moe_ctx *ctx) {
+int check_ctx(const moe_ctx *ctx) {
     if (!ctx) return set_error(MOE_EINVAL, "null context");
     return MOE_OK;
 }
 
-static int check_layer(moe_ctx *ctx, int layer, bool need_init) {
+int check_layer(moe_ctx *ctx, int layer, bool need_init) {
     if (int r = check_ctx(ctx)) return r;
     if (layer < 0 || layer >= ctx->g.L) return set_error(MOE_EINVAL, "layer out of range");
     if (need_init && !ctx->layers[layer].init)
         return set_error(MOE_ESTATE, "layer has no banks (call moe_init_banks first)");
     return MOE_OK;
 }
-
-struct DeviceGuard {
-    int prev = -1;
-    explicit DeviceGuard(int dev) {
-        cudaGetDevice(&prev);
-        if (prev != dev) cudaSetDevice(dev);
-    }
-    ~DeviceGuard() {
-        int cur;
-        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
-    }
-};
 
 }  // namespace moe
 
@@ -454,21 +442,32 @@ int moe_swap_rows(moe_ctx *ctx, int layer, int n, const int32_t *promote, const 
     Layer &L = ctx->layers[layer];
     const Geom &g = ctx->g;
     int done = 0;
+    if (applied)
+        for (int i = 0; i < n; ++i) applied[i] = 0;
     for (int i = 0; i < n; ++i) {
         int32_t c = promote[i], h = demote[i];
         bool ok = c >= 0 && c < g.E && h >= 0 && h < g.E && c != h && L.rowmap[c] < 0 && L.rowmap[h] >= 0;
-        if (applied) applied[i] = ok ? 1 : 0;
         if (!ok) continue;
         int32_t hot_row = L.rowmap[h];
         int32_t cold_row = -1 - L.rowmap[c];
         uint8_t *hot_p = L.hot + (size_t)hot_row * g.eb;
         uint8_t *cold_p = L.cold_host + (size_t)cold_row * g.eb;
-        MOE_CUDA_TRY(cudaMemcpyAsync(ctx->staging, hot_p, g.eb, cudaMemcpyDeviceToDevice, s));
-        MOE_CUDA_TRY(cudaMemcpyAsync(hot_p, cold_p, g.eb, cudaMemcpyHostToDevice, s));
-        MOE_CUDA_TRY(cudaMemcpyAsync(cold_p, ctx->staging, g.eb, cudaMemcpyDeviceToHost, s));
-        if (int r = launch_rowmap_write(L.rowmap_dev, c, hot_row, h, -1 - cold_row, s)) return r;
+        // A failure after the first copy may leave a bank row holding neither
+        // expert whole: the layer is then marked as needing moe_init_banks,
+        // and this pair is not reported as applied.
+        cudaError_t e = cudaMemcpyAsync(ctx->staging, hot_p, g.eb, cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(hot_p, cold_p, g.eb, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(cold_p, ctx->staging, g.eb, cudaMemcpyDeviceToHost, s);
+        int r = e == cudaSuccess ? launch_rowmap_write(L.rowmap_dev, c, hot_row, h, -1 - cold_row, s)
+                                 : cuda_error(e, "moe_swap_rows copy");
+        if (r != MOE_OK) {
+            L.init = false;
+            return set_error(r, std::string(moe_last_error()) + "; layer " + std::to_string(layer) +
+                                    " must be placed again with moe_init_banks");
+        }
         L.rowmap[c] = hot_row;
         L.rowmap[h] = -1 - cold_row;
+        if (applied) applied[i] = 1;
         ++done;
     }
     return done;

@@ -205,6 +205,27 @@ namespace moe {
 // error reporting (per thread)
 int set_error(int code, const std::string &msg);
 int cuda_error(cudaError_t e, const char *what);
+// argument checks shared by the entry points: a non-null context; a layer
+// index in range (and, with need_init, a layer whose banks are placed)
+int check_ctx(const moe_ctx *ctx);
+int check_layer(moe_ctx *ctx, int layer, bool need_init);
+
+// Makes `dev` the calling thread's current device for the guard's lifetime
+// and restores the previous one after.  status() is the cudaSetDevice result
+// (cudaSuccess when the device was already current).
+struct DeviceGuard {
+    int prev = -1;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != dev) err = cudaSetDevice(dev);
+    }
+    cudaError_t status() const { return err; }
+    ~DeviceGuard() {
+        int cur;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
 #define MOE_CUDA_TRY(call)                                   \
     do {                                                     \
         cudaError_t e_ = (call);                             \

@@ -37,6 +37,8 @@ __device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
 
 // One warp routes one token: k rounds of a warp-wide argmax (larger logit
 // first, ties to the lower expert id), then fp32 softmax over the k picks.
+// A NaN logit is read as -infinity (ranked below every number, weight
+// exp(-inf) = 0 beside a finite first pick), so the k ids are always valid.
 // Lane j < k returns pick j in (*id_out, *w_out); other lanes return -1.
 __device__ __forceinline__ void warp_route_token(const float *__restrict__ l, int E, int k, int lane,
                                                  int *id_out, float *w_out) {
@@ -45,7 +47,8 @@ __device__ __forceinline__ void warp_route_token(const float *__restrict__ l, in
 #pragma unroll
     for (int i = 0; i < kMaxLanesVals; ++i) {
         int e = lane + 32 * i;
-        lv[i] = e < E ? l[e] : -INFINITY;
+        const float v = e < E ? l[e] : -INFINITY;
+        lv[i] = isnan(v) ? -INFINITY : v;
         if (e >= E) taken |= 1u << i;
     }
     float sel_v[kMaxK];

@@ -128,7 +128,9 @@ int moe_workspace_bytes(const moe_ctx *ctx, int T, size_t *bytes);
  * masked relaxed atomic add per pick into the usage table; only steps of at
  * most count_tmax tokens are counted).
  *   logits: device fp32 [T][E].  Top-k per token (ties: lower expert id
- *           first); w = softmax over the k picked logits in fp32.
+ *           first); w = softmax over the k picked logits in fp32.  A NaN
+ *           logit is read as -infinity (ranked last, weight 0 beside a
+ *           finite first pick), so ids are always valid expert ids.
  *   ids:    device int32 [T][k] out, descending logit order (the k order).
  *   w:      device fp32  [T][k] out.
  *   ws:     device workspace (moe_workspace_bytes) receiving both banks'
@@ -219,7 +221,11 @@ int moe_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_
  * two-element device row-map write ordered after the copies.  promote,
  * demote: host int32 [n]; applied: host int32 [n] out (may be NULL).  Returns
  * the number applied (>= 0) or an error code.  Never call it while a step of
- * this layer is in flight on another stream. */
+ * this layer is in flight on another stream.  If enqueuing a pair's copies or
+ * map write fails, the call returns that error (MOE_ECUDA or MOE_ENOMEM),
+ * applied[] marks only the pairs completed before it, and the layer is left
+ * unplaced: every later call on it returns MOE_ESTATE until moe_init_banks
+ * places it again (a bank row may hold neither expert whole). */
 int moe_swap_rows(moe_ctx *ctx, int layer, int n, const int32_t *promote, const int32_t *demote,
                   int32_t *applied, void *stream);
 

@@ -107,9 +107,13 @@ static int ranks_before(float la, int a, float lb, int b) {
     return a < b;
 }
 
+/* A logit as routing reads it: NaN -> -infinity. */
+static float routing_logit(float v) { return isnan(v) ? -INFINITY : v; }
+
 void orc_route(const float *logits, int T, int E, int k, int32_t *ids, float *w) {
+    float *l = (float *)malloc(sizeof(float) * (size_t)(E > 0 ? E : 1));
     for (int t = 0; t < T; ++t) {
-        const float *l = logits + (int64_t)t * E;
+        for (int e = 0; e < E; ++e) l[e] = routing_logit(logits[(int64_t)t * E + e]);
         int32_t *id = ids + (int64_t)t * k;
         /* selection: k passes, each taking the best expert not yet taken */
         for (int j = 0; j < k; ++j) {
@@ -132,6 +136,7 @@ void orc_route(const float *logits, int T, int E, int k, int32_t *ids, float *w)
         }
         for (int j = 0; j < k; ++j) w[(int64_t)t * k + j] = ex[j] / sum;
     }
+    free(l);
 }
 
 /* ------------------------------------------------------------- residency */

@@ -63,7 +63,9 @@ void orc_router_logits(const uint16_t *x, const uint16_t *w_router, const float 
 /* ---- routing: top-k over fp32 logits, softmax over the k picks ----
  * ids[t][j]: the j-th largest logit of token t (ties: lower expert id first);
  * w[t][j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k picks, in fp32,
- * summed in j order. */
+ * summed in j order.  The pages assume finite logits; a NaN logit is read
+ * as -infinity for both the ranking and the weights (reading: a score that
+ * is not a number ranks below every score, so k valid ids always come out). */
 void orc_route(const float *logits, int T, int E, int k, int32_t *ids, float *w);
 
 /* ---- residency: row map and split ----

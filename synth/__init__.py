@@ -65,6 +65,10 @@ class Config:
     beta: float = 0.0               # bias scale on ln p_rank
     scale_lo: int = 123             # e8m0 byte range (inclusive)
     scale_hi: int = 127
+    # "unit-scale" variants: subtracted from every W13 / W2 scale byte, so
+    # the layer's outputs are O(1) (0 = the drawn bytes as they are)
+    w13_scale_shift: int = 0
+    w2_scale_shift: int = 0
     hbm_layers: tuple = ()          # layers kept all-HBM regardless of n_hot
     steps: int = 1
     shift_at: int = -1              # step at which the Zipf ranking is re-drawn
@@ -222,6 +226,10 @@ def expert_weights(cfg: Config, layer: int, expert: int, seed: int | None = None
     w13_s = _scales(_key(s, "w13s", layer, expert), 2 * I * H // 32, cfg.scale_lo, cfg.scale_hi).reshape(2 * I, H // 32)
     w2_q = stream_bytes(_key(s, "w2q", layer, expert), H * I // 2).reshape(H, I // 2)
     w2_s = _scales(_key(s, "w2s", layer, expert), H * I // 32, cfg.scale_lo, cfg.scale_hi).reshape(H, I // 32)
+    if cfg.w13_scale_shift:
+        w13_s = (w13_s.astype(np.int16) - cfg.w13_scale_shift).astype(np.uint8)
+    if cfg.w2_scale_shift:
+        w2_s = (w2_s.astype(np.int16) - cfg.w2_scale_shift).astype(np.uint8)
     return w13_q, w13_s, w2_q, w2_s
 
 

@@ -37,6 +37,76 @@ def assert_close_bf16(got_bits, ref_bits, what=""):
     return rel_l2, max_rel
 
 
+def assert_rows_close_bf16(got_bits, ref_bits, what="", rel=REL_L2):
+    """Relative L2 <= rel in every row (last axis) with a nonzero reference:
+    a wrong K block or a wrong token in one row cannot hide in the norm of
+    the whole tensor."""
+    g = f32(got_bits).reshape(-1, np.asarray(got_bits).shape[-1])
+    r = f32(ref_bits).reshape(g.shape)
+    nr = np.linalg.norm(r, axis=1)
+    err = np.linalg.norm(g - r, axis=1)
+    ok = nr > 0
+    worst = float((err[ok] / nr[ok]).max()) if ok.any() else 0.0
+    assert np.all(err[~ok] == 0), f"{what}: rows with a zero reference differ"
+    assert worst <= rel, f"{what}: worst row rel_l2={worst:.3g}"
+    return worst
+
+
+def bf16_ulp(v):
+    """Spacing of bf16 numbers at |v| (8 significant bits)."""
+    a = np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
+def ffn_error_bound(weights, e, x_bits):
+    """Per-element bound on |Y_gpu - Y_oracle| for one pick (expert e of the
+    stacked logical weights, token row x_bits), from the CUDA path's
+    arithmetic:
+      - a row v carried as two e4m3 pieces after a power-of-two scaling that
+        puts max|v| in (224, 448]: |dv| <= 2^-8 |v| + 2^-14 * max|v| / 224
+        (e4m3 has 3 mantissa bits; the second piece holds 16x the first's
+        error; subnormal pieces leave at most 2^-14 of the scaled unit);
+      - fp32 accumulation of exact products: at most K * 2^-24 of sum |W||v|;
+      - SwiGLU: |d silu/dz| <= 1.1, and a few fp32 ulps for exp and divide;
+      - both sides round y to bf16: one bf16 ulp.
+    First order in the errors, widened by 1.25 for the second-order terms."""
+    import oracle
+    w13_q, w13_s, w2_q, w2_s = (np.asarray(a[e]) for a in weights)
+    I2, H = w13_q.shape[0], w13_q.shape[1] * 2
+    I = I2 // 2
+    W13 = oracle.dequant(w13_q, w13_s)
+    W2 = oracle.dequant(w2_q, w2_s)
+    x = f32(x_bits).reshape(H)
+    ax = np.abs(x)
+    floor_x = 2.0 ** -14 * ax.max() / 224.0
+    A13 = np.abs(W13)
+    S = A13 @ ax
+    R = A13.sum(axis=1)
+    B13 = (2.0 ** -8 + H * 2.0 ** -24) * S + floor_x * R
+    gu = W13 @ x
+    g, u = gu[:I], gu[I:]
+    Bg, Bu = B13[:I], B13[I:]
+    sg = g / (1.0 + np.exp(-np.clip(g, -700, 700)))
+    h = sg * u
+    Bh = 1.1 * Bg * (np.abs(u) + Bu) + np.abs(sg) * Bu + 2.0 ** -20 * np.abs(h)
+    hm = np.abs(h) + Bh
+    Bh_rep = Bh + 2.0 ** -8 * hm + 2.0 ** -14 * hm.max() / 224.0
+    A2 = np.abs(W2)
+    By = A2 @ Bh_rep + I * 2.0 ** -24 * (A2 @ hm)
+    y = W2 @ h
+    return 1.25 * By + bf16_ulp(np.abs(y) + By)
+
+
+def assert_within_elem_bound(got_bits, ref_bits, bound, what=""):
+    g, r = f32(got_bits).ravel(), f32(ref_bits).ravel()
+    d = np.abs(g - r)
+    b = np.asarray(bound, np.float64).ravel()
+    bad = np.flatnonzero(~(d <= b))
+    assert bad.size == 0, (f"{what}: {bad.size} elements over their bound; first at {bad[0]}: "
+                           f"|d|={d[bad[0]]:.4g} bound={b[bad[0]]:.4g}")
+    return float((d / b).max())
+
+
 def to_dev(a, dtype=None):
     t = torch.from_numpy(np.ascontiguousarray(a))
     if dtype is not None:

@@ -205,6 +205,23 @@ def test_route_ties_lower_id_first():
     assert w[0, 0] == w[0, 1] == w[0, 2]
 
 
+def test_route_nan_logits_rank_below_every_number():
+    """A NaN logit is read as -infinity: it is never picked while k finite
+    logits remain, an all-NaN row yields the k lowest ids, and a pick read as
+    -infinity gets weight 0 beside a finite first pick."""
+    nan = np.float32(np.nan)
+    lg = np.array([[nan, 0.5, nan, 2.0, -1.0, nan],
+                   [nan, nan, nan, nan, nan, nan],
+                   [nan, -np.inf, 1.0, nan, nan, nan]], np.float32)
+    ids, w = oracle.route(lg, 3)
+    assert ids[0].tolist() == [3, 1, 4]
+    assert np.allclose(w[0], np.exp([0.0, -1.5, -3.0]) / np.exp([0.0, -1.5, -3.0]).sum(), rtol=2e-6)
+    assert ids[1].tolist() == [0, 1, 2] and np.all(np.isnan(w[1]))
+    # finite 1.0 first, then the -inf logit and the NaN ones tie at -inf: lower id first
+    assert ids[2].tolist() == [2, 0, 1]
+    assert w[2].tolist() == [1.0, 0.0, 0.0]
+
+
 def test_route_weights_are_softmax_over_picks():
     lg, (ids, w) = _route_case()
     sel = np.take_along_axis(lg, ids, axis=1).astype(np.float64)
