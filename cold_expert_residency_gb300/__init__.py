@@ -21,6 +21,7 @@ from ._build import LIB as _LIB_PATH, build  # noqa: F401
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTALE, MOE_ETIMEOUT, MOE_ESTATE = 0, -1, -2, -3, -4, -5, -6
 MOE_BANK_HOT, MOE_BANK_COLD, MOE_BANK_BOTH = 0, 1, 2
 MOE_FFN_TCGEN05, MOE_FFN_SIMT = 0, 1
+MOE_FAULT_NONE, MOE_FAULT_WITHHOLD_COPY = 0, 1
 
 _lib = None
 
@@ -77,6 +78,9 @@ def lib():
         "moe_probe_link": (i32, [P, sz, i32, C.POINTER(C.c_double), C.POINTER(C.c_double)]),
         "moe_device_status": (i32, [P, C.POINTER(C.c_int32)]),
         "moe_kernel_launches": (i64, []),
+        "moe_memory_in_use": (i32, [C.POINTER(i64), C.POINTER(i64)]),
+        "moe_set_wait_limit": (i32, [P, C.c_uint64]),
+        "moe_inject_fault": (i32, [P, i32]),
         "moe_policy_create": (i32, [i32, C.c_double, C.c_double, C.c_double, C.c_double, i32, P, C.POINTER(P)]),
         "moe_policy_destroy": (i32, [P]),
         "moe_policy_read": (i32, [P, P, P, P, P]),
@@ -284,6 +288,21 @@ def moe_device_status(ctx):
 
 def moe_kernel_launches():
     return int(lib().moe_kernel_launches())
+
+
+def moe_memory_in_use():
+    """(device bytes, pinned host bytes) the library holds in this process."""
+    d, p = C.c_int64(), C.c_int64()
+    _err("moe_memory_in_use", lib().moe_memory_in_use(C.byref(d), C.byref(p)))
+    return d.value, p.value
+
+
+def moe_set_wait_limit(ctx, ns):
+    return _err("moe_set_wait_limit", lib().moe_set_wait_limit(ctx, int(ns)))
+
+
+def moe_inject_fault(ctx, kind):
+    return _err("moe_inject_fault", lib().moe_inject_fault(ctx, kind))
 
 
 def moe_plan_restore(row_map, target, max_pairs):

@@ -59,7 +59,6 @@ namespace moe {
 namespace {
 
 constexpr uint32_t kWaitLimit = 1u << 22;        // polls of the teardown drains
-constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s bound of a pipeline wait
 
 struct TcArgs {
     const uint8_t *bank[2];  // device-visible base of the hot (HBM) and cold (mapped host) bank
@@ -78,18 +77,20 @@ struct TcArgs {
     int32_t *status;
     int32_t *sched;         // [2 banks][2 phases] work counters (zeroed before the launch)
     int32_t *claim;         // [SM] first-CTA claims (zeroed before the launch)
+    uint64_t wait_ns;       // bound of every pipeline wait (wall-clock ns)
+    int32_t withhold;       // fault injection: the CTA that takes unit 0 of a bank skips its first group's copies
 };
 
 constexpr int kQ = 4;       // unit queue depth (producer -> the other roles)
 constexpr int kMaxStages = 8;
 
-// Bounded mbarrier wait: gives up after kWaitNs of wall-clock time, raising
+// Bounded mbarrier wait: gives up after limit_ns of wall-clock time, raising
 // the CTA's abort flag and the launch status.  SUSP: each poll may suspend the
 // thread (up to 20 us) instead of returning at once -- used by the decode
 // tiles, whose CTAs share an SM.
 template <bool SUSP>
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         int32_t *status) {
+                                         int32_t *status, uint64_t limit_ns) {
     uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
         if (SUSP ? ptx::mbar_try_wait_suspend(bar, parity, 20000u) : ptx::mbar_try_wait(bar, parity)) return true;
@@ -98,7 +99,7 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile
             const uint64_t now = ptx::globaltimer_ns();
             if (i == 0) {
                 t0 = now;
-            } else if (now - t0 > kWaitNs) {
+            } else if (now - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicCAS(status, 0, MOE_ETIMEOUT);
                 return false;
@@ -109,10 +110,10 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile
 
 template <bool SUSP>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status) {
+                                          int32_t *status, uint64_t limit_ns) {
     // the warps that spread the weights mostly find their phase complete: a
     // non-blocking check costs less than a suspend-hinted wait
-    bool ok = (SUSP && ptx::mbar_test_wait(bar, parity)) || wait_one<SUSP>(bar, parity, abort_flag, status);
+    bool ok = (SUSP && ptx::mbar_test_wait(bar, parity)) || wait_one<SUSP>(bar, parity, abort_flag, status, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -377,8 +378,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
     // entry 2u + bank (unit u of that bank), or -1 at the end
     auto take_unit = [&](uint32_t ui, bool warp_wide, bool &ok) -> int {
         const int qs = ui % kQ;
-        const bool w = warp_wide ? wait_warp<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status)
-                                 : wait_one<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status);
+        const bool w = warp_wide ? wait_warp<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status, args.wait_ns)
+                                 : wait_one<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status, args.wait_ns);
         if (!w) {
             ok = false;
             return -1;
@@ -410,7 +411,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
                 float re[NB];
                 load_meta<NB>(L, args, 0, 1, nn, p0 + n0, goff + p0 + n0, lane, rs, re);
                 const int db = j % DB;
-                if (!wait_warp<SUSP>(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status)) { ok = false; break; }
+                if (!wait_warp<SUSP>(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
                 ptx::tc_fence_after();
                 epilogue_cols<PHASE, NB, C::kStack, C::kSplit, C::kRowQ>(args, tmem + lane_base + C::kDCol + db * C::kDW, 0, 1,
                                                                         nn, goff + p0 + n0, mt, quarter, lane, rs, re);
@@ -432,12 +433,12 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
         }
         bool dry_pref = false, dry_other = args.b >= 0;
         uint32_t it = 0;
-        bool ok = true;
+        bool ok = true, withheld = false;
         for (uint32_t ui = 0; ok; ++ui) {
             // take the next unit from the launch's work counter and publish it
             const int qs = ui % kQ;
             if (ui >= (uint32_t)kQ &&
-                !wait_one<SUSP>(bar(UQEMPTY + qs), ((ui / kQ) - 1) & 1, abort_flag, args.status)) {
+                !wait_one<SUSP>(bar(UQEMPTY + qs), ((ui / kQ) - 1) & 1, abort_flag, args.status, args.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -469,12 +470,18 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
                 for (int s = s0; s < s1; ++s, ++it) {
                     const int st = it % S;
                     const uint32_t rnd = it / S;
-                    if (rnd > 0 && !wait_one<SUSP>(bar(DONE + st), (rnd - 1) & 1, abort_flag, args.status)) {
+                    if (rnd > 0 && !wait_one<SUSP>(bar(DONE + st), (rnd - 1) & 1, abort_flag, args.status, args.wait_ns)) {
                         ok = false;
                         break;
                     }
                     int slot, tidx, kb0, nkb;
                     part.group(mt, s, slot, tidx, kb0, nkb);
+                    if (args.withhold && it == 0 && (e >> 1) == 0) {
+                        // injected fault: this stage's copies are never issued, so
+                        // the roles waiting for it time out
+                        withheld = true;
+                        continue;
+                    }
                     // the code block counts its packed (global) bytes; the token-row
                     // box counts in full (a half group's second chunk is past the
                     // rows' end: zero fill, unused)
@@ -490,6 +497,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
             // let the copies this thread issued land before the CTA goes away
             const uint32_t first = it > (uint32_t)S ? it - S : 0u;
             for (uint32_t i = first; i < it; ++i) {
+                if (withheld && i == 0) continue;   // nothing was issued for it
                 for (uint32_t t = 0; t < kWaitLimit; ++t)
                     if (ptx::mbar_try_wait(bar(FULL + i % S), (i / S) & 1)) break;
             }
@@ -512,7 +520,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
                 const uint32_t idesc0 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 0, 0);   // | (K block << 29): A scale byte
                 const int db = j % DB;
                 if (j >= (uint32_t)DB &&
-                    !wait_one<SUSP>(bar(ACCFREE + db), ((j / DB) - 1) & 1, abort_flag, args.status)) {
+                    !wait_one<SUSP>(bar(ACCFREE + db), ((j / DB) - 1) & 1, abort_flag, args.status, args.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -520,7 +528,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
                 const uint32_t d_tmem = tmem + C::kDCol + db * C::kDW;
                 for (int s = s0; s < s1; ++s, ++it) {
                     const int st = it % S;
-                    if (!wait_one<SUSP>(bar(FULL + st), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
+                    if (!wait_one<SUSP>(bar(FULL + st), (it / S) & 1, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
                     ptx::tc_fence_after();
                     int slot, tidx, kb0, nkb;
                     part.group(mt, s, slot, tidx, kb0, nkb);
@@ -528,7 +536,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
                     // it - NSF (the slot's last reader) have completed
                     if (it >= (uint32_t)NSF) {
                         const uint32_t prev = it - NSF;
-                        if (!wait_one<SUSP>(bar(DONE + prev % S), (prev / S) & 1, abort_flag, args.status)) {
+                        if (!wait_one<SUSP>(bar(DONE + prev % S), (prev / S) & 1, abort_flag, args.status, args.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -1011,7 +1019,11 @@ int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int b, const uint16_t *x, in
     // SM claims: a launch over both banks, or a cold-bank launch (one each;
     // the hot bank's concurrent launches never read them)
     a1.claim = (a1.b < 0 || a1.b == MOE_BANK_COLD) ? (int32_t *)(ws + lay.claim) : nullptr;
+    a1.wait_ns = ctx->wait_ns;
+    a1.withhold = ctx->inject_withhold ? 1 : 0;   // test hook, consumed by this call's gate/up GEMM
+    ctx->inject_withhold = false;
     TcArgs a2 = a1;
+    a2.withhold = 0;
     a2.claim = a1.claim ? a1.claim + 1024 : nullptr;   // the down GEMM's own claims
     a2.part = g.w2;
     a2.bexp = (const int32_t *)(ws + lay.hexp);

@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
     auto units_of = [&](int bk) { return args.lists[0].hdr[kHdrNAct + bk] * part.tiles * args.ks; };
     auto take_unit = [&](uint32_t ui, bool warp_wide, bool &ok) -> int {
         const int qs = ui % kQ;
-        const bool w = warp_wide ? wait_warp<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status)
-                                 : wait_one<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status);
+        const bool w = warp_wide ? wait_warp<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status, args.wait_ns)
+                                 : wait_one<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status, args.wait_ns);
         if (!w) {
             ok = false;
             return -1;
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
                 load_meta<NB>(L, args, 0, 1, nn, p0 + n0, goff + p0 + n0, lane, rs, re);
                 for (int s = s0; ok && s < s1; ++s, ++it) {
                     const int st = it % S;
-                    if (!wait_warp<SUSP>(bar(FULL + st), (it / S) & 1, abort_flag, args.status)) { ok = false; break; }
+                    if (!wait_warp<SUSP>(bar(FULL + st), (it / S) & 1, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
                     int slot, tidx, kb0, nkb;
                     part.group(mt, s, slot, tidx, kb0, nkb);
                     const uint8_t *grp = sA + st * kGroupBytes;
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
                         const int abuf = ci % NA;
                         // the slot's previous chunk (ci - NA) must have been consumed
                         if (ci >= (uint32_t)NA &&
-                            !wait_warp<SUSP>(bar(ADONE + abuf), ((ci / NA) - 1) & 1, abort_flag, args.status)) {
+                            !wait_warp<SUSP>(bar(ADONE + abuf), ((ci / NA) - 1) & 1, abort_flag, args.status, args.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
                     }
                 }
                 if (!ok) break;
-                if (!wait_warp<SUSP>(bar(ACCREADY), j & 1, abort_flag, args.status)) { ok = false; break; }
+                if (!wait_warp<SUSP>(bar(ACCREADY), j & 1, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
                 ptx::tc_fence_after();
                 epilogue_cols<PHASE, NB, C::kStack, C::kSplit, C::kRowQ>(args, tmem + lane_base + C::kDCol, 0, 1, nn,
                                                                         goff + p0 + n0, mt, quarter, lane, rs, re);
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
         }
         bool dry_pref = false, dry_other = args.b >= 0;
         uint32_t it = 0;
-        bool ok = true;
+        bool ok = true, withheld = false;
         // The down GEMM's token rows are prep_h's output: the ring's first round
         // of weight copies goes out at once, its token-row boxes once prep_h
         // has finished (before any stage is reused, and at the end).
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
         for (uint32_t ui = 0; ok; ++ui) {
             const int qs = ui % kQ;
             if (ui >= (uint32_t)kQ &&
-                !wait_one<SUSP>(bar(UQEMPTY + qs), ((ui / kQ) - 1) & 1, abort_flag, args.status)) {
+                !wait_one<SUSP>(bar(UQEMPTY + qs), ((ui / kQ) - 1) & 1, abort_flag, args.status, args.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -281,12 +281,18 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
                     const int st = it % S;
                     const uint32_t rnd = it / S;
                     if (rnd > 0) release_rows();
-                    if (rnd > 0 && !wait_one<SUSP>(bar(DONEG + st), (rnd - 1) & 1, abort_flag, args.status)) {
+                    if (rnd > 0 && !wait_one<SUSP>(bar(DONEG + st), (rnd - 1) & 1, abort_flag, args.status, args.wait_ns)) {
                         ok = false;
                         break;
                     }
                     int slot, tidx, kb0, nkb;
                     part.group(mt, s, slot, tidx, kb0, nkb);
+                    if (PHASE == 1 && args.withhold && it == 0 && (e >> 1) == 0) {
+                        // injected fault: this stage's copies are never issued, so
+                        // the roles waiting for it time out
+                        withheld = true;
+                        continue;
+                    }
                     // a half group's second token-row chunk is past the rows' end:
                     // zero fill, counted, unused
                     ptx::mbar_arrive_expect_tx(bar(FULL + st), (uint32_t)(kGroupBytes + C::kBStage));
@@ -307,6 +313,7 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
             // let the copies this thread issued land before the CTA goes away
             const uint32_t first = it > (uint32_t)S ? it - S : 0u;
             for (uint32_t i = first; i < it; ++i) {
+                if (withheld && i == 0) continue;   // nothing was issued for it
                 for (uint32_t t = 0; t < kWaitLimit; ++t)
                     if (ptx::mbar_try_wait(bar(FULL + i % S), (i / S) & 1)) break;
             }
@@ -327,7 +334,7 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
                 const int Nr = (nn + C::kRowQ - 1) / C::kRowQ * C::kRowQ;
                 const int Nm = C::kStack ? 2 * Nr : Nr;   // B rows of one MMA
                 const uint32_t idesc0 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 0, 0);   // | (scale byte << 29)
-                if (j >= 1u && !wait_one<SUSP>(bar(ACCFREE), (j - 1) & 1, abort_flag, args.status)) {
+                if (j >= 1u && !wait_one<SUSP>(bar(ACCFREE), (j - 1) & 1, abort_flag, args.status, args.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
                     part.group(mt, s, slot, tidx, kb0, nkb);
                     for (int ch = 0; ch < nkb / 2; ++ch, ++ci) {
                         const int abuf = ci % NA;
-                        if (!wait_one<SUSP>(bar(AREADY + abuf), (ci / NA) & 1, abort_flag, args.status)) {
+                        if (!wait_one<SUSP>(bar(AREADY + abuf), (ci / NA) & 1, abort_flag, args.status, args.wait_ns)) {
                             ok = false;
                             break;
                         }

@@ -5,9 +5,12 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <sys/mman.h>
 #include <thread>
+#include <unordered_map>
 
 namespace moe {
 
@@ -23,6 +26,59 @@ int cuda_error(cudaError_t e, const char *what) {
     std::string m = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
     if (e == cudaErrorMemoryAllocation) return set_error(MOE_ENOMEM, m);
     return set_error(MOE_ECUDA, m);
+}
+
+// ---- library-owned memory, tracked process-wide (moe_memory_in_use) -------
+static std::mutex g_mem_mu;
+static std::unordered_map<const void *, std::pair<size_t, int>> g_mem;   // address -> (bytes, 0 device / 1 pinned)
+static int64_t g_mem_bytes[2] = {0, 0};
+
+static void track(const void *p, size_t n, int kind) {
+    std::lock_guard<std::mutex> lock(g_mem_mu);
+    g_mem[p] = {n, kind};
+    g_mem_bytes[kind] += (int64_t)n;
+}
+
+static void untrack(const void *p) {
+    std::lock_guard<std::mutex> lock(g_mem_mu);
+    auto it = g_mem.find(p);
+    if (it == g_mem.end()) return;
+    g_mem_bytes[it->second.second] -= (int64_t)it->second.first;
+    g_mem.erase(it);
+}
+
+// Test hook for the failure path of allocations: when the environment
+// variable MOE_INJECT_ALLOC_FAIL names an allocation site, that site reports
+// cudaErrorMemoryAllocation without allocating.
+static bool injected_failure(const char *site) {
+    const char *v = std::getenv("MOE_INJECT_ALLOC_FAIL");
+    return v && std::strcmp(v, site) == 0;
+}
+
+static cudaError_t dev_alloc(void **p, size_t n, const char *site) {
+    if (injected_failure(site)) return cudaErrorMemoryAllocation;
+    cudaError_t e = cudaMalloc(p, n);
+    if (e == cudaSuccess) track(*p, n, 0);
+    return e;
+}
+
+static void dev_free(void *p) {
+    if (!p) return;
+    untrack(p);
+    cudaFree(p);
+}
+
+static cudaError_t pinned_alloc(void **p, size_t n, unsigned flags, const char *site) {
+    if (injected_failure(site)) return cudaErrorMemoryAllocation;
+    cudaError_t e = cudaHostAlloc(p, n, flags);
+    if (e == cudaSuccess) track(*p, n, 1);
+    return e;
+}
+
+static void pinned_free(void *p) {
+    if (!p) return;
+    untrack(p);
+    cudaFreeHost(p);
 }
 
 // Run f(i) for i in [0, n) on up to `threads` host threads.
@@ -104,6 +160,7 @@ static bool repack_expert(const Geom &g, const uint8_t *w13_q, const uint8_t *w1
 // fails falls back to cudaHostAlloc.
 static cudaError_t alloc_cold_bank(size_t bytes, moe::Layer &L) {
     constexpr size_t kAlign = 512ull << 20;
+    if (injected_failure("cold_bank")) return cudaErrorMemoryAllocation;
     if (bytes >= (256ull << 20)) {
         const size_t span = (bytes + kAlign - 1) / kAlign * kAlign;
         void *m = mmap(nullptr, span + kAlign, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE,
@@ -116,6 +173,7 @@ static cudaError_t alloc_cold_bank(size_t bytes, moe::Layer &L) {
                     L.cold_host = a;
                     L.cold_map = m;
                     L.cold_map_bytes = span + kAlign;
+                    track(a, span, 1);
                     return cudaSuccess;
                 }
                 cudaHostUnregister(a);
@@ -124,20 +182,21 @@ static cudaError_t alloc_cold_bank(size_t bytes, moe::Layer &L) {
             munmap(m, span + kAlign);
         }
     }
-    cudaError_t e = cudaHostAlloc(&L.cold_host, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    cudaError_t e = pinned_alloc((void **)&L.cold_host, bytes, cudaHostAllocMapped | cudaHostAllocPortable, "cold_bank");
     if (e == cudaSuccess) e = cudaHostGetDevicePointer((void **)&L.cold_dev, L.cold_host, 0);
     return e;
 }
 
 static void free_layer(moe::Layer &L) {
-    if (L.hot) cudaFree(L.hot);
+    dev_free(L.hot);
     if (L.cold_map) {
+        untrack(L.cold_host);
         cudaHostUnregister(L.cold_host);
         munmap(L.cold_map, L.cold_map_bytes);
-    } else if (L.cold_host) {
-        cudaFreeHost(L.cold_host);
+    } else {
+        pinned_free(L.cold_host);
     }
-    if (L.rowmap_dev) cudaFree(L.rowmap_dev);
+    dev_free(L.rowmap_dev);
     L = moe::Layer();
 }
 
@@ -209,10 +268,10 @@ int moe_create(const moe_geom *geom, int device, moe_ctx **out) {
     cudaDeviceProp prop;
     cudaError_t e = cudaGetDeviceProperties(&prop, device);
     if (e == cudaSuccess) ctx->sms = prop.multiProcessorCount;
-    if (e == cudaSuccess) e = cudaMalloc(&ctx->counts_dev, sizeof(int32_t) * g.layers * g.experts);
+    if (e == cudaSuccess) e = dev_alloc((void **)&ctx->counts_dev, sizeof(int32_t) * g.layers * g.experts, "create_counts");
     if (e == cudaSuccess) e = cudaMemset(ctx->counts_dev, 0, sizeof(int32_t) * g.layers * g.experts);
-    if (e == cudaSuccess) e = cudaMalloc(&ctx->staging, ctx->g.eb);
-    if (e == cudaSuccess) e = cudaMalloc(&ctx->status_dev, sizeof(int32_t) * 4);
+    if (e == cudaSuccess) e = dev_alloc((void **)&ctx->staging, ctx->g.eb, "create_staging");
+    if (e == cudaSuccess) e = dev_alloc((void **)&ctx->status_dev, sizeof(int32_t) * 4, "create_status");
     if (e == cudaSuccess) e = cudaMemset(ctx->status_dev, 0, sizeof(int32_t) * 4);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -229,11 +288,11 @@ int moe_destroy(moe_ctx *ctx) {
     DeviceGuard guard(ctx->device);
     cudaDeviceSynchronize();
     for (auto &L : ctx->layers) free_layer(L);
-    if (ctx->counts_dev) cudaFree(ctx->counts_dev);
-    if (ctx->staging) cudaFree(ctx->staging);
-    if (ctx->status_dev) cudaFree(ctx->status_dev);
-    if (ctx->probe_host) cudaFreeHost(ctx->probe_host);
-    if (ctx->probe_dev) cudaFree(ctx->probe_dev);
+    dev_free(ctx->counts_dev);
+    dev_free(ctx->staging);
+    dev_free(ctx->status_dev);
+    pinned_free(ctx->probe_host);
+    dev_free(ctx->probe_dev);
     delete ctx;
     return MOE_OK;
 }
@@ -273,11 +332,11 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
     nl.n_cold = (int)cold_ids.size();
     cudaError_t e = cudaSuccess;
     std::atomic<bool> scales_ok{true};
-    if (nl.n_hot) e = cudaMalloc(&nl.hot, (size_t)nl.n_hot * g.eb);
+    if (nl.n_hot) e = dev_alloc((void **)&nl.hot, (size_t)nl.n_hot * g.eb, "hot_bank");
     if (e == cudaSuccess && nl.n_cold) {
         e = alloc_cold_bank((size_t)nl.n_cold * g.eb, nl);
     }
-    if (e == cudaSuccess) e = cudaMalloc(&nl.rowmap_dev, sizeof(int32_t) * g.E);
+    if (e == cudaSuccess) e = dev_alloc((void **)&nl.rowmap_dev, sizeof(int32_t) * g.E, "rowmap");
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(nl.rowmap_dev, rowmap.data(), sizeof(int32_t) * g.E, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) {
@@ -293,7 +352,7 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
     if (nl.n_hot) {
         const int batch = std::min(nl.n_hot, 16);
         uint8_t *pin = nullptr;
-        e = cudaHostAlloc(&pin, (size_t)batch * g.eb, cudaHostAllocDefault);
+        e = pinned_alloc((void **)&pin, (size_t)batch * g.eb, cudaHostAllocDefault, "init_staging");
         for (int b0 = 0; e == cudaSuccess && b0 < nl.n_hot; b0 += batch) {
             int nb = std::min(batch, nl.n_hot - b0);
             parallel_for(nb, [&](int i) {
@@ -302,7 +361,7 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
             e = cudaMemcpyAsync(nl.hot + (size_t)b0 * g.eb, pin, (size_t)nb * g.eb, cudaMemcpyHostToDevice, s);
             if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         }
-        if (pin) cudaFreeHost(pin);
+        pinned_free(pin);
     }
     if (e == cudaSuccess && nl.n_cold) {
         touch_host_bank_kernel<<<4 * ctx->sms, 256, 0, s>>>(nl.cold_dev, (size_t)nl.n_cold * g.eb, nullptr);
@@ -539,21 +598,21 @@ int moe_probe_link(moe_ctx *ctx, size_t bytes, int iters, double *gbps, double *
     bytes &= ~size_t(4095);
     DeviceGuard guard(ctx->device);
     if (ctx->probe_bytes < bytes) {
-        if (ctx->probe_host) cudaFreeHost(ctx->probe_host);
-        if (ctx->probe_dev) cudaFree(ctx->probe_dev);
+        pinned_free(ctx->probe_host);
+        dev_free(ctx->probe_dev);
         ctx->probe_host = nullptr;
         ctx->probe_dev = nullptr;
         ctx->probe_bytes = 0;
-        MOE_CUDA_TRY(cudaHostAlloc(&ctx->probe_host, bytes, cudaHostAllocMapped | cudaHostAllocPortable));
+        MOE_CUDA_TRY(pinned_alloc((void **)&ctx->probe_host, bytes, cudaHostAllocMapped | cudaHostAllocPortable, "probe"));
         std::memset(ctx->probe_host, 0x5A, bytes);
-        MOE_CUDA_TRY(cudaMalloc(&ctx->probe_dev, bytes));
+        MOE_CUDA_TRY(dev_alloc((void **)&ctx->probe_dev, bytes, "probe"));
         MOE_CUDA_TRY(cudaMemset(ctx->probe_dev, 0x5A, bytes));
         ctx->probe_bytes = bytes;
     }
     uint8_t *host_dev = nullptr;
     MOE_CUDA_TRY(cudaHostGetDevicePointer((void **)&host_dev, ctx->probe_host, 0));
     uint64_t *sink = nullptr;
-    MOE_CUDA_TRY(cudaMalloc(&sink, sizeof(uint64_t) * 65536));
+    MOE_CUDA_TRY(dev_alloc((void **)&sink, sizeof(uint64_t) * 65536, "probe"));
     cudaEvent_t a, b;
     cudaEventCreate(&a);
     cudaEventCreate(&b);
@@ -575,7 +634,7 @@ int moe_probe_link(moe_ctx *ctx, size_t bytes, int iters, double *gbps, double *
     if (!r && hbm_gbps) r = measure(ctx->probe_dev, hbm_gbps);
     cudaEventDestroy(a);
     cudaEventDestroy(b);
-    cudaFree(sink);
+    dev_free(sink);
     return r;
 }
 
@@ -591,5 +650,25 @@ int moe_device_status(moe_ctx *ctx, int32_t *status) {
 }
 
 int64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moe_memory_in_use(int64_t *device_bytes, int64_t *pinned_bytes) {
+    std::lock_guard<std::mutex> lock(g_mem_mu);
+    if (device_bytes) *device_bytes = g_mem_bytes[0];
+    if (pinned_bytes) *pinned_bytes = g_mem_bytes[1];
+    return MOE_OK;
+}
+
+int moe_set_wait_limit(moe_ctx *ctx, uint64_t ns) {
+    if (int r = check_ctx(ctx)) return r;
+    ctx->wait_ns = ns ? ns : kDefaultWaitNs;
+    return MOE_OK;
+}
+
+int moe_inject_fault(moe_ctx *ctx, int kind) {
+    if (int r = check_ctx(ctx)) return r;
+    if (kind != MOE_FAULT_NONE && kind != MOE_FAULT_WITHHOLD_COPY) return set_error(MOE_EINVAL, "unknown fault kind");
+    ctx->inject_withhold = kind == MOE_FAULT_WITHHOLD_COPY;
+    return MOE_OK;
+}
 
 }  // extern "C"

@@ -186,11 +186,17 @@ struct Layer {
 
 }  // namespace moe
 
+namespace moe {
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;   // 1 s bound of a device pipeline wait
+}
+
 struct moe_ctx {
     moe::Geom g;
     int device = 0;
     int sms = 0;
     int ffn_impl = MOE_FFN_TCGEN05;
+    uint64_t wait_ns = moe::kDefaultWaitNs;   // bound of every FFN pipeline wait
+    bool inject_withhold = false;             // test hook: the next FFN call withholds one copy
     int32_t *counts_dev = nullptr;   // [L][E]
     uint8_t *staging = nullptr;      // one expert row in HBM
     int32_t *status_dev = nullptr;   // bounded-wait status word

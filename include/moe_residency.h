@@ -260,6 +260,37 @@ int moe_device_status(moe_ctx *ctx, int32_t *status);
 /* Number of kernels this library has launched in this process. */
 int64_t moe_kernel_launches(void);
 
+/* Bytes of device memory and of pinned host memory the library holds in
+ * this process (banks, row maps, usage tables, staging rows, probe buffers of
+ * every live context).  Either pointer may be NULL.  Lets a caller check that
+ * a failed call left nothing behind. */
+int moe_memory_in_use(int64_t *device_bytes, int64_t *pinned_bytes);
+
+/* ---- failure handling (no GPU fault is ever raised on purpose) ----
+ * Every pipeline wait of the FFN kernels is bounded by wall-clock time.  A
+ * wait that runs out sets the status word to MOE_ETIMEOUT (read it with
+ * moe_device_status), raises an abort flag that ends the CTA's other roles'
+ * waits, lets the copies and MMAs the CTA already issued finish, frees its
+ * tensor memory and returns; the rows of that call are then incomplete.
+ * The next call needs no reset: each call re-initialises its work counters
+ * and partial-sum rows.
+ * moe_set_wait_limit: the bound in nanoseconds for this context's later FFN
+ * calls (default 1 s; 0 restores the default). */
+int moe_set_wait_limit(moe_ctx *ctx, uint64_t ns);
+
+/* Host-set test hook for that path.  MOE_FAULT_WITHHOLD_COPY: in the next
+ * FFN call's gate/up GEMM, the CTA that takes the first unit of a bank skips
+ * the copies of its first K group, so every role waiting for them runs out
+ * its wait.  MOE_FAULT_NONE clears a pending injection.  The allocation
+ * failure path is tested through the environment instead: while
+ * MOE_INJECT_ALLOC_FAIL names an allocation site ("cold_bank", "hot_bank",
+ * "rowmap", "init_staging", "create_counts", "create_staging",
+ * "create_status", "probe"), that site reports an
+ * allocation failure without allocating (MOE_ENOMEM; moe_init_banks then
+ * leaves the layer unplaced and frees what it had allocated). */
+enum { MOE_FAULT_NONE = 0, MOE_FAULT_WITHHOLD_COPY = 1 };
+int moe_inject_fault(moe_ctx *ctx, int kind);
+
 /* ---- adaptive policy (host, between steps) ----
  * "We Built the Counter", sections 2 and 9: read the usage table every N
  * steps, keep a decaying average, queue swaps decided against a CPU copy of

@@ -165,3 +165,13 @@ def test_policy_and_counter_defaults_are_the_printed_ones(lib):
     assert inspect.signature(restore_placement).parameters["budget"].default == g["max_swaps_per_step"]
     # the usage table: int32 per (layer, expert), 40 x 384 x 4 B = 61 KB (rounded down)
     assert int(g["table_layers"] * g["table_experts"] * 4 / 1000) == g["table_kb"]
+
+
+def test_failure_hooks_without_a_device(lib):
+    """The memory accounting and the failure-path hooks load and validate
+    their arguments without a GPU (no context can exist here)."""
+    d, p = moe.moe_memory_in_use()
+    assert d >= 0 and p >= 0
+    for fn, args in ((lib.moe_set_wait_limit, (None, 1000)), (lib.moe_inject_fault, (None, 1))):
+        assert fn(*args) == moe.MOE_EINVAL
+    assert lib.moe_memory_in_use(None, None) == moe.MOE_OK
