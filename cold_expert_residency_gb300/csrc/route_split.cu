@@ -11,6 +11,13 @@
 // row, its picks as slot indices s = t*k + j in increasing order.  The order
 // is a pure function of (ids, row map), so the FFN that consumes it sees the
 // same token order for an expert whichever bank holds it.
+//
+// Steps of at most 256 tokens (decode) run in one CTA of 512 threads, whose
+// work after routing is sized by the step's picks, not by the experts: one
+// block-wide scan over the per-row pick counts gives every active row its
+// list position and offset, and each pick finds its place by counting the
+// earlier picks of its expert.  Larger steps (prefill) route with one warp per
+// token and build the lists in two more kernels.
 #include "moe_internal.cuh"
 
 #include <climits>
@@ -19,8 +26,9 @@ namespace moe {
 
 namespace {
 
-constexpr int kMaxLanesVals = 32;   // E <= 1024 => at most 32 logits per lane
-constexpr int kMaxK = 16;
+constexpr int kSmallThreads = 512;
+constexpr int kSmallMaxT = 256;
+constexpr int kSmallMaxP = 4096;
 
 struct WsPtrs {
     int32_t *hdr, *act_row, *act_off, *picks, *epos;
@@ -31,60 +39,91 @@ __device__ __forceinline__ void red_relaxed_add(int32_t *p, int v) {
     asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// a ranks before b: larger logit first, equal logits by lower expert id
 __device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
     return va > vb || (va == vb && ea < eb);
 }
 
-// One warp routes one token: k rounds of a warp-wide argmax (larger logit
-// first, ties to the lower expert id), then fp32 softmax over the k picks.
-// A NaN logit is read as -infinity (ranked below every number, weight
-// exp(-inf) = 0 beside a finite first pick), so the k ids are always valid.
-// Lane j < k returns pick j in (*id_out, *w_out); other lanes return -1.
-__device__ __forceinline__ void warp_route_token(const float *__restrict__ l, int E, int k, int lane,
-                                                 int *id_out, float *w_out) {
-    float lv[kMaxLanesVals];
-    uint32_t taken = 0;
+// A token's logits as one lane holds them: experts lane, lane+32, ... (NV
+// values, NV*32 >= E), loaded together so their latencies overlap.  A NaN
+// logit is read as -infinity.
+template <int NV>
+__device__ __forceinline__ void load_logits(const float *__restrict__ l, int E, int lane, float (&v)[NV]) {
 #pragma unroll
-    for (int i = 0; i < kMaxLanesVals; ++i) {
-        int e = lane + 32 * i;
-        const float v = e < E ? l[e] : -INFINITY;
-        lv[i] = isnan(v) ? -INFINITY : v;
-        if (e >= E) taken |= 1u << i;
+    for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        const float raw = e < E ? l[e] : -INFINITY;
+        v[i] = isnan(raw) ? -INFINITY : raw;
     }
-    float sel_v[kMaxK];
-    int sel_e[kMaxK];
+}
+
+// One warp routes one token from its logits in registers.  Each lane keeps
+// the best KM of its own values in a sorted register list; the warp then
+// takes k rounds of an argmax over the lanes' list heads, and the winning lane
+// pops its head.  NaN logits arrive as -infinity (ranked below every number,
+// weight exp(-inf) = 0 beside a finite first pick), so the k ids are always
+// valid.  Then fp32 softmax over the k picks, shifted by the first and summed
+// in pick order.  Lane j < k returns pick j in (*id_out, *w_out); other lanes
+// return -1.
+template <int KM, int NV>
+__device__ __forceinline__ void warp_route_token(const float (&v)[NV], int E, int k, int lane, int *id_out,
+                                                 float *w_out) {
+    float lv[KM];
+    int le[KM];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-        if (j < k) {
-            float bv = -INFINITY;
-            int be = INT_MAX;
+    for (int j = 0; j < KM; ++j) {
+        lv[j] = -INFINITY;
+        le[j] = INT_MAX;
+    }
 #pragma unroll
-            for (int i = 0; i < kMaxLanesVals; ++i) {
-                int e = lane + 32 * i;
-                if (!((taken >> i) & 1u) && better(lv[i], e, bv, be)) {
-                    bv = lv[i];
-                    be = e;
-                }
+    for (int i = 0; i < NV; ++i) {
+        float cv = v[i];
+        int ce = lane + 32 * i < E ? lane + 32 * i : INT_MAX;
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {   // insert, pushing the worse entries down
+            if (better(cv, ce, lv[j], le[j])) {
+                const float tv = lv[j];
+                const int te = le[j];
+                lv[j] = cv;
+                le[j] = ce;
+                cv = tv;
+                ce = te;
             }
+        }
+    }
+    float sel_v[KM];
+    int sel_e[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        if (j < k) {
+            float bv = lv[0];
+            int be = le[0];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
-                float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
                 if (better(ov, oe, bv, be)) {
                     bv = ov;
                     be = oe;
                 }
             }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            if (be == le[0]) {   // this lane held the winner: pop its head
+#pragma unroll
+                for (int q = 0; q + 1 < KM; ++q) {
+                    lv[q] = lv[q + 1];
+                    le[q] = le[q + 1];
+                }
+                lv[KM - 1] = -INFINITY;
+                le[KM - 1] = INT_MAX;
+            }
             sel_v[j] = bv;
             sel_e[j] = be;
         }
     }
-    // softmax over the picks, shifted by the largest (pick 0), summed in j order
-    float ex[kMaxK];
+    float ex[KM];
     float sum = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KM; ++j) {
         if (j < k) {
             ex[j] = expf(sel_v[j] - sel_v[0]);
             sum = sum + ex[j];
@@ -93,7 +132,7 @@ __device__ __forceinline__ void warp_route_token(const float *__restrict__ l, in
     int myid = -1;
     float myw = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KM; ++j) {
         if (j < k && j == lane) {
             myid = sel_e[j];
             myw = __fdiv_rn(ex[j], sum);
@@ -101,6 +140,136 @@ __device__ __forceinline__ void warp_route_token(const float *__restrict__ l, in
     }
     *id_out = myid;
     *w_out = myw;
+}
+
+// Route token t from logits in registers and write its picks.
+template <int KM, int NV>
+__device__ __forceinline__ void route_one(const float (&v)[NV], int t, int E, int k, int lane, int32_t *counts,
+                                          int32_t *ids, float *w, int32_t *s_ids) {
+    int id;
+    float wv;
+    warp_route_token<KM, NV>(v, E, k, lane, &id, &wv);
+    if (lane < k) {
+        ids[t * k + lane] = id;
+        w[t * k + lane] = wv;
+        if (s_ids) s_ids[t * k + lane] = id;
+        if (counts) red_relaxed_add(counts + id, 1);
+    }
+}
+
+// Block-wide inclusive scan of one int per thread (blockDim.x = 512).
+__device__ __forceinline__ int block_scan(int v, int *warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < kSmallThreads / 32 ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, t, off);
+            if (lane >= off) t += o;
+        }
+        if (lane < kSmallThreads / 32) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    return v + (warp ? warp_tot[warp - 1] : 0);
+}
+
+// Decode steps (T <= 256, T*k <= 4096): route, count and build both banks'
+// lists in one CTA of 512 threads.
+//  - every thread: row map -> shared memory; per-row pick counts cleared
+//  - warp w routes tokens w, w+16, ...
+//  - each pick adds 1 to its row's count (rows of both banks in one array:
+//    hot row r at r, cold row r at n_hot + r)
+//  - one scan over that array (two rows per thread), the count in the low 16
+//    bits and "active" in the high 16: a row's exclusive prefix gives its
+//    offset in its bank's pick list and its index among its bank's active rows
+//  - each pick's place: its row's offset + the number of earlier picks (lower
+//    slots) of the same expert.
+template <int KM, int NV>
+__global__ void __launch_bounds__(kSmallThreads) route_split_small(
+    const float *__restrict__ logits, int T, int E, int k, const int32_t *__restrict__ rowmap,
+    int n_hot, int32_t *counts, int32_t *__restrict__ ids, float *__restrict__ w, WsPtrs ws) {
+    extern __shared__ int32_t sm[];
+    __shared__ int warp_tot[32];
+    __shared__ int base1;           // bank 0's totals: the prefix bank 1's rows start from
+    const int P = ws.P;
+    int32_t *s_ids = sm;            // [P] expert of each pick
+    int32_t *s_rm = s_ids + P;      // [E] row map
+    int32_t *s_cnt = s_rm + E;      // [E] picks per row (both banks), then row offsets
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int e = tid; e < E; e += kSmallThreads) {
+        s_rm[e] = rowmap[e];
+        s_cnt[e] = 0;
+    }
+    if (tid == 0) base1 = 0;
+    {
+        // each warp routes tokens warp, warp+16, ...; the next token's logits
+        // are loaded while this one is routed
+        constexpr int kWarps = kSmallThreads / 32;
+        float cur[NV], nxt[NV];
+        if (warp < T) load_logits<NV>(logits + (size_t)warp * E, E, lane, cur);
+        for (int t = warp; t < T; t += kWarps) {
+            if (t + kWarps < T) load_logits<NV>(logits + (size_t)(t + kWarps) * E, E, lane, nxt);
+            route_one<KM, NV>(cur, t, E, k, lane, counts, ids, w, s_ids);
+#pragma unroll
+            for (int i = 0; i < NV; ++i) cur[i] = nxt[i];
+        }
+    }
+    __syncthreads();
+    for (int s = tid; s < P; s += kSmallThreads) {
+        const int m = s_rm[s_ids[s]];
+        atomicAdd(&s_cnt[m >= 0 ? m : n_hot + (-1 - m)], 1);
+    }
+    __syncthreads();
+    // the scan: E <= 1024 rows, rows 2*tid and 2*tid+1 in this thread
+    const int r0 = 2 * tid, r1 = r0 + 1;
+    const int c0 = r0 < E ? s_cnt[r0] : 0, c1 = r1 < E ? s_cnt[r1] : 0;
+    const int v0 = c0 | ((c0 > 0) << 16), v1 = c1 | ((c1 > 0) << 16);
+    const int incl1 = block_scan(v0 + v1, warp_tot);   // through row r1
+    const int incl0 = incl1 - v1;                      // through row r0
+    if (n_hot > 0) {   // the thread holding row n_hot - 1 publishes bank 0's totals
+        if (r0 == n_hot - 1) base1 = incl0;
+        if (r1 == n_hot - 1) base1 = incl1;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int r = h ? r1 : r0, c = h ? c1 : c0, incl = h ? incl1 : incl0, v = h ? v1 : v0;
+        if (r >= E) continue;
+        const int b = r >= n_hot;
+        const int excl = incl - v - (b ? base1 : 0);
+        const int off = excl & 0xFFFF, a = excl >> 16;
+        s_cnt[r] = off;   // this row's offset in its bank's pick list
+        if (c > 0) {
+            ws.act_row[b * P + a] = b ? r - n_hot : r;
+            ws.act_off[b * (P + 1) + a + 1] = off + c;
+        }
+        if (r == E - 1) {   // the thread of the last row holds both banks' totals
+            const int tot1 = incl - base1;
+            ws.hdr[kHdrNAct + 0] = base1 >> 16;
+            ws.hdr[kHdrNPicks + 0] = base1 & 0xFFFF;
+            ws.hdr[kHdrNAct + 1] = tot1 >> 16;
+            ws.hdr[kHdrNPicks + 1] = tot1 & 0xFFFF;
+            ws.act_off[0] = 0;
+            ws.act_off[P + 1] = 0;
+        }
+    }
+    __syncthreads();
+    for (int s = tid; s < P; s += kSmallThreads) {
+        const int e = s_ids[s];
+        const int m = s_rm[e];
+        const int b = m < 0;
+        int pos = 0;
+        for (int q = 0; q < s; ++q) pos += s_ids[q] == e;
+        ws.picks[b * P + s_cnt[b ? n_hot + (-1 - m) : m] + pos] = s;
+    }
 }
 
 // Build the active-row lists of bank b from per-expert pick counts.
@@ -149,66 +318,18 @@ __device__ __forceinline__ void warp_fill_expert(int e, int b, int pos, const in
     }
 }
 
-// Small steps (T <= 32, T*k <= 4096): route, count, scan and fill in one
-// CTA of 8 warps.
-__global__ void __launch_bounds__(256) route_split_small(
-    const float *__restrict__ logits, int T, int E, int k, const int32_t *__restrict__ rowmap,
-    int n_hot, int n_cold, int32_t *counts, int32_t *__restrict__ ids, float *__restrict__ w, WsPtrs ws) {
-    extern __shared__ int32_t sm[];
-    const int P = ws.P;
-    int32_t *s_ids = sm;            // [P]
-    int32_t *cnt = s_ids + P;       // [E]
-    int32_t *rmap = cnt + E;        // [E]
-    int32_t *rowexp = rmap + E;     // [2][E]
-    int32_t *epos = rowexp + 2 * E; // [E]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-
-    for (int t = warp; t < T; t += nwarps) {
-        int id;
-        float wv;
-        warp_route_token(logits + (size_t)t * E, E, k, lane, &id, &wv);
-        if (lane < k) {
-            ids[t * k + lane] = id;
-            w[t * k + lane] = wv;
-            s_ids[t * k + lane] = id;
-            if (counts) red_relaxed_add(counts + id, 1);
-        }
-    }
-    for (int e = tid; e < E; e += blockDim.x) {
-        cnt[e] = 0;
-        int m = rowmap[e];
-        rmap[e] = m;
-        if (m >= 0) rowexp[m] = e;
-        else rowexp[E + (-1 - m)] = e;
-    }
-    __syncthreads();
-    for (int s = tid; s < P; s += blockDim.x) atomicAdd(&cnt[s_ids[s]], 1);
-    __syncthreads();
-    if (warp < 2) warp_scan_bank(warp, warp == 0 ? n_hot : n_cold, E, rowexp, cnt, epos, ws, lane);
-    __syncthreads();
-    for (int e = warp; e < E; e += nwarps) {
-        if (cnt[e] == 0) continue;
-        int m = rmap[e];
-        warp_fill_expert(e, m >= 0 ? 0 : 1, epos[e], s_ids, ws, lane);
-    }
-}
-
 // Large steps, stage 1: one warp per token.
+template <int KM, int NV>
 __global__ void __launch_bounds__(256) route_tokens(const float *__restrict__ logits, int T, int E, int k,
                                                    int32_t *counts, int32_t *__restrict__ ids,
                                                    float *__restrict__ w, int32_t *ecnt) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
-    int id;
-    float wv;
-    warp_route_token(logits + (size_t)t * E, E, k, lane, &id, &wv);
-    if (lane < k) {
-        ids[t * k + lane] = id;
-        w[t * k + lane] = wv;
-        if (counts) red_relaxed_add(counts + id, 1);
-        red_relaxed_add(ecnt + id, 1);   // picks per expert for the split (order-free)
-    }
+    float v[NV];
+    load_logits<NV>(logits + (size_t)t * E, E, lane, v);
+    route_one<KM, NV>(v, t, E, k, lane, counts, ids, w, nullptr);
+    if (lane < k) red_relaxed_add(ecnt + ids[t * k + lane], 1);   // picks per expert for the split (order-free)
 }
 
 // Large steps, stage 2: the active-row scan over the per-expert counts (one CTA).
@@ -241,6 +362,38 @@ __global__ void __launch_bounds__(256) split_fill(const int32_t *__restrict__ id
     warp_fill_expert(e, rowmap[e] >= 0 ? 0 : 1, pos, ids, ws, lane);
 }
 
+template <int KM, int NV>
+int launch_route_km(const moe_ctx *ctx, const Layer &L, const float *logits, int T, int32_t *counts, int32_t *ids,
+                    float *w, WsPtrs ws, int32_t *ecnt, cudaStream_t s) {
+    const Geom &g = ctx->g;
+    const int P = ws.P;
+    if (T <= kSmallMaxT && P <= kSmallMaxP) {
+        const size_t smem = sizeof(int32_t) * ((size_t)P + 2 * (size_t)g.E);
+        route_split_small<KM, NV><<<1, kSmallThreads, smem, s>>>(logits, T, g.E, g.k, L.rowmap_dev, L.n_hot, counts, ids,
+                                                             w, ws);
+        MOE_LAUNCH_CHECK();
+        return MOE_OK;
+    }
+    MOE_CUDA_TRY(cudaMemsetAsync(ecnt, 0, sizeof(int32_t) * g.E, s));
+    route_tokens<KM, NV><<<(T + 7) / 8, 256, 0, s>>>(logits, T, g.E, g.k, counts, ids, w, ecnt);
+    MOE_LAUNCH_CHECK();
+    split_scan<<<1, 1024, sizeof(int32_t) * 3 * (size_t)g.E, s>>>(ecnt, g.E, L.rowmap_dev, L.n_hot, L.n_cold, ws);
+    MOE_LAUNCH_CHECK();
+    split_fill<<<(g.E + 7) / 8, 256, 0, s>>>(ids, g.E, L.rowmap_dev, ws);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+template <int KM>
+int launch_route_nv(const moe_ctx *ctx, const Layer &L, const float *logits, int T, int32_t *counts, int32_t *ids,
+                    float *w, WsPtrs ws, int32_t *ecnt, cudaStream_t s) {
+    const int E = ctx->g.E;
+    if (E <= 128) return launch_route_km<KM, 4>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
+    if (E <= 256) return launch_route_km<KM, 8>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
+    if (E <= 512) return launch_route_km<KM, 16>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
+    return launch_route_km<KM, 32>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
+}
+
 }  // namespace
 
 int launch_route_split(moe_ctx *ctx, int layer, const float *logits, int T, int count_on,
@@ -260,24 +413,12 @@ int launch_route_split(moe_ctx *ctx, int layer, const float *logits, int T, int 
         return MOE_OK;
     }
     int32_t *counts = (count_on && T <= g.count_tmax) ? ctx->counts_dev + (size_t)layer * g.E : nullptr;
-    const int P = ws.P;
-    if (T <= 32 && P <= 4096) {
-        size_t smem = sizeof(int32_t) * ((size_t)P + 5 * (size_t)g.E);
-        route_split_small<<<1, 256, smem, s>>>(logits, T, g.E, g.k, L.rowmap_dev, L.n_hot, L.n_cold,
-                                                counts, ids, w, ws);
-        MOE_LAUNCH_CHECK();
-        return MOE_OK;
-    }
     int32_t *ecnt = (int32_t *)(ws_base + lay.ecnt);
-    MOE_CUDA_TRY(cudaMemsetAsync(ecnt, 0, sizeof(int32_t) * g.E, s));
-    route_tokens<<<(T + 7) / 8, 256, 0, s>>>(logits, T, g.E, g.k, counts, ids, w, ecnt);
-    MOE_LAUNCH_CHECK();
-    split_scan<<<1, 1024, sizeof(int32_t) * 3 * (size_t)g.E, s>>>(ecnt, g.E, L.rowmap_dev, L.n_hot,
-                                                                  L.n_cold, ws);
-    MOE_LAUNCH_CHECK();
-    split_fill<<<(g.E + 7) / 8, 256, 0, s>>>(ids, g.E, L.rowmap_dev, ws);
-    MOE_LAUNCH_CHECK();
-    return MOE_OK;
+    // the lanes' sorted lists hold KM >= k entries; each lane holds NV >= E/32
+    // of a token's logits
+    if (g.k <= 4) return launch_route_nv<4>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
+    if (g.k <= 8) return launch_route_nv<8>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
+    return launch_route_nv<16>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
 }
 
 // Two-element row-map write, ordered on the stream after a swap's copies.
