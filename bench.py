@@ -787,28 +787,40 @@ def measure_adaptive(S, ctx, n_layers, acfg, args, layer=0):
     }
 
 
-def measure_prefill(S, ctx, pcfg, args, layer):
-    """The 8192-token prefill chunk on context layer `layer` (all experts in HBM)."""
+def measure_prefill(S, ctx, pcfg, args, layer, fmt=0):
+    """The 8192-token prefill chunk on context layer `layer` (all experts in
+    HBM), with the token rows as two e4m3 pieces (fmt 0, the default) or in
+    the MXFP8 format (fmt 1: one MMA per product)."""
     T = pcfg.T
     steps = max(3, min(args.steps, 20))
-    run = StepRunner(S, ctx, pcfg, [layer], T, 2, False, input_layers=[0])
-    run.capture()
-    run.settle(max(3, min(args.warmup, 5)))
-    step_ms, clocks = run.timed(steps, 0)
-    ffn = run.ffn_in_step_ms(min(steps, 10))[layer]
+    S.moe.moe_set_act_format(ctx, fmt)
+    try:
+        run = StepRunner(S, ctx, pcfg, [layer], T, 2, False, input_layers=[0])
+        run.capture()
+        run.settle(max(3, min(args.warmup, 5)))
+        step_ms, clocks = run.timed(steps, 0)
+        ffn = run.ffn_in_step_ms(min(steps, 10))[layer]
+    finally:
+        S.moe.moe_set_act_format(ctx, 0)
     eb = S.moe.moe_expert_bytes(pcfg.H, pcfg.I)
     picks = T * pcfg.k
     flops = picks * 2.0 * 3.0 * pcfg.I * pcfg.H
     tf = flops / (float(np.mean(ffn)) * 1e-3) / 1e12
+    if fmt == 0:
+        peak, src = S.tf_burst, (f"{S.peak_src} bf16 dense burst ('of measured'): rows carry bf16-class precision "
+                                 "as two e4m3 pieces, two fp8-rate MMAs per product = the bf16 rate")
+        kern = "ffn_tc_kernel<192,1,hot,false> + <192,2,hot,false> with prep_x, prep_h"
+    else:
+        peak, src = 2.0 * S.tf_burst, (f"{S.peak_src} bf16 dense burst x 2 (the nominal fp8 : bf16 dense ratio, "
+                                       "4.5 : 2.25 PFLOP/s; 'of measured'): one fp8-rate MMA per product")
+        kern = "ffn_tc_kernel<192,1,hot,true> + <192,2,hot,true> with tile_scan, prep_x_mx8, prep_h_mx8"
     return {
         "workload": WORKLOADS["prefill"], "tokens_per_step": T, "steps": steps,
+        "activations": "two e4m3 pieces per value (bf16-class)" if fmt == 0 else "MXFP8 (e4m3, e8m0 per 32)",
         "us_per_layer_step": float(np.mean(step_ms)) * 1e3, "tokens_per_s": T / (float(np.mean(step_ms)) * 1e-3),
         "step_us_pct": pct(step_ms),
-        "roofline": {"kernel": "FFN call inside the step (ffn_tc_kernel<192,1,hot> + <192,2,hot> with prep_x, "
-                               "prep_h)", "bound": "tensor", "achieved": tf, "peak": S.tf_burst, "unit": "TFLOP/s",
-                     "frac": tf / S.tf_burst, "flops_per_launch": flops,
-                     "peak_source": f"{S.peak_src} bf16 dense burst ('of measured'): rows carry bf16-class precision "
-                                    "as two e4m3 pieces, two fp8-rate MMAs per product = the bf16 rate",
+        "roofline": {"kernel": f"FFN call inside the step ({kern})", "bound": "tensor", "achieved": tf, "peak": peak,
+                     "unit": "TFLOP/s", "frac": tf / peak, "flops_per_launch": flops, "peak_source": src,
                      "hbm_gbs_achieved": 384 * eb / (float(np.mean(ffn)) * 1e-3) / 1e9,
                      "traffic": None, "us_per_launch": float(np.mean(ffn)) * 1e3},
         "clocks": clocks, "launches_per_step": run.launches_per_step,
@@ -898,6 +910,8 @@ def run_all(S, args):
             hbm_layer = next(l for l in range(cfg.L) if masks[l].all())
             p = measure_prefill(S, ctx, pcfg, args, hbm_layer)
             p["workload"] += f" (layer {hbm_layer} of this context)"
+            p["mxfp8"] = measure_prefill(S, ctx, pcfg, args, hbm_layer, fmt=1)
+            p["mxfp8"].pop("workload")
             subs["prefill"] = p
         line["configs"] = subs
     finally:

@@ -22,6 +22,7 @@ MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTALE, MOE_ETIMEOUT, MOE_ESTATE 
 MOE_BANK_HOT, MOE_BANK_COLD, MOE_BANK_BOTH = 0, 1, 2
 MOE_FFN_TCGEN05, MOE_FFN_SIMT = 0, 1
 MOE_FAULT_NONE, MOE_FAULT_WITHHOLD_COPY = 0, 1
+MOE_ACT_E4M3X2, MOE_ACT_MXFP8 = 0, 1
 
 _lib = None
 
@@ -59,6 +60,7 @@ def lib():
         "moe_create": (i32, [C.POINTER(moe_geom), i32, C.POINTER(P)]),
         "moe_destroy": (i32, [P]),
         "moe_set_ffn_impl": (i32, [P, i32]),
+        "moe_set_act_format": (i32, [P, i32]),
         "moe_init_banks": (i32, [P, i32, P, P, P, P, P, P]),
         "moe_workspace_bytes": (i32, [P, i32, C.POINTER(sz)]),
         "moe_route_split_count": (i32, [P, i32, P, i32, i32, P, P, P, P]),
@@ -173,6 +175,10 @@ def moe_destroy(ctx):
 
 def moe_set_ffn_impl(ctx, impl):
     return _err("moe_set_ffn_impl", lib().moe_set_ffn_impl(ctx, impl))
+
+
+def moe_set_act_format(ctx, fmt):
+    return _err("moe_set_act_format", lib().moe_set_act_format(ctx, fmt))
 
 
 def moe_init_banks(ctx, layer, w13_q, w13_s, w2_q, w2_s, is_hot, stream=None):

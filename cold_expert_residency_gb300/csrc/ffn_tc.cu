@@ -79,6 +79,11 @@ struct TcArgs {
     int32_t *claim;         // [SM] first-CTA claims (zeroed before the launch)
     uint64_t wait_ns;       // bound of every pipeline wait (wall-clock ns)
     int32_t withhold;       // fault injection: the CTA that takes unit 0 of a bank skips its first group's copies
+    // MXFP8 prefill tiles: per bank, the first tile of each active row and
+    // the tiles' B-operand block scales [tile][group][kSfbGroupBytes]
+    const int32_t *tile_off[2];
+    const uint8_t *sfb[2];
+    int sf_groups;          // K groups per tile in sfb
 };
 
 constexpr int kQ = 4;       // unit queue depth (producer -> the other roles)
@@ -133,23 +138,25 @@ __device__ __forceinline__ int bank_offset(const BankLists &L, int b, int P) {
     return b == 0 ? 0 : P - L.hdr[kHdrNPicks + 1];
 }
 
-template <int NMAX>
+template <int NMAX, bool MX = false>
 struct TcCfg {
     // This kernel runs the prefill tiles; decode tiles run ffn_tc_decode_kernel.
     static_assert(NMAX >= 128 && NMAX <= 256 && NMAX % 16 == 0, "prefill tile");
-    static constexpr bool kWide = true;
     static constexpr bool kStack = false;                   // one MMA per e4m3 piece
-    // One 4-D tensor-TMA box per stage brings the tile's token rows: both
-    // e4m3 pieces of both 64-wide chunks, as [chunk][piece][NMAX rows][64 B]
-    // with 64-byte swizzle (rows past the tile's tokens are loaded and unused).
-    static constexpr int kBChunk = 2 * NMAX * 64;           // one chunk: both pieces
+    // One 4-D tensor-TMA box per stage brings the tile's token rows: the
+    // e4m3 pieces (two, or one in the MXFP8 format) of both 64-wide chunks, as
+    // [chunk][piece][NMAX rows][64 B] with 64-byte swizzle (rows past the
+    // tile's tokens are loaded and unused).
+    static constexpr int kPieces = MX ? 1 : 2;
+    static constexpr int kBChunk = kPieces * NMAX * 64;     // one chunk: its pieces
     static constexpr int kBStage = 2 * kBChunk;
     static constexpr int kRowQ = 16;                        // token rows of a piece, padded to 16
     static constexpr int kAStage = 2 * kGroupQBytes;        // padded code block: 16 KB
+    static constexpr int kSfbStage = MX ? kSfbGroupBytes : 0;   // the tile's B block scales of one group
     // One stage holds a group's 8.5 KB of weights as 16.5 KB of padded codes
-    // and scales, plus the token rows; the host sizes the ring per launch
-    // from the SM's shared memory.
-    static constexpr int kStageBytes = kAStage + kBStage + kSfAtomBytes;
+    // and scales, plus the token rows (and their block scales); the host
+    // sizes the ring per launch from the SM's shared memory.
+    static constexpr int kStageBytes = kAStage + kBStage + kSfAtomBytes + kSfbStage;
     static constexpr int kDBufs = 2;                        // accumulators in TMEM
     static constexpr int kDW = NMAX;                        // columns of one accumulator
     static constexpr int kNCol = (kDW + 31) / 32;           // B scale columns of one piece
@@ -157,8 +164,10 @@ struct TcCfg {
     // it % kNsf after the MMAs of iteration it - kNsf have completed.
     static constexpr int kNsf = 3;
     // Tensor memory columns: slot i's A scales at 32 i (four columns written
-    // by tcgen05.cp); slot 0's block also holds the B scale columns of piece
-    // 0 at +8 and of piece 1 at +16; then the accumulators.
+    // by tcgen05.cp); slot 0's block also holds the constant B scale columns
+    // of piece 0 at +8 and of piece 1 at +16 -- in the MXFP8 format, slot i's
+    // own B scale columns sit at 32 i + 8 (token blocks 0..7, two tcgen05.cp
+    // of the stage's scales); then the accumulators.
     static constexpr uint32_t kSfbCol = 8;
     static constexpr uint32_t kSfbStride = 8;
     static constexpr uint32_t kDCol = 32 * kNsf;
@@ -286,11 +295,11 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
 // BANKS names the launch (0 hot bank, 1 cold bank, 2 both banks); the code
 // is the same, every unit carries its bank.  tmA0 / tmA1: the hot and cold
 // bank's code-block maps of this GEMM's part; tmB: the token-row records.
-template <int NMAX, int PHASE, int BANKS>
-__global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
+template <int NMAX, int PHASE, int BANKS, bool MX>
+__global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0,
                   const __grid_constant__ CUtensorMap tmA1, TcArgs args) {
-    using C = TcCfg<NMAX>;
+    using C = TcCfg<NMAX, MX>;
     constexpr int DB = C::kDBufs, NSF = C::kNsf;
     const int S = args.S;
     extern __shared__ uint8_t smem_raw[];
@@ -299,7 +308,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
     uint8_t *sA = smem;                          // [S][16 KB] padded code blocks
     uint8_t *sB = sA + S * C::kAStage;           // [S][2 chunks][2 pieces][NMAX rows][64 B] token rows
     uint8_t *sSF = sB + S * C::kBStage;          // [S][512] scale atoms
-    uint64_t *bars = (uint64_t *)(sSF + S * kSfAtomBytes);
+    uint8_t *sSFB = sSF + S * kSfAtomBytes;      // [S][kSfbStage] token rows' block scales (MXFP8)
+    uint64_t *bars = (uint64_t *)(sSFB + S * C::kSfbStage);
     uint32_t *holder = (uint32_t *)(bars + C::kBars);
     volatile int *abort_flag = (volatile int *)(holder + 1);
     volatile int *uq = (volatile int *)(holder + 2);   // [kQ] unit queue
@@ -354,7 +364,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *holder;
-    if (warp < 4) {
+    if (warp < 4 && !MX) {
         // B scale columns, constant, in every lane quarter (each quarter
         // reads its own): 2^0; wide tiles scale the second piece by 2^-4
         // here, stacked tiles in the epilogue
@@ -485,11 +495,18 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
                     // the code block counts its packed (global) bytes; the token-row
                     // box counts in full (a half group's second chunk is past the
                     // rows' end: zero fill, unused)
-                    ptx::mbar_arrive_expect_tx(bar(FULL + st), (uint32_t)(kGroupQBytes + kSfAtomBytes + C::kBStage));
+                    ptx::mbar_arrive_expect_tx(bar(FULL + st),
+                                               (uint32_t)(kGroupQBytes + kSfAtomBytes + C::kBStage + C::kSfbStage));
                     ptx::tma_load_5d(ptx::smem_addr(sA + st * C::kAStage), tmA, 0, 0, slot, tidx, row, bar(FULL + st));
                     ptx::bulk_g2s(ptx::smem_addr(sSF + st * kSfAtomBytes), expert + part.group_off(slot, tidx) + kGroupQBytes,
                                   kSfAtomBytes, bar(FULL + st));
                     ptx::tma_load_4d(ptx::smem_addr(sB + st * C::kBStage), &tmB, 0, brow, 0, 2 * s, bar(FULL + st));
+                    if (MX) {   // the tile's block scales of this group
+                        const int64_t tile = args.tile_off[bk][a] + n0 / NMAX;
+                        ptx::bulk_g2s(ptx::smem_addr(sSFB + st * C::kSfbStage),
+                                      args.sfb[bk] + (tile * args.sf_groups + s) * kSfbGroupBytes, kSfbGroupBytes,
+                                      bar(FULL + st));
+                    }
                 }
             }
         }
@@ -543,6 +560,11 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
                     }
                     const uint32_t sfa = tmem + 32u * (it % NSF);
                     ptx::tmem_cp_32x128b_warpx4(sfa, ptx::smem_desc_noswizzle(ptx::smem_addr(sSF + st * kSfAtomBytes), 128, 128));
+                    if (MX) {   // token blocks 0-3 and 4-7 of the tile's block scales
+                        const uint32_t sb = ptx::smem_addr(sSFB + st * C::kSfbStage);
+                        ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol, ptx::smem_desc_noswizzle(sb, 128, 128));
+                        ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol + 4, ptx::smem_desc_noswizzle(sb + 512, 128, 128));
+                    }
                     const uint32_t a_addr = ptx::smem_addr(sA + st * C::kAStage);
                     for (int i = 0; i < nkb; ++i) {
                         const int kb = kb0 + i;   // K block of the group (A bytes kb*32.., scale byte kb)
@@ -550,10 +572,14 @@ __global__ void __launch_bounds__(TcCfg<NMAX>::kThreads, 1)
                         // this tile's chunk i/2 of the group, its K block i%2
                         const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage + (i >> 1) * C::kBChunk) + (i & 1) * 32;
 #pragma unroll
-                        for (int pc = 0; pc < (C::kStack ? 1 : 2); ++pc) {   // e4m3 piece of B (unstacked tiles)
+                        for (int pc = 0; pc < (C::kStack ? 1 : C::kPieces); ++pc) {   // e4m3 piece of B (unstacked tiles)
                             const uint64_t bd = ptx::smem_desc_sw64(b_addr + pc * NMAX * 64);
-                            ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29), sfa, tmem + C::kSfbCol + pc * C::kSfbStride,
-                                                 (s != s0) | i | pc);
+                            if (MX)   // B's scale: byte i (the token rows' K block) of the slot's own columns
+                                ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29) | ((uint32_t)i << 4), sfa,
+                                                     sfa + C::kSfbCol, (s != s0) | i);
+                            else
+                                ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29), sfa,
+                                                     tmem + C::kSfbCol + pc * C::kSfbStride, (s != s0) | i | pc);
                         }
                     }
                     ptx::mma_commit(bar(DONE + st));
@@ -764,6 +790,154 @@ __global__ void __launch_bounds__(256) round_y_kernel(BankLists L0, BankLists L1
     }
 }
 
+// ---------------------------------------------------------------------------
+// MXFP8 rows for prefill tiles (moe_set_act_format(MOE_ACT_MXFP8))
+// ---------------------------------------------------------------------------
+
+// The first prefill tile of each active row, per bank: tile_off[b][a] =
+// sum over a' < a of ceil(n_a' / 192); tile_off[b][n_act] = the bank's tiles.
+// One warp per bank.
+__global__ void __launch_bounds__(64) tile_scan_kernel(BankLists L0, BankLists L1, int b0, int P, int32_t *tile_off) {
+    const int b = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (b0 >= 0 && b != b0) return;
+    const BankLists &L = b ? L1 : L0;
+    const int na = L.hdr[kHdrNAct + b];
+    int32_t *to = tile_off + (size_t)b * (P + 1);
+    int run = 0;
+    for (int base = 0; base < na; base += 32) {
+        const int a = base + lane;
+        const int n = a < na ? L.act_off[a + 1] - L.act_off[a] : 0;
+        const int t = (n + kPrefillTile - 1) / kPrefillTile;
+        int incl = t;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (a < na) to[a] = run + incl - t;
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) to[na] = run;
+}
+
+// Values 8i..8i+7 of a row -> MXFP8: the 32-element block of these values
+// lies in lanes 4j..4j+3 of the warp (all 32 lanes call this together); the
+// block's exponent e makes its largest |value| fit 448 (the same rule as a
+// row's exponent, held to the e8m0 range), and each value becomes
+// e4m3(v 2^-e), rounded to nearest even.  Returns the 8 bytes and the
+// block's e.
+__device__ __forceinline__ uint2 mx8_values(const float (&v)[8], int &e) {
+    float mx = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(v[q]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    e = min(127, max(-127, row_exponent(mx)));   // an e8m0 scale spans 2^-127 .. 2^127
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        w[q] = __nv_cvt_float2_to_fp8x2(make_float2(ldexpf(v[2 * q], -e), ldexpf(v[2 * q + 1], -e)), __NV_SATFINITE,
+                                        __NV_E4M3);
+    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
+// Where pick p of bank b sits among the prefill tiles: its active row a (the
+// largest a with act_off[a] <= p), its tile and its row in the tile.
+__device__ __forceinline__ void pick_tile(const BankLists &L, int b, int p, const int32_t *tile_off, int P, int &tile,
+                                          int &r) {
+    int lo = 0, hi = L.hdr[kHdrNAct + b] - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (L.act_off[mid] <= p) lo = mid;
+        else hi = mid - 1;
+    }
+    const int q = p - L.act_off[lo];
+    tile = tile_off[(size_t)b * (P + 1) + lo] + q / kPrefillTile;
+    r = q % kPrefillTile;
+}
+
+// Byte of a tile's block-scale slab holding token row r's scale for K block
+// kblk of the row (group kblk / 4, block kblk % 4).
+__device__ __forceinline__ int sfb_byte(int r, int kblk) {
+    const int j = r >> 5, l = r & 31;
+    return (kblk >> 2) * kSfbGroupBytes + (j >> 2) * 512 + l * 16 + (j & 3) * 4 + (kblk & 3);
+}
+
+// One row of K values (8 per thread per pass; n8 = K / 8, a multiple of 4)
+// to its MXFP8 bytes (dst, K bytes, logical order) and its block scales in
+// the tile's slab.
+template <class Load8>
+__device__ __forceinline__ void mx8_row(int n8, Load8 load8, uint8_t *__restrict__ dst, uint8_t *__restrict__ slab,
+                                        int r) {
+    for (int i0 = 0; i0 < n8; i0 += blockDim.x) {   // every thread takes part in each pass (warp shuffles)
+        const int i = i0 + threadIdx.x;
+        float v[8];
+        if (i < n8) {
+            load8(i, v);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = 0.0f;
+        }
+        int e;
+        const uint2 q8 = mx8_values(v, e);
+        if (i < n8) {
+            *(uint2 *)(dst + (int64_t)i * 8) = q8;
+            if ((i & 3) == 0) slab[sfb_byte(r, i >> 2)] = (uint8_t)(127 + e);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) prep_x_mx8_kernel(const uint16_t *__restrict__ x, int H, int k, BankLists L0,
+                                                         BankLists L1, int b0, int P, uint8_t *__restrict__ xq,
+                                                         int32_t *__restrict__ xgexp, int32_t *sched, int32_t *claim,
+                                                         const int32_t *__restrict__ tile_off, uint8_t *__restrict__ sfx,
+                                                         int max_tiles) {
+    const int p = blockIdx.x, b = b0 >= 0 ? b0 : (int)blockIdx.y;
+    const BankLists &L = b ? L1 : L0;
+    if (p == 0 && blockIdx.y == 0) {
+        if (threadIdx.x < 4 && (b0 < 0 || (int)threadIdx.x / 2 == b0)) sched[threadIdx.x] = 0;
+        if (claim)
+            for (int i = threadIdx.x; i < 2 * 1024; i += blockDim.x) claim[i] = 0;
+    }
+    if (p >= L.hdr[kHdrNPicks + b]) return;
+    const int g = bank_offset(L, b, P) + p;
+    int tile, r;
+    pick_tile(L, b, p, tile_off, P, tile, r);
+    const int groups = H / kKG;
+    uint8_t *slab = sfx + ((int64_t)b * max_tiles + tile) * groups * kSfbGroupBytes;
+    const uint4 *row = (const uint4 *)(x + (int64_t)(L.picks[p] / k) * H);
+    mx8_row(H / 8, [&](int i, float (&v)[8]) {
+        const uint4 u = row[i];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[2 * q] = __uint_as_float(w[q] << 16);
+            v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+        }
+    }, xq + (int64_t)g * H, slab, r);
+    if (threadIdx.x == 0) xgexp[g] = 0;   // the block scales carry the magnitudes
+}
+
+__global__ void __launch_bounds__(256) prep_h_mx8_kernel(BankLists L0, BankLists L1, int b0, int P, int I,
+                                                         const float *__restrict__ h32, uint8_t *__restrict__ hq,
+                                                         int32_t *__restrict__ hexp, const int32_t *__restrict__ tile_off,
+                                                         uint8_t *__restrict__ sfh, int max_tiles) {
+    const int p = blockIdx.x, b = b0 >= 0 ? b0 : (int)blockIdx.y;
+    const BankLists &L = b ? L1 : L0;
+    if (p >= L.hdr[kHdrNPicks + b]) return;
+    const int g = bank_offset(L, b, P) + p;
+    int tile, r;
+    pick_tile(L, b, p, tile_off, P, tile, r);
+    const int groups = (I + kKG - 1) / kKG;
+    uint8_t *slab = sfh + ((int64_t)b * max_tiles + tile) * groups * kSfbGroupBytes;
+    const float4 *row = (const float4 *)(h32 + (int64_t)g * I);
+    mx8_row(I / 8, [&](int i, float (&v)[8]) {
+        const float4 a = row[2 * i], c = row[2 * i + 1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+    }, hq + (int64_t)g * I, slab, r);
+    if (threadIdx.x == 0) hexp[g] = 0;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -777,16 +951,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Tensor map over the [rows][K/64][2 pieces][64 B] records of K-element
-// rows, viewed as (byte, row, piece, chunk): a box of box_rows rows x both
-// pieces x two chunks lands as [chunk][piece][row][64 B], 64-byte swizzle,
-// zero fill past the last row or chunk.
-int make_piece_map(CUtensorMap *map, const void *base, int K, int rows, int box_rows) {
+// Tensor map over the [rows][K/64][pieces][64 B] records of K-element rows
+// (two e4m3 pieces, or one in the MXFP8 format), viewed as (byte, row,
+// piece, chunk): a box of box_rows rows x every piece x two chunks lands as
+// [chunk][piece][row][64 B], 64-byte swizzle, zero fill past the last row or
+// chunk.
+int make_piece_map(CUtensorMap *map, const void *base, int K, int rows, int box_rows, int pieces = 2) {
     auto enc = tensor_map_encoder();
     if (!enc) return set_error(MOE_ECUDA, "cuTensorMapEncodeTiled unavailable");
-    cuuint64_t dims[4] = {64, (cuuint64_t)rows, 2, (cuuint64_t)K / 64};
-    cuuint64_t strides[3] = {(cuuint64_t)K * 2, 64, 128};
-    cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, 2, 2};
+    cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)pieces, (cuuint64_t)K / 64};
+    cuuint64_t strides[3] = {(cuuint64_t)K * pieces, 64, (cuuint64_t)64 * pieces};
+    cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, (cuuint32_t)pieces, 2};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -795,11 +970,11 @@ int make_piece_map(CUtensorMap *map, const void *base, int K, int rows, int box_
     return MOE_OK;
 }
 
-template <int NMAX, int PHASE, int BANKS>
+template <int NMAX, int PHASE, int BANKS, bool MX>
 int launch_one(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap &mA1, const TcArgs &args, int blocks,
                cudaStream_t s) {
-    using C = TcCfg<NMAX>;
-    auto kern = ffn_tc_kernel<NMAX, PHASE, BANKS>;
+    using C = TcCfg<NMAX, MX>;
+    auto kern = ffn_tc_kernel<NMAX, PHASE, BANKS, MX>;
     const size_t smem = C::smem_bytes(args.S);
     MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     if (blocks < 1) return MOE_OK;
@@ -819,9 +994,9 @@ struct LaunchPlan {
 // worth for a cold bank when the layer has both banks, so the two banks'
 // launches run side by side), and a ring as deep as the SM's shared memory
 // allows.
-template <int NMAX>
+template <int NMAX, bool MX>
 LaunchPlan plan_for(const moe_ctx *ctx, int b, bool shared, int units_max) {
-    using C = TcCfg<NMAX>;
+    using C = TcCfg<NMAX, MX>;
     const long per = (long)kSmSmem - (long)kCtaReserve - (long)C::kFixedSmem;
     LaunchPlan p;
     p.S = std::max(C::kNsf, std::min(kMaxStages, (int)(per / C::kStageBytes)));
@@ -832,38 +1007,61 @@ LaunchPlan plan_for(const moe_ctx *ctx, int b, bool shared, int units_max) {
     return p;
 }
 
-template <int NMAX, int PHASE>
+template <int NMAX, int PHASE, bool MX>
 int launch_gemm(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap &mA1, const TcArgs &a, int blocks,
                 cudaStream_t s) {
-    if (a.b < 0) return launch_one<NMAX, PHASE, 2>(mB, mA0, mA1, a, blocks, s);
-    if (a.b == MOE_BANK_COLD) return launch_one<NMAX, PHASE, 1>(mB, mA0, mA1, a, blocks, s);
-    return launch_one<NMAX, PHASE, 0>(mB, mA0, mA1, a, blocks, s);
+    if (a.b < 0) return launch_one<NMAX, PHASE, 2, MX>(mB, mA0, mA1, a, blocks, s);
+    if (a.b == MOE_BANK_COLD) return launch_one<NMAX, PHASE, 1, MX>(mB, mA0, mA1, a, blocks, s);
+    return launch_one<NMAX, PHASE, 0, MX>(mB, mA0, mA1, a, blocks, s);
 }
 
-template <int NMAX>
+template <int NMAX, bool MX>
 int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs a2, int units1, int units2,
                 const uint16_t *x, const WsLayout &lay, uint8_t *ws, cudaStream_t s) {
     const Geom &g = ctx->g;
     const int P = a1.P;
-    // K parts per unit: two halves for narrow tiles, unless the tile has a
-    // single K group
-    a1.ks = std::min(TcCfg<NMAX>::kSplit, a1.part.steps());
-    a2.ks = std::min(TcCfg<NMAX>::kSplit, a2.part.steps());
-    const LaunchPlan p1 = plan_for<NMAX>(ctx, a1.b, shared, units1), p2 = plan_for<NMAX>(ctx, a1.b, shared, units2);
+    a1.ks = std::min(TcCfg<NMAX, MX>::kSplit, a1.part.steps());
+    a2.ks = std::min(TcCfg<NMAX, MX>::kSplit, a2.part.steps());
+    const LaunchPlan p1 = plan_for<NMAX, MX>(ctx, a1.b, shared, units1), p2 = plan_for<NMAX, MX>(ctx, a1.b, shared, units2);
     a1.S = p1.S;
     a2.S = p2.S;
     const dim3 grid_p(P, a1.b < 0 ? 2 : 1);   // one block per pick (of each bank)
+    const int pieces = MX ? 1 : 2;
     CUtensorMap m1, m2;
-    if (int r = make_piece_map(&m1, ws + lay.xq, g.H, P, NMAX)) return r;
-    if (int r = make_piece_map(&m2, ws + lay.hq, g.I, P, NMAX)) return r;
-    prep_x_kernel<false><<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
-                                         (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
+    if (int r = make_piece_map(&m1, ws + lay.xq, g.H, P, NMAX, pieces)) return r;
+    if (int r = make_piece_map(&m2, ws + lay.hq, g.I, P, NMAX, pieces)) return r;
+    if (MX) {
+        int32_t *tile_off = (int32_t *)(ws + lay.tile_off);
+        const int gx = g.H / kKG, gh = (g.I + kKG - 1) / kKG;
+        for (int bk = 0; bk < 2; ++bk) {
+            a1.tile_off[bk] = a2.tile_off[bk] = tile_off + (size_t)bk * (P + 1);
+            a1.sfb[bk] = ws + lay.sfx + (size_t)bk * lay.max_tiles * gx * kSfbGroupBytes;
+            a2.sfb[bk] = ws + lay.sfh + (size_t)bk * lay.max_tiles * gh * kSfbGroupBytes;
+        }
+        a1.sf_groups = gx;
+        a2.sf_groups = gh;
+        tile_scan_kernel<<<1, 64, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, tile_off);
+        MOE_LAUNCH_CHECK();
+        prep_x_mx8_kernel<<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
+                                                 (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, tile_off, ws + lay.sfx,
+                                                 lay.max_tiles);
+    } else {
+        prep_x_kernel<false><<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
+                                                    (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
+    }
     MOE_LAUNCH_CHECK();
-    if (int r = launch_gemm<NMAX, 1>(m1, layer.wmap[0][0], layer.wmap[1][0], a1, p1.blocks, s)) return r;
-    prep_h_kernel<false><<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
-                                         a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
+    if (int r = launch_gemm<NMAX, 1, MX>(m1, layer.wmap[0][0], layer.wmap[1][0], a1, p1.blocks, s)) return r;
+    if (MX) {
+        prep_h_mx8_kernel<<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
+                                                 ws + lay.hq, (int32_t *)(ws + lay.hexp),
+                                                 (const int32_t *)(ws + lay.tile_off), ws + lay.sfh, lay.max_tiles);
+    } else {
+        prep_h_kernel<false><<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I,
+                                                    (const float *)(ws + lay.h32), a1.gu_out, ws + lay.hq,
+                                                    (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
+    }
     MOE_LAUNCH_CHECK();
-    if (int r = launch_gemm<NMAX, 2>(m2, layer.wmap[0][1], layer.wmap[1][1], a2, p2.blocks, s)) return r;
+    if (int r = launch_gemm<NMAX, 2, MX>(m2, layer.wmap[0][1], layer.wmap[1][1], a2, p2.blocks, s)) return r;
     if (!a2.y_out) return MOE_OK;
     round_y_kernel<<<grid_p, 256, 0, s>>>(a2.lists[0], a2.lists[1], a2.b, g.H, a2.y_out, a2.Y);
     MOE_LAUNCH_CHECK();
@@ -1047,7 +1245,9 @@ int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int b, const uint16_t *x, in
     if (T <= 8) return launch_bank_decode<8>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
     if (T <= 16) return launch_bank_decode<16>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
     if (T <= kNarrowMaxT) return launch_bank_decode<32>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
-    return launch_bank<192>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
+    if (ctx->act_format == MOE_ACT_MXFP8)
+        return launch_bank<kPrefillTile, true>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
+    return launch_bank<kPrefillTile, false>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
 }
 
 }  // namespace moe

@@ -304,6 +304,13 @@ int moe_set_ffn_impl(moe_ctx *ctx, int impl) {
     return MOE_OK;
 }
 
+int moe_set_act_format(moe_ctx *ctx, int format) {
+    if (int r = check_ctx(ctx)) return r;
+    if (format != MOE_ACT_E4M3X2 && format != MOE_ACT_MXFP8) return set_error(MOE_EINVAL, "unknown activation format");
+    ctx->act_format = format;
+    return MOE_OK;
+}
+
 int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t *w13_s,
                    const uint8_t *w2_q, const uint8_t *w2_s, const uint8_t *is_hot, void *stream) {
     if (int r = check_layer(ctx, layer, false)) return r;

@@ -8,6 +8,7 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <string>
@@ -118,7 +119,12 @@ inline Geom make_geom(const moe_geom &g) {
 // pick's index in its bank's list), so the two banks never share a row and
 // each expert's rows are contiguous.
 struct WsLayout {
-    size_t hdr, act_row, act_off, picks, epos, ecnt, xq, xgexp, h32, hq, hexp, gu32, y32, claim, total;
+    size_t hdr, act_row, act_off, picks, epos, ecnt, xq, xgexp, h32, hq, hexp, gu32, y32, claim;
+    // prefill-sized steps with MXFP8 activations: per bank, the first token
+    // tile of each active row, and the tiles' B-operand block scales
+    size_t tile_off, sfx, sfh;
+    int max_tiles;          // token tiles per bank, at most
+    size_t total;
 };
 // header words
 // kHdrSched + 2*bank + phase: work counters of the FFN kernels' dynamic
@@ -131,6 +137,14 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // two K halves per unit.
 constexpr int kNarrowMaxT = 256;
 inline bool split_k_steps(int T) { return T <= kNarrowMaxT; }
+
+// Token rows per prefill tile, and the bytes of one K group's B-operand
+// block scales of one tile in the MXFP8 format: two 32-row x 16-byte atoms,
+// row l of atom c holding tokens 32*(4c + q) + l (q = 0..3), 4 bytes each
+// (the group's four 32-wide K blocks) -- what tcgen05.cp puts where the
+// block-scaled MMA reads token n's scale (column n/32, lane n%32).
+constexpr int kPrefillTile = 192;
+constexpr int kSfbGroupBytes = 1024;
 
 inline WsLayout ws_layout(const Geom &g, int T) {
     WsLayout w;
@@ -154,6 +168,13 @@ inline WsLayout ws_layout(const Geom &g, int T) {
     w.gu32 = take(ks * P * (size_t)g.I * 2 * 4); // [P][2I] gate/up sums before SwiGLU, by g
     w.y32 = take(ks * P * (size_t)g.H * 4);     // [P][H] down-GEMM sums, by slot
     w.claim = take(2 * 1024 * 4);               // [GEMM][SM] first-CTA claims of a launch over both banks
+    // prefill tiles, MXFP8 format: a bank's tiles are at most one per active
+    // row (<= min(P, E) rows) plus P / 192
+    const size_t wide = split_k_steps(T) ? 0 : 1;
+    w.max_tiles = (int)(wide * (std::min<size_t>(P, (size_t)g.E) + P / kPrefillTile + 1));
+    w.tile_off = take(wide * 2 * (P + 1) * 4);  // [2][P+1] int32
+    w.sfx = take((size_t)2 * w.max_tiles * (g.H / kKG) * kSfbGroupBytes);
+    w.sfh = take((size_t)2 * w.max_tiles * ((g.I + kKG - 1) / kKG) * kSfbGroupBytes);
     w.total = off;
     return w;
 }
@@ -195,6 +216,7 @@ struct moe_ctx {
     int device = 0;
     int sms = 0;
     int ffn_impl = MOE_FFN_TCGEN05;
+    int act_format = MOE_ACT_E4M3X2;          // token rows of prefill-sized steps
     uint64_t wait_ns = moe::kDefaultWaitNs;   // bound of every FFN pipeline wait
     bool inject_withhold = false;             // test hook: the next FFN call withholds one copy
     int32_t *counts_dev = nullptr;   // [L][E]

@@ -12,12 +12,14 @@
 // is a pure function of (ids, row map), so the FFN that consumes it sees the
 // same token order for an expert whichever bank holds it.
 //
-// Steps of at most 256 tokens (decode) run in one CTA of 512 threads, whose
-// work after routing is sized by the step's picks, not by the experts: one
+// Decode steps (at most 256 tokens) build the lists in one CTA of 512 threads
+// whose work is sized by the step's picks, not by the experts: one
 // block-wide scan over the per-row pick counts gives every active row its
 // list position and offset, and each pick finds its place by counting the
-// earlier picks of its expert.  Larger steps (prefill) route with one warp per
-// token and build the lists in two more kernels.
+// earlier picks of its expert.  Steps of at most 32 tokens route in the same
+// CTA; larger decode steps route with one warp per token across CTAs first.
+// Larger steps (prefill) route the same way and build the lists from
+// per-expert counts in two more kernels.
 #include "moe_internal.cuh"
 
 #include <climits>
@@ -27,7 +29,8 @@ namespace moe {
 namespace {
 
 constexpr int kSmallThreads = 512;
-constexpr int kSmallMaxT = 256;
+constexpr int kFusedMaxT = 32;      // one CTA routes and splits
+constexpr int kSmallMaxT = 256;     // routing over many CTAs, then one CTA splits
 constexpr int kSmallMaxP = 4096;
 
 struct WsPtrs {
@@ -180,10 +183,9 @@ __device__ __forceinline__ int block_scan(int v, int *warp_tot) {
     return v + (warp ? warp_tot[warp - 1] : 0);
 }
 
-// Decode steps (T <= 256, T*k <= 4096): route, count and build both banks'
-// lists in one CTA of 512 threads.
-//  - every thread: row map -> shared memory; per-row pick counts cleared
-//  - warp w routes tokens w, w+16, ...
+// Both banks' pick lists from the step's picks, in one CTA of 512 threads.
+// On entry: s_ids [P] holds each pick's expert, s_rm [E] the row map, s_cnt
+// [E] zeros, base1 zero (all visible after a barrier).
 //  - each pick adds 1 to its row's count (rows of both banks in one array:
 //    hot row r at r, cold row r at n_hot + r)
 //  - one scan over that array (two rows per thread), the count in the low 16
@@ -191,38 +193,9 @@ __device__ __forceinline__ int block_scan(int v, int *warp_tot) {
 //    offset in its bank's pick list and its index among its bank's active rows
 //  - each pick's place: its row's offset + the number of earlier picks (lower
 //    slots) of the same expert.
-template <int KM, int NV>
-__global__ void __launch_bounds__(kSmallThreads) route_split_small(
-    const float *__restrict__ logits, int T, int E, int k, const int32_t *__restrict__ rowmap,
-    int n_hot, int32_t *counts, int32_t *__restrict__ ids, float *__restrict__ w, WsPtrs ws) {
-    extern __shared__ int32_t sm[];
-    __shared__ int warp_tot[32];
-    __shared__ int base1;           // bank 0's totals: the prefix bank 1's rows start from
-    const int P = ws.P;
-    int32_t *s_ids = sm;            // [P] expert of each pick
-    int32_t *s_rm = s_ids + P;      // [E] row map
-    int32_t *s_cnt = s_rm + E;      // [E] picks per row (both banks), then row offsets
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    for (int e = tid; e < E; e += kSmallThreads) {
-        s_rm[e] = rowmap[e];
-        s_cnt[e] = 0;
-    }
-    if (tid == 0) base1 = 0;
-    {
-        // each warp routes tokens warp, warp+16, ...; the next token's logits
-        // are loaded while this one is routed
-        constexpr int kWarps = kSmallThreads / 32;
-        float cur[NV], nxt[NV];
-        if (warp < T) load_logits<NV>(logits + (size_t)warp * E, E, lane, cur);
-        for (int t = warp; t < T; t += kWarps) {
-            if (t + kWarps < T) load_logits<NV>(logits + (size_t)(t + kWarps) * E, E, lane, nxt);
-            route_one<KM, NV>(cur, t, E, k, lane, counts, ids, w, s_ids);
-#pragma unroll
-            for (int i = 0; i < NV; ++i) cur[i] = nxt[i];
-        }
-    }
-    __syncthreads();
+__device__ __forceinline__ void build_lists(const int32_t *s_ids, const int32_t *s_rm, int32_t *s_cnt, int *warp_tot,
+                                            int &base1, int P, int E, int n_hot, WsPtrs ws) {
+    const int tid = threadIdx.x;
     for (int s = tid; s < P; s += kSmallThreads) {
         const int m = s_rm[s_ids[s]];
         atomicAdd(&s_cnt[m >= 0 ? m : n_hot + (-1 - m)], 1);
@@ -270,6 +243,64 @@ __global__ void __launch_bounds__(kSmallThreads) route_split_small(
         for (int q = 0; q < s; ++q) pos += s_ids[q] == e;
         ws.picks[b * P + s_cnt[b ? n_hot + (-1 - m) : m] + pos] = s;
     }
+}
+
+// One-user steps (T <= 32): route, count and build both banks' lists in one
+// CTA of 512 threads; warp w routes tokens w and w+16, loading the second
+// token's logits while it routes the first.
+template <int KM, int NV>
+__global__ void __launch_bounds__(kSmallThreads) route_split_small(
+    const float *__restrict__ logits, int T, int E, int k, const int32_t *__restrict__ rowmap,
+    int n_hot, int32_t *counts, int32_t *__restrict__ ids, float *__restrict__ w, WsPtrs ws) {
+    extern __shared__ int32_t sm[];
+    __shared__ int warp_tot[32];
+    __shared__ int base1;           // bank 0's totals: the prefix bank 1's rows start from
+    const int P = ws.P;
+    int32_t *s_ids = sm;            // [P] expert of each pick
+    int32_t *s_rm = s_ids + P;      // [E] row map
+    int32_t *s_cnt = s_rm + E;      // [E] picks per row (both banks), then row offsets
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int e = tid; e < E; e += kSmallThreads) {
+        s_rm[e] = rowmap[e];
+        s_cnt[e] = 0;
+    }
+    if (tid == 0) base1 = 0;
+    {
+        constexpr int kWarps = kSmallThreads / 32;
+        float cur[NV], nxt[NV];
+        if (warp < T) load_logits<NV>(logits + (size_t)warp * E, E, lane, cur);
+        for (int t = warp; t < T; t += kWarps) {
+            if (t + kWarps < T) load_logits<NV>(logits + (size_t)(t + kWarps) * E, E, lane, nxt);
+            route_one<KM, NV>(cur, t, E, k, lane, counts, ids, w, s_ids);
+#pragma unroll
+            for (int i = 0; i < NV; ++i) cur[i] = nxt[i];
+        }
+    }
+    __syncthreads();
+    build_lists(s_ids, s_rm, s_cnt, warp_tot, base1, P, E, n_hot, ws);
+}
+
+// Decode steps of 33..256 tokens, after route_tokens: both banks' lists in
+// one CTA from the routed ids.
+__global__ void __launch_bounds__(kSmallThreads) split_picks(const int32_t *__restrict__ ids, int E,
+                                                            const int32_t *__restrict__ rowmap, int n_hot, WsPtrs ws) {
+    extern __shared__ int32_t sm[];
+    __shared__ int warp_tot[32];
+    __shared__ int base1;
+    const int P = ws.P;
+    int32_t *s_ids = sm;
+    int32_t *s_rm = s_ids + P;
+    int32_t *s_cnt = s_rm + E;
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += kSmallThreads) {
+        s_rm[e] = rowmap[e];
+        s_cnt[e] = 0;
+    }
+    for (int q = tid; q < P; q += kSmallThreads) s_ids[q] = ids[q];
+    if (tid == 0) base1 = 0;
+    __syncthreads();
+    build_lists(s_ids, s_rm, s_cnt, warp_tot, base1, P, E, n_hot, ws);
 }
 
 // Build the active-row lists of bank b from per-expert pick counts.
@@ -329,7 +360,7 @@ __global__ void __launch_bounds__(256) route_tokens(const float *__restrict__ lo
     float v[NV];
     load_logits<NV>(logits + (size_t)t * E, E, lane, v);
     route_one<KM, NV>(v, t, E, k, lane, counts, ids, w, nullptr);
-    if (lane < k) red_relaxed_add(ecnt + ids[t * k + lane], 1);   // picks per expert for the split (order-free)
+    if (ecnt && lane < k) red_relaxed_add(ecnt + ids[t * k + lane], 1);   // picks per expert for the split (order-free)
 }
 
 // Large steps, stage 2: the active-row scan over the per-expert counts (one CTA).
@@ -367,10 +398,17 @@ int launch_route_km(const moe_ctx *ctx, const Layer &L, const float *logits, int
                     float *w, WsPtrs ws, int32_t *ecnt, cudaStream_t s) {
     const Geom &g = ctx->g;
     const int P = ws.P;
-    if (T <= kSmallMaxT && P <= kSmallMaxP) {
-        const size_t smem = sizeof(int32_t) * ((size_t)P + 2 * (size_t)g.E);
+    const size_t smem = sizeof(int32_t) * ((size_t)P + 2 * (size_t)g.E);
+    if (T <= kFusedMaxT) {
         route_split_small<KM, NV><<<1, kSmallThreads, smem, s>>>(logits, T, g.E, g.k, L.rowmap_dev, L.n_hot, counts, ids,
-                                                             w, ws);
+                                                                 w, ws);
+        MOE_LAUNCH_CHECK();
+        return MOE_OK;
+    }
+    if (T <= kSmallMaxT && P <= kSmallMaxP) {
+        route_tokens<KM, NV><<<(T + 7) / 8, 256, 0, s>>>(logits, T, g.E, g.k, counts, ids, w, nullptr);
+        MOE_LAUNCH_CHECK();
+        split_picks<<<1, kSmallThreads, smem, s>>>(ids, g.E, L.rowmap_dev, L.n_hot, ws);
         MOE_LAUNCH_CHECK();
         return MOE_OK;
     }

@@ -106,6 +106,21 @@ int moe_destroy(moe_ctx *ctx);
 /* Select the FFN kernel implementation (MOE_FFN_*) for later calls. */
 int moe_set_ffn_impl(moe_ctx *ctx, int impl);
 
+/* Activation format of the tensor-core FFN on prefill-sized steps (more
+ * than 256 tokens; decode-sized steps always use MOE_ACT_E4M3X2), for later
+ * calls.  The pages leave the activation format of the routed MXFP4 kernel
+ * unstated ("vLLM: Pin Hot Experts", Where the experts live today).
+ *  MOE_ACT_E4M3X2 (default): each token row and h row is scaled by a power
+ *    of two and carried as two e4m3 pieces (bf16-class precision, about 2^-8
+ *    of each value); two MMAs per product.
+ *  MOE_ACT_MXFP8: OCP MXFP8 -- each 32-element block of a row shares an e8m0
+ *    scale (the smallest 2^e with max|v| 2^-e <= 448) and its elements are
+ *    e4m3, rounded to nearest even; one MMA per product, at e4m3 precision
+ *    (rows within about 8e-2 relative L2 of the exact FFN).
+ * MOE_EINVAL for another value. */
+enum { MOE_ACT_E4M3X2 = 0, MOE_ACT_MXFP8 = 1 };
+int moe_set_act_format(moe_ctx *ctx, int format);
+
 /* Place one layer's experts ("vLLM: Pin Hot Experts", The one open door):
  * experts with is_hot[e] != 0 go to an HBM bank, the rest to a pinned host
  * bank mapped into the device address space; hot rows are assigned in

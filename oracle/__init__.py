@@ -61,6 +61,11 @@ def _load():
             "orc_finalize": (None, [P, P, i32, i32, i32, P]),
             "orc_layer_step": (None, [P, P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P, P, P, i32, i32]),
             "orc_rows_for_slots": (None, [P, P, P, P, i32, i32, i32, P, P, P, i32, P]),
+            "orc_rows_for_slots_fmt": (None, [P, P, P, P, i32, i32, i32, P, P, P, i32, P, i32]),
+            "orc_e4m3_rne": (f64, [f64]),
+            "orc_mx8_block_exponent": (i32, [f64]),
+            "orc_mx8_quantize": (None, [P, i64, P]),
+            "orc_expert_ffn_mx8": (None, [P, P, P, P, i32, i32, P, i32, P, i32, i32]),
             "orc_swap": (i32, [P, i32, i32, P, P, P]),
             "orc_plan_restore": (i32, [P, P, i32, i32, P, P]),
             "orc_policy_init": (None, [P, i32, P, P, P]),
@@ -228,8 +233,9 @@ def layer_step(weights, logits: np.ndarray, x: np.ndarray, k: int, counts=None,
     return ids, w, Y, out
 
 
-def rows_for_slots(weights, ids: np.ndarray, x: np.ndarray, slots) -> np.ndarray:
-    """Expert rows Y[s] for the given slot indices s = t*k + j only."""
+def rows_for_slots(weights, ids: np.ndarray, x: np.ndarray, slots, mx8: bool = False) -> np.ndarray:
+    """Expert rows Y[s] for the given slot indices s = t*k + j only; with
+    mx8, the token rows and h read as MXFP8 (expert_ffn_mx8)."""
     w13_q, w13_s, w2_q, w2_s = (_c(a, np.uint8) for a in weights)
     ids = _c(ids, np.int32)
     x = _c(x, np.uint16)
@@ -238,9 +244,37 @@ def rows_for_slots(weights, ids: np.ndarray, x: np.ndarray, slots) -> np.ndarray
     H = x.shape[1]
     I = w2_q.shape[2] * 2
     Y = np.empty((slots.size, H), np.uint16)
-    _load().orc_rows_for_slots(_p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s), H, I, k, _p(ids), _p(x),
-                               _p(slots), slots.size, _p(Y))
+    _load().orc_rows_for_slots_fmt(_p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s), H, I, k, _p(ids), _p(x),
+                                   _p(slots), slots.size, _p(Y), 1 if mx8 else 0)
     return Y
+
+
+def e4m3(v: float) -> float:
+    """FP8 E4M3 value nearest v (ties to even), saturated at +-448."""
+    return float(_load().orc_e4m3_rne(float(v)))
+
+
+def mx8_block_exponent(amax: float) -> int:
+    return int(_load().orc_mx8_block_exponent(float(amax)))
+
+
+def mx8_quantize(v: np.ndarray) -> np.ndarray:
+    """MXFP8 reading of a vector (length a multiple of 32), float64."""
+    v = _c(v, np.float64)
+    out = np.empty_like(v)
+    _load().orc_mx8_quantize(_p(v), v.size, _p(out))
+    return out
+
+
+def expert_ffn_mx8(w13_q, w13_s, w2_q, w2_s, x: np.ndarray, qx: bool = True, qh: bool = True) -> np.ndarray:
+    """expert_ffn with the token rows (qx) and h (qh) read as MXFP8."""
+    w13_q, w13_s, w2_q, w2_s = (_c(a, np.uint8) for a in (w13_q, w13_s, w2_q, w2_s))
+    x = _c(x, np.uint16)
+    n, H = x.shape
+    I = w2_q.shape[1] * 2
+    y = np.empty((n, H), np.uint16)
+    _load().orc_expert_ffn_mx8(_p(w13_q), _p(w13_s), _p(w2_q), _p(w2_s), H, I, _p(x), n, _p(y), int(qx), int(qh))
+    return y
 
 
 # ------------------------------------------------------------ swaps/policy

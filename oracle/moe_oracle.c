@@ -203,11 +203,76 @@ static void dequant_row(const uint8_t *q, const uint8_t *s, int64_t row, int K, 
 
 static float silu_f32(float z) { return z / (1.0f + expf(-z)); }
 
+/* ------------------------------------------------------ MXFP8 activations */
+
+/* FP8 E4M3 (the OCP "E4M3" element type: exponent bias 7, 3 mantissa bits,
+ * largest finite 448, no infinities): round to nearest, ties to even, and
+ * saturate to +-448.  Normal binades [2^m, 2^(m+1)) for m >= -6 have spacing
+ * 2^(m-3); below 2^-6 the subnormal spacing is 2^-9. */
+double orc_e4m3_rne(double v) {
+    if (isnan(v)) return v;
+    double a = fabs(v);
+    if (a == 0.0) return v;
+    int ex;
+    frexp(a, &ex);             /* a in [2^(ex-1), 2^ex) */
+    int m = ex - 1;
+    if (m < -6) m = -6;
+    double step = ldexp(1.0, m - 3);
+    double q = nearbyint(a / step) * step;   /* default rounding mode: ties to even */
+    if (q > 448.0) q = 448.0;
+    return copysign(q, v);
+}
+
+/* Shared exponent of one block: the smallest e with amax * 2^-e <= 448 (so no
+ * element saturates), held to the e8m0 scale's range [-127, 127]; 0 for an
+ * all-zero block. */
+int orc_mx8_block_exponent(double amax) {
+    if (!(amax > 0.0)) return 0;
+    int e = (int)ceil(log2(amax / 448.0));
+    while (ldexp(amax, -e) > 448.0) ++e;
+    while (ldexp(amax, -(e - 1)) <= 448.0) --e;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* MXFP8 reading of a vector (n % 32 == 0): each block of 32 consecutive
+ * elements shares 2^e (e from its largest |value|); out = e4m3(v 2^-e) 2^e. */
+void orc_mx8_quantize(const double *v, int64_t n, double *out) {
+    for (int64_t b = 0; b < n; b += 32) {
+        double amax = 0.0;
+        for (int i = 0; i < 32; ++i) amax = fmax(amax, fabs(v[b + i]));
+        int e = orc_mx8_block_exponent(amax);
+        for (int i = 0; i < 32; ++i) out[b + i] = ldexp(orc_e4m3_rne(ldexp(v[b + i], -e)), e);
+    }
+}
+
+/* The expert FFN below, with the token rows (qx) and/or the gate/up output h
+ * (qh) read as MXFP8 before the GEMM that consumes them. */
+static void expert_ffn_impl(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w2_q,
+                            const uint8_t *w2_s, int H, int I, const uint16_t *x, int n, uint16_t *y,
+                            int qx, int qh);
+
 void orc_expert_ffn(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w2_q,
                     const uint8_t *w2_s, int H, int I, const uint16_t *x, int n, uint16_t *y) {
+    expert_ffn_impl(w13_q, w13_s, w2_q, w2_s, H, I, x, n, y, 0, 0);
+}
+
+void orc_expert_ffn_mx8(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w2_q,
+                        const uint8_t *w2_s, int H, int I, const uint16_t *x, int n, uint16_t *y,
+                        int qx, int qh) {
+    expert_ffn_impl(w13_q, w13_s, w2_q, w2_s, H, I, x, n, y, qx, qh);
+}
+
+static void expert_ffn_impl(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w2_q,
+                            const uint8_t *w2_s, int H, int I, const uint16_t *x, int n, uint16_t *y,
+                            int qx, int qh) {
     double *xd = (double *)malloc(sizeof(double) * (size_t)n * H);
     float *h = (float *)malloc(sizeof(float) * (size_t)n * I);
+    double *hd = (double *)malloc(sizeof(double) * (size_t)n * I);
     for (int64_t i = 0; i < (int64_t)n * H; ++i) xd[i] = (double)orc_bf16_to_f32(x[i]);
+    if (qx)
+        for (int t = 0; t < n; ++t) orc_mx8_quantize(xd + (int64_t)t * H, H, xd + (int64_t)t * H);
 
     /* gate/up: row i of W13 is the gate of unit i, row I+i its up projection */
 #pragma omp parallel
@@ -232,6 +297,10 @@ void orc_expert_ffn(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w
         free(wu);
     }
 
+    for (int64_t i = 0; i < (int64_t)n * I; ++i) hd[i] = (double)h[i];
+    if (qh)
+        for (int t = 0; t < n; ++t) orc_mx8_quantize(hd + (int64_t)t * I, I, hd + (int64_t)t * I);
+
     /* down: y_o = sum_i W2[o][i] h_i */
 #pragma omp parallel
     {
@@ -241,7 +310,7 @@ void orc_expert_ffn(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w
             dequant_row(w2_q, w2_s, o, I, w2);
             for (int t = 0; t < n; ++t) {
                 double acc = 0.0;
-                for (int i = 0; i < I; ++i) acc += w2[i] * (double)h[(int64_t)t * I + i];
+                for (int i = 0; i < I; ++i) acc += w2[i] * hd[(int64_t)t * I + i];
                 y[(int64_t)t * H + o] = orc_f32_to_bf16((float)acc);
             }
         }
@@ -249,6 +318,7 @@ void orc_expert_ffn(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w
     }
     free(xd);
     free(h);
+    free(hd);
 }
 
 /* ---------------------------------------------------------------- finalize */
@@ -286,6 +356,13 @@ void orc_rows_for_slots(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_
                         const uint8_t *w2_s, int H, int I, int k, const int32_t *ids,
                         const uint16_t *x, const int32_t *slots, int n_slots,
                         uint16_t *Y_out) {
+    orc_rows_for_slots_fmt(w13_q, w13_s, w2_q, w2_s, H, I, k, ids, x, slots, n_slots, Y_out, 0);
+}
+
+void orc_rows_for_slots_fmt(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w2_q,
+                            const uint8_t *w2_s, int H, int I, int k, const int32_t *ids,
+                            const uint16_t *x, const int32_t *slots, int n_slots,
+                            uint16_t *Y_out, int mx8) {
     int *done = (int *)calloc((size_t)n_slots, sizeof(int));
     int *sel = (int *)malloc(sizeof(int) * (size_t)n_slots);
     uint16_t *xs = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n_slots * H);
@@ -304,7 +381,7 @@ void orc_rows_for_slots(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_
         }
         const uint8_t *p13q, *p13s, *p2q, *p2s;
         expert_ptrs(w13_q, w13_s, w2_q, w2_s, H, I, e, &p13q, &p13s, &p2q, &p2s);
-        orc_expert_ffn(p13q, p13s, p2q, p2s, H, I, xs, n, ys);
+        expert_ffn_impl(p13q, p13s, p2q, p2s, H, I, xs, n, ys, mx8, mx8);
         for (int i = 0; i < n; ++i)
             memcpy(Y_out + (int64_t)sel[i] * H, ys + (int64_t)i * H, sizeof(uint16_t) * H);
     }

@@ -99,6 +99,26 @@ void orc_count(int32_t *counts, int E, const int32_t *ids, int T, int k, int cou
 void orc_expert_ffn(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w2_q,
                     const uint8_t *w2_s, int H, int I, const uint16_t *x, int n, uint16_t *y);
 
+/* ---- MXFP8 activations (the opt-in one-piece prefill format) ----
+ * The pages do not state the activation format of the routed MXFP4 kernel
+ * ("vLLM: Pin Hot Experts", Where the experts live today).  This reading is
+ * the OCP MX v1.0 MXFP8 format: blocks of 32 consecutive elements share a
+ * power of two 2^e, elements are FP8 E4M3 (round to nearest even, saturating
+ * at +-448).  e is the smallest integer with amax * 2^-e <= 448, so no element
+ * saturates, held to the e8m0 range [-127, 127].
+ * orc_e4m3_rne: the E4M3 value nearest v (ties to even), saturated.
+ * orc_mx8_block_exponent: e for a block whose largest |value| is amax.
+ * orc_mx8_quantize: the MXFP8 reading of v (n % 32 == 0), as doubles.
+ * orc_expert_ffn_mx8: orc_expert_ffn with the token rows (qx != 0) and the
+ * gate/up output h (qh != 0) read as MXFP8 before the GEMM that consumes
+ * them; qx = qh = 0 is orc_expert_ffn exactly. */
+double orc_e4m3_rne(double v);
+int orc_mx8_block_exponent(double amax);
+void orc_mx8_quantize(const double *v, int64_t n, double *out);
+void orc_expert_ffn_mx8(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w2_q,
+                        const uint8_t *w2_s, int H, int I, const uint16_t *x, int n, uint16_t *y,
+                        int qx, int qh);
+
 /* ---- finalize ----
  * out[t][c] = bf16( fma-chain over j = 0..k-1 of w[t][j] * Y[t][j][c] ),
  * accumulator fp32 starting at +0, one cast at the end. */
@@ -121,6 +141,11 @@ void orc_rows_for_slots(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_
                         const uint8_t *w2_s, int H, int I, int k, const int32_t *ids,
                         const uint16_t *x, const int32_t *slots, int n_slots,
                         uint16_t *Y_out);
+/* The same with mx8 != 0: x and h read as MXFP8 (orc_expert_ffn_mx8). */
+void orc_rows_for_slots_fmt(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w2_q,
+                            const uint8_t *w2_s, int H, int I, int k, const int32_t *ids,
+                            const uint16_t *x, const int32_t *slots, int n_slots,
+                            uint16_t *Y_out, int mx8);
 
 /* ---- swaps (true swaps with stale check) ----
  * For each pair i in order: promote[i] must currently be cold and demote[i]

@@ -536,3 +536,85 @@ def test_restore_reaches_the_saved_hot_set_in_the_fewest_swaps(seed):
     assert np.array_equal(rm >= 0, saved >= 0)
     hot_rows = sorted(rm[rm >= 0].tolist())
     assert hot_rows == list(range(n_hot))                   # still a bijection onto the bank rows
+
+
+# ------------------------------------------------------- MXFP8 activations
+
+def test_e4m3_rounding_matches_torch_float8():
+    """The oracle's E4M3 rounding, written from the format's definition,
+    against torch's float32 -> float8_e4m3fn cast on values inside +-448:
+    random magnitudes across the normal and subnormal binades, and every
+    midpoint between neighbouring E4M3 values (the ties)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    v = (rng.standard_normal(20000) * np.exp2(rng.integers(-14, 9, 20000))).astype(np.float32)
+    v = v[np.abs(v) <= 448]
+    grid = torch.arange(0, 256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    grid = np.unique(np.abs(grid[np.isfinite(grid)]))
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    vals = np.concatenate([v, mids, -mids, grid.astype(np.float32)])
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).float().numpy()
+    got = np.array([oracle.e4m3(float(a)) for a in vals])
+    assert np.array_equal(got, ref.astype(np.float64))
+
+
+def test_e4m3_hand_values():
+    # 1.0625 lies halfway between 1.0 and 1.125: ties to the even mantissa 1.0
+    assert oracle.e4m3(1.0625) == 1.0
+    # 1.1875 lies halfway between 1.125 (odd) and 1.25 (even)
+    assert oracle.e4m3(1.1875) == 1.25
+    # subnormal spacing 2^-9: 2^-10 ties to 0, 3 * 2^-10 ties to 2^-8
+    assert oracle.e4m3(2.0 ** -10) == 0.0 and oracle.e4m3(3 * 2.0 ** -10) == 2.0 ** -8
+    assert oracle.e4m3(448.0) == 448.0 and oracle.e4m3(464.0) == 448.0 and oracle.e4m3(-1e6) == -448.0
+    assert oracle.e4m3(-0.3) == -0.3125          # 0.3 / 2^-5 = 9.6 -> 10 steps
+
+
+def test_mx8_block_exponent_boundaries():
+    # the smallest e with amax * 2^-e <= 448
+    assert oracle.mx8_block_exponent(0.0) == 0
+    assert oracle.mx8_block_exponent(448.0) == 0
+    assert oracle.mx8_block_exponent(448.0001) == 1
+    assert oracle.mx8_block_exponent(224.0) == -1        # 224 * 2 = 448 still fits
+    assert oracle.mx8_block_exponent(224.0001) == 0
+    assert oracle.mx8_block_exponent(1.0) == -8          # 256 <= 448 < 512
+    assert oracle.mx8_block_exponent(2.0 ** -20) == -28
+    # held to the e8m0 scale's range
+    assert oracle.mx8_block_exponent(2.0 ** -200) == -127 and oracle.mx8_block_exponent(2.0 ** 200) == 127
+
+
+def test_mx8_quantize_blocks_are_independent_and_exact_values_stay():
+    rng = np.random.default_rng(3)
+    # values with 4 significant bits, within one binade of the block max:
+    # exactly representable after the shared scaling
+    v = (rng.integers(8, 16, 64) * np.exp2(rng.integers(-3, 0, 64)) * rng.choice([-1, 1], 64)).astype(np.float64)
+    assert np.array_equal(oracle.mx8_quantize(v), v)
+    # a large value in block 0 coarsens block 0 only
+    w = v.copy()
+    w[0] = 2.0 ** 20
+    q = oracle.mx8_quantize(w)
+    assert np.array_equal(q[32:], v[32:])
+    assert not np.array_equal(q[1:32], v[1:32])
+    e = oracle.mx8_block_exponent(2.0 ** 20)
+    for a, b in zip(q[:32], w[:32]):      # each element is its own e4m3 rounding at the block's scale
+        assert a == np.ldexp(oracle.e4m3(np.ldexp(b, -e)), e)
+
+
+def test_expert_ffn_mx8_composition():
+    """qx = qh = 0 is the pinned FFN bit for bit; qx alone is the pinned FFN
+    applied to the MXFP8 reading of x (exact in bf16: 4 significant bits);
+    adding qh changes the rows by e4m3-level relative error."""
+    cfg = synth.get_config("tiny")
+    w = synth.expert_weights(cfg, 0, 3)
+    x = synth.activations(cfg, 0, 0)[:4]
+    base = oracle.expert_ffn(*w, x)
+    assert np.array_equal(oracle.expert_ffn_mx8(*w, x, qx=False, qh=False), base)
+    xq = np.stack([oracle.mx8_quantize(synth.bf16_bits_to_f32(r).astype(np.float64)) for r in x])
+    xq_bits = synth._f32_to_bf16_bits(xq.astype(np.float32))
+    assert np.array_equal(synth.bf16_bits_to_f32(xq_bits).astype(np.float64), xq)
+    only_x = oracle.expert_ffn_mx8(*w, x, qx=True, qh=False)
+    assert np.array_equal(only_x, oracle.expert_ffn(*w, xq_bits))
+    both = oracle.expert_ffn_mx8(*w, x, qx=True, qh=True)
+    a = synth.bf16_bits_to_f32(both).astype(np.float64)
+    b = synth.bf16_bits_to_f32(only_x).astype(np.float64)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert 1e-3 < rel < 0.08
