@@ -408,7 +408,9 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
 int moe_workspace_bytes(const moe_ctx *ctx, int T, size_t *bytes) {
     if (int r = check_ctx(ctx)) return r;
     if (!bytes || T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "T out of range");
-    *bytes = ws_layout(ctx->g, T).total;
+    // The layout is not monotonic in T: steps of at most kNarrowMaxT tokens
+    // also hold fp32 partial-sum rows.  Size for the largest step of each kind.
+    *bytes = std::max(ws_layout(ctx->g, T).total, ws_layout(ctx->g, std::min(T, kNarrowMaxT)).total);
     return MOE_OK;
 }
 

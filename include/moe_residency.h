@@ -134,8 +134,9 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
                    const uint8_t *w2_q, const uint8_t *w2_s, const uint8_t *is_hot,
                    void *stream);
 
-/* Bytes of the caller-owned device workspace for steps of up to T tokens
- * (split lists, per-bank scratch for the FFN's intermediate rows). */
+/* Bytes of the caller-owned device workspace that serves every step of at
+ * most T tokens (split lists, per-bank scratch for the FFN's intermediate
+ * rows); non-decreasing in T. */
 int moe_workspace_bytes(const moe_ctx *ctx, int T, size_t *bytes);
 
 /* Route, split and count (async).  "vLLM: Pin Hot Experts", Results (split
