@@ -11,6 +11,8 @@ context holding the 16-stream decode's four layers (layers 0 and 2 split
 295 hot / 89 cold, layers 1 and 3 all in HBM):
   - headline: the 16-stream decode step (4 layers, 112 tokens);
   - ``configs.decode1``: the one-user decode step on layer 0 (7 tokens);
+  - ``configs.prefill_shift``: an 8192-token chunk on split layer 0 right
+    after a domain shift, with the cold staging pool off and on;
   - ``configs.adaptive``: 128 one-user steps on layer 0 with a domain shift
     at step 64, counts read every 16 steps and the policy's swaps applied
     between steps (up to 8 per step), timing steps and swaps;
@@ -827,6 +829,55 @@ def measure_prefill(S, ctx, pcfg, args, layer, fmt=0):
     }
 
 
+def measure_prefill_shift(S, ctx, args, layer=0, slots=16):
+    """An 8192-token prefill chunk on split context layer `layer` (295 hot /
+    89 cold by the first ranking) right after the domain shift: the logits
+    follow the redrawn ranking, so the new domain's popular experts are
+    still cold and draw several 192-token tiles each.  Timed with the cold
+    staging pool off and on (`slots` rows)."""
+    acfg = synth.get_config("adaptive")
+    scfg = dataclasses.replace(acfg, name="prefill_shift", T=8192, shift_at=0, steps=1)
+    T, eb = scfg.T, S.moe.moe_expert_bytes(scfg.H, scfg.I)
+    mask = synth.hot_mask(acfg, 0)
+    out = {"workload": "prefill chunk right after a domain shift: 8192 tokens on a split layer (295 hot / 89 cold by "
+                       "the first ranking), logits from the redrawn ranking (Spearman 0.15), top-6, Zipf(1.1) skew",
+           "tokens_per_step": T}
+    for mode, n_slots in (("unstaged", 0), ("staged", slots)):
+        S.moe.moe_set_cold_staging(ctx, n_slots)
+        try:
+            steps = max(3, min(args.steps, 8))
+            run = StepRunner(S, ctx, scfg, [layer], T, 2, False, input_layers=[0])
+            run.capture()
+            run.settle(3)
+            step_ms, clocks = run.timed(steps, 0)
+            rows = S.moe.moe_read_stage(ctx, run.steps[0].buf.ws_ptr, T) if n_slots else None
+        finally:
+            S.moe.moe_set_cold_staging(ctx, 0)
+        out[mode] = {"us_per_layer_step": float(np.mean(step_ms)) * 1e3, "step_us_pct": pct(step_ms),
+                     "tokens_per_s": T / (float(np.mean(step_ms)) * 1e-3), "clocks": clocks}
+        if rows is not None:
+            out[mode]["staged_experts"] = int((rows >= 0).sum())
+    # host-link reads per step: one per cold (expert, token tile) unstaged; one
+    # per distinct cold expert when every multi-tile expert is staged
+    ids = np.argsort(-run.pool_lg[0][0], axis=1, kind="stable")[:, :scfg.k]
+    u, n = np.unique(ids, return_counts=True)
+    cold = mask[u] == 0
+    tiles = np.ceil(n[cold] / kPrefillTile)
+    multi = np.sort(n[cold][tiles > 1])[::-1][:slots]
+    saved = float(np.sum(np.ceil(multi / kPrefillTile) - 1))
+    out["cold_tiles_unstaged"] = int(tiles.sum())
+    out["cold_link_bytes_unstaged"] = float(tiles.sum() * eb)
+    out["cold_link_bytes_staged"] = float((tiles.sum() - saved) * eb)
+    out["link_gbs"] = S.link_gbs
+    out["speedup"] = out["unstaged"]["us_per_layer_step"] / out["staged"]["us_per_layer_step"]
+    out["note"] = ("staged: the FFN call first copies each cold expert with more picks than one token tile into an "
+                   "HBM pool (once per step) and its units read it there; rows bit-identical to unstaged")
+    return out
+
+
+kPrefillTile = 192
+
+
 def line_for(S, name, cfg, m, args, cpu):
     """The JSON line of a decode workload measured by measure_decode16/1."""
     world = S.world
@@ -902,6 +953,8 @@ def run_all(S, args):
                                                   slowest_rank_ms(sum(m1["e2e_ms"]), S.dist, S.dev)),
                         "unit": "tokens/s", "h2d_bytes_per_step": m1["h2d"], "d2h_bytes_per_step": m1["d2h"]},
                 "clocks": m1["clocks"]}
+        if "prefill_shift" not in skip:   # before the adaptive run moves layer 0's rows
+            subs["prefill_shift"] = measure_prefill_shift(S, ctx, args, layer=0)
         if "adaptive" not in skip:
             acfg = synth.get_config("adaptive")
             subs["adaptive"] = measure_adaptive(S, ctx, cfg.L, acfg, args, layer=0)

@@ -61,6 +61,8 @@ def lib():
         "moe_destroy": (i32, [P]),
         "moe_set_ffn_impl": (i32, [P, i32]),
         "moe_set_act_format": (i32, [P, i32]),
+        "moe_set_cold_staging": (i32, [P, i32]),
+        "moe_read_stage": (i32, [P, P, i32, P, P]),
         "moe_init_banks": (i32, [P, i32, P, P, P, P, P, P]),
         "moe_workspace_bytes": (i32, [P, i32, C.POINTER(sz)]),
         "moe_route_split_count": (i32, [P, i32, P, i32, i32, P, P, P, P]),
@@ -175,6 +177,18 @@ def moe_destroy(ctx):
 
 def moe_set_ffn_impl(ctx, impl):
     return _err("moe_set_ffn_impl", lib().moe_set_ffn_impl(ctx, impl))
+
+
+def moe_set_cold_staging(ctx, slots):
+    return _err("moe_set_cold_staging", lib().moe_set_cold_staging(ctx, slots))
+
+
+def moe_read_stage(ctx, ws, T, stream=None):
+    """Cold-bank rows copied into the staging pool's slots by the last staged
+    FFN call on this workspace (-1: slot unused)."""
+    rows = np.zeros(64, np.int32)
+    _err("moe_read_stage", lib().moe_read_stage(ctx, _ptr(ws), T, _ptr(rows), _stream(stream)))
+    return rows
 
 
 def moe_set_act_format(ctx, fmt):

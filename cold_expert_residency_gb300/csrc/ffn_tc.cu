@@ -84,7 +84,16 @@ struct TcArgs {
     const int32_t *tile_off[2];
     const uint8_t *sfb[2];
     int sf_groups;          // K groups per tile in sfb
+    // cold staging: the pool slot of each cold active row (or -1; null: no
+    // staging in this call) and the pool's base
+    const int32_t *stage_slot;
+    const uint8_t *stage_pool;
 };
+
+// The pool slot that holds unit row a of bank bk this call, or -1.
+__device__ __forceinline__ int staged_slot(const TcArgs &args, int bk, int a) {
+    return (bk == 1 && args.stage_slot) ? args.stage_slot[a] : -1;
+}
 
 constexpr int kQ = 4;       // unit queue depth (producer -> the other roles)
 constexpr int kMaxStages = 8;
@@ -161,8 +170,10 @@ struct TcCfg {
     static constexpr int kDW = NMAX;                        // columns of one accumulator
     static constexpr int kNCol = (kDW + 31) / 32;           // B scale columns of one piece
     // A scale slots in TMEM, reused round-robin: the MMA thread refills slot
-    // it % kNsf after the MMAs of iteration it - kNsf have completed.
-    static constexpr int kNsf = 3;
+    // it % kNsf after the MMAs of iteration it - kNsf have completed (the
+    // ring holds at least kNsf stages, so that iteration's barrier phase is
+    // still the one waited for).  The MXFP8 ring is deeper and takes a fourth.
+    static constexpr int kNsf = MX ? 4 : 3;
     // Tensor memory columns: slot i's A scales at 32 i (four columns written
     // by tcgen05.cp); slot 0's block also holds the constant B scale columns
     // of piece 0 at +8 and of piece 1 at +16 -- in the MXFP8 format, slot i's
@@ -298,7 +309,7 @@ __device__ __forceinline__ void epilogue_cols(const TcArgs &args, uint32_t dt, i
 template <int NMAX, int PHASE, int BANKS, bool MX>
 __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0,
-                  const __grid_constant__ CUtensorMap tmA1, TcArgs args) {
+                  const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmA2, TcArgs args) {
     using C = TcCfg<NMAX, MX>;
     constexpr int DB = C::kDBufs, NSF = C::kNsf;
     const int S = args.S;
@@ -355,6 +366,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
         ptx::prefetch_tmap(&tmB);
         ptx::prefetch_tmap(&tmA0);
         ptx::prefetch_tmap(&tmA1);
+        if (args.stage_slot) ptx::prefetch_tmap(&tmA2);
     }
     if (warp == C::kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_addr(holder), C::kCols);
@@ -471,10 +483,12 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
             const int goff = bank_offset(L, bk, args.P);
             int a, mt, s0, s1;
             unit_pos(e >> 1, part.tiles, ns, args.ks, a, mt, s0, s1);
-            const int row = L.act_row[a];
+            // a staged cold row is read from its pool slot (tmA2), not the host bank
+            const int sslot = staged_slot(args, bk, a);
+            const int row = sslot >= 0 ? sslot : L.act_row[a];
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
-            const CUtensorMap *tmA = bk ? &tmA1 : &tmA0;
-            const uint8_t *expert = args.bank[bk] + (int64_t)row * args.eb;
+            const CUtensorMap *tmA = sslot >= 0 ? &tmA2 : (bk ? &tmA1 : &tmA0);
+            const uint8_t *expert = (sslot >= 0 ? args.stage_pool : args.bank[bk]) + (int64_t)row * args.eb;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX) {
                 const int brow = goff + p0 + n0;
                 for (int s = s0; s < s1; ++s, ++it) {
@@ -971,14 +985,14 @@ int make_piece_map(CUtensorMap *map, const void *base, int K, int rows, int box_
 }
 
 template <int NMAX, int PHASE, int BANKS, bool MX>
-int launch_one(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap &mA1, const TcArgs &args, int blocks,
-               cudaStream_t s) {
+int launch_one(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap &mA1, const CUtensorMap &mA2,
+               const TcArgs &args, int blocks, cudaStream_t s) {
     using C = TcCfg<NMAX, MX>;
     auto kern = ffn_tc_kernel<NMAX, PHASE, BANKS, MX>;
     const size_t smem = C::smem_bytes(args.S);
     MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     if (blocks < 1) return MOE_OK;
-    kern<<<blocks, C::kThreads, smem, s>>>(mB, mA0, mA1, args);
+    kern<<<blocks, C::kThreads, smem, s>>>(mB, mA0, mA1, mA2, args);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
@@ -1008,11 +1022,11 @@ LaunchPlan plan_for(const moe_ctx *ctx, int b, bool shared, int units_max) {
 }
 
 template <int NMAX, int PHASE, bool MX>
-int launch_gemm(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap &mA1, const TcArgs &a, int blocks,
-                cudaStream_t s) {
-    if (a.b < 0) return launch_one<NMAX, PHASE, 2, MX>(mB, mA0, mA1, a, blocks, s);
-    if (a.b == MOE_BANK_COLD) return launch_one<NMAX, PHASE, 1, MX>(mB, mA0, mA1, a, blocks, s);
-    return launch_one<NMAX, PHASE, 0, MX>(mB, mA0, mA1, a, blocks, s);
+int launch_gemm(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap &mA1, const CUtensorMap &mA2,
+                const TcArgs &a, int blocks, cudaStream_t s) {
+    if (a.b < 0) return launch_one<NMAX, PHASE, 2, MX>(mB, mA0, mA1, mA2, a, blocks, s);
+    if (a.b == MOE_BANK_COLD) return launch_one<NMAX, PHASE, 1, MX>(mB, mA0, mA1, mA2, a, blocks, s);
+    return launch_one<NMAX, PHASE, 0, MX>(mB, mA0, mA1, mA2, a, blocks, s);
 }
 
 template <int NMAX, bool MX>
@@ -1050,7 +1064,11 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
                                                     (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
     }
     MOE_LAUNCH_CHECK();
-    if (int r = launch_gemm<NMAX, 1, MX>(m1, layer.wmap[0][0], layer.wmap[1][0], a1, p1.blocks, s)) return r;
+    // the staging pool's maps stand in for units read from it (the cold maps
+    // where no pool exists: then no unit reads them)
+    const CUtensorMap &sm1 = ctx->stage_pool ? ctx->stage_map[0] : layer.wmap[1][0];
+    const CUtensorMap &sm2 = ctx->stage_pool ? ctx->stage_map[1] : layer.wmap[1][1];
+    if (int r = launch_gemm<NMAX, 1, MX>(m1, layer.wmap[0][0], layer.wmap[1][0], sm1, a1, p1.blocks, s)) return r;
     if (MX) {
         prep_h_mx8_kernel<<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
                                                  ws + lay.hq, (int32_t *)(ws + lay.hexp),
@@ -1061,7 +1079,7 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
                                                     (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
     }
     MOE_LAUNCH_CHECK();
-    if (int r = launch_gemm<NMAX, 2, MX>(m2, layer.wmap[0][1], layer.wmap[1][1], a2, p2.blocks, s)) return r;
+    if (int r = launch_gemm<NMAX, 2, MX>(m2, layer.wmap[0][1], layer.wmap[1][1], sm2, a2, p2.blocks, s)) return r;
     if (!a2.y_out) return MOE_OK;
     round_y_kernel<<<grid_p, 256, 0, s>>>(a2.lists[0], a2.lists[1], a2.b, g.H, a2.y_out, a2.Y);
     MOE_LAUNCH_CHECK();
@@ -1220,6 +1238,19 @@ int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int b, const uint16_t *x, in
     a1.wait_ns = ctx->wait_ns;
     a1.withhold = ctx->inject_withhold ? 1 : 0;   // test hook, consumed by this call's gate/up GEMM
     ctx->inject_withhold = false;
+    // Big-batch cold staging: a call that covers the cold bank copies the cold
+    // rows with more picks than one token tile into the pool first (steps of
+    // at most 16 tokens never route more picks to an expert than one tile).
+    a1.stage_slot = nullptr;
+    a1.stage_pool = nullptr;
+    if (ctx->stage_slots > 0 && layer.n_cold > 0 && a1.b != MOE_BANK_HOT && T > 16) {
+        int32_t *slot_of = (int32_t *)(ws + lay.stage_slot);
+        if (int r = launch_cold_staging(ctx, layer, tile_width(T), a1.lists[1], slot_of,
+                                        (int32_t *)(ws + lay.stage_src), s))
+            return r;
+        a1.stage_slot = slot_of;
+        a1.stage_pool = ctx->stage_pool;
+    }
     TcArgs a2 = a1;
     a2.withhold = 0;
     a2.claim = a1.claim ? a1.claim + 1024 : nullptr;   // the down GEMM's own claims

@@ -274,7 +274,10 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
             unit_pos(e >> 1, part.tiles, ns, args.ks, a, mt, s0, s1);
             const int row = L.act_row[a];
             const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
-            const uint8_t *expert = args.bank[bk] + (int64_t)row * args.eb;
+            // a staged cold row is read from its pool slot in HBM, not the host bank
+            const int sslot = staged_slot(args, bk, a);
+            const uint8_t *expert = sslot >= 0 ? args.stage_pool + (int64_t)sslot * args.eb
+                                               : args.bank[bk] + (int64_t)row * args.eb;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX) {
                 const int brow = goff + p0 + n0;
                 for (int s = s0; s < s1; ++s, ++it) {

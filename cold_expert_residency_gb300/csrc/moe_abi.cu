@@ -293,6 +293,7 @@ int moe_destroy(moe_ctx *ctx) {
     dev_free(ctx->status_dev);
     pinned_free(ctx->probe_host);
     dev_free(ctx->probe_dev);
+    dev_free(ctx->stage_pool);
     delete ctx;
     return MOE_OK;
 }
@@ -301,6 +302,41 @@ int moe_set_ffn_impl(moe_ctx *ctx, int impl) {
     if (int r = check_ctx(ctx)) return r;
     if (impl != MOE_FFN_TCGEN05 && impl != MOE_FFN_SIMT) return set_error(MOE_EINVAL, "unknown FFN impl");
     ctx->ffn_impl = impl;
+    return MOE_OK;
+}
+
+int moe_set_cold_staging(moe_ctx *ctx, int slots) {
+    if (int r = check_ctx(ctx)) return r;
+    if (slots < 0 || slots > kMaxStageSlots) return set_error(MOE_EINVAL, "staging slots out of range (0..64)");
+    DeviceGuard guard(ctx->device);
+    if (guard.status() != cudaSuccess) return cuda_error(guard.status(), "cudaSetDevice(context device)");
+    MOE_CUDA_TRY(cudaDeviceSynchronize());   // no call in flight may still read the old pool
+    dev_free(ctx->stage_pool);
+    ctx->stage_pool = nullptr;
+    ctx->stage_slots = 0;
+    if (slots == 0) return MOE_OK;
+    uint8_t *pool = nullptr;
+    MOE_CUDA_TRY(dev_alloc((void **)&pool, (size_t)slots * ctx->g.eb, "stage_pool"));
+    int r = make_weight_map(&ctx->stage_map[0], pool, ctx->g, ctx->g.w13, slots);
+    if (r == MOE_OK) r = make_weight_map(&ctx->stage_map[1], pool, ctx->g, ctx->g.w2, slots);
+    if (r != MOE_OK) {
+        dev_free(pool);
+        return r;
+    }
+    ctx->stage_pool = pool;
+    ctx->stage_slots = slots;
+    return MOE_OK;
+}
+
+int moe_read_stage(moe_ctx *ctx, const void *ws, int T, int32_t *rows, void *stream) {
+    if (int r = check_ctx(ctx)) return r;
+    if (!ws || !rows || T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "bad moe_read_stage arguments");
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    const WsLayout lay = ws_layout(ctx->g, T);
+    MOE_CUDA_TRY(cudaMemcpyAsync(rows, (const uint8_t *)ws + lay.stage_src, sizeof(int32_t) * kMaxStageSlots,
+                                 cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
     return MOE_OK;
 }
 

@@ -124,6 +124,9 @@ struct WsLayout {
     // tile of each active row, and the tiles' B-operand block scales
     size_t tile_off, sfx, sfh;
     int max_tiles;          // token tiles per bank, at most
+    // cold staging: the slot of each cold active row (or -1), the cold row of
+    // each slot (or -1)
+    size_t stage_slot, stage_src;
     size_t total;
 };
 // header words
@@ -145,6 +148,12 @@ inline bool split_k_steps(int T) { return T <= kNarrowMaxT; }
 // block-scaled MMA reads token n's scale (column n/32, lane n%32).
 constexpr int kPrefillTile = 192;
 constexpr int kSfbGroupBytes = 1024;
+
+// Slots of a context's cold-staging pool, at most.
+constexpr int kMaxStageSlots = 64;
+
+// Token rows per tile of the FFN kernels for a step of T tokens.
+inline int tile_width(int T) { return T <= 8 ? 8 : T <= 16 ? 16 : T <= kNarrowMaxT ? 32 : kPrefillTile; }
 
 inline WsLayout ws_layout(const Geom &g, int T) {
     WsLayout w;
@@ -175,6 +184,8 @@ inline WsLayout ws_layout(const Geom &g, int T) {
     w.tile_off = take(wide * 2 * (P + 1) * 4);  // [2][P+1] int32
     w.sfx = take((size_t)2 * w.max_tiles * (g.H / kKG) * kSfbGroupBytes);
     w.sfh = take((size_t)2 * w.max_tiles * ((g.I + kKG - 1) / kKG) * kSfbGroupBytes);
+    w.stage_slot = take(P * 4);
+    w.stage_src = take(kMaxStageSlots * 4);
     w.total = off;
     return w;
 }
@@ -217,6 +228,9 @@ struct moe_ctx {
     int sms = 0;
     int ffn_impl = MOE_FFN_TCGEN05;
     int act_format = MOE_ACT_E4M3X2;          // token rows of prefill-sized steps
+    int stage_slots = 0;                      // cold-staging pool: slots (0 = off)
+    uint8_t *stage_pool = nullptr;            // stage_slots expert rows in HBM
+    CUtensorMap stage_map[2];                 // code-block maps over the pool (W13, W2)
     uint64_t wait_ns = moe::kDefaultWaitNs;   // bound of every FFN pipeline wait
     bool inject_withhold = false;             // test hook: the next FFN call withholds one copy
     int32_t *counts_dev = nullptr;   // [L][E]
@@ -288,6 +302,10 @@ int launch_router(const uint16_t *x, const uint16_t *w_router, const float *bias
                   float *logits, int32_t *status, int sms, cudaStream_t s);
 int launch_rowmap_write(int32_t *rowmap_dev, int32_t e0, int32_t v0, int32_t e1, int32_t v1,
                         cudaStream_t s);
+// Select the step's cold rows to stage (tile width W) and copy them into the
+// context's pool (cold_stage.cu).
+int launch_cold_staging(moe_ctx *ctx, const Layer &layer, int W, const BankLists &cold_lists, int32_t *slot_of,
+                        int32_t *src_of, cudaStream_t s);
 int launch_probe_read(const uint8_t *src, size_t bytes, uint64_t *sink, int blocks,
                       cudaStream_t s);
 

@@ -139,6 +139,28 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
  * rows); non-decreasing in T. */
 int moe_workspace_bytes(const moe_ctx *ctx, int T, size_t *bytes);
 
+/* Big-batch cold staging ("We Built the Counter", section 6: copying an
+ * expert on a miss is a tool for big batches; "Should a GB300 Prefetch Its
+ * Cold Experts?", section 6: staging offloaded experts for prefill-sized
+ * steps).  The FFN streams a unit's weights once per token tile (8, 16, 32
+ * or 192 tokens by step size), so a cold expert with picks in several tiles
+ * would cross the host link once per tile.  With a pool of `slots` expert
+ * rows in HBM (0..64; 0 frees it and turns staging off, the default), every
+ * later FFN call that covers the cold bank of a step of more than 16 tokens
+ * first picks the cold rows with more picks than one tile -- most picks
+ * first, ties to the lower row, at most `slots` -- and copies each once into
+ * the pool; their units then read the pool.  Same bytes, same arithmetic: the
+ * rows of Y are bit-identical to unstaged steps.  The pool belongs to the
+ * context and is rewritten by each such call, so calls of different layers
+ * that use it must not overlap on the GPU.  Synchronizes the device;
+ * MOE_ENOMEM if the pool cannot be allocated (staging is then off). */
+int moe_set_cold_staging(moe_ctx *ctx, int slots);
+
+/* After a staged FFN call: the cold-bank row copied into each pool slot, or
+ * -1 (rows: host int32 [64]).  ws and T as in the call.  Synchronizes
+ * stream. */
+int moe_read_stage(moe_ctx *ctx, const void *ws, int T, int32_t *rows, void *stream);
+
 /* Route, split and count (async).  "vLLM: Pin Hot Experts", Results (split
  * each token's k ids by residency); "We Built the Counter", section 2 (one
  * masked relaxed atomic add per pick into the usage table; only steps of at
