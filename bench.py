@@ -84,6 +84,8 @@ def parse(argv=None):
     ap.add_argument("--hot", type=int, default=0, help="hot-bank experts for --experts")
     ap.add_argument("--tokens", type=int, default=0, help="profiling-size variant: tokens per step")
     ap.add_argument("--skip", default="", help="comma-separated sub-configs of --config all to leave out")
+    ap.add_argument("--act", default="e4m3x2", choices=["e4m3x2", "mxfp8"],
+                    help="activation format of prefill-sized steps for --config prefill")
     return ap.parse_args(argv)
 
 
@@ -996,7 +998,7 @@ def run_single(S, args):
                     "config": {"workload": WORKLOADS[name]}, "adaptive": a, "clocks": a["clocks"],
                     "cpu_baseline": cpu_baseline(S, cfg, keep, args)}
         else:
-            p = measure_prefill(S, ctx, cfg, args, 0)
+            p = measure_prefill(S, ctx, cfg, args, 0, fmt=1 if args.act == "mxfp8" else 0)
             line = {"metric": METRIC, "value": p["tokens_per_s"], "unit": "tokens/s", "n_gpus": S.world,
                     "steps": p["steps"], "warmup": 3, "ms_per_step": p["us_per_layer_step"] * 1e-3,
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
