@@ -84,8 +84,6 @@ def parse(argv=None):
     ap.add_argument("--hot", type=int, default=0, help="hot-bank experts for --experts")
     ap.add_argument("--tokens", type=int, default=0, help="profiling-size variant: tokens per step")
     ap.add_argument("--skip", default="", help="comma-separated sub-configs of --config all to leave out")
-    ap.add_argument("--ffn", default="tcgen05", choices=["tcgen05", "unpack"],
-                    help="decode tiles' weights into tensor memory by tensor-memory copies (default) or by warps")
     ap.add_argument("--act", default="e4m3x2", choices=["e4m3x2", "mxfp8"],
                     help="activation format of prefill-sized steps for --config prefill")
     return ap.parse_args(argv)
@@ -365,8 +363,6 @@ class Session:
         Returns (ctx, weights kept for the CPU sample's layers)."""
         moe = self.moe
         ctx = moe.moe_create(len(layer_masks), cfg.E, cfg.k, cfg.H, cfg.I, T_max, device=self.local)
-        if self.args.ffn == "unpack":
-            moe.moe_set_ffn_impl(ctx, moe.MOE_FFN_TCGEN05_UNPACK)
         keep = {}
         for l, m in enumerate(layer_masks):
             w = synth.layer_weights(cfg, l)

@@ -20,7 +20,7 @@ from ._build import LIB as _LIB_PATH, build  # noqa: F401
 
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ESTALE, MOE_ETIMEOUT, MOE_ESTATE = 0, -1, -2, -3, -4, -5, -6
 MOE_BANK_HOT, MOE_BANK_COLD, MOE_BANK_BOTH = 0, 1, 2
-MOE_FFN_TCGEN05, MOE_FFN_SIMT, MOE_FFN_TCGEN05_UNPACK = 0, 1, 2
+MOE_FFN_TCGEN05, MOE_FFN_SIMT = 0, 1
 MOE_FAULT_NONE, MOE_FAULT_WITHHOLD_COPY = 0, 1
 MOE_ACT_E4M3X2, MOE_ACT_MXFP8 = 0, 1
 

@@ -619,7 +619,6 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
 }
 
 #include "ffn_tc_decode.cuh"
-#include "ffn_tc_decode_cp.cuh"
 
 // Exponent e of a row whose largest |value| is mx: mx * 2^-e lies in
 // (224, 448], the top binade of e4m3 (largest finite 448 = 0.875 * 2^9).
@@ -1112,49 +1111,37 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
     return cudaLaunchKernelExC(&cfg, (const void *)kern, pargs);
 }
 
-template <int NMAX, int PHASE, int BANKS, bool CP>
-int launch_decode_one(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap &mA1, const CUtensorMap &mA2,
-                      const TcArgs &args, int blocks, bool dependent, cudaStream_t s) {
-    if (CP) {
-        using C = DecCpCfg<NMAX>;
-        auto kern = ffn_tc_decode_cp_kernel<NMAX, PHASE, BANKS>;
-        MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem));
-        if (blocks < 1) return MOE_OK;
-        if (PHASE == 2 && dependent) {
-            MOE_CUDA_TRY(launch_dependent(kern, dim3(blocks), dim3(C::kThreads), C::kSmem, s, mB, mA0, mA1, mA2, args));
-        } else {
-            kern<<<blocks, C::kThreads, C::kSmem, s>>>(mB, mA0, mA1, mA2, args);
-        }
+template <int NMAX, int PHASE, int BANKS>
+int launch_decode_one(const CUtensorMap &mB, const TcArgs &args, int blocks, bool dependent, cudaStream_t s) {
+    using C = DecCfg<NMAX>;
+    auto kern = ffn_tc_decode_kernel<NMAX, PHASE, BANKS>;
+    MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem));
+    if (blocks < 1) return MOE_OK;
+    if (PHASE == 2 && dependent) {
+        // the down GEMM depends on prep_h programmatically: it claims units
+        // and streams weights before prep_h's rows exist
+        MOE_CUDA_TRY(launch_dependent(kern, dim3(blocks), dim3(C::kThreads), C::kSmem, s, mB, args));
     } else {
-        using C = DecCfg<NMAX>;
-        auto kern = ffn_tc_decode_kernel<NMAX, PHASE, BANKS>;
-        MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem));
-        if (blocks < 1) return MOE_OK;
-        if (PHASE == 2 && dependent) {
-            // the down GEMM depends on prep_h programmatically: it claims units
-            // and streams weights before prep_h's rows exist
-            MOE_CUDA_TRY(launch_dependent(kern, dim3(blocks), dim3(C::kThreads), C::kSmem, s, mB, args));
-        } else {
-            kern<<<blocks, C::kThreads, C::kSmem, s>>>(mB, args);
-        }
+        kern<<<blocks, C::kThreads, C::kSmem, s>>>(mB, args);
     }
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
-template <int NMAX, int PHASE, bool CP>
-int launch_decode_gemm(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap &mA1, const CUtensorMap &mA2,
-                       const TcArgs &a, int blocks, bool dependent, cudaStream_t s) {
-    if (a.b < 0) return launch_decode_one<NMAX, PHASE, 2, CP>(mB, mA0, mA1, mA2, a, blocks, dependent, s);
-    if (a.b == MOE_BANK_COLD) return launch_decode_one<NMAX, PHASE, 1, CP>(mB, mA0, mA1, mA2, a, blocks, dependent, s);
-    return launch_decode_one<NMAX, PHASE, 0, CP>(mB, mA0, mA1, mA2, a, blocks, dependent, s);
+template <int NMAX, int PHASE>
+int launch_decode_gemm(const CUtensorMap &mB, const TcArgs &a, int blocks, bool dependent, cudaStream_t s) {
+    if (a.b < 0) return launch_decode_one<NMAX, PHASE, 2>(mB, a, blocks, dependent, s);
+    if (a.b == MOE_BANK_COLD) return launch_decode_one<NMAX, PHASE, 1>(mB, a, blocks, dependent, s);
+    return launch_decode_one<NMAX, PHASE, 0>(mB, a, blocks, dependent, s);
 }
 
-// Grid of a decode-tile GEMM launch: per_sm CTAs per SM fill the SM; a
+// Grid of a decode-tile GEMM launch: kPerSm CTAs per SM fill the SM; a
 // cold-bank launch takes one per SM (the host link needs a few MB in flight
 // GPU-wide) and, beside it, a hot-bank launch the SM's other slots, so the
 // two banks' launches run side by side.
-int decode_blocks(const moe_ctx *ctx, int per_sm, int b, bool shared, int units_max) {
+template <int NMAX>
+int decode_blocks(const moe_ctx *ctx, int b, bool shared, int units_max) {
+    const int per_sm = DecCfg<NMAX>::kPerSm;
     int blocks;
     if (b < 0 || (b == MOE_BANK_HOT && !shared)) blocks = ctx->sms * per_sm;
     else if (b == MOE_BANK_COLD) blocks = ctx->sms;
@@ -1162,48 +1149,35 @@ int decode_blocks(const moe_ctx *ctx, int per_sm, int b, bool shared, int units_
     return std::max(1, std::min(units_max, blocks));
 }
 
-// CP: the kernel whose tensor memory copies spread the codes
-// (ffn_tc_decode_cp_kernel, logical K order); else the one whose warps do
-// (ffn_tc_decode_kernel, K order permuted within groups of eight, as the
-// token rows are written for it).
-template <int NMAX, bool CP>
-int launch_bank_decode(moe_ctx *ctx, const Layer &layer, bool shared, bool cold_rows, TcArgs a1, TcArgs a2, int units1,
-                       int units2, const uint16_t *x, const WsLayout &lay, uint8_t *ws, cudaStream_t s) {
+template <int NMAX>
+int launch_bank_decode(moe_ctx *ctx, bool shared, bool cold_rows, TcArgs a1, TcArgs a2, int units1, int units2,
+                       const uint16_t *x, const WsLayout &lay, uint8_t *ws, cudaStream_t s) {
     const Geom &g = ctx->g;
     const int P = a1.P;
-    const int per_sm = CP ? DecCpCfg<NMAX>::kPerSm : DecCfg<NMAX>::kPerSm;
-    a1.ks = std::min(CP ? DecCpCfg<NMAX>::kSplit : DecCfg<NMAX>::kSplit, a1.part.steps());
-    a2.ks = std::min(CP ? DecCpCfg<NMAX>::kSplit : DecCfg<NMAX>::kSplit, a2.part.steps());
+    a1.ks = std::min(DecCfg<NMAX>::kSplit, a1.part.steps());
+    a2.ks = std::min(DecCfg<NMAX>::kSplit, a2.part.steps());
     const dim3 grid_p(P, a1.b < 0 ? 2 : 1);   // one block per pick (of each bank)
     CUtensorMap m1, m2;
     if (int r = make_piece_map(&m1, ws + lay.xq, g.H, P, NMAX)) return r;
     if (int r = make_piece_map(&m2, ws + lay.hq, g.I, P, NMAX)) return r;
-    prep_x_kernel<!CP><<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
-                                              (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
+    prep_x_kernel<true><<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
+                                               (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
     MOE_LAUNCH_CHECK();
-    // the staging pool's maps stand in for units read from it (the cold maps
-    // where no pool exists: then no unit reads them)
-    const CUtensorMap &sm1 = ctx->stage_pool ? ctx->stage_map[0] : layer.wmap[1][0];
-    const CUtensorMap &sm2 = ctx->stage_pool ? ctx->stage_map[1] : layer.wmap[1][1];
-    if (int r = launch_decode_gemm<NMAX, 1, CP>(m1, layer.wmap[0][0], layer.wmap[1][0], sm1, a1,
-                                                decode_blocks(ctx, per_sm, a1.b, shared, units1), false, s))
-        return r;
+    if (int r = launch_decode_gemm<NMAX, 1>(m1, a1, decode_blocks<NMAX>(ctx, a1.b, shared, units1), false, s)) return r;
     // A call that streams the cold bank chains prep_h and the down GEMM to
     // the gate/up GEMM as programmatic dependents, so the host link restarts
     // before prep_h ends; an HBM-only call measured faster without.
     const bool dependent = a1.b != MOE_BANK_HOT && cold_rows;
     if (dependent) {
-        MOE_CUDA_TRY(launch_dependent(prep_h_kernel<!CP>, grid_p, dim3(256), 0, s, a1.lists[0], a1.lists[1], a1.b, P,
+        MOE_CUDA_TRY(launch_dependent(prep_h_kernel<true>, grid_p, dim3(256), 0, s, a1.lists[0], a1.lists[1], a1.b, P,
                                       g.I, (const float *)(ws + lay.h32), (const float *)a1.gu_out, ws + lay.hq,
                                       (int32_t *)(ws + lay.hexp), a2.y_out, g.H));
     } else {
-        prep_h_kernel<!CP><<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
-                                                  a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
+        prep_h_kernel<true><<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
+                                                   a1.gu_out, ws + lay.hq, (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
     }
     MOE_LAUNCH_CHECK();
-    if (int r = launch_decode_gemm<NMAX, 2, CP>(m2, layer.wmap[0][1], layer.wmap[1][1], sm2, a2,
-                                                decode_blocks(ctx, per_sm, a1.b, shared, units2), dependent, s))
-        return r;
+    if (int r = launch_decode_gemm<NMAX, 2>(m2, a2, decode_blocks<NMAX>(ctx, a1.b, shared, units2), dependent, s)) return r;
     round_y_kernel<<<grid_p, 256, 0, s>>>(a2.lists[0], a2.lists[1], a2.b, g.H, a2.y_out, a2.Y);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
@@ -1299,14 +1273,9 @@ int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int b, const uint16_t *x, in
     // prefill-sized steps use 192-wide tiles (an expert's ~T*k/E tokens in
     // one tile) in the shared-memory-A kernel, one CTA per SM.
     const bool cold_rows = layer.n_cold > 0;
-    const bool cp = ctx->ffn_impl != MOE_FFN_TCGEN05_UNPACK;
-#define MOE_DECODE(N)                                                                                                 \
-    (cp ? launch_bank_decode<N, true>(ctx, layer, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s)             \
-        : launch_bank_decode<N, false>(ctx, layer, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s))
-    if (T <= 8) return MOE_DECODE(8);
-    if (T <= 16) return MOE_DECODE(16);
-    if (T <= kNarrowMaxT) return MOE_DECODE(32);
-#undef MOE_DECODE
+    if (T <= 8) return launch_bank_decode<8>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= 16) return launch_bank_decode<16>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
+    if (T <= kNarrowMaxT) return launch_bank_decode<32>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
     if (ctx->act_format == MOE_ACT_MXFP8)
         return launch_bank<kPrefillTile, true>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
     return launch_bank<kPrefillTile, false>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);

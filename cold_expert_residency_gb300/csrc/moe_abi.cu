@@ -300,8 +300,7 @@ int moe_destroy(moe_ctx *ctx) {
 
 int moe_set_ffn_impl(moe_ctx *ctx, int impl) {
     if (int r = check_ctx(ctx)) return r;
-    if (impl != MOE_FFN_TCGEN05 && impl != MOE_FFN_SIMT && impl != MOE_FFN_TCGEN05_UNPACK)
-        return set_error(MOE_EINVAL, "unknown FFN impl");
+    if (impl != MOE_FFN_TCGEN05 && impl != MOE_FFN_SIMT) return set_error(MOE_EINVAL, "unknown FFN impl");
     ctx->ffn_impl = impl;
     return MOE_OK;
 }

@@ -210,15 +210,6 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
 __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
-// Shared -> tensor memory copy of a 128-row x 32-byte matrix of padded 4-bit
-// elements (smem descriptor; each 16-byte unit holds 16 codes in its first 8
-// bytes), decompressed to one 8-bit element per code: row m lands in lane m,
-// 8 columns from taddr, element j in byte j with the code in bits 5..2 -- the
-// form in which a block-scaled MMA reads an e2m1 A operand from tensor memory.
-// Ordered with the same thread's later tcgen05.mma.
-__device__ __forceinline__ void tmem_cp_128x256b_unpack4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x256b.b8x16.b4x16_p64 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
 // Arrive on `bar` once all prior tcgen05 async ops of this thread complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

@@ -54,13 +54,9 @@ enum {
 
 enum { MOE_BANK_HOT = 0, MOE_BANK_COLD = 1, MOE_BANK_BOTH = 2 };
 
-/* FFN kernel implementation: tensor cores (tcgen05 + TMEM, default), a
- * CUDA-core kernel kept for cross-checking, or the tensor-core kernels with
- * the decode tiles' weights spread into tensor memory by the SM's warps
- * instead of by tensor-memory copies (MOE_FFN_TCGEN05_UNPACK; decode tiles
- * then sum each group of eight products in another order, so their rows may
- * differ from the default's in the last bits). */
-enum { MOE_FFN_TCGEN05 = 0, MOE_FFN_SIMT = 1, MOE_FFN_TCGEN05_UNPACK = 2 };
+/* FFN kernel implementation: tensor cores (tcgen05 + TMEM, default) or a
+ * CUDA-core kernel kept for cross-checking. */
+enum { MOE_FFN_TCGEN05 = 0, MOE_FFN_SIMT = 1 };
 
 typedef struct moe_ctx moe_ctx;
 

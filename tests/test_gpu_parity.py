@@ -14,7 +14,7 @@ from gpu_util import Harness, assert_close_bf16, f32
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-IMPLS = [0, 1, 2]   # MOE_FFN_TCGEN05, MOE_FFN_SIMT, MOE_FFN_TCGEN05_UNPACK
+IMPLS = [0, 1]   # MOE_FFN_TCGEN05, MOE_FFN_SIMT
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -247,13 +247,11 @@ def test_counts_only_for_small_steps_and_when_on():
         h.close()
 
 
-@pytest.mark.parametrize("impl", [0, 2])
-@pytest.mark.parametrize("T", [1, 5, 12, 33, 64, 65, 130])
-def test_token_counts_and_ragged_tiles(T, impl):
-    """Every decode tile width (8, 16, 32 tokens) and the prefill tile, ragged
-    token counts, both ways of spreading the decode tiles' weights."""
+@pytest.mark.parametrize("T", [1, 5, 33, 64, 65, 130])
+def test_token_counts_and_ragged_tiles(T):
+    """Several N-tile widths (16 / 64 / 256 variants) and ragged token counts."""
     cfg = synth.get_config("tiny", T=T)
-    h = Harness(cfg, impl=impl)
+    h = Harness(cfg)
     try:
         lg = synth.router_logits(cfg, 0, 3, T=T)
         x = synth.activations(cfg, 0, 3, T=T)
