@@ -98,6 +98,19 @@ __device__ __forceinline__ int staged_slot(const TcArgs &args, int bk, int a) {
 constexpr int kQ = 4;       // unit queue depth (producer -> the other roles)
 constexpr int kMaxStages = 8;
 
+// Position in a ring of S stages: the stage and the parity of its round,
+// advanced without dividing by the launch-time S (a division by a runtime
+// value costs about as much as the rest of a K step's bookkeeping).
+struct RingPos {
+    uint32_t st = 0, ph = 0;
+    __device__ __forceinline__ void next(uint32_t S) {
+        if (++st == S) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 // Bounded mbarrier wait: gives up after limit_ns of wall-clock time, raising
 // the CTA's abort flag and the launch status.  SUSP: each poll may suspend the
 // thread (up to 20 us) instead of returning at once -- used by the decode
@@ -397,17 +410,21 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
     auto units_of = [&](int bk) { return args.lists[0].hdr[kHdrNAct + bk] * part.tiles * args.ks; };
 
     // every role but the producer reads the unit sequence from the queue:
-    // entry 2u + bank (unit u of that bank), or -1 at the end
-    auto take_unit = [&](uint32_t ui, bool warp_wide, bool &ok) -> int {
+    // entry 2u + bank (unit u of that bank), or -1 at the end.  The epilogue
+    // warps wait with a suspend hint (a spinning warp takes issue slots from
+    // the producer and MMA warps that share its scheduler); the MMA warp
+    // spins, and only its lane 0 counts as a reader.
+    auto take_unit = [&](uint32_t ui, bool epilogue, bool &ok) -> int {
         const int qs = ui % kQ;
-        const bool w = warp_wide ? wait_warp<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status, args.wait_ns)
-                                 : wait_one<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status, args.wait_ns);
+        const uint32_t ph = (ui / kQ) & 1;
+        const bool w = epilogue ? wait_warp<true>(bar(UQFULL + qs), ph, abort_flag, args.status, args.wait_ns)
+                                : wait_warp<SUSP>(bar(UQFULL + qs), ph, abort_flag, args.status, args.wait_ns);
         if (!w) {
             ok = false;
             return -1;
         }
         const int u = uq[qs];
-        ptx::mbar_arrive(bar(UQEMPTY + qs));
+        if (epilogue || lane == 0) ptx::mbar_arrive(bar(UQEMPTY + qs));
         return u;
     };
 
@@ -433,7 +450,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
                 float re[NB];
                 load_meta<NB>(L, args, 0, 1, nn, p0 + n0, goff + p0 + n0, lane, rs, re);
                 const int db = j % DB;
-                if (!wait_warp<SUSP>(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
+                if (!wait_warp<true>(bar(ACCREADY + db), (j / DB) & 1, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
                 ptx::tc_fence_after();
                 epilogue_cols<PHASE, NB, C::kStack, C::kSplit, C::kRowQ>(args, tmem + lane_base + C::kDCol + db * C::kDW, 0, 1,
                                                                         nn, goff + p0 + n0, mt, quarter, lane, rs, re);
@@ -455,6 +472,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
         }
         bool dry_pref = false, dry_other = args.b >= 0;
         uint32_t it = 0;
+        RingPos pos;   // stage of iteration it
         bool ok = true, withheld = false;
         for (uint32_t ui = 0; ok; ++ui) {
             // take the next unit from the launch's work counter and publish it
@@ -491,10 +509,10 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
             const uint8_t *expert = (sslot >= 0 ? args.stage_pool : args.bank[bk]) + (int64_t)row * args.eb;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX) {
                 const int brow = goff + p0 + n0;
-                for (int s = s0; s < s1; ++s, ++it) {
-                    const int st = it % S;
-                    const uint32_t rnd = it / S;
-                    if (rnd > 0 && !wait_one<SUSP>(bar(DONE + st), (rnd - 1) & 1, abort_flag, args.status, args.wait_ns)) {
+                for (int s = s0; s < s1; ++s, ++it, pos.next(S)) {
+                    const int st = pos.st;
+                    // the stage's previous round must have been consumed
+                    if (it >= (uint32_t)S && !wait_one<SUSP>(bar(DONE + st), pos.ph ^ 1u, abort_flag, args.status, args.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -533,17 +551,21 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
                     if (ptx::mbar_try_wait(bar(FULL + i % S), (i / S) & 1)) break;
             }
         }
-    } else if (warp == C::kMmaWarp && lane == 0) {
+    } else if (warp == C::kMmaWarp) {
         // ----------------------------------------------------------- MMA issue
+        // The whole warp runs the loop (values read from memory are taken
+        // from lane 0, so the warp holds them uniformly); one elected lane
+        // issues the tensor-core instructions.
         uint32_t it = 0, j = 0;
+        RingPos pos, prev_pos;   // stages of iterations it and it - NSF
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
-            const int e = take_unit(ui, false, ok);
+            const int e = __shfl_sync(0xffffffffu, take_unit(ui, false, ok), 0);
             if (e < 0) break;
             const BankLists &L = args.lists[e & 1];
             int a, mt, s0, s1;
             unit_pos(e >> 1, part.tiles, ns, args.ks, a, mt, s0, s1);
-            const int n = L.act_off[a + 1] - L.act_off[a];
+            const int n = __shfl_sync(0xffffffffu, L.act_off[a + 1] - L.act_off[a], 0);
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
                 const int Nr = (nn + C::kRowQ - 1) / C::kRowQ * C::kRowQ;
@@ -551,55 +573,60 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
                 const uint32_t idesc0 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 0, 0);   // | (K block << 29): A scale byte
                 const int db = j % DB;
                 if (j >= (uint32_t)DB &&
-                    !wait_one<SUSP>(bar(ACCFREE + db), ((j / DB) - 1) & 1, abort_flag, args.status, args.wait_ns)) {
+                    !wait_warp<SUSP>(bar(ACCFREE + db), ((j / DB) - 1) & 1, abort_flag, args.status, args.wait_ns)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + C::kDCol + db * C::kDW;
-                for (int s = s0; s < s1; ++s, ++it) {
-                    const int st = it % S;
-                    if (!wait_one<SUSP>(bar(FULL + st), (it / S) & 1, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
+                for (int s = s0; s < s1; ++s, ++it, pos.next(S)) {
+                    const int st = pos.st;
+                    if (!wait_warp<SUSP>(bar(FULL + st), pos.ph, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
                     ptx::tc_fence_after();
                     int slot, tidx, kb0, nkb;
                     part.group(mt, s, slot, tidx, kb0, nkb);
                     // the group's scales -> slot it % NSF, once the MMAs of iteration
                     // it - NSF (the slot's last reader) have completed
                     if (it >= (uint32_t)NSF) {
-                        const uint32_t prev = it - NSF;
-                        if (!wait_one<SUSP>(bar(DONE + prev % S), (prev / S) & 1, abort_flag, args.status, args.wait_ns)) {
+                        if (!wait_warp<SUSP>(bar(DONE + prev_pos.st), prev_pos.ph, abort_flag, args.status, args.wait_ns)) {
                             ok = false;
                             break;
                         }
+                        prev_pos.next(S);
                     }
                     const uint32_t sfa = tmem + 32u * (it % NSF);
-                    ptx::tmem_cp_32x128b_warpx4(sfa, ptx::smem_desc_noswizzle(ptx::smem_addr(sSF + st * kSfAtomBytes), 128, 128));
-                    if (MX) {   // token blocks 0-3 and 4-7 of the tile's block scales
-                        const uint32_t sb = ptx::smem_addr(sSFB + st * C::kSfbStage);
-                        ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol, ptx::smem_desc_noswizzle(sb, 128, 128));
-                        ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol + 4, ptx::smem_desc_noswizzle(sb + 512, 128, 128));
-                    }
-                    const uint32_t a_addr = ptx::smem_addr(sA + st * C::kAStage);
-                    for (int i = 0; i < nkb; ++i) {
-                        const int kb = kb0 + i;   // K block of the group (A bytes kb*32.., scale byte kb)
-                        const uint64_t ad = ptx::smem_desc_sw128(a_addr + kb * 32);
-                        // this tile's chunk i/2 of the group, its K block i%2
-                        const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage + (i >> 1) * C::kBChunk) + (i & 1) * 32;
-#pragma unroll
-                        for (int pc = 0; pc < (C::kStack ? 1 : C::kPieces); ++pc) {   // e4m3 piece of B (unstacked tiles)
-                            const uint64_t bd = ptx::smem_desc_sw64(b_addr + pc * NMAX * 64);
-                            if (MX)   // B's scale: byte i (the token rows' K block) of the slot's own columns
-                                ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29) | ((uint32_t)i << 4), sfa,
-                                                     sfa + C::kSfbCol, (s != s0) | i);
-                            else
-                                ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29), sfa,
-                                                     tmem + C::kSfbCol + pc * C::kSfbStride, (s != s0) | i | pc);
+                    if (ptx::elect_one()) {
+                        ptx::tmem_cp_32x128b_warpx4(
+                            sfa, ptx::smem_desc_noswizzle(ptx::smem_addr(sSF + st * kSfAtomBytes), 128, 128));
+                        if (MX) {   // token blocks 0-3 and 4-7 of the tile's block scales
+                            const uint32_t sb = ptx::smem_addr(sSFB + st * C::kSfbStage);
+                            ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol, ptx::smem_desc_noswizzle(sb, 128, 128));
+                            ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol + 4, ptx::smem_desc_noswizzle(sb + 512, 128, 128));
                         }
+                        const uint32_t a_addr = ptx::smem_addr(sA + st * C::kAStage);
+                        for (int i = 0; i < nkb; ++i) {
+                            const int kb = kb0 + i;   // K block of the group (A bytes kb*32.., scale byte kb)
+                            const uint64_t ad = ptx::smem_desc_sw128(a_addr + kb * 32);
+                            // this tile's chunk i/2 of the group, its K block i%2
+                            const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage + (i >> 1) * C::kBChunk) + (i & 1) * 32;
+#pragma unroll
+                            for (int pc = 0; pc < (C::kStack ? 1 : C::kPieces); ++pc) {   // e4m3 piece of B (unstacked tiles)
+                                const uint64_t bd = ptx::smem_desc_sw64(b_addr + pc * NMAX * 64);
+                                if (MX)   // B's scale: byte i (the token rows' K block) of the slot's own columns
+                                    ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29) | ((uint32_t)i << 4), sfa,
+                                                         sfa + C::kSfbCol, (s != s0) | i);
+                                else
+                                    ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29), sfa,
+                                                         tmem + C::kSfbCol + pc * C::kSfbStride, (s != s0) | i | pc);
+                            }
+                        }
+                        ptx::mma_commit(bar(DONE + st));
                     }
-                    ptx::mma_commit(bar(DONE + st));
+                    __syncwarp();
                 }
                 if (!ok) break;
-                ptx::mma_commit(bar(ACCREADY + db));
+                if (ptx::elect_one()) ptx::mma_commit(bar(ACCREADY + db));
+                __syncwarp();
             }
         }
         if (!ok && it > 0) {
