@@ -19,9 +19,10 @@
 //             the token rows of decode tiles are written with the same
 //             permutation, so every dot product is unchanged.  The same warps
 //             run the epilogue.
-//   MMA       one thread: per chunk, tcgen05.mma kind::mxf8f6f4 with A and its
-//             scales from TMEM, B from shared memory; commits free the A slot
-//             (per chunk) and the stage (per group).
+//   MMA       one warp, one elected lane issuing: per chunk, tcgen05.mma
+//             kind::mxf8f6f4 with A and its scales from TMEM, B from shared
+//             memory; commits free the A slot (per chunk) and the stage (per
+//             group).
 //
 // Bounded waits and teardown as in the shared-memory-A kernel.
 
@@ -139,16 +140,16 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
     const PartLayout &part = args.part;
     const int ns = part.steps();
     auto units_of = [&](int bk) { return args.lists[0].hdr[kHdrNAct + bk] * part.tiles * args.ks; };
-    auto take_unit = [&](uint32_t ui, bool warp_wide, bool &ok) -> int {
+    // the unpack warps and the MMA warp read the unit sequence warp-wide;
+    // of the MMA warp only lane 0 counts as a reader
+    auto take_unit = [&](uint32_t ui, bool all_lanes, bool &ok) -> int {
         const int qs = ui % kQ;
-        const bool w = warp_wide ? wait_warp<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status, args.wait_ns)
-                                 : wait_one<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status, args.wait_ns);
-        if (!w) {
+        if (!wait_warp<SUSP>(bar(UQFULL + qs), (ui / kQ) & 1, abort_flag, args.status, args.wait_ns)) {
             ok = false;
             return -1;
         }
         const int u = uq[qs];
-        ptx::mbar_arrive(bar(UQEMPTY + qs));
+        if (all_lanes || lane == 0) ptx::mbar_arrive(bar(UQEMPTY + qs));
         return u;
     };
 
@@ -321,23 +322,24 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
                     if (ptx::mbar_try_wait(bar(FULL + i % S), (i / S) & 1)) break;
             }
         }
-    } else if (warp == C::kMmaWarp && lane == 0) {
+    } else if (warp == C::kMmaWarp) {
         // ----------------------------------------------------------- MMA issue
+        // the whole warp runs the loop; one elected lane issues
         uint32_t it = 0, ci = 0, j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
-            const int e = take_unit(ui, false, ok);
+            const int e = __shfl_sync(0xffffffffu, take_unit(ui, false, ok), 0);
             if (e < 0) break;
             const BankLists &L = args.lists[e & 1];
             int a, mt, s0, s1;
             unit_pos(e >> 1, part.tiles, ns, args.ks, a, mt, s0, s1);
-            const int n = L.act_off[a + 1] - L.act_off[a];
+            const int n = __shfl_sync(0xffffffffu, L.act_off[a + 1] - L.act_off[a], 0);
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
                 const int Nr = (nn + C::kRowQ - 1) / C::kRowQ * C::kRowQ;
                 const int Nm = C::kStack ? 2 * Nr : Nr;   // B rows of one MMA
                 const uint32_t idesc0 = ptx::idesc_mx_e2m1_e4m3(128, Nm, 0, 0);   // | (scale byte << 29)
-                if (j >= 1u && !wait_one<SUSP>(bar(ACCFREE), (j - 1) & 1, abort_flag, args.status, args.wait_ns)) {
+                if (j >= 1u && !wait_warp<SUSP>(bar(ACCFREE), (j - 1) & 1, abort_flag, args.status, args.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -349,31 +351,36 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
                     part.group(mt, s, slot, tidx, kb0, nkb);
                     for (int ch = 0; ch < nkb / 2; ++ch, ++ci) {
                         const int abuf = ci % NA;
-                        if (!wait_one<SUSP>(bar(AREADY + abuf), (ci / NA) & 1, abort_flag, args.status, args.wait_ns)) {
+                        if (!wait_warp<SUSP>(bar(AREADY + abuf), (ci / NA) & 1, abort_flag, args.status, args.wait_ns)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
                         const uint32_t a_tm = tmem + C::kACol + abuf * 32, sfa = tmem + C::kSfaCol + abuf * 32;
                         const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage + ch * C::kBChunk);
+                        if (ptx::elect_one()) {
 #pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            const uint32_t idesc = idesc0 | ((uint32_t)(kb0 + 2 * ch + kk) << 29);
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const uint32_t idesc = idesc0 | ((uint32_t)(kb0 + 2 * ch + kk) << 29);
 #pragma unroll
-                            for (int pc = 0; pc < (C::kStack ? 1 : 2); ++pc) {
-                                const uint64_t bd = ptx::smem_desc_sw64(b_addr + pc * NMAX * 64 + kk * 32);
-                                ptx::mma_mxf8f6f4_ts(d_tmem, a_tm + kk * 8, bd, idesc, sfa,
-                                                     tmem + C::kSfbCol + pc * C::kSfbStride,
-                                                     (s != s0) | ch | kk | pc);
+                                for (int pc = 0; pc < (C::kStack ? 1 : 2); ++pc) {
+                                    const uint64_t bd = ptx::smem_desc_sw64(b_addr + pc * NMAX * 64 + kk * 32);
+                                    ptx::mma_mxf8f6f4_ts(d_tmem, a_tm + kk * 8, bd, idesc, sfa,
+                                                         tmem + C::kSfbCol + pc * C::kSfbStride,
+                                                         (s != s0) | ch | kk | pc);
+                                }
                             }
+                            ptx::mma_commit(bar(ADONE + abuf));
                         }
-                        ptx::mma_commit(bar(ADONE + abuf));
+                        __syncwarp();
                     }
                     if (!ok) break;
-                    ptx::mma_commit(bar(DONEG + st));
+                    if (ptx::elect_one()) ptx::mma_commit(bar(DONEG + st));
+                    __syncwarp();
                 }
                 if (!ok) break;
-                ptx::mma_commit(bar(ACCREADY));
+                if (ptx::elect_one()) ptx::mma_commit(bar(ACCREADY));
+                __syncwarp();
             }
         }
         if (!ok && ci > 0) {
