@@ -65,7 +65,6 @@ struct TcArgs {
     int64_t eb;              // bytes per expert
     PartLayout part;         // this GEMM's part of an expert (W13 or W2)
     int ks;                  // K parts per (expert, M-tile) unit
-    int S;                   // stages of the shared-memory ring (2 .. kMaxStages)
     BankLists lists[2];      // both banks' split lists
     int b;                   // the bank this launch covers, or -1: both banks in one launch
     int k, H, I, P;
@@ -96,7 +95,6 @@ __device__ __forceinline__ int staged_slot(const TcArgs &args, int bk, int a) {
 }
 
 constexpr int kQ = 4;       // unit queue depth (producer -> the other roles)
-constexpr int kMaxStages = 8;
 
 // Position in a ring of S stages: the stage and the parity of its round,
 // advanced without dividing by the launch-time S (a division by a runtime
@@ -176,25 +174,25 @@ struct TcCfg {
     static constexpr int kAStage = 2 * kGroupQBytes;        // padded code block: 16 KB
     static constexpr int kSfbStage = MX ? kSfbGroupBytes : 0;   // the tile's B block scales of one group
     // One stage holds a group's 8.5 KB of weights as 16.5 KB of padded codes
-    // and scales, plus the token rows (and their block scales); the host
-    // sizes the ring per launch from the SM's shared memory.
+    // and scales, plus the token rows (and their block scales).
     static constexpr int kStageBytes = kAStage + kBStage + kSfAtomBytes + kSfbStage;
     static constexpr int kDBufs = 2;                        // accumulators in TMEM
     static constexpr int kDW = NMAX;                        // columns of one accumulator
     static constexpr int kNCol = (kDW + 31) / 32;           // B scale columns of one piece
-    // A scale slots in TMEM, reused round-robin: the MMA thread refills slot
-    // it % kNsf after the MMAs of iteration it - kNsf have completed (the
-    // ring holds at least kNsf stages, so that iteration's barrier phase is
-    // still the one waited for).  The MXFP8 ring is deeper and takes a fourth.
-    static constexpr int kNsf = MX ? 4 : 3;
+    // Ring stages, each with its own scale slot in tensor memory: stage s's
+    // scales are copied into slot s, so a slot is rewritten only after the
+    // producer has seen the stage's previous MMAs complete (the MMA warp
+    // needs no wait of its own).  As many stages as shared memory holds,
+    // up to what tensor memory leaves for slots beside the accumulators.
+    static constexpr int kStages = MX ? 4 : 3;
     // Tensor memory columns: slot i's A scales at 32 i (four columns written
     // by tcgen05.cp); slot 0's block also holds the constant B scale columns
     // of piece 0 at +8 and of piece 1 at +16 -- in the MXFP8 format, slot i's
-    // own B scale columns sit at 32 i + 8 (token blocks 0..7, two tcgen05.cp
-    // of the stage's scales); then the accumulators.
+    // own B scale columns sit at 32 i + 8 (token blocks 0..7, one tcgen05.cp
+    // per four blocks); then the accumulators.
     static constexpr uint32_t kSfbCol = 8;
     static constexpr uint32_t kSfbStride = 8;
-    static constexpr uint32_t kDCol = 32 * kNsf;
+    static constexpr uint32_t kDCol = 32 * kStages;
     static constexpr uint32_t kColsUsed = kDCol + kDBufs * kDW;
     static constexpr uint32_t kCols = 512;                  // one CTA per SM
     static_assert(kColsUsed <= kCols, "tile does not fit in tensor memory");
@@ -202,9 +200,11 @@ struct TcCfg {
     static constexpr int kSplit = 1;                        // whole-K units
     static constexpr int kProducer = 4, kMmaWarp = 5;
     static constexpr int kThreads = 192;
-    static constexpr int kBars = 2 * kMaxStages + 2 * kDBufs + 2 * kQ;
+    static constexpr int kBars = 2 * kStages + 2 * kDBufs + 2 * kQ;
     static constexpr size_t kFixedSmem = 1024 + kBars * 8 + 16 + 4 * kQ;   // alignment slack, barriers, queue
-    static size_t smem_bytes(int S) { return kFixedSmem + (size_t)S * kStageBytes; }
+    static constexpr size_t kSmem = kFixedSmem + (size_t)kStages * kStageBytes;
+    // one CTA per SM: 228 KB of shared memory less the 1 KB the system keeps
+    static_assert(kSmem + 1024 <= 228u * 1024u, "ring does not fit in shared memory");
 };
 
 // Epilogue metadata of NBLK column blocks of 16: lane q of block i holds, for
@@ -324,8 +324,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA0,
                   const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmA2, TcArgs args) {
     using C = TcCfg<NMAX, MX>;
-    constexpr int DB = C::kDBufs, NSF = C::kNsf;
-    const int S = args.S;
+    constexpr int DB = C::kDBufs, S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled stages need 1024-byte alignment
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -340,7 +339,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
     // FULL: stage landed.  DONE: the stage's MMAs completed (stage and scale
     // slot free again).  ACCREADY / ACCFREE: accumulator handover.
-    const int FULL = 0, DONE = kMaxStages, ACCREADY = 2 * kMaxStages, ACCFREE = ACCREADY + DB, UQFULL = ACCFREE + DB,
+    const int FULL = 0, DONE = S, ACCREADY = 2 * S, ACCFREE = ACCREADY + DB, UQFULL = ACCFREE + DB,
               UQEMPTY = UQFULL + kQ;
     constexpr int kQueueReaders = 128 + 1;   // the epilogue warps and the MMA thread
     constexpr bool SUSP = false;             // one CTA per SM: plain polling
@@ -557,7 +556,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
         // from lane 0, so the warp holds them uniformly); one elected lane
         // issues the tensor-core instructions.
         uint32_t it = 0, j = 0;
-        RingPos pos, prev_pos;   // stages of iterations it and it - NSF
+        RingPos pos;   // stage of iteration it
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
             const int e = __shfl_sync(0xffffffffu, take_unit(ui, false, ok), 0);
@@ -585,23 +584,16 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
                     ptx::tc_fence_after();
                     int slot, tidx, kb0, nkb;
                     part.group(mt, s, slot, tidx, kb0, nkb);
-                    // the group's scales -> slot it % NSF, once the MMAs of iteration
-                    // it - NSF (the slot's last reader) have completed
-                    if (it >= (uint32_t)NSF) {
-                        if (!wait_warp<SUSP>(bar(DONE + prev_pos.st), prev_pos.ph, abort_flag, args.status, args.wait_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        prev_pos.next(S);
-                    }
-                    const uint32_t sfa = tmem + 32u * (it % NSF);
+                    // the group's scales -> the stage's own slot
+                    const uint32_t sfa = tmem + 32u * st;
                     if (ptx::elect_one()) {
                         ptx::tmem_cp_32x128b_warpx4(
                             sfa, ptx::smem_desc_noswizzle(ptx::smem_addr(sSF + st * kSfAtomBytes), 128, 128));
-                        if (MX) {   // token blocks 0-3 and 4-7 of the tile's block scales
+                        if (MX) {   // token blocks 0-3 and (tiles past 128 rows) 4-7 of the tile's block scales
                             const uint32_t sb = ptx::smem_addr(sSFB + st * C::kSfbStage);
                             ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol, ptx::smem_desc_noswizzle(sb, 128, 128));
-                            ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol + 4, ptx::smem_desc_noswizzle(sb + 512, 128, 128));
+                            if (Nm > 128)
+                                ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol + 4, ptx::smem_desc_noswizzle(sb + 512, 128, 128));
                         }
                         const uint32_t a_addr = ptx::smem_addr(sA + st * C::kAStage);
                         for (int i = 0; i < nkb; ++i) {
@@ -1016,7 +1008,7 @@ int launch_one(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap 
                const TcArgs &args, int blocks, cudaStream_t s) {
     using C = TcCfg<NMAX, MX>;
     auto kern = ffn_tc_kernel<NMAX, PHASE, BANKS, MX>;
-    const size_t smem = C::smem_bytes(args.S);
+    const size_t smem = C::kSmem;
     MOE_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     if (blocks < 1) return MOE_OK;
     kern<<<blocks, C::kThreads, smem, s>>>(mB, mA0, mA1, mA2, args);
@@ -1024,28 +1016,15 @@ int launch_one(const CUtensorMap &mB, const CUtensorMap &mA0, const CUtensorMap 
     return MOE_OK;
 }
 
-constexpr size_t kSmSmem = 228u * 1024u;   // shared memory of one SM
-constexpr size_t kCtaReserve = 1024;       // reserved by the system per resident CTA
-
-struct LaunchPlan {
-    int blocks, S;
-};
-
-// Grid and ring depth of one prefill GEMM launch: one CTA per SM (32 SMs'
-// worth for a cold bank when the layer has both banks, so the two banks'
-// launches run side by side), and a ring as deep as the SM's shared memory
-// allows.
-template <int NMAX, bool MX>
-LaunchPlan plan_for(const moe_ctx *ctx, int b, bool shared, int units_max) {
-    using C = TcCfg<NMAX, MX>;
-    const long per = (long)kSmSmem - (long)kCtaReserve - (long)C::kFixedSmem;
-    LaunchPlan p;
-    p.S = std::max(C::kNsf, std::min(kMaxStages, (int)(per / C::kStageBytes)));
+// Grid of one prefill GEMM launch: one CTA per SM (32 SMs' worth for a cold
+// bank when the layer has both banks, so the two banks' launches run side by
+// side).
+int prefill_blocks(const moe_ctx *ctx, int b, bool shared, int units_max) {
     const int cold_ctas = 32;
-    if (b < 0 || !shared) p.blocks = ctx->sms;
-    else p.blocks = b == MOE_BANK_COLD ? cold_ctas : ctx->sms - cold_ctas;
-    p.blocks = std::max(1, std::min(units_max, p.blocks));
-    return p;
+    int blocks;
+    if (b < 0 || !shared) blocks = ctx->sms;
+    else blocks = b == MOE_BANK_COLD ? cold_ctas : ctx->sms - cold_ctas;
+    return std::max(1, std::min(units_max, blocks));
 }
 
 template <int NMAX, int PHASE, bool MX>
@@ -1063,9 +1042,7 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
     const int P = a1.P;
     a1.ks = std::min(TcCfg<NMAX, MX>::kSplit, a1.part.steps());
     a2.ks = std::min(TcCfg<NMAX, MX>::kSplit, a2.part.steps());
-    const LaunchPlan p1 = plan_for<NMAX, MX>(ctx, a1.b, shared, units1), p2 = plan_for<NMAX, MX>(ctx, a1.b, shared, units2);
-    a1.S = p1.S;
-    a2.S = p2.S;
+    const int blocks1 = prefill_blocks(ctx, a1.b, shared, units1), blocks2 = prefill_blocks(ctx, a1.b, shared, units2);
     const dim3 grid_p(P, a1.b < 0 ? 2 : 1);   // one block per pick (of each bank)
     const int pieces = MX ? 1 : 2;
     CUtensorMap m1, m2;
@@ -1095,7 +1072,7 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
     // where no pool exists: then no unit reads them)
     const CUtensorMap &sm1 = ctx->stage_pool ? ctx->stage_map[0] : layer.wmap[1][0];
     const CUtensorMap &sm2 = ctx->stage_pool ? ctx->stage_map[1] : layer.wmap[1][1];
-    if (int r = launch_gemm<NMAX, 1, MX>(m1, layer.wmap[0][0], layer.wmap[1][0], sm1, a1, p1.blocks, s)) return r;
+    if (int r = launch_gemm<NMAX, 1, MX>(m1, layer.wmap[0][0], layer.wmap[1][0], sm1, a1, blocks1, s)) return r;
     if (MX) {
         prep_h_mx8_kernel<<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
                                                  ws + lay.hq, (int32_t *)(ws + lay.hexp),
@@ -1106,7 +1083,7 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
                                                     (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
     }
     MOE_LAUNCH_CHECK();
-    if (int r = launch_gemm<NMAX, 2, MX>(m2, layer.wmap[0][1], layer.wmap[1][1], sm2, a2, p2.blocks, s)) return r;
+    if (int r = launch_gemm<NMAX, 2, MX>(m2, layer.wmap[0][1], layer.wmap[1][1], sm2, a2, blocks2, s)) return r;
     if (!a2.y_out) return MOE_OK;
     round_y_kernel<<<grid_p, 256, 0, s>>>(a2.lists[0], a2.lists[1], a2.b, g.H, a2.y_out, a2.Y);
     MOE_LAUNCH_CHECK();
