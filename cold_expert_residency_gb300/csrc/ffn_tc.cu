@@ -39,8 +39,8 @@
 //             row's power of two undone, then SwiGLU (gate and up rows meet
 //             in lanes l and l^16) or the bf16 row.  Two accumulators, so a
 //             tile's epilogue overlaps the next tile's MMAs.
-// Prefill tiles (192 tokens) run one CTA per SM; the ring's depth is set per
-// launch from the SM's shared memory.
+// Prefill tiles (144 tokens with two-piece rows, 160 with MXFP8 rows) run one
+// CTA per SM, the ring as deep as shared and tensor memory allow.
 //
 // The arithmetic of a pick depends only on its expert's weights, its token
 // row and the step's token count (which fixes the tile), never on the bank,
@@ -182,9 +182,16 @@ struct TcCfg {
     // Ring stages, each with its own scale slot in tensor memory: stage s's
     // scales are copied into slot s, so a slot is rewritten only after the
     // producer has seen the stage's previous MMAs complete (the MMA warp
-    // needs no wait of its own).  As many stages as shared memory holds,
-    // up to what tensor memory leaves for slots beside the accumulators.
-    static constexpr int kStages = MX ? 4 : 3;
+    // needs no wait of its own).  As many stages as shared memory holds (one
+    // CTA per SM: 227 KB, less alignment slack, barriers and a few static
+    // words), up to what tensor memory leaves for 32-column slots beside the
+    // accumulators.
+    static constexpr size_t kFixedSmem = 1024 + (2 * 8 + 2 * kDBufs + 2 * kQ) * 8 + 16 + 4 * kQ + 64;
+    static constexpr int kSmemStages = (int)((227u * 1024u - kFixedSmem) / kStageBytes);
+    static constexpr int kTmemStages = (512 - kDBufs * kDW) / 32;
+    static constexpr int kStages = kSmemStages < kTmemStages ? (kSmemStages < 8 ? kSmemStages : 8)
+                                                             : (kTmemStages < 8 ? kTmemStages : 8);
+    static_assert(kStages >= 2, "ring too shallow");
     // Tensor memory columns: slot i's A scales at 32 i (four columns written
     // by tcgen05.cp); slot 0's block also holds the constant B scale columns
     // of piece 0 at +8 and of piece 1 at +16 -- in the MXFP8 format, slot i's
@@ -201,10 +208,8 @@ struct TcCfg {
     static constexpr int kProducer = 4, kMmaWarp = 5;
     static constexpr int kThreads = 192;
     static constexpr int kBars = 2 * kStages + 2 * kDBufs + 2 * kQ;
-    static constexpr size_t kFixedSmem = 1024 + kBars * 8 + 16 + 4 * kQ;   // alignment slack, barriers, queue
-    static constexpr size_t kSmem = kFixedSmem + (size_t)kStages * kStageBytes;
-    // one CTA per SM: 228 KB of shared memory less the 1 KB the system keeps
-    static_assert(kSmem + 1024 <= 228u * 1024u, "ring does not fit in shared memory");
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBars * 8 + 16 + 4 * kQ;
+    static_assert(kSmem + 64 <= 227u * 1024u, "ring does not fit in shared memory");
 };
 
 // Epilogue metadata of NBLK column blocks of 16: lane q of block i holds, for
@@ -828,7 +833,7 @@ __global__ void __launch_bounds__(256) round_y_kernel(BankLists L0, BankLists L1
 // ---------------------------------------------------------------------------
 
 // The first prefill tile of each active row, per bank: tile_off[b][a] =
-// sum over a' < a of ceil(n_a' / 192); tile_off[b][n_act] = the bank's tiles.
+// sum over a' < a of ceil(n_a' / kPrefillTileMx); tile_off[b][n_act] = the bank's tiles.
 // One warp per bank.
 __global__ void __launch_bounds__(64) tile_scan_kernel(BankLists L0, BankLists L1, int b0, int P, int32_t *tile_off) {
     const int b = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -840,7 +845,7 @@ __global__ void __launch_bounds__(64) tile_scan_kernel(BankLists L0, BankLists L
     for (int base = 0; base < na; base += 32) {
         const int a = base + lane;
         const int n = a < na ? L.act_off[a + 1] - L.act_off[a] : 0;
-        const int t = (n + kPrefillTile - 1) / kPrefillTile;
+        const int t = (n + kPrefillTileMx - 1) / kPrefillTileMx;
         int incl = t;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -885,8 +890,8 @@ __device__ __forceinline__ void pick_tile(const BankLists &L, int b, int p, cons
         else hi = mid - 1;
     }
     const int q = p - L.act_off[lo];
-    tile = tile_off[(size_t)b * (P + 1) + lo] + q / kPrefillTile;
-    r = q % kPrefillTile;
+    tile = tile_off[(size_t)b * (P + 1) + lo] + q / kPrefillTileMx;
+    r = q % kPrefillTileMx;
 }
 
 // Byte of a tile's block-scale slab holding token row r's scale for K block
@@ -1249,7 +1254,7 @@ int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int b, const uint16_t *x, in
     a1.stage_pool = nullptr;
     if (ctx->stage_slots > 0 && layer.n_cold > 0 && a1.b != MOE_BANK_HOT && T > 16) {
         int32_t *slot_of = (int32_t *)(ws + lay.stage_slot);
-        if (int r = launch_cold_staging(ctx, layer, tile_width(T), a1.lists[1], slot_of,
+        if (int r = launch_cold_staging(ctx, layer, tile_width(T, ctx->act_format == MOE_ACT_MXFP8), a1.lists[1], slot_of,
                                         (int32_t *)(ws + lay.stage_src), s))
             return r;
         a1.stage_slot = slot_of;
@@ -1270,18 +1275,19 @@ int launch_ffn_tc(moe_ctx *ctx, const Layer &layer, int b, const uint16_t *x, in
     a2.y_out = split ? (float *)(ws + lay.y32) : nullptr;
 
     const int units1 = 4 * P * g.mt13, units2 = 4 * P * g.mt2;   // bound: active rows never exceed the picks
-    // The token-tile width depends only on T, so an expert's arithmetic is
-    // the same in either bank.  Decode-sized steps use narrow tiles (8, 16 or
-    // 32 tokens; an expert with more tokens loops over token tiles) in the
-    // decode-tile kernel, which keeps more weight bytes in flight per SM;
-    // prefill-sized steps use 192-wide tiles (an expert's ~T*k/E tokens in
-    // one tile) in the shared-memory-A kernel, one CTA per SM.
+    // The token-tile width depends only on T (and the activation format), so
+    // an expert's arithmetic is the same in either bank.  Decode-sized steps
+    // use narrow tiles (8, 16 or 32 tokens; an expert with more tokens loops
+    // over token tiles) in the decode-tile kernel, which keeps more weight
+    // bytes in flight per SM; prefill-sized steps use 144- or 160-wide tiles
+    // (an 8192-token step's ~128 tokens per expert in one tile) in the
+    // shared-memory-A kernel, one CTA per SM.
     const bool cold_rows = layer.n_cold > 0;
     if (T <= 8) return launch_bank_decode<8>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
     if (T <= 16) return launch_bank_decode<16>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
     if (T <= kNarrowMaxT) return launch_bank_decode<32>(ctx, shared, cold_rows, a1, a2, units1, units2, x, lay, ws, s);
     if (ctx->act_format == MOE_ACT_MXFP8)
-        return launch_bank<kPrefillTile, true>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
+        return launch_bank<kPrefillTileMx, true>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
     return launch_bank<kPrefillTile, false>(ctx, layer, shared, a1, a2, units1, units2, x, lay, ws, s);
 }
 

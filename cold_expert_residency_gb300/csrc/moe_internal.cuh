@@ -141,19 +141,25 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 constexpr int kNarrowMaxT = 256;
 inline bool split_k_steps(int T) { return T <= kNarrowMaxT; }
 
-// Token rows per prefill tile, and the bytes of one K group's B-operand
-// block scales of one tile in the MXFP8 format: two 32-row x 16-byte atoms,
-// row l of atom c holding tokens 32*(4c + q) + l (q = 0..3), 4 bytes each
-// (the group's four 32-wide K blocks) -- what tcgen05.cp puts where the
-// block-scaled MMA reads token n's scale (column n/32, lane n%32).
-constexpr int kPrefillTile = 192;
+// Token rows per prefill tile: 144 with two e4m3 pieces per value (a ring of
+// four 53 KB stages), 160 in the MXFP8 format (six 38 KB stages); an expert
+// with more picks takes further tiles.  And the bytes of one K group's
+// B-operand block scales of one tile in the MXFP8 format: two 32-row x
+// 16-byte atoms, row l of atom c holding tokens 32*(4c + q) + l (q = 0..3),
+// 4 bytes each (the group's four 32-wide K blocks) -- what tcgen05.cp puts
+// where the block-scaled MMA reads token n's scale (column n/32, lane n%32).
+constexpr int kPrefillTile = 144;
+constexpr int kPrefillTileMx = 160;
 constexpr int kSfbGroupBytes = 1024;
 
 // Slots of a context's cold-staging pool, at most.
 constexpr int kMaxStageSlots = 64;
 
-// Token rows per tile of the FFN kernels for a step of T tokens.
-inline int tile_width(int T) { return T <= 8 ? 8 : T <= 16 ? 16 : T <= kNarrowMaxT ? 32 : kPrefillTile; }
+// Token rows per tile of the FFN kernels for a step of T tokens (mx: the
+// MXFP8 activation format).
+inline int tile_width(int T, bool mx) {
+    return T <= 8 ? 8 : T <= 16 ? 16 : T <= kNarrowMaxT ? 32 : (mx ? kPrefillTileMx : kPrefillTile);
+}
 
 inline WsLayout ws_layout(const Geom &g, int T) {
     WsLayout w;
@@ -178,9 +184,9 @@ inline WsLayout ws_layout(const Geom &g, int T) {
     w.y32 = take(ks * P * (size_t)g.H * 4);     // [P][H] down-GEMM sums, by slot
     w.claim = take(2 * 1024 * 4);               // [GEMM][SM] first-CTA claims of a launch over both banks
     // prefill tiles, MXFP8 format: a bank's tiles are at most one per active
-    // row (<= min(P, E) rows) plus P / 192
+    // row (<= min(P, E) rows) plus P / kPrefillTileMx
     const size_t wide = split_k_steps(T) ? 0 : 1;
-    w.max_tiles = (int)(wide * (std::min<size_t>(P, (size_t)g.E) + P / kPrefillTile + 1));
+    w.max_tiles = (int)(wide * (std::min<size_t>(P, (size_t)g.E) + P / kPrefillTileMx + 1));
     w.tile_off = take(wide * 2 * (P + 1) * 4);  // [2][P+1] int32
     w.sfx = take((size_t)2 * w.max_tiles * (g.H / kKG) * kSfbGroupBytes);
     w.sfh = take((size_t)2 * w.max_tiles * ((g.I + kKG - 1) / kKG) * kSfbGroupBytes);

@@ -142,8 +142,9 @@ int moe_workspace_bytes(const moe_ctx *ctx, int T, size_t *bytes);
 /* Big-batch cold staging ("We Built the Counter", section 6: copying an
  * expert on a miss is a tool for big batches; "Should a GB300 Prefetch Its
  * Cold Experts?", section 6: staging offloaded experts for prefill-sized
- * steps).  The FFN streams a unit's weights once per token tile (8, 16, 32
- * or 192 tokens by step size), so a cold expert with picks in several tiles
+ * steps).  The FFN streams a unit's weights once per token tile (8, 16 or
+ * 32 tokens by step size; on steps of more than 256 tokens 144, or 160 in
+ * the MXFP8 format), so a cold expert with picks in several tiles
  * would cross the host link once per tile.  With a pool of `slots` expert
  * rows in HBM (0..64; 0 frees it and turns staging off, the default), every
  * later FFN call that covers the cold bank of a step of more than 16 tokens

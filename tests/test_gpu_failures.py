@@ -6,7 +6,7 @@
   issued copies land, free its tensor memory and return; the call ends, the
   status word reads MOE_ETIMEOUT, and the next step (default bound) equals a
   clean step bit for bit.  Each FFN kernel is covered: 8- and 32-token decode
-  tiles and the 192-token prefill tile, over both banks and one bank.
+  tiles and the 144-token prefill tile, over both banks and one bank.
 - Allocation failures ("a host-memory floor instead of an out-of-memory
   kill"): with MOE_INJECT_ALLOC_FAIL naming an allocation site,
   moe_init_banks returns MOE_ENOMEM, leaves the layer unplaced and holds no

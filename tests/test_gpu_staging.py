@@ -5,7 +5,7 @@ domain shift), so a step routes more picks to some cold experts than one
 token tile holds.  With a staging pool those rows are copied once into HBM
 and read from there.  Checked:
 - the rows of Y and the layer output are bit-identical to the unstaged step
-  and to an all-HBM placement, for 32-token and 192-token tiles, both
+  and to an all-HBM placement, for 32-token and prefill-sized tiles, both
   activation formats, one call over both banks and two calls on two streams;
 - the device picks the rows the rule names: cold active rows with more picks
   than one tile, most picks first, ties to the lower row, at most the pool's
@@ -37,12 +37,12 @@ def _popular_cold(cfg):
     return (rank > 4).astype(np.uint8)
 
 
-def _expected_stage(h, lg, T, slots):
+def _expected_stage(h, lg, T, slots, fmt=0):
     cfg = h.cfg
     ids, _ = oracle.route(lg, cfg.k)
     rm = h.moe.moe_get_rowmap(h.ctx, 0, cfg.E)
     cold = oracle.split(rm, ids)[1]
-    W = 8 if T <= 8 else 16 if T <= 16 else 32 if T <= 256 else 192
+    W = 8 if T <= 8 else 16 if T <= 16 else 32 if T <= 256 else (160 if fmt else 144)
     n = np.diff(cold["act_off"])
     cand = [(-int(c), a) for a, c in enumerate(n) if c > W]
     cand.sort()
@@ -66,7 +66,7 @@ def test_staged_rows_are_bit_identical(T, fmt):
         lg = synth.router_logits(cfg, 0, 3, T=T)
         x = synth.activations(cfg, 0, 3, T=T)
         a = staged.run(0, lg, x)
-        exp_rows, n_cand = _expected_stage(staged, lg, T, 8)
+        exp_rows, n_cand = _expected_stage(staged, lg, T, 8, fmt)
         assert n_cand > 0, "the workload should route several tiles to a cold expert"
         got_rows = moe.moe_read_stage(staged.ctx, staged.step.buf.ws_ptr, T)
         assert got_rows.tolist() == exp_rows

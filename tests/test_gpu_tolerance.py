@@ -52,7 +52,7 @@ UNIT_CASES = [("tiny", 8, 5, 4), ("tiny", 2048, 5, 5), ("decode1", 7, 7, 6)]
 
 @pytest.mark.parametrize("name,T,s13,s2", UNIT_CASES)
 def test_unit_scale_literal_tolerance(name, T, s13, s2):
-    """tiny: 8-token tiles; tiny at 2048 tokens: full 192-token tiles plus a
+    """tiny: 8-token tiles; tiny at 2048 tokens: full 144-token tiles plus a
     ragged one per expert; decode1: the one-user step at full geometry."""
     cfg = synth.get_config(name, T=T, w13_scale_shift=s13, w2_scale_shift=s2)
     h = Harness(cfg)
@@ -88,7 +88,7 @@ def _check_bound(h, res, x, slots, what):
 @pytest.mark.parametrize("T", [8, 40, 300])
 def test_per_element_bound_tiny(T):
     """Every element of every routed row (T = 8: 8-token tiles; 40: 32-token
-    tiles; 300: 192-token tiles) within its bound."""
+    tiles; 300: 144-token tiles) within its bound."""
     cfg = synth.get_config("tiny", T=T)
     h = Harness(cfg)
     try:
