@@ -186,7 +186,7 @@ struct TcCfg {
     // CTA per SM: 227 KB, less alignment slack, barriers and a few static
     // words), up to what tensor memory leaves for 32-column slots beside the
     // accumulators.
-    static constexpr size_t kFixedSmem = 1024 + (2 * 8 + 2 * kDBufs + 2 * kQ) * 8 + 16 + 4 * kQ + 64;
+    static constexpr size_t kFixedSmem = 1024 + (2 * 8 + 2 * kDBufs + 2 * kQ) * 8 + 16 + 16 * kQ + 64;
     static constexpr int kSmemStages = (int)((227u * 1024u - kFixedSmem) / kStageBytes);
     static constexpr int kTmemStages = (512 - kDBufs * kDW) / 32;
     static constexpr int kStages = kSmemStages < kTmemStages ? (kSmemStages < 8 ? kSmemStages : 8)
@@ -208,7 +208,7 @@ struct TcCfg {
     static constexpr int kProducer = 4, kMmaWarp = 5;
     static constexpr int kThreads = 192;
     static constexpr int kBars = 2 * kStages + 2 * kDBufs + 2 * kQ;
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBars * 8 + 16 + 4 * kQ;
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBars * 8 + 16 + 16 * kQ;
     static_assert(kSmem + 64 <= 227u * 1024u, "ring does not fit in shared memory");
 };
 
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
     uint64_t *bars = (uint64_t *)(sSFB + S * C::kSfbStage);
     uint32_t *holder = (uint32_t *)(bars + C::kBars);
     volatile int *abort_flag = (volatile int *)(holder + 1);
-    volatile int *uq = (volatile int *)(holder + 2);   // [kQ] unit queue
+    volatile int *uq = (volatile int *)(holder + 4);   // [kQ][4] unit queue
     auto bar = [&](int i) { return ptx::smem_addr(bars + i); };
     // FULL: stage landed.  DONE: the stage's MMAs completed (stage and scale
     // slot free again).  ACCREADY / ACCFREE: accumulator handover.
@@ -413,21 +413,34 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
     const int ns = part.steps();
     auto units_of = [&](int bk) { return args.lists[0].hdr[kHdrNAct + bk] * part.tiles * args.ks; };
 
-    // every role but the producer reads the unit sequence from the queue:
-    // entry 2u + bank (unit u of that bank), or -1 at the end.  The epilogue
-    // warps wait with a suspend hint (a spinning warp takes issue slots from
-    // the producer and MMA warps that share its scheduler); the MMA warp
-    // spins, and only its lane 0 counts as a reader.
-    auto take_unit = [&](uint32_t ui, bool epilogue, bool &ok) -> int {
+    // every role but the producer reads the unit sequence from the queue.
+    // An entry is the unit as the producer resolved it: 2u + bank (unit u
+    // of that bank, -1 at the end), its token count n, its first pick p0 and
+    // its M-tile and K-step range -- so the other roles load nothing to
+    // start a unit.  The epilogue warps wait with a suspend hint (a spinning
+    // warp takes issue slots from the producer and MMA warps that share its
+    // scheduler); the MMA warp spins, and only its lane 0 counts as a reader.
+    struct Unit {
+        int e, n, p0, mt, s0, s1;
+    };
+    auto take_unit = [&](uint32_t ui, bool epilogue, bool &ok) -> Unit {
         const int qs = ui % kQ;
         const uint32_t ph = (ui / kQ) & 1;
         const bool w = epilogue ? wait_warp<true>(bar(UQFULL + qs), ph, abort_flag, args.status, args.wait_ns)
                                 : wait_warp<SUSP>(bar(UQFULL + qs), ph, abort_flag, args.status, args.wait_ns);
+        Unit u{-1, 0, 0, 0, 0, 0};
         if (!w) {
             ok = false;
-            return -1;
+            return u;
         }
-        const int u = uq[qs];
+        // lane 0's reads, so the warp holds the values uniformly
+        u.e = __shfl_sync(0xffffffffu, uq[4 * qs + 0], 0);
+        u.n = __shfl_sync(0xffffffffu, uq[4 * qs + 1], 0);
+        u.p0 = __shfl_sync(0xffffffffu, uq[4 * qs + 2], 0);
+        const int r = __shfl_sync(0xffffffffu, uq[4 * qs + 3], 0);
+        u.mt = r & 0xFF;
+        u.s0 = (r >> 8) & 0xFF;
+        u.s1 = r >> 16;
         if (epilogue || lane == 0) ptx::mbar_arrive(bar(UQEMPTY + qs));
         return u;
     };
@@ -440,14 +453,12 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
         uint32_t j = 0;
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
-            const int e = take_unit(ui, true, ok);
-            if (e < 0) break;
-            const int bk = e & 1;
+            const Unit un = take_unit(ui, true, ok);
+            if (un.e < 0) break;
+            const int bk = un.e & 1;
             const BankLists &L = args.lists[bk];
             const int goff = bank_offset(L, bk, args.P);
-            int a, mt, s0, s1;
-            unit_pos(e >> 1, part.tiles, ns, args.ks, a, mt, s0, s1);
-            const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
+            const int mt = un.mt, p0 = un.p0, n = un.n;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
                 int rs[NB];
@@ -497,18 +508,25 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
                 if (u < units_of(1 - pref)) e = 2 * u + (1 - pref);
                 else dry_other = true;
             }
-            uq[qs] = e;
-            ptx::mbar_arrive(bar(UQFULL + qs));
-            if (e < 0) break;
+            if (e < 0) {
+                uq[4 * qs] = -1;
+                ptx::mbar_arrive(bar(UQFULL + qs));
+                break;
+            }
             const int bk = e & 1;
             const BankLists &L = args.lists[bk];
             const int goff = bank_offset(L, bk, args.P);
             int a, mt, s0, s1;
             unit_pos(e >> 1, part.tiles, ns, args.ks, a, mt, s0, s1);
+            const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
+            uq[4 * qs + 0] = e;
+            uq[4 * qs + 1] = n;
+            uq[4 * qs + 2] = p0;
+            uq[4 * qs + 3] = mt | (s0 << 8) | (s1 << 16);
+            ptx::mbar_arrive(bar(UQFULL + qs));
             // a staged cold row is read from its pool slot (tmA2), not the host bank
             const int sslot = staged_slot(args, bk, a);
             const int row = sslot >= 0 ? sslot : L.act_row[a];
-            const int p0 = L.act_off[a], n = L.act_off[a + 1] - p0;
             const CUtensorMap *tmA = sslot >= 0 ? &tmA2 : (bk ? &tmA1 : &tmA0);
             const uint8_t *expert = (sslot >= 0 ? args.stage_pool : args.bank[bk]) + (int64_t)row * args.eb;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX) {
@@ -557,19 +575,18 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
         }
     } else if (warp == C::kMmaWarp) {
         // ----------------------------------------------------------- MMA issue
-        // The whole warp runs the loop (values read from memory are taken
-        // from lane 0, so the warp holds them uniformly); one elected lane
-        // issues the tensor-core instructions.
+        // The whole warp runs the loop (holding the unit's values uniformly);
+        // one elected lane issues the tensor-core instructions.  Once a
+        // stage has landed, that lane keeps issuing the following groups
+        // whose stages have landed too (a non-blocking check each), so the
+        // per-group handshakes of the warp are paid once per burst.
         uint32_t it = 0, j = 0;
         RingPos pos;   // stage of iteration it
         bool ok = true;
         for (uint32_t ui = 0; ok; ++ui) {
-            const int e = __shfl_sync(0xffffffffu, take_unit(ui, false, ok), 0);
-            if (e < 0) break;
-            const BankLists &L = args.lists[e & 1];
-            int a, mt, s0, s1;
-            unit_pos(e >> 1, part.tiles, ns, args.ks, a, mt, s0, s1);
-            const int n = __shfl_sync(0xffffffffu, L.act_off[a + 1] - L.act_off[a], 0);
+            const Unit un = take_unit(ui, false, ok);
+            if (un.e < 0) break;
+            const int mt = un.mt, s0 = un.s0, s1 = un.s1, n = un.n;
             for (int n0 = 0; ok && n0 < n; n0 += NMAX, ++j) {
                 const int nn = min(NMAX, n - n0);
                 const int Nr = (nn + C::kRowQ - 1) / C::kRowQ * C::kRowQ;
@@ -583,43 +600,57 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + C::kDCol + db * C::kDW;
-                for (int s = s0; s < s1; ++s, ++it, pos.next(S)) {
-                    const int st = pos.st;
-                    if (!wait_warp<SUSP>(bar(FULL + st), pos.ph, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
+                for (int s = s0; s < s1;) {
+                    if (!wait_warp<SUSP>(bar(FULL + pos.st), pos.ph, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    int slot, tidx, kb0, nkb;
-                    part.group(mt, s, slot, tidx, kb0, nkb);
-                    // the group's scales -> the stage's own slot
-                    const uint32_t sfa = tmem + 32u * st;
+                    int issued = 0;
                     if (ptx::elect_one()) {
-                        ptx::tmem_cp_32x128b_warpx4(
-                            sfa, ptx::smem_desc_noswizzle(ptx::smem_addr(sSF + st * kSfAtomBytes), 128, 128));
-                        if (MX) {   // token blocks 0-3 and (tiles past 128 rows) 4-7 of the tile's block scales
-                            const uint32_t sb = ptx::smem_addr(sSFB + st * C::kSfbStage);
-                            ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol, ptx::smem_desc_noswizzle(sb, 128, 128));
-                            if (Nm > 128)
-                                ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol + 4, ptx::smem_desc_noswizzle(sb + 512, 128, 128));
-                        }
-                        const uint32_t a_addr = ptx::smem_addr(sA + st * C::kAStage);
-                        for (int i = 0; i < nkb; ++i) {
-                            const int kb = kb0 + i;   // K block of the group (A bytes kb*32.., scale byte kb)
-                            const uint64_t ad = ptx::smem_desc_sw128(a_addr + kb * 32);
-                            // this tile's chunk i/2 of the group, its K block i%2
-                            const uint32_t b_addr = ptx::smem_addr(sB + st * C::kBStage + (i >> 1) * C::kBChunk) + (i & 1) * 32;
-#pragma unroll
-                            for (int pc = 0; pc < (C::kStack ? 1 : C::kPieces); ++pc) {   // e4m3 piece of B (unstacked tiles)
-                                const uint64_t bd = ptx::smem_desc_sw64(b_addr + pc * NMAX * 64);
-                                if (MX)   // B's scale: byte i (the token rows' K block) of the slot's own columns
-                                    ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29) | ((uint32_t)i << 4), sfa,
-                                                         sfa + C::kSfbCol, (s != s0) | i);
-                                else
-                                    ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29), sfa,
-                                                         tmem + C::kSfbCol + pc * C::kSfbStride, (s != s0) | i | pc);
+                        RingPos p = pos;
+                        for (int ss = s;;) {
+                            const int st = p.st;
+                            int slot, tidx, kb0, nkb;
+                            part.group(mt, ss, slot, tidx, kb0, nkb);
+                            // the group's scales -> the stage's own slot
+                            const uint32_t sfa = tmem + 32u * st;
+                            ptx::tmem_cp_32x128b_warpx4(
+                                sfa, ptx::smem_desc_noswizzle(ptx::smem_addr(sSF + st * kSfAtomBytes), 128, 128));
+                            if (MX) {   // token blocks 0-3 and (tiles past 128 rows) 4-7 of the tile's block scales
+                                const uint32_t sb = ptx::smem_addr(sSFB + st * C::kSfbStage);
+                                ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol, ptx::smem_desc_noswizzle(sb, 128, 128));
+                                if (Nm > 128)
+                                    ptx::tmem_cp_32x128b_warpx4(sfa + C::kSfbCol + 4,
+                                                                ptx::smem_desc_noswizzle(sb + 512, 128, 128));
                             }
+                            const uint32_t a_addr = ptx::smem_addr(sA + st * C::kAStage);
+                            for (int i = 0; i < nkb; ++i) {
+                                const int kb = kb0 + i;   // K block of the group (A bytes kb*32.., scale byte kb)
+                                const uint64_t ad = ptx::smem_desc_sw128(a_addr + kb * 32);
+                                // this tile's chunk i/2 of the group, its K block i%2
+                                const uint32_t b_addr =
+                                    ptx::smem_addr(sB + st * C::kBStage + (i >> 1) * C::kBChunk) + (i & 1) * 32;
+#pragma unroll
+                                for (int pc = 0; pc < (C::kStack ? 1 : C::kPieces); ++pc) {   // e4m3 piece of B
+                                    const uint64_t bd = ptx::smem_desc_sw64(b_addr + pc * NMAX * 64);
+                                    if (MX)   // B's scale: byte i (the token rows' K block) of the slot's own columns
+                                        ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29) | ((uint32_t)i << 4),
+                                                             sfa, sfa + C::kSfbCol, (ss != s0) | i);
+                                    else
+                                        ptx::mma_mxf8f6f4_ss(d_tmem, ad, bd, idesc0 | ((uint32_t)kb << 29), sfa,
+                                                             tmem + C::kSfbCol + pc * C::kSfbStride, (ss != s0) | i | pc);
+                                }
+                            }
+                            ptx::mma_commit(bar(DONE + st));
+                            ++issued;
+                            ++ss;
+                            p.next(S);
+                            if (ss >= s1 || !ptx::mbar_test_wait(bar(FULL + p.st), p.ph)) break;
+                            ptx::tc_fence_after();
                         }
-                        ptx::mma_commit(bar(DONE + st));
                     }
-                    __syncwarp();
+                    issued = __reduce_max_sync(0xffffffffu, issued);
+                    s += issued;
+                    it += issued;
+                    for (int k = 0; k < issued; ++k) pos.next(S);
                 }
                 if (!ok) break;
                 if (ptx::elect_one()) ptx::mma_commit(bar(ACCREADY + db));
