@@ -569,6 +569,34 @@ class StepRunner:
             ts.append(ev0.elapsed_time(ev1) * 1e3)
         return ts
 
+    def call_alone_us(self, call, n):
+        """µs of one call alone: events captured inside a replayed graph just
+        around it (so the graph's launch is outside the timed span), after an
+        L2 flush; plain stream events when graphs cannot hold events."""
+        S, torch = self.S, self.S.torch
+        ea = (S.event(), S.event())
+        g = None
+        if self.graph is not None and S.in_graph_events:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=S.main):
+                ea[0].record(S.main)
+                call()
+                ea[1].record(S.main)
+        ts = []
+        for i in range(n):
+            self.load_inputs(i, S.main)
+            with torch.cuda.stream(S.main):
+                S.flush.zero_()
+                if g is not None:
+                    g.replay()
+                else:
+                    ea[0].record(S.main)
+                    call()
+                    ea[1].record(S.main)
+            S.main.synchronize()
+            ts.append(ea[0].elapsed_time(ea[1]) * 1e3)
+        return ts
+
     def bank_alone_ms(self, layer_idx, bank, n):
         """One FFN call over `bank` of one layer after its routing, with events
         around the call inside a replayed graph; returns (ms list, distinct
@@ -693,16 +721,16 @@ def measure_decode1(S, ctx, cfg, masks, args, layer=0, want_breakdown=True):
     if want_breakdown and run.graph is not None:
         b = run.steps[0].buf
         moe = S.moe
-        route_us = run.replay_graph_us(lambda: moe.moe_route_split_count(
+        route_us = run.call_alone_us(lambda: moe.moe_route_split_count(
             ctx, layer, b.logits, T, run.count_on, b.ids, b.w, b.ws_ptr, S.main), n)
         wr = S.torch.from_numpy(synth.router_weights(cfg, 0).view(np.int16)).to(S.dev)
         bias = S.torch.from_numpy(synth.router_bias(cfg, 0)).to(S.dev)
         lo = S.torch.empty((T, cfg.E), dtype=S.torch.float32, device=S.dev)
-        router_us = run.replay_graph_us(lambda: moe.moe_router_logits(ctx, b.x, wr, bias, T, cfg.E, cfg.H, lo, S.main), n)
+        router_us = run.call_alone_us(lambda: moe.moe_router_logits(ctx, b.x, wr, bias, T, cfg.E, cfg.H, lo, S.main), n)
         cold_ms = run.bank_alone_ms(0, moe.MOE_BANK_COLD, n)
         out["breakdown"] = {"route_us": float(np.mean(route_us)), "router_gemm_us": float(np.mean(router_us)),
                             "hot_alone_us": float(np.mean(hot_ms)) * 1e3, "cold_alone_us": float(np.mean(cold_ms)) * 1e3,
-                            "note": "graph-replayed after an L2 flush: the routing call alone, the router GEMM "
+                            "note": "in-graph events after an L2 flush: the routing call alone, the router GEMM "
                                     "(hidden states -> logits, outside the step) alone, each bank's FFN call "
                                     "alone after routing"}
         if run.count_on:

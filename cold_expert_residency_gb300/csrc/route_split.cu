@@ -60,47 +60,48 @@ __device__ __forceinline__ void load_logits(const float *__restrict__ l, int E, 
     }
 }
 
-// One warp routes one token from its logits in registers.  Each lane keeps
-// the best KM of its own values in a sorted register list; the warp then
-// takes k rounds of an argmax over the lanes' list heads, and the winning lane
-// pops its head.  NaN logits arrive as -infinity (ranked below every number,
-// weight exp(-inf) = 0 beside a finite first pick), so the k ids are always
-// valid.  Then fp32 softmax over the k picks, shifted by the first and summed
-// in pick order.  Lane j < k returns pick j in (*id_out, *w_out); other lanes
-// return -1.
+// One warp routes one token from its logits in registers, in k rounds: each
+// lane takes the best of its values not yet picked (a pairwise tree, lower
+// expert id on equal values), a butterfly takes the best over the lanes, and
+// the lane that held it marks it picked.  NaN logits arrive as -infinity
+// (ranked below every number, weight exp(-inf) = 0 beside a finite first
+// pick), so the k ids are always valid.  Then fp32 softmax over the k picks,
+// shifted by the first and summed in pick order.  Lane j < k returns pick j in
+// (*id_out, *w_out); other lanes return -1.
 template <int KM, int NV>
 __device__ __forceinline__ void warp_route_token(const float (&v)[NV], int E, int k, int lane, int *id_out,
                                                  float *w_out) {
-    float lv[KM];
-    int le[KM];
+    uint32_t taken = 0;   // bit i: value i of this lane picked, or past E
 #pragma unroll
-    for (int j = 0; j < KM; ++j) {
-        lv[j] = -INFINITY;
-        le[j] = INT_MAX;
-    }
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        float cv = v[i];
-        int ce = lane + 32 * i < E ? lane + 32 * i : INT_MAX;
-#pragma unroll
-        for (int j = 0; j < KM; ++j) {   // insert, pushing the worse entries down
-            if (better(cv, ce, lv[j], le[j])) {
-                const float tv = lv[j];
-                const int te = le[j];
-                lv[j] = cv;
-                le[j] = ce;
-                cv = tv;
-                ce = te;
-            }
-        }
-    }
+    for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i >= E) taken |= 1u << i;
     float sel_v[KM];
     int sel_e[KM];
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
         if (j < k) {
-            float bv = lv[0];
-            int be = le[0];
+            // this lane's best unpicked value: a tree over (value, index), the
+            // lower index on equal values (its expert id is lower too)
+            float tv[NV];
+            int ti[NV];
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const bool free_i = !((taken >> i) & 1u);
+                tv[i] = free_i ? v[i] : -INFINITY;
+                ti[i] = free_i ? i : NV + i;   // picked values lose every tie
+            }
+#pragma unroll
+            for (int w = 1; w < NV; w <<= 1) {
+#pragma unroll
+                for (int i = 0; i + w < NV; i += 2 * w) {
+                    if (tv[i + w] > tv[i] || (tv[i + w] == tv[i] && ti[i + w] < ti[i])) {
+                        tv[i] = tv[i + w];
+                        ti[i] = ti[i + w];
+                    }
+                }
+            }
+            float bv = tv[0];
+            int be = ti[0] < NV ? lane + 32 * ti[0] : INT_MAX;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
@@ -110,15 +111,7 @@ __device__ __forceinline__ void warp_route_token(const float (&v)[NV], int E, in
                     be = oe;
                 }
             }
-            if (be == le[0]) {   // this lane held the winner: pop its head
-#pragma unroll
-                for (int q = 0; q + 1 < KM; ++q) {
-                    lv[q] = lv[q + 1];
-                    le[q] = le[q + 1];
-                }
-                lv[KM - 1] = -INFINITY;
-                le[KM - 1] = INT_MAX;
-            }
+            if ((be & 31) == lane && be != INT_MAX) taken |= 1u << (be >> 5);   // this lane held the pick
             sel_v[j] = bv;
             sel_e[j] = be;
         }
@@ -145,10 +138,12 @@ __device__ __forceinline__ void warp_route_token(const float (&v)[NV], int E, in
     *w_out = myw;
 }
 
-// Route token t from logits in registers and write its picks.
+// Route token t from logits in registers and write its picks (and, in the
+// one-CTA path, each pick's expert and the token's bit in its expert's token
+// mask in shared memory).
 template <int KM, int NV>
 __device__ __forceinline__ void route_one(const float (&v)[NV], int t, int E, int k, int lane, int32_t *counts,
-                                          int32_t *ids, float *w, int32_t *s_ids) {
+                                          int32_t *ids, float *w, int32_t *s_ids, uint32_t *s_tmask) {
     int id;
     float wv;
     warp_route_token<KM, NV>(v, E, k, lane, &id, &wv);
@@ -156,6 +151,7 @@ __device__ __forceinline__ void route_one(const float (&v)[NV], int t, int E, in
         ids[t * k + lane] = id;
         w[t * k + lane] = wv;
         if (s_ids) s_ids[t * k + lane] = id;
+        if (s_tmask) atomicOr(&s_tmask[id], 1u << t);
         if (counts) red_relaxed_add(counts + id, 1);
     }
 }
@@ -185,16 +181,19 @@ __device__ __forceinline__ int block_scan(int v, int *warp_tot) {
 
 // Both banks' pick lists from the step's picks, in one CTA of 512 threads.
 // On entry: s_ids [P] holds each pick's expert, s_rm [E] the row map, s_cnt
-// [E] zeros, base1 zero (all visible after a barrier).
+// [E] zeros, base1 zero, and for steps of at most 32 tokens s_tmask [E] each
+// expert's token mask (else null) -- all visible after a barrier.
 //  - each pick adds 1 to its row's count (rows of both banks in one array:
 //    hot row r at r, cold row r at n_hot + r)
 //  - one scan over that array (two rows per thread), the count in the low 16
 //    bits and "active" in the high 16: a row's exclusive prefix gives its
 //    offset in its bank's pick list and its index among its bank's active rows
 //  - each pick's place: its row's offset + the number of earlier picks (lower
-//    slots) of the same expert.
+//    slots) of the same expert -- a token picks an expert at most once, so
+//    with a token mask that is the mask's bits below the pick's token.
 __device__ __forceinline__ void build_lists(const int32_t *s_ids, const int32_t *s_rm, int32_t *s_cnt, int *warp_tot,
-                                            int &base1, int P, int E, int n_hot, WsPtrs ws) {
+                                            int &base1, int P, int E, int k, int n_hot, const uint32_t *s_tmask,
+                                            WsPtrs ws) {
     const int tid = threadIdx.x;
     for (int s = tid; s < P; s += kSmallThreads) {
         const int m = s_rm[s_ids[s]];
@@ -240,7 +239,11 @@ __device__ __forceinline__ void build_lists(const int32_t *s_ids, const int32_t 
         const int m = s_rm[e];
         const int b = m < 0;
         int pos = 0;
-        for (int q = 0; q < s; ++q) pos += s_ids[q] == e;
+        if (s_tmask) {
+            pos = __popc(s_tmask[e] & ((1u << (s / k)) - 1u));
+        } else {
+            for (int q = 0; q < s; ++q) pos += s_ids[q] == e;
+        }
         ws.picks[b * P + s_cnt[b ? n_hot + (-1 - m) : m] + pos] = s;
     }
 }
@@ -259,12 +262,15 @@ __global__ void __launch_bounds__(kSmallThreads) route_split_small(
     int32_t *s_ids = sm;            // [P] expert of each pick
     int32_t *s_rm = s_ids + P;      // [E] row map
     int32_t *s_cnt = s_rm + E;      // [E] picks per row (both banks), then row offsets
+    uint32_t *s_tmask = (uint32_t *)(s_cnt + E);   // [E] tokens that picked each expert
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     for (int e = tid; e < E; e += kSmallThreads) {
         s_rm[e] = rowmap[e];
         s_cnt[e] = 0;
+        s_tmask[e] = 0u;
     }
+    __syncthreads();   // the masks are zero before any token sets a bit
     if (tid == 0) base1 = 0;
     {
         constexpr int kWarps = kSmallThreads / 32;
@@ -272,13 +278,13 @@ __global__ void __launch_bounds__(kSmallThreads) route_split_small(
         if (warp < T) load_logits<NV>(logits + (size_t)warp * E, E, lane, cur);
         for (int t = warp; t < T; t += kWarps) {
             if (t + kWarps < T) load_logits<NV>(logits + (size_t)(t + kWarps) * E, E, lane, nxt);
-            route_one<KM, NV>(cur, t, E, k, lane, counts, ids, w, s_ids);
+            route_one<KM, NV>(cur, t, E, k, lane, counts, ids, w, s_ids, s_tmask);
 #pragma unroll
             for (int i = 0; i < NV; ++i) cur[i] = nxt[i];
         }
     }
     __syncthreads();
-    build_lists(s_ids, s_rm, s_cnt, warp_tot, base1, P, E, n_hot, ws);
+    build_lists(s_ids, s_rm, s_cnt, warp_tot, base1, P, E, k, n_hot, s_tmask, ws);
 }
 
 // Decode steps of 33..256 tokens, after route_tokens: both banks' lists in
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(kSmallThreads) split_picks(const int32_t *__re
     for (int q = tid; q < P; q += kSmallThreads) s_ids[q] = ids[q];
     if (tid == 0) base1 = 0;
     __syncthreads();
-    build_lists(s_ids, s_rm, s_cnt, warp_tot, base1, P, E, n_hot, ws);
+    build_lists(s_ids, s_rm, s_cnt, warp_tot, base1, P, E, 1, n_hot, nullptr, ws);
 }
 
 // Build the active-row lists of bank b from per-expert pick counts.
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(256) route_tokens(const float *__restrict__ lo
     if (t >= T) return;
     float v[NV];
     load_logits<NV>(logits + (size_t)t * E, E, lane, v);
-    route_one<KM, NV>(v, t, E, k, lane, counts, ids, w, nullptr);
+    route_one<KM, NV>(v, t, E, k, lane, counts, ids, w, nullptr, nullptr);
     if (ecnt && lane < k) red_relaxed_add(ecnt + ids[t * k + lane], 1);   // picks per expert for the split (order-free)
 }
 
@@ -400,8 +406,8 @@ int launch_route_km(const moe_ctx *ctx, const Layer &L, const float *logits, int
     const int P = ws.P;
     const size_t smem = sizeof(int32_t) * ((size_t)P + 2 * (size_t)g.E);
     if (T <= kFusedMaxT) {
-        route_split_small<KM, NV><<<1, kSmallThreads, smem, s>>>(logits, T, g.E, g.k, L.rowmap_dev, L.n_hot, counts, ids,
-                                                                 w, ws);
+        route_split_small<KM, NV><<<1, kSmallThreads, smem + sizeof(uint32_t) * g.E, s>>>(
+            logits, T, g.E, g.k, L.rowmap_dev, L.n_hot, counts, ids, w, ws);
         MOE_LAUNCH_CHECK();
         return MOE_OK;
     }

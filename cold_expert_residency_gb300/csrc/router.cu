@@ -9,12 +9,18 @@
 // fp32 logits written where the routing kernel reads them.
 //
 // Two kernels:
-//  * up to 32 tokens (decode): CUDA cores.  One CTA per (expert, group of 8
-//    tokens); its 8 warps split K, so every lane has at most a couple of
-//    16-byte weight loads in flight and the 3 MB of router weights (E = 384,
-//    H = 4096) stream from HBM across the whole GPU.  Each lane sums its
-//    columns in order, a butterfly adds the 32 lanes, the 8 warps' sums are
-//    added in warp order, then the bias.
+//  * up to 32 tokens (decode): CUDA cores.  A cluster of four CTAs per
+//    (group of 4 experts, group of 8 tokens); CTA q of the cluster takes the
+//    q-th quarter of K, 64 threads per expert.  A thread issues its weight
+//    loads first (at H = 4096: two 16-byte columns), so the 3 MB of router
+//    weights (E = 384) stream from HBM across the whole GPU in about one
+//    memory latency, while the CTA stages its tokens' quarter of x in shared
+//    memory, each column read once per CTA (x is small and read by every
+//    expert group: re-reading it per expert floods the L2 lines that hold
+//    it).  A thread sums its columns in order; a butterfly adds the 32 lanes; the
+//    expert's two warps are added in warp order; CTA 0 of the cluster adds
+//    the four quarters in order through distributed shared memory, then the
+//    bias -- a fixed order, so the logits are reproducible.
 //  * more tokens: a dense bf16 GEMM on the tensor cores (tcgen05.mma
 //    kind::f16, fp32 accumulator in tensor memory).  One CTA per (128-token
 //    tile, BN-expert tile); one thread issues TMA loads of 64-wide K slices of
@@ -29,6 +35,7 @@
 #include "moe_internal.cuh"
 #include "sm103_ptx.cuh"
 
+#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 namespace moe {
@@ -37,8 +44,10 @@ namespace {
 
 // ---------------------------------------------------------------- CUDA cores
 
-constexpr int kTok = 8;      // tokens per CTA
-constexpr int kKWarps = 8;   // warps splitting K
+constexpr int kTok = 8;       // tokens per CTA
+constexpr int kRE = 4;        // experts per CTA (64 threads each)
+constexpr int kKParts = 4;    // CTAs per cluster: the quarters of K
+constexpr int kRThreads = 64 * kRE;
 
 __device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
     const uint32_t p[4] = {v.x, v.y, v.z, v.w};
@@ -49,46 +58,81 @@ __device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
     }
 }
 
-__global__ void __launch_bounds__(32 * kKWarps) router_simt_kernel(const uint4 *__restrict__ x,
-                                                                   const uint4 *__restrict__ w,
-                                                                   const float *__restrict__ bias, int T, int E,
-                                                                   int H8, float *__restrict__ logits) {
-    __shared__ float part[kKWarps][kTok];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int e = blockIdx.x;
+constexpr int kXCols = 256;   // 16-byte columns of x staged in shared memory at a time (32 KB for 8 tokens)
+
+__global__ void __cluster_dims__(kKParts, 1, 1) __launch_bounds__(kRThreads)
+    router_simt_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ w, const float *__restrict__ bias, int T,
+                       int E, int H8, float *__restrict__ logits) {
+    namespace cg = cooperative_groups;
+    __shared__ float part[kRE][2][kTok];   // [expert][its warp][token]
+    __shared__ uint4 xs[kTok][kXCols];     // the CTA's tokens over a span of its K quarter
+    cg::cluster_group cluster = cg::this_cluster();
+    const int kp = (int)cluster.block_rank();   // this CTA's quarter of K
+    const int grp = blockIdx.x / kKParts;
+    const int tid = threadIdx.x, el = tid >> 6, r = tid & 63, lane = tid & 31, wp = (tid >> 5) & 1;
+    const int e = grp * kRE + el;
     const int t0 = blockIdx.y * kTok;
-    const int nt = min(kTok, T - t0);            // >= 1: the grid covers T exactly
-    const uint4 *wr = w + (size_t)e * H8;
+    const int nt = min(kTok, T - t0);   // >= 1: the grid covers T exactly
+    const int c0 = kp * H8 / kKParts, c1 = (kp + 1) * H8 / kKParts;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 *wr = w + (size_t)min(e, E - 1) * H8;
     const uint4 *xr = x + (size_t)t0 * H8;
     float acc[kTok];
 #pragma unroll
     for (int j = 0; j < kTok; ++j) acc[j] = 0.0f;
-    for (int c = warp * 32 + lane; c < H8; c += 32 * kKWarps) {
-        float wf[8];
-        bf16x8(__ldg(wr + c), wf);
+    for (int cs = c0; cs < c1; cs += kXCols) {
+        const int ce = min(c1, cs + kXCols);
+        // this thread's weight columns of the span first (in flight while x is staged)
+        uint4 wv[kXCols / 64];
 #pragma unroll
-        for (int j = 0; j < kTok; ++j) {
-            if (j < nt) {
-                float xf[8];
-                bf16x8(__ldg(xr + (size_t)j * H8 + c), xf);
+        for (int q = 0; q < kXCols / 64; ++q) {
+            const int c = cs + r + 64 * q;
+            wv[q] = (e < E && c < ce) ? __ldg(wr + c) : zero;
+        }
+        // the span of x, each 16-byte column read once per CTA
+        for (int i = tid; i < nt * (ce - cs); i += kRThreads) {
+            const int j = i / (ce - cs), c = i - j * (ce - cs);
+            xs[j][c] = __ldg(xr + (size_t)j * H8 + cs + c);
+        }
+        __syncthreads();
 #pragma unroll
-                for (int q = 0; q < 8; ++q) acc[j] = __fmaf_rn(xf[q], wf[q], acc[j]);
+        for (int q = 0; q < kXCols / 64; ++q) {
+            const int c = r + 64 * q;   // column within the span, in increasing order per thread
+            if (cs + c < ce) {
+                float wf[8], xf[8];
+                bf16x8(wv[q], wf);
+#pragma unroll
+                for (int j = 0; j < kTok; ++j) {
+                    if (j < nt) {
+                        bf16x8(xs[j][c], xf);
+#pragma unroll
+                        for (int qq = 0; qq < 8; ++qq) acc[j] = __fmaf_rn(xf[qq], wf[qq], acc[j]);
+                    }
+                }
             }
         }
+        __syncthreads();   // the span's x is read before the next one overwrites it
     }
 #pragma unroll
     for (int j = 0; j < kTok; ++j) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
-        if (lane == 0) part[warp][j] = acc[j];
+        if (lane == 0) part[el][wp][j] = acc[j];
     }
-    __syncthreads();
-    if (threadIdx.x < nt) {
-        float sum = 0.0f;
+    cluster.sync();   // every quarter's sums are in its CTA's shared memory
+    if (kp == 0 && tid < kRE * kTok) {
+        const int el2 = tid / kTok, j = tid % kTok, e2 = grp * kRE + el2;
+        if (e2 < E && j < nt) {
+            float sum = 0.0f;
 #pragma unroll
-        for (int q = 0; q < kKWarps; ++q) sum += part[q][threadIdx.x];
-        logits[(size_t)(t0 + threadIdx.x) * E + e] = sum + (bias ? __ldg(bias + e) : 0.0f);
+            for (int q = 0; q < kKParts; ++q) {
+                const float *rp = cluster.map_shared_rank(&part[0][0][0], q);
+                sum += rp[(el2 * 2 + 0) * kTok + j] + rp[(el2 * 2 + 1) * kTok + j];
+            }
+            logits[(size_t)(t0 + j) * E + e2] = sum + (bias ? __ldg(bias + e2) : 0.0f);
+        }
     }
+    cluster.sync();   // the other quarters' shared memory stays until CTA 0 has read it
 }
 
 // -------------------------------------------------------------- tensor cores
@@ -312,9 +356,9 @@ int launch_router_tc(const uint16_t *x, const uint16_t *w_router, const float *b
 int launch_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int E, int H,
                   float *logits, int32_t *status, int sms, cudaStream_t s) {
     if (T <= 32) {
-        const dim3 grid(E, (T + kTok - 1) / kTok);
-        router_simt_kernel<<<grid, 32 * kKWarps, 0, s>>>((const uint4 *)x, (const uint4 *)w_router, bias, T, E, H / 8,
-                                                         logits);
+        const dim3 grid(kKParts * ((E + kRE - 1) / kRE), (T + kTok - 1) / kTok);
+        router_simt_kernel<<<grid, kRThreads, 0, s>>>((const uint4 *)x, (const uint4 *)w_router, bias, T, E, H / 8,
+                                                      logits);
         MOE_LAUNCH_CHECK();
         return MOE_OK;
     }
