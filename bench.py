@@ -524,24 +524,25 @@ class StepRunner:
         return dh, dc, hp
 
     def e2e_ms(self, n):
-        """Host inputs -> device -> step -> host outputs, all inside the events."""
-        S, torch = self.S, self.S.torch
+        """Host inputs -> step -> host outputs through the library's host-buffer
+        call (moe_layer_step_host: copies in, route, both banks' FFN, finalize,
+        copy out), one call per layer, all inside the events."""
+        S, torch, moe = self.S, self.S.torch, self.S.moe
         T, L = self.T, len(self.layers)
         h_lg = self.d_lg.cpu().pin_memory()
         h_x = self.d_x.cpu().pin_memory()
         h_out = torch.zeros((L, T, self.cfg.H), dtype=torch.int16).pin_memory()
+        scratch = torch.empty(moe.moe_step_scratch_bytes(self.ctx, T) + 256, dtype=torch.uint8, device=S.dev)
+        sp = (scratch.data_ptr() + 255) // 256 * 256
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ts = []
         for i in range(n):
             with torch.cuda.stream(S.main):
                 S.flush.zero_()
                 ev0.record(S.main)
-                for m, st in enumerate(self.steps):
-                    st.buf.logits[:T].copy_(h_lg[i % self.npool, m], non_blocking=True)
-                    st.buf.x[:T].copy_(h_x[i % self.npool, m], non_blocking=True)
-                self.run_step()
-                for m, st in enumerate(self.steps):
-                    h_out[m].copy_(st.buf.out[:T], non_blocking=True)
+                for m, l in enumerate(self.layers):
+                    moe.moe_layer_step_host(self.ctx, l, h_lg[i % self.npool, m], h_x[i % self.npool, m], T,
+                                            self.count_on, h_out[m], sp, S.main)
                 ev1.record(S.main)
             S.main.synchronize()
             ts.append(ev0.elapsed_time(ev1))
@@ -936,7 +937,7 @@ def line_for(S, name, cfg, m, args, cpu):
         "cpu_baseline": cpu,
         "e2e": {"value": job_tokens_per_s(world, cfg.T, len(m["e2e_ms"]), e2e_total), "unit": "tokens/s",
                 "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
-                "path": "pinned host inputs copied in, the step through the C ABI, outputs copied back, per step"},
+                "path": "moe_layer_step_host per layer: pinned host inputs copied in, route, both banks' FFN, finalize, output rows copied back, all in the C ABI call"},
         "gpu_launches": m["launches_per_step"] * len(m["step_ms"]),
         "clocks": m["clocks"],
     }

@@ -72,6 +72,8 @@ def lib():
         "moe_static_scratch_bytes": (sz, []),
         "moe_finalize": (i32, [P, P, i32, i32, i32, P, P]),
         "moe_router_logits": (i32, [P, P, P, P, i32, i32, i32, P, P]),
+        "moe_step_scratch_bytes": (i32, [P, i32, C.POINTER(sz)]),
+        "moe_layer_step_host": (i32, [P, i32, P, P, i32, i32, P, P, P]),
         "moe_swap_rows": (i32, [P, i32, i32, P, P, P, P]),
         "moe_read_counts": (i32, [P, P, P]),
         "moe_reset_counts": (i32, [P, P]),
@@ -238,6 +240,20 @@ def moe_expert_ffn_bank_static(ctx, layer, bank, x, T, split_ws, Y, stream=None)
 
 def moe_static_scratch_bytes():
     return int(lib().moe_static_scratch_bytes())
+
+
+def moe_step_scratch_bytes(ctx, T):
+    n = C.c_size_t()
+    _err("moe_step_scratch_bytes", lib().moe_step_scratch_bytes(ctx, T, C.byref(n)))
+    return n.value
+
+
+def moe_layer_step_host(ctx, layer, logits, x, T, count_on, out, scratch, stream=None):
+    """One layer-step from host buffers (logits fp32 [T][E], x bf16 bits
+    [T][H] in, out bf16 bits [T][H]); out is valid once the stream has
+    reached the end of the call."""
+    return _err("moe_layer_step_host", lib().moe_layer_step_host(
+        ctx, layer, _ptr(logits), _ptr(x), T, int(count_on), _ptr(out), _ptr(scratch), _stream(stream)))
 
 
 def moe_finalize(Y, w, T, k, H, out, stream=None):

@@ -524,6 +524,72 @@ int moe_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_
     return launch_finalize(Y, w, T, k, H, out, (cudaStream_t)stream);
 }
 
+namespace {
+
+// Parts of a host-buffer step's scratch area for a step of T tokens, each on
+// a 256-byte boundary: the workspace, then the step's device buffers.
+struct StepScratch {
+    size_t ws, logits, x, ids, w, Y, out, total;
+};
+
+StepScratch step_scratch(const moe_ctx *ctx, int T, size_t ws_bytes) {
+    const moe::Geom &g = ctx->g;
+    StepScratch p;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = (off + bytes + 255) / 256 * 256;
+        return o;
+    };
+    p.ws = take(ws_bytes);
+    p.logits = take((size_t)T * g.E * 4);
+    p.x = take((size_t)T * g.H * 2);
+    p.ids = take((size_t)T * g.k * 4);
+    p.w = take((size_t)T * g.k * 4);
+    p.Y = take((size_t)T * g.k * g.H * 2);
+    p.out = take((size_t)T * g.H * 2);
+    p.total = off;
+    return p;
+}
+
+}  // namespace
+
+int moe_step_scratch_bytes(const moe_ctx *ctx, int T, size_t *bytes) {
+    if (int r = check_ctx(ctx)) return r;
+    if (!bytes || T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "T out of range");
+    size_t ws = 0;
+    if (int r = moe_workspace_bytes(ctx, T, &ws)) return r;
+    *bytes = step_scratch(ctx, T, ws).total;
+    return MOE_OK;
+}
+
+int moe_layer_step_host(moe_ctx *ctx, int layer, const float *logits, const uint16_t *x, int T, int count_on,
+                        uint16_t *out, void *scratch, void *stream) {
+    if (int r = check_layer(ctx, layer, true)) return r;
+    if (T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "T out of range");
+    if (T == 0) return MOE_OK;
+    if (!logits || !x || !out || !scratch) return set_error(MOE_EINVAL, "null pointer");
+    if ((uintptr_t)scratch % 256) return set_error(MOE_EINVAL, "scratch must be 256-byte aligned");
+    const moe::Geom &g = ctx->g;
+    size_t ws = 0;
+    if (int r = moe_workspace_bytes(ctx, T, &ws)) return r;
+    const StepScratch p = step_scratch(ctx, T, ws);
+    uint8_t *base = (uint8_t *)scratch;
+    float *d_logits = (float *)(base + p.logits);
+    uint16_t *d_x = (uint16_t *)(base + p.x), *d_Y = (uint16_t *)(base + p.Y), *d_out = (uint16_t *)(base + p.out);
+    int32_t *d_ids = (int32_t *)(base + p.ids);
+    float *d_w = (float *)(base + p.w);
+    DeviceGuard guard(ctx->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    MOE_CUDA_TRY(cudaMemcpyAsync(d_logits, logits, (size_t)T * g.E * 4, cudaMemcpyHostToDevice, s));
+    MOE_CUDA_TRY(cudaMemcpyAsync(d_x, x, (size_t)T * g.H * 2, cudaMemcpyHostToDevice, s));
+    if (int r = moe_route_split_count(ctx, layer, d_logits, T, count_on, d_ids, d_w, base + p.ws, stream)) return r;
+    if (int r = moe_expert_ffn_bank(ctx, layer, MOE_BANK_BOTH, d_x, T, base + p.ws, d_Y, stream)) return r;
+    if (int r = moe_finalize(d_Y, d_w, T, g.k, g.H, d_out, stream)) return r;
+    MOE_CUDA_TRY(cudaMemcpyAsync(out, d_out, (size_t)T * g.H * 2, cudaMemcpyDeviceToHost, s));
+    return MOE_OK;
+}
+
 int moe_router_logits(moe_ctx *ctx, const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int E,
                       int H, float *logits, void *stream) {
     if (!ctx) return set_error(MOE_EINVAL, "null context");

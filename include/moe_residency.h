@@ -227,6 +227,28 @@ int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t
                                const void *split_ws, uint16_t *Y, void *stream);
 size_t moe_static_scratch_bytes(void);
 
+/* One whole layer-step from host buffers: the call an application that holds
+ * its logits, hidden states and output rows in (pinned) host memory makes.
+ * "vLLM: Pin Hot Experts", Results: route and split each token's k picks,
+ * run the routed FFN over both banks, finalize the k weighted rows.  In order
+ * on `stream`: the logits and hidden states are copied host -> device, then
+ * moe_route_split_count (count_on as there), moe_expert_ffn_bank over both
+ * banks and moe_finalize run on the scratch area, then the output rows are
+ * copied device -> host.  The result is bit-identical to those calls made on
+ * device buffers.
+ *   logits: host fp32 [T][E]; x: host bf16 [T][H]; out: host bf16 [T][H] out.
+ * Pinned host memory (cudaHostAlloc) makes the copies asynchronous; with
+ * pageable memory they still complete, but they synchronize with the host.
+ * out is written when the stream reaches the end of the call: synchronize the
+ * stream before reading it.  scratch: device memory of at least
+ * moe_step_scratch_bytes(ctx, Tcap) bytes, 256-byte aligned, for any T <=
+ * Tcap; caller-owned, and calls that share it must not overlap on the GPU.
+ * T == 0 is a no-op.  MOE_EINVAL on a bad argument; errors of the inner calls
+ * are returned as they come. */
+int moe_step_scratch_bytes(const moe_ctx *ctx, int T, size_t *bytes);
+int moe_layer_step_host(moe_ctx *ctx, int layer, const float *logits, const uint16_t *x, int T, int count_on,
+                        uint16_t *out, void *scratch, void *stream);
+
 /* Router GEMM (async): the logits the routing call reads.  "vLLM: Pin Hot
  * Experts", Where the experts live today: each MoE layer's router scores all
  * experts for every token, whatever bank they sit in.

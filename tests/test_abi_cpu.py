@@ -54,6 +54,8 @@ def test_null_and_shape_checks_fail_cleanly(lib):
     assert lib.moe_policy_create(0, 64.0, 500.0, 1.5, 8.0, 2, None, C.byref(C.c_void_p())) == moe.MOE_EINVAL
     # router: context, shape and pointer checks come before any device work
     assert lib.moe_router_logits(None, None, None, None, 0, 16, 256, None, None) == moe.MOE_EINVAL
+    assert lib.moe_step_scratch_bytes(None, 8, C.byref(C.c_size_t())) == moe.MOE_EINVAL
+    assert lib.moe_layer_step_host(None, 0, None, None, 8, 1, None, None, None) == moe.MOE_EINVAL
     assert b"context" in lib.moe_last_error()
 
 

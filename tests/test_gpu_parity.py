@@ -358,3 +358,32 @@ def test_decode1_full_size_against_oracle():
         assert sp[1]["n_picks"] > 0, "decode step should touch the cold bank"
     finally:
         h.close()
+
+
+@pytest.mark.parametrize("T", [7, 40, 300])
+def test_host_buffer_step_equals_the_device_calls(T):
+    """moe_layer_step_host (host logits and hidden states in, host output rows
+    out) gives the same bits as the device calls it stands for, at 8-, 32- and
+    prefill-sized tiles, on a split layer; a scratch area sized for the
+    largest step serves a smaller one; T = 0 is a no-op."""
+    cfg = synth.get_config("tiny", T=T)
+    h = Harness(cfg, T_max=300)
+    moe = h.moe
+    try:
+        lg = synth.router_logits(cfg, 0, 11, T=T)
+        x = synth.activations(cfg, 0, 11, T=T)
+        ref = h.run(0, lg, x)
+        scratch = torch.empty(moe.moe_step_scratch_bytes(h.ctx, 300) + 256, dtype=torch.uint8, device="cuda")
+        sp = (scratch.data_ptr() + 255) // 256 * 256
+        h_lg = torch.from_numpy(np.ascontiguousarray(lg)).pin_memory()
+        h_x = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
+        h_out = torch.full((T, cfg.H), -1, dtype=torch.int16).pin_memory()
+        moe.moe_layer_step_host(h.ctx, 0, h_lg, h_x, T, True, h_out, sp)
+        torch.cuda.synchronize()
+        assert np.array_equal(h_out.numpy().view(np.uint16), ref["out"])
+        moe.moe_layer_step_host(h.ctx, 0, h_lg, h_x, 0, True, h_out, sp)   # T = 0: nothing changes
+        torch.cuda.synchronize()
+        assert np.array_equal(h_out.numpy().view(np.uint16), ref["out"])
+        assert moe.moe_device_status(h.ctx) == 0
+    finally:
+        h.close()
