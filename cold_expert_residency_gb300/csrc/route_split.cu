@@ -42,11 +42,6 @@ __device__ __forceinline__ void red_relaxed_add(int32_t *p, int v) {
     asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// a ranks before b: larger logit first, equal logits by lower expert id
-__device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
-    return va > vb || (va == vb && ea < eb);
-}
-
 // A token's logits as one lane holds them: experts lane, lane+32, ... (NV
 // values, NV*32 >= E), loaded together so their latencies overlap.  A NaN
 // logit is read as -infinity.
@@ -60,14 +55,52 @@ __device__ __forceinline__ void load_logits(const float *__restrict__ l, int E, 
     }
 }
 
-// One warp routes one token from its logits in registers, in k rounds: each
-// lane takes the best of its values not yet picked (a pairwise tree, lower
-// expert id on equal values), a butterfly takes the best over the lanes, and
-// the lane that held it marks it picked.  NaN logits arrive as -infinity
-// (ranked below every number, weight exp(-inf) = 0 beside a finite first
-// pick), so the k ids are always valid.  Then fp32 softmax over the k picks,
-// shifted by the first and summed in pick order.  Lane j < k returns pick j in
-// (*id_out, *w_out); other lanes return -1.
+// Order-preserving 32-bit key of a logit: a larger key for a larger value,
+// -0.0 read as +0.0 (equal logits must tie, so the lower expert id decides).
+__device__ __forceinline__ uint32_t logit_key(float f) {
+    const uint32_t b = __float_as_uint(f == 0.0f ? 0.0f : f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// A lane's best two values not yet picked, as (value, index) with index NV
+// for none: higher value first, the lower index on equal values (a lane's
+// expert ids rise with the index).  One pass in index order.
+template <int NV>
+__device__ __forceinline__ void lane_top2(const float (&v)[NV], uint32_t taken, float &v1, int &i1, float &v2,
+                                          int &i2) {
+    v1 = -INFINITY;
+    v2 = -INFINITY;
+    i1 = NV;
+    i2 = NV;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        if ((taken >> i) & 1u) continue;
+        if (i1 == NV || v[i] > v1) {
+            v2 = v1;
+            i2 = i1;
+            v1 = v[i];
+            i1 = i;
+        } else if (i2 == NV || v[i] > v2) {
+            v2 = v[i];
+            i2 = i;
+        }
+    }
+}
+
+// One warp routes one token from its logits in registers, in k rounds.  Each
+// lane offers its best value not yet picked; one warp reduction takes the
+// largest key over the lanes, a second the lowest expert id among the lanes
+// that offer it, and the lane that held the pick marks it picked and offers
+// its second best next.  A lane whose second best is used up too finds its
+// next two again (the warp takes that branch only when some lane needs it).
+// NaN logits arrive as -infinity (ranked below every number, weight
+// exp(-inf) = 0 beside a finite first pick), so the k ids are always valid.
+// Then fp32 softmax over the k picks, shifted by the first and summed in pick
+// order.  Lane j < k returns pick j in (*id_out, *w_out); other lanes
+// return -1.
 template <int KM, int NV>
 __device__ __forceinline__ void warp_route_token(const float (&v)[NV], int E, int k, int lane, int *id_out,
                                                  float *w_out) {
@@ -75,45 +108,37 @@ __device__ __forceinline__ void warp_route_token(const float (&v)[NV], int E, in
 #pragma unroll
     for (int i = 0; i < NV; ++i)
         if (lane + 32 * i >= E) taken |= 1u << i;
+    float v1, v2;
+    int i1, i2;
+    lane_top2<NV>(v, taken, v1, i1, v2, i2);
+    bool second = true;   // (v2, i2) is this lane's second best
     float sel_v[KM];
     int sel_e[KM];
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
         if (j < k) {
-            // this lane's best unpicked value: a tree over (value, index), the
-            // lower index on equal values (its expert id is lower too)
-            float tv[NV];
-            int ti[NV];
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const bool free_i = !((taken >> i) & 1u);
-                tv[i] = free_i ? v[i] : -INFINITY;
-                ti[i] = free_i ? i : NV + i;   // picked values lose every tie
-            }
-#pragma unroll
-            for (int w = 1; w < NV; w <<= 1) {
-#pragma unroll
-                for (int i = 0; i + w < NV; i += 2 * w) {
-                    if (tv[i + w] > tv[i] || (tv[i + w] == tv[i] && ti[i + w] < ti[i])) {
-                        tv[i] = tv[i + w];
-                        ti[i] = ti[i + w];
-                    }
+            // a lane without a candidate offers key 0, below every logit's key
+            const bool has = i1 < NV;
+            const uint32_t key = has ? logit_key(v1) : 0u;
+            const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
+            const uint32_t be = __reduce_min_sync(0xffffffffu, has && key == mk ? (uint32_t)(lane + 32 * i1) : 0xFFFFFFFFu);
+            bool refill = false;
+            if ((int)(be & 31u) == lane) {   // this lane held the pick
+                taken |= 1u << (be >> 5);
+                if (second) {
+                    v1 = v2;
+                    i1 = i2;
+                    second = false;
+                } else {
+                    refill = true;
                 }
             }
-            float bv = tv[0];
-            int be = ti[0] < NV ? lane + 32 * ti[0] : INT_MAX;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (better(ov, oe, bv, be)) {
-                    bv = ov;
-                    be = oe;
-                }
+            if (__any_sync(0xffffffffu, refill) && refill) {
+                lane_top2<NV>(v, taken, v1, i1, v2, i2);
+                second = true;
             }
-            if ((be & 31) == lane && be != INT_MAX) taken |= 1u << (be >> 5);   // this lane held the pick
-            sel_v[j] = bv;
-            sel_e[j] = be;
+            sel_v[j] = key_logit(mk);
+            sel_e[j] = (int)be;
         }
     }
     float ex[KM];
@@ -126,16 +151,16 @@ __device__ __forceinline__ void warp_route_token(const float (&v)[NV], int E, in
         }
     }
     int myid = -1;
-    float myw = 0.0f;
+    float myex = 0.0f;
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
         if (j < k && j == lane) {
             myid = sel_e[j];
-            myw = __fdiv_rn(ex[j], sum);
+            myex = ex[j];
         }
     }
     *id_out = myid;
-    *w_out = myw;
+    *w_out = lane < k ? __fdiv_rn(myex, sum) : 0.0f;
 }
 
 // Route token t from logits in registers and write its picks (and, in the
