@@ -289,9 +289,11 @@ __global__ void __launch_bounds__(kSmallThreads) route_split_small(
     int32_t *s_cnt = s_rm + E;      // [E] picks per row (both banks), then row offsets
     uint32_t *s_tmask = (uint32_t *)(s_cnt + E);   // [E] tokens that picked each expert
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
+    // the row map is read only by the list building: its loads (E <= 1024,
+    // two per thread) stay in flight while the tokens are routed
+    const int rm0 = tid < E ? rowmap[tid] : 0;
+    const int rm1 = tid + kSmallThreads < E ? rowmap[tid + kSmallThreads] : 0;
     for (int e = tid; e < E; e += kSmallThreads) {
-        s_rm[e] = rowmap[e];
         s_cnt[e] = 0;
         s_tmask[e] = 0u;
     }
@@ -308,6 +310,8 @@ __global__ void __launch_bounds__(kSmallThreads) route_split_small(
             for (int i = 0; i < NV; ++i) cur[i] = nxt[i];
         }
     }
+    if (tid < E) s_rm[tid] = rm0;
+    if (tid + kSmallThreads < E) s_rm[tid + kSmallThreads] = rm1;
     __syncthreads();
     build_lists(s_ids, s_rm, s_cnt, warp_tot, base1, P, E, k, n_hot, s_tmask, ws);
 }
@@ -459,6 +463,7 @@ int launch_route_nv(const moe_ctx *ctx, const Layer &L, const float *logits, int
     const int E = ctx->g.E;
     if (E <= 128) return launch_route_km<KM, 4>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
     if (E <= 256) return launch_route_km<KM, 8>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
+    if (E <= 384) return launch_route_km<KM, 12>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
     if (E <= 512) return launch_route_km<KM, 16>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
     return launch_route_km<KM, 32>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
 }
