@@ -11,13 +11,12 @@
 // Two kernels:
 //  * up to 32 tokens (decode): CUDA cores.  A cluster of four CTAs per
 //    (group of 4 experts, group of 8 tokens); CTA q of the cluster takes the
-//    q-th quarter of K, 64 threads per expert.  A thread issues its weight
-//    loads first (at H = 4096: two 16-byte columns), so the 3 MB of router
-//    weights (E = 384) stream from HBM across the whole GPU in about one
-//    memory latency, while the CTA stages its tokens' quarter of x in shared
-//    memory, each column read once per CTA (x is small and read by every
-//    expert group: re-reading it per expert floods the L2 lines that hold
-//    it).  A thread sums its columns in order; a butterfly adds the 32 lanes; the
+//    q-th quarter of K, 64 threads per expert.  One thread issues a bulk
+//    asynchronous copy of each expert row's quarter and of each token row's
+//    quarter into shared memory (at H = 4096: 4 x 2 KB and up to 8 x 2 KB), so
+//    the 3 MB of router weights (E = 384) move from HBM across the whole GPU
+//    in about one memory latency, without one 16-byte request per thread.  A
+//    thread sums its columns in order; a butterfly adds the 32 lanes; the
 //    expert's two warps are added in warp order; CTA 0 of the cluster adds
 //    the four quarters in order through distributed shared memory, then the
 //    bias -- a fixed order, so the logits are reproducible.
@@ -58,60 +57,82 @@ __device__ __forceinline__ void bf16x8(const uint4 v, float (&f)[8]) {
     }
 }
 
-constexpr int kXCols = 256;   // 16-byte columns of x staged in shared memory at a time (32 KB for 8 tokens)
+constexpr int kSpan = 224;                     // 16-byte columns of a K quarter staged at a time
+constexpr uint64_t kSimtWaitNs = 1000000000ull;   // bound of the copies' wait
 
 __global__ void __cluster_dims__(kKParts, 1, 1) __launch_bounds__(kRThreads)
     router_simt_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ w, const float *__restrict__ bias, int T,
-                       int E, int H8, float *__restrict__ logits) {
+                       int E, int H8, float *__restrict__ logits, int32_t *status) {
     namespace cg = cooperative_groups;
-    __shared__ float part[kRE][2][kTok];   // [expert][its warp][token]
-    __shared__ uint4 xs[kTok][kXCols];     // the CTA's tokens over a span of its K quarter
+    __shared__ __align__(128) uint4 wsm[kRE][kSpan];   // the CTA's experts over a span of its K quarter
+    __shared__ __align__(128) uint4 xs[kTok][kSpan];   // its tokens over the same span
+    __shared__ float part[kRE][2][kTok];                // [expert][its warp][token]
+    __shared__ __align__(8) uint64_t full;
     cg::cluster_group cluster = cg::this_cluster();
     const int kp = (int)cluster.block_rank();   // this CTA's quarter of K
     const int grp = blockIdx.x / kKParts;
     const int tid = threadIdx.x, el = tid >> 6, r = tid & 63, lane = tid & 31, wp = (tid >> 5) & 1;
     const int e = grp * kRE + el;
+    const int ne = min(kRE, E - grp * kRE);   // experts of this group, >= 1
     const int t0 = blockIdx.y * kTok;
-    const int nt = min(kTok, T - t0);   // >= 1: the grid covers T exactly
+    const int nt = min(kTok, T - t0);         // >= 1: the grid covers T exactly
     const int c0 = kp * H8 / kKParts, c1 = (kp + 1) * H8 / kKParts;
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    const uint4 *wr = w + (size_t)min(e, E - 1) * H8;
-    const uint4 *xr = x + (size_t)t0 * H8;
+    const uint32_t bar = ptx::smem_addr(&full);
+    if (tid == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
     float acc[kTok];
 #pragma unroll
     for (int j = 0; j < kTok; ++j) acc[j] = 0.0f;
-    for (int cs = c0; cs < c1; cs += kXCols) {
-        const int ce = min(c1, cs + kXCols);
-        // this thread's weight columns of the span first (in flight while x is staged)
-        uint4 wv[kXCols / 64];
-#pragma unroll
-        for (int q = 0; q < kXCols / 64; ++q) {
-            const int c = cs + r + 64 * q;
-            wv[q] = (e < E && c < ce) ? __ldg(wr + c) : zero;
+    bool ok = true;
+    uint32_t phase = 0;
+    for (int cs = c0; ok && cs < c1; cs += kSpan, phase ^= 1u) {
+        const int len = min(c1, cs + kSpan) - cs;   // 16-byte columns in this span
+        if (tid == 0) {
+            // one bulk copy per expert row and per token row of the span
+            ptx::mbar_arrive_expect_tx(bar, (uint32_t)((ne + nt) * len * 16));
+            for (int q = 0; q < ne; ++q)
+                ptx::bulk_g2s(ptx::smem_addr(&wsm[q][0]), w + (size_t)(grp * kRE + q) * H8 + cs, (uint32_t)len * 16, bar);
+            for (int j = 0; j < nt; ++j)
+                ptx::bulk_g2s(ptx::smem_addr(&xs[j][0]), x + (size_t)(t0 + j) * H8 + cs, (uint32_t)len * 16, bar);
         }
-        // the span of x, each 16-byte column read once per CTA
-        for (int i = tid; i < nt * (ce - cs); i += kRThreads) {
-            const int j = i / (ce - cs), c = i - j * (ce - cs);
-            xs[j][c] = __ldg(xr + (size_t)j * H8 + cs + c);
+        uint64_t tw = 0;
+        for (uint32_t i = 0;; ++i) {   // bounded wait for the span
+            if (ptx::mbar_try_wait(bar, phase)) break;
+            if ((i & 255u) == 0u) {
+                const uint64_t now = ptx::globaltimer_ns();
+                if (i == 0) {
+                    tw = now;
+                } else if (now - tw > kSimtWaitNs) {
+                    atomicCAS(status, 0, MOE_ETIMEOUT);
+                    ok = false;
+                    break;
+                }
+            }
         }
-        __syncthreads();
-#pragma unroll
-        for (int q = 0; q < kXCols / 64; ++q) {
-            const int c = r + 64 * q;   // column within the span, in increasing order per thread
-            if (cs + c < ce) {
+        if (!ok) break;
+        if (e < E) {
+            for (int c = r; c < len; c += 64) {   // this thread's columns in increasing order
                 float wf[8], xf[8];
-                bf16x8(wv[q], wf);
+                bf16x8(wsm[el][c], wf);
 #pragma unroll
                 for (int j = 0; j < kTok; ++j) {
                     if (j < nt) {
                         bf16x8(xs[j][c], xf);
 #pragma unroll
-                        for (int qq = 0; qq < 8; ++qq) acc[j] = __fmaf_rn(xf[qq], wf[qq], acc[j]);
+                        for (int q = 0; q < 8; ++q) acc[j] = __fmaf_rn(xf[q], wf[q], acc[j]);
                     }
                 }
             }
         }
-        __syncthreads();   // the span's x is read before the next one overwrites it
+        __syncthreads();   // the span is read before the next one is copied over it
+    }
+    if (!ok) {
+        // let this CTA's copies land before it goes away (bounded)
+        for (uint32_t i = 0; i < (1u << 22); ++i)
+            if (ptx::mbar_try_wait(bar, phase)) break;
     }
 #pragma unroll
     for (int j = 0; j < kTok; ++j) {
@@ -120,7 +141,7 @@ __global__ void __cluster_dims__(kKParts, 1, 1) __launch_bounds__(kRThreads)
         if (lane == 0) part[el][wp][j] = acc[j];
     }
     cluster.sync();   // every quarter's sums are in its CTA's shared memory
-    if (kp == 0 && tid < kRE * kTok) {
+    if (kp == 0 && tid < kRE * kTok && ok) {
         const int el2 = tid / kTok, j = tid % kTok, e2 = grp * kRE + el2;
         if (e2 < E && j < nt) {
             float sum = 0.0f;
@@ -358,7 +379,7 @@ int launch_router(const uint16_t *x, const uint16_t *w_router, const float *bias
     if (T <= 32) {
         const dim3 grid(kKParts * ((E + kRE - 1) / kRE), (T + kTok - 1) / kTok);
         router_simt_kernel<<<grid, kRThreads, 0, s>>>((const uint4 *)x, (const uint4 *)w_router, bias, T, E, H / 8,
-                                                      logits);
+                                                      logits, status);
         MOE_LAUNCH_CHECK();
         return MOE_OK;
     }
