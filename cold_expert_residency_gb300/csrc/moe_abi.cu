@@ -270,7 +270,12 @@ int moe_create(const moe_geom *geom, int device, moe_ctx **out) {
     if (e == cudaSuccess) ctx->sms = prop.multiProcessorCount;
     if (e == cudaSuccess) e = dev_alloc((void **)&ctx->counts_dev, sizeof(int32_t) * g.layers * g.experts, "create_counts");
     if (e == cudaSuccess) e = cudaMemset(ctx->counts_dev, 0, sizeof(int32_t) * g.layers * g.experts);
-    if (e == cudaSuccess) e = dev_alloc((void **)&ctx->staging, ctx->g.eb, "create_staging");
+    if (e == cudaSuccess) e = dev_alloc((void **)&ctx->staging, 2 * ctx->g.eb, "create_staging");
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ctx->swap_stream, cudaStreamNonBlocking);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+        e = cudaEventCreateWithFlags(&ctx->swap_in[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->swap_out[i], cudaEventDisableTiming);
+    }
     if (e == cudaSuccess) e = dev_alloc((void **)&ctx->status_dev, sizeof(int32_t) * 4, "create_status");
     if (e == cudaSuccess) e = cudaMemset(ctx->status_dev, 0, sizeof(int32_t) * 4);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -290,6 +295,11 @@ int moe_destroy(moe_ctx *ctx) {
     for (auto &L : ctx->layers) free_layer(L);
     dev_free(ctx->counts_dev);
     dev_free(ctx->staging);
+    for (int i = 0; i < 2; ++i) {
+        if (ctx->swap_in[i]) cudaEventDestroy(ctx->swap_in[i]);
+        if (ctx->swap_out[i]) cudaEventDestroy(ctx->swap_out[i]);
+    }
+    if (ctx->swap_stream) cudaStreamDestroy(ctx->swap_stream);
     dev_free(ctx->status_dev);
     pinned_free(ctx->probe_host);
     dev_free(ctx->probe_dev);
@@ -614,6 +624,34 @@ int moe_swap_rows(moe_ctx *ctx, int layer, int n, const int32_t *promote, const 
     int done = 0;
     if (applied)
         for (int i = 0; i < n; ++i) applied[i] = 0;
+    // Applied pairs alternate between two staging rows.  Pair k: hot row ->
+    // staging[k % 2] and cold row -> hot slot on `stream`; staging -> cold
+    // slot on the swap stream, after those two (so it overlaps pair k+1's
+    // copy into HBM: the host link carries both directions at once).  Pair
+    // k's row-map write goes on `stream` once its copy back has landed:
+    // before pair k+2 reuses its staging row, or at the end.
+    struct Pending {
+        int32_t c, hot_row, h, cold_row;
+    };
+    Pending pend[2];
+    int npend = 0;   // pairs whose copy back is not yet joined (the last one or two)
+    int32_t last_cold = -1;
+    auto fail = [&](int r) {
+        L.init = false;
+        return set_error(r, std::string(moe_last_error()) + "; layer " + std::to_string(layer) +
+                                " must be placed again with moe_init_banks");
+    };
+    // join the oldest pending pair: wait for its copy back, then write its two map entries
+    auto join_oldest = [&]() -> int {
+        const Pending q = pend[0];
+        const int buf = (done - npend) % 2;
+        cudaError_t e = cudaStreamWaitEvent(s, ctx->swap_out[buf], 0);
+        if (e != cudaSuccess) return cuda_error(e, "moe_swap_rows join");
+        if (int r = launch_rowmap_write(L.rowmap_dev, q.c, q.hot_row, q.h, -1 - q.cold_row, s)) return r;
+        pend[0] = pend[1];
+        --npend;
+        return MOE_OK;
+    };
     for (int i = 0; i < n; ++i) {
         int32_t c = promote[i], h = demote[i];
         bool ok = c >= 0 && c < g.E && h >= 0 && h < g.E && c != h && L.rowmap[c] < 0 && L.rowmap[h] >= 0;
@@ -622,24 +660,32 @@ int moe_swap_rows(moe_ctx *ctx, int layer, int n, const int32_t *promote, const 
         int32_t cold_row = -1 - L.rowmap[c];
         uint8_t *hot_p = L.hot + (size_t)hot_row * g.eb;
         uint8_t *cold_p = L.cold_host + (size_t)cold_row * g.eb;
+        const int buf = done % 2;
+        uint8_t *stage = ctx->staging + (size_t)buf * g.eb;
+        // this staging row's previous pair must be joined first; so must the
+        // pair before whose copy back still writes the cold row read here
+        if (npend == 2)
+            if (int r = join_oldest()) return fail(r);
+        if (npend == 1 && pend[0].cold_row == cold_row)
+            if (int r = join_oldest()) return fail(r);
         // A failure after the first copy may leave a bank row holding neither
         // expert whole: the layer is then marked as needing moe_init_banks,
         // and this pair is not reported as applied.
-        cudaError_t e = cudaMemcpyAsync(ctx->staging, hot_p, g.eb, cudaMemcpyDeviceToDevice, s);
+        cudaError_t e = cudaMemcpyAsync(stage, hot_p, g.eb, cudaMemcpyDeviceToDevice, s);
         if (e == cudaSuccess) e = cudaMemcpyAsync(hot_p, cold_p, g.eb, cudaMemcpyHostToDevice, s);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(cold_p, ctx->staging, g.eb, cudaMemcpyDeviceToHost, s);
-        int r = e == cudaSuccess ? launch_rowmap_write(L.rowmap_dev, c, hot_row, h, -1 - cold_row, s)
-                                 : cuda_error(e, "moe_swap_rows copy");
-        if (r != MOE_OK) {
-            L.init = false;
-            return set_error(r, std::string(moe_last_error()) + "; layer " + std::to_string(layer) +
-                                    " must be placed again with moe_init_banks");
-        }
+        if (e == cudaSuccess) e = cudaEventRecord(ctx->swap_in[buf], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->swap_stream, ctx->swap_in[buf], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(cold_p, stage, g.eb, cudaMemcpyDeviceToHost, ctx->swap_stream);
+        if (e == cudaSuccess) e = cudaEventRecord(ctx->swap_out[buf], ctx->swap_stream);
+        if (e != cudaSuccess) return fail(cuda_error(e, "moe_swap_rows copy"));
+        pend[npend++] = Pending{c, hot_row, h, cold_row};
         L.rowmap[c] = hot_row;
         L.rowmap[h] = -1 - cold_row;
         if (applied) applied[i] = 1;
         ++done;
     }
+    while (npend > 0)
+        if (int r = join_oldest()) return fail(r);
     return done;
 }
 

@@ -240,7 +240,9 @@ struct moe_ctx {
     uint64_t wait_ns = moe::kDefaultWaitNs;   // bound of every FFN pipeline wait
     bool inject_withhold = false;             // test hook: the next FFN call withholds one copy
     int32_t *counts_dev = nullptr;   // [L][E]
-    uint8_t *staging = nullptr;      // one expert row in HBM
+    uint8_t *staging = nullptr;      // two expert rows in HBM (swaps alternate between them)
+    cudaStream_t swap_stream = nullptr;   // a swap's copy back to the host bank
+    cudaEvent_t swap_in[2] = {nullptr, nullptr}, swap_out[2] = {nullptr, nullptr};
     int32_t *status_dev = nullptr;   // bounded-wait status word
     uint8_t *probe_host = nullptr;   // pinned probe buffer for moe_probe_link
     uint8_t *probe_dev = nullptr;

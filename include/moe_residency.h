@@ -278,8 +278,13 @@ int moe_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_
  * order: promote[i] must be cold and demote[i] hot in the library's CPU copy
  * of the placement, else applied[i] = 0 (stale, nothing changes).  An applied
  * pair enqueues on `stream`: hot row -> HBM staging, cold row -> the hot
- * slot, staging -> the cold slot (weights and scales together), then a
- * two-element device row-map write ordered after the copies.  promote,
+ * slot, then staging -> the cold slot (weights and scales together) on the
+ * context's own swap stream, ordered after the first two, so that it runs
+ * beside the next pair's copy into HBM (the host link carries both
+ * directions at once; consecutive pairs alternate between two staging
+ * rows); then a two-element device row-map write on `stream`, ordered after
+ * all three copies.  Work enqueued on `stream` after the call sees every
+ * applied pair complete.  promote,
  * demote: host int32 [n]; applied: host int32 [n] out (may be NULL).  Returns
  * the number applied (>= 0) or an error code.  Never call it while a step of
  * this layer is in flight on another stream.  If enqueuing a pair's copies or
