@@ -119,7 +119,7 @@ inline Geom make_geom(const moe_geom &g) {
 // pick's index in its bank's list), so the two banks never share a row and
 // each expert's rows are contiguous.
 struct WsLayout {
-    size_t hdr, act_row, act_off, picks, epos, ecnt, xq, xgexp, h32, hq, hexp, gu32, y32, claim;
+    size_t hdr, act_row, act_off, picks, epos, ecnt, ccnt, xq, xgexp, h32, hq, hexp, gu32, y32, claim;
     // prefill-sized steps with MXFP8 activations: per bank, the first token
     // tile of each active row, and the tiles' B-operand block scales
     size_t tile_off, sfx, sfh;
@@ -172,6 +172,9 @@ inline WsLayout ws_layout(const Geom &g, int T) {
     w.picks = take(2 * P * 4);                // [2][P]
     w.epos = take((size_t)g.E * 4);           // [E] start of expert e's picks in its bank list
     w.ecnt = take((size_t)g.E * 4);           // [E] picks per expert (large-step routing path)
+    // large steps: picks per expert in each 32-token chunk, then each chunk's
+    // first place in its expert's list ([E][chunks], expert-major)
+    w.ccnt = take(split_k_steps(T) ? 0 : (size_t)g.E * ((T + 31) / 32) * 4);
     w.xq = take(P * (size_t)g.H * 2);         // [P][H/64][2][64] e4m3 token rows in pick order (two pieces)
     w.xgexp = take(P * 4);                    // [P] int32 scale exponents of those rows
     w.h32 = take(P * (size_t)g.I * 4);        // [P][I] fp32 gate/up output (by g; by slot on CUDA cores)

@@ -371,35 +371,30 @@ __device__ void warp_scan_bank(int b, int rows, int E, const int32_t *rowexp, co
     }
 }
 
-// Fill expert e's picks (in slot order) starting at pos in bank b's list.
-__device__ __forceinline__ void warp_fill_expert(int e, int b, int pos, const int32_t *ids, WsPtrs ws,
-                                                 int lane) {
-    const int P = ws.P;
-    for (int base = 0; base < P; base += 32) {
-        int s = base + lane;
-        bool hit = s < P && ids[s] == e;
-        unsigned msk = __ballot_sync(0xffffffffu, hit);
-        if (hit) ws.picks[b * P + pos + __popc(msk & ((1u << lane) - 1u))] = s;
-        pos += __popc(msk);
-    }
-}
-
-// Large steps, stage 1: one warp per token.
+// Large steps, stage 1: one warp per token.  For the split it also counts,
+// order-free, the picks of each expert and of each (expert, 32-token chunk).
 template <int KM, int NV>
 __global__ void __launch_bounds__(256) route_tokens(const float *__restrict__ logits, int T, int E, int k,
                                                    int32_t *counts, int32_t *__restrict__ ids,
-                                                   float *__restrict__ w, int32_t *ecnt) {
+                                                   float *__restrict__ w, int32_t *ecnt, int32_t *ccnt) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
     float v[NV];
     load_logits<NV>(logits + (size_t)t * E, E, lane, v);
     route_one<KM, NV>(v, t, E, k, lane, counts, ids, w, nullptr, nullptr);
-    if (ecnt && lane < k) red_relaxed_add(ecnt + ids[t * k + lane], 1);   // picks per expert for the split (order-free)
+    if (ecnt && lane < k) {
+        const int e = ids[t * k + lane];
+        red_relaxed_add(ecnt + e, 1);
+        red_relaxed_add(ccnt + (size_t)e * ((T + 31) / 32) + t / 32, 1);
+    }
 }
 
-// Large steps, stage 2: the active-row scan over the per-expert counts (one CTA).
-__global__ void __launch_bounds__(1024) split_scan(const int32_t *__restrict__ ecnt, int E,
+// Large steps, stage 2 (one CTA): the active-row scan over the per-expert
+// counts, then for each active expert the first place of each 32-token
+// chunk's picks in its bank list (its list start plus the earlier chunks'
+// counts: one warp scan per expert), written over the chunk counts.
+__global__ void __launch_bounds__(1024) split_scan(const int32_t *__restrict__ ecnt, int32_t *ccnt, int nch, int E,
                                                    const int32_t *__restrict__ rowmap, int n_hot,
                                                    int n_cold, WsPtrs ws) {
     extern __shared__ int32_t sm[];
@@ -415,22 +410,58 @@ __global__ void __launch_bounds__(1024) split_scan(const int32_t *__restrict__ e
     }
     __syncthreads();
     if (warp < 2) warp_scan_bank(warp, warp == 0 ? n_hot : n_cold, E, rowexp, cnt, ws.epos, ws, lane);
+    __syncthreads();   // every active expert's list start is in ws.epos
+    for (int e = warp; e < E; e += (int)(blockDim.x >> 5)) {
+        int base = ws.epos[e];
+        if (base < 0) continue;   // no picks (warp-uniform)
+        int32_t *row = ccnt + (size_t)e * nch;
+        for (int c0 = 0; c0 < nch; c0 += 32) {
+            const int c = c0 + lane;
+            const int v = c < nch ? row[c] : 0;
+            int inc = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += o;
+            }
+            if (c < nch) row[c] = base + inc - v;
+            base += __shfl_sync(0xffffffffu, inc, 31);
+        }
+    }
 }
 
-// Large steps, stage 3: one warp per active expert fills its picks.
-__global__ void __launch_bounds__(256) split_fill(const int32_t *__restrict__ ids, int E,
-                                                  const int32_t *__restrict__ rowmap, WsPtrs ws) {
-    const int lane = threadIdx.x & 31;
-    const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (e >= E) return;
-    int pos = ws.epos[e];
-    if (pos < 0) return;
-    warp_fill_expert(e, rowmap[e] >= 0 ? 0 : 1, pos, ids, ws, lane);
+// Large steps, stage 3: one warp per 32-token chunk places the chunk's picks,
+// 32 slots at a time in slot order: the lanes holding the same expert
+// (__match_any_sync) take consecutive places from that expert's cursor for
+// this chunk, lower slots first, so each expert's picks stay in slot order.
+__global__ void __launch_bounds__(32) split_place(const int32_t *__restrict__ ids, int T, int k, int E,
+                                                   const int32_t *__restrict__ coff, const int32_t *__restrict__ rowmap,
+                                                   WsPtrs ws) {
+    extern __shared__ int32_t cur[];   // [E] the chunk's next place per expert
+    const int lane = threadIdx.x, c = blockIdx.x, nch = (T + 31) / 32;
+    for (int e = lane; e < E; e += 32) cur[e] = coff[(size_t)e * nch + c];
+    __syncwarp();
+    const int P = ws.P;
+    const int s0 = c * 32 * k, s1 = min(P, s0 + 32 * k);
+    for (int base = s0; base < s1; base += 32) {
+        const int s = base + lane;
+        const bool live = s < s1;
+        const int e = live ? ids[s] : -1;
+        const unsigned grp = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(grp & ((1u << lane) - 1u));
+        const int start = live ? cur[e] : 0;
+        __syncwarp();
+        if (live) {
+            ws.picks[(rowmap[e] < 0 ? P : 0) + start + rank] = s;
+            if (rank == 0) cur[e] = start + __popc(grp);
+        }
+        __syncwarp();
+    }
 }
 
 template <int KM, int NV>
 int launch_route_km(const moe_ctx *ctx, const Layer &L, const float *logits, int T, int32_t *counts, int32_t *ids,
-                    float *w, WsPtrs ws, int32_t *ecnt, cudaStream_t s) {
+                    float *w, WsPtrs ws, int32_t *ecnt, int32_t *ccnt, cudaStream_t s) {
     const Geom &g = ctx->g;
     const int P = ws.P;
     const size_t smem = sizeof(int32_t) * ((size_t)P + 2 * (size_t)g.E);
@@ -441,31 +472,34 @@ int launch_route_km(const moe_ctx *ctx, const Layer &L, const float *logits, int
         return MOE_OK;
     }
     if (T <= kSmallMaxT && P <= kSmallMaxP) {
-        route_tokens<KM, NV><<<(T + 7) / 8, 256, 0, s>>>(logits, T, g.E, g.k, counts, ids, w, nullptr);
+        route_tokens<KM, NV><<<(T + 7) / 8, 256, 0, s>>>(logits, T, g.E, g.k, counts, ids, w, nullptr, nullptr);
         MOE_LAUNCH_CHECK();
         split_picks<<<1, kSmallThreads, smem, s>>>(ids, g.E, L.rowmap_dev, L.n_hot, ws);
         MOE_LAUNCH_CHECK();
         return MOE_OK;
     }
+    const int nch = (T + 31) / 32;
     MOE_CUDA_TRY(cudaMemsetAsync(ecnt, 0, sizeof(int32_t) * g.E, s));
-    route_tokens<KM, NV><<<(T + 7) / 8, 256, 0, s>>>(logits, T, g.E, g.k, counts, ids, w, ecnt);
+    MOE_CUDA_TRY(cudaMemsetAsync(ccnt, 0, sizeof(int32_t) * g.E * nch, s));
+    route_tokens<KM, NV><<<(T + 7) / 8, 256, 0, s>>>(logits, T, g.E, g.k, counts, ids, w, ecnt, ccnt);
     MOE_LAUNCH_CHECK();
-    split_scan<<<1, 1024, sizeof(int32_t) * 3 * (size_t)g.E, s>>>(ecnt, g.E, L.rowmap_dev, L.n_hot, L.n_cold, ws);
+    split_scan<<<1, 1024, sizeof(int32_t) * 3 * (size_t)g.E, s>>>(ecnt, ccnt, nch, g.E, L.rowmap_dev, L.n_hot,
+                                                                   L.n_cold, ws);
     MOE_LAUNCH_CHECK();
-    split_fill<<<(g.E + 7) / 8, 256, 0, s>>>(ids, g.E, L.rowmap_dev, ws);
+    split_place<<<nch, 32, sizeof(int32_t) * (size_t)g.E, s>>>(ids, T, g.k, g.E, ccnt, L.rowmap_dev, ws);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
 
 template <int KM>
 int launch_route_nv(const moe_ctx *ctx, const Layer &L, const float *logits, int T, int32_t *counts, int32_t *ids,
-                    float *w, WsPtrs ws, int32_t *ecnt, cudaStream_t s) {
+                    float *w, WsPtrs ws, int32_t *ecnt, int32_t *ccnt, cudaStream_t s) {
     const int E = ctx->g.E;
-    if (E <= 128) return launch_route_km<KM, 4>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
-    if (E <= 256) return launch_route_km<KM, 8>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
-    if (E <= 384) return launch_route_km<KM, 12>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
-    if (E <= 512) return launch_route_km<KM, 16>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
-    return launch_route_km<KM, 32>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
+    if (E <= 128) return launch_route_km<KM, 4>(ctx, L, logits, T, counts, ids, w, ws, ecnt, ccnt, s);
+    if (E <= 256) return launch_route_km<KM, 8>(ctx, L, logits, T, counts, ids, w, ws, ecnt, ccnt, s);
+    if (E <= 384) return launch_route_km<KM, 12>(ctx, L, logits, T, counts, ids, w, ws, ecnt, ccnt, s);
+    if (E <= 512) return launch_route_km<KM, 16>(ctx, L, logits, T, counts, ids, w, ws, ecnt, ccnt, s);
+    return launch_route_km<KM, 32>(ctx, L, logits, T, counts, ids, w, ws, ecnt, ccnt, s);
 }
 
 }  // namespace
@@ -488,11 +522,12 @@ int launch_route_split(moe_ctx *ctx, int layer, const float *logits, int T, int 
     }
     int32_t *counts = (count_on && T <= g.count_tmax) ? ctx->counts_dev + (size_t)layer * g.E : nullptr;
     int32_t *ecnt = (int32_t *)(ws_base + lay.ecnt);
+    int32_t *ccnt = (int32_t *)(ws_base + lay.ccnt);
     // the lanes' sorted lists hold KM >= k entries; each lane holds NV >= E/32
     // of a token's logits
-    if (g.k <= 4) return launch_route_nv<4>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
-    if (g.k <= 8) return launch_route_nv<8>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
-    return launch_route_nv<16>(ctx, L, logits, T, counts, ids, w, ws, ecnt, s);
+    if (g.k <= 4) return launch_route_nv<4>(ctx, L, logits, T, counts, ids, w, ws, ecnt, ccnt, s);
+    if (g.k <= 8) return launch_route_nv<8>(ctx, L, logits, T, counts, ids, w, ws, ecnt, ccnt, s);
+    return launch_route_nv<16>(ctx, L, logits, T, counts, ids, w, ws, ecnt, ccnt, s);
 }
 
 // Two-element row-map write, ordered on the stream after a swap's copies.
