@@ -675,6 +675,8 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
 
 #include "ffn_tc_decode.cuh"
 
+constexpr int kKeep = 4;   // 16-byte (x) or 8-value (h) columns a prep thread keeps in registers
+
 // Exponent e of a row whose largest |value| is mx: mx * 2^-e lies in
 // (224, 448], the top binade of e4m3 (largest finite 448 = 0.875 * 2^9).
 __device__ __forceinline__ int row_exponent(float mx) {
@@ -754,18 +756,31 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict_
     const int t = L.picks[p] / k;
     const uint4 *row = (const uint4 *)(x + (int64_t)t * H);
     const int n8 = H / 8;
+    // a row of up to kKeep 16-byte columns per thread (H <= 8192) is read once
+    // and kept in registers for the conversion; a wider one is read twice
+    const bool keep = n8 <= kKeep * (int)blockDim.x;
+    uint4 kv[kKeep];
     float mx = 0.0f;
-    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-        const uint4 v = row[i];
+    auto row_max = [&](const uint4 v) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
             mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[q] << 16)), fabsf(__uint_as_float(w[q] & 0xFFFF0000u))));
+    };
+    if (keep) {
+#pragma unroll
+        for (int c = 0; c < kKeep; ++c) {
+            const int i = threadIdx.x + c * blockDim.x;
+            kv[c] = i < n8 ? row[i] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int c = 0; c < kKeep; ++c) row_max(kv[c]);   // zero columns past the row change no maximum
+    } else {
+        for (int i = threadIdx.x; i < n8; i += blockDim.x) row_max(row[i]);
     }
     const int e = row_exponent(block_max(mx, red));
     uint8_t *dst = xq + (int64_t)g * H * 2;
-    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-        const uint4 v = row[i];
+    auto convert = [&](const uint4 v, int i) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         float f[8];
 #pragma unroll
@@ -774,6 +789,15 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict_
             f[2 * q + 1] = ldexpf(__uint_as_float(w[q] & 0xFFFF0000u), -e);
         }
         store_pieces<PERM>(dst, i, f);
+    };
+    if (keep) {
+#pragma unroll
+        for (int c = 0; c < kKeep; ++c) {
+            const int i = threadIdx.x + c * blockDim.x;
+            if (i < n8) convert(kv[c], i);
+        }
+    } else {
+        for (int i = threadIdx.x; i < n8; i += blockDim.x) convert(row[i], i);
     }
     if (threadIdx.x == 0) xgexp[g] = e;
     if (gu32) {   // split units: clear this pick's gate/up sums before the gate/up GEMM adds into them
@@ -820,21 +844,50 @@ __global__ void __launch_bounds__(256) prep_h_kernel(BankLists L0, BankLists L1,
     if (p >= L.hdr[kHdrNPicks + b]) return;
     const int g = bank_offset(L, b, P) + p;
     const int n8 = I / 8;
+    // a row of up to kKeep 8-value columns per thread (I <= 8192) is read once
+    // and kept in registers for the conversion; a wider one is read twice
+    const bool keep = n8 <= kKeep * (int)blockDim.x;
+    float kf[kKeep][8];
     float mx = 0.0f;
-    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-        float f[8];
-        h_values(h32, gu32, g, I, i, f);
+    if (keep) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(f[q]));
+        for (int c = 0; c < kKeep; ++c) {
+            const int i = threadIdx.x + c * blockDim.x;
+            if (i < n8) {
+                h_values(h32, gu32, g, I, i, kf[c]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(kf[c][q]));
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+            float f[8];
+            h_values(h32, gu32, g, I, i, f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(f[q]));
+        }
     }
     const int e = row_exponent(block_max(mx, red));
     uint8_t *dst = hq + (int64_t)g * I * 2;
-    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-        float f[8];
-        h_values(h32, gu32, g, I, i, f);
+    if (keep) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) f[q] = ldexpf(f[q], -e);
-        store_pieces<PERM>(dst, i, f);
+        for (int c = 0; c < kKeep; ++c) {
+            const int i = threadIdx.x + c * blockDim.x;
+            if (i < n8) {
+                float f[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) f[q] = ldexpf(kf[c][q], -e);
+                store_pieces<PERM>(dst, i, f);
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+            float f[8];
+            h_values(h32, gu32, g, I, i, f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] = ldexpf(f[q], -e);
+            store_pieces<PERM>(dst, i, f);
+        }
     }
     if (threadIdx.x == 0) hexp[g] = e;
     if (y32) {
