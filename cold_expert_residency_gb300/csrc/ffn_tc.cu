@@ -736,30 +736,39 @@ __device__ __forceinline__ float block_max(float mx, float *red) {
 // two e4m3 pieces per 64-wide chunk, each row scaled by 2^-e (e in xgexp).
 // b0 >= 0: that bank; b0 < 0: both banks, bank = blockIdx.y.  PERM: decode
 // tiles' K order (see store_pieces).
+constexpr int kPrepWarps = 8;    // picks per prep_x block (one warp each) on large steps; 1 on small ones
+constexpr int kLaneCols = 16;    // 16-byte columns of a row a lane keeps (H <= 4096)
+
+// Gather one pick's token row, scale it by the power of two that puts its
+// largest |value| in (224, 448], split it into the two e4m3 pieces: one warp
+// per pick, the row in the lanes' registers, the maximum a warp reduction.
+// Blocks of blockDim.x / 32 picks (a small step spreads its picks over more
+// blocks).
 template <bool PERM>
-__global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict__ x, int H, int k, BankLists L0,
-                                                     BankLists L1, int b0, int P, uint8_t *__restrict__ xq,
-                                                     int32_t *__restrict__ xgexp, int32_t *sched, int32_t *claim,
-                                                     float *__restrict__ gu32, int I) {
-    __shared__ float red[8];
-    const int p = blockIdx.x, b = b0 >= 0 ? b0 : (int)blockIdx.y;
+__global__ void __launch_bounds__(32 * kPrepWarps) prep_x_kernel(const uint16_t *__restrict__ x, int H, int k,
+                                                                BankLists L0, BankLists L1, int b0, int P,
+                                                                uint8_t *__restrict__ xq, int32_t *__restrict__ xgexp,
+                                                                int32_t *sched, int32_t *claim,
+                                                                float *__restrict__ gu32, int I) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int p = blockIdx.x * (int)(blockDim.x >> 5) + warp, b = b0 >= 0 ? b0 : (int)blockIdx.y;
     const BankLists &L = b ? L1 : L0;
-    if (p == 0 && blockIdx.y == 0) {
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
         // reset the work counters (and both GEMMs' SM claims) of this call's launches,
         // stream-ordered before them; a one-bank call leaves the other bank's alone
         if (threadIdx.x < 4 && (b0 < 0 || (int)threadIdx.x / 2 == b0)) sched[threadIdx.x] = 0;
         if (claim)
             for (int i = threadIdx.x; i < 2 * 1024; i += blockDim.x) claim[i] = 0;
     }
-    if (p >= L.hdr[kHdrNPicks + b]) return;
+    if (p >= L.hdr[kHdrNPicks + b]) return;   // warp-uniform
     const int g = bank_offset(L, b, P) + p;
     const int t = L.picks[p] / k;
     const uint4 *row = (const uint4 *)(x + (int64_t)t * H);
     const int n8 = H / 8;
-    // a row of up to kKeep 16-byte columns per thread (H <= 8192) is read once
-    // and kept in registers for the conversion; a wider one is read twice
-    const bool keep = n8 <= kKeep * (int)blockDim.x;
-    uint4 kv[kKeep];
+    // a row of up to kLaneCols 16-byte columns per lane is read once and kept
+    // for the conversion; a wider one is read twice
+    const bool keep = n8 <= 32 * kLaneCols;
+    uint4 kv[kLaneCols];
     float mx = 0.0f;
     auto row_max = [&](const uint4 v) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -769,16 +778,18 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict_
     };
     if (keep) {
 #pragma unroll
-        for (int c = 0; c < kKeep; ++c) {
-            const int i = threadIdx.x + c * blockDim.x;
+        for (int c = 0; c < kLaneCols; ++c) {
+            const int i = lane + 32 * c;
             kv[c] = i < n8 ? row[i] : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int c = 0; c < kKeep; ++c) row_max(kv[c]);   // zero columns past the row change no maximum
+        for (int c = 0; c < kLaneCols; ++c) row_max(kv[c]);   // zero columns past the row change no maximum
     } else {
-        for (int i = threadIdx.x; i < n8; i += blockDim.x) row_max(row[i]);
+        for (int i = lane; i < n8; i += 32) row_max(row[i]);
     }
-    const int e = row_exponent(block_max(mx, red));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const int e = row_exponent(mx);
     uint8_t *dst = xq + (int64_t)g * H * 2;
     auto convert = [&](const uint4 v, int i) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -792,17 +803,17 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t *__restrict_
     };
     if (keep) {
 #pragma unroll
-        for (int c = 0; c < kKeep; ++c) {
-            const int i = threadIdx.x + c * blockDim.x;
+        for (int c = 0; c < kLaneCols; ++c) {
+            const int i = lane + 32 * c;
             if (i < n8) convert(kv[c], i);
         }
     } else {
-        for (int i = threadIdx.x; i < n8; i += blockDim.x) convert(row[i], i);
+        for (int i = lane; i < n8; i += 32) convert(row[i], i);
     }
-    if (threadIdx.x == 0) xgexp[g] = e;
+    if (lane == 0) xgexp[g] = e;
     if (gu32) {   // split units: clear this pick's gate/up sums before the gate/up GEMM adds into them
         float4 *z = (float4 *)(gu32 + (int64_t)g * 2 * I);
-        for (int i = threadIdx.x; i < I / 2; i += blockDim.x) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = lane; i < I / 2; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -1133,6 +1144,8 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
     a2.ks = std::min(TcCfg<NMAX, MX>::kSplit, a2.part.steps());
     const int blocks1 = prefill_blocks(ctx, a1.b, shared, units1), blocks2 = prefill_blocks(ctx, a1.b, shared, units2);
     const dim3 grid_p(P, a1.b < 0 ? 2 : 1);   // one block per pick (of each bank)
+    const int xw = P >= 4096 ? kPrepWarps : 1;   // picks per prep_x block
+    const dim3 grid_x((P + xw - 1) / xw, a1.b < 0 ? 2 : 1);
     const int pieces = MX ? 1 : 2;
     CUtensorMap m1, m2;
     if (int r = make_piece_map(&m1, ws + lay.xq, g.H, P, NMAX, pieces)) return r;
@@ -1153,7 +1166,7 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
                                                  (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, tile_off, ws + lay.sfx,
                                                  lay.max_tiles);
     } else {
-        prep_x_kernel<false><<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
+        prep_x_kernel<false><<<grid_x, 32 * xw, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
                                                     (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
     }
     MOE_LAUNCH_CHECK();
@@ -1250,10 +1263,12 @@ int launch_bank_decode(moe_ctx *ctx, bool shared, bool cold_rows, TcArgs a1, TcA
     a1.ks = std::min(DecCfg<NMAX>::kSplit, a1.part.steps());
     a2.ks = std::min(DecCfg<NMAX>::kSplit, a2.part.steps());
     const dim3 grid_p(P, a1.b < 0 ? 2 : 1);   // one block per pick (of each bank)
+    const int xw = P >= 4096 ? kPrepWarps : 1;   // picks per prep_x block
+    const dim3 grid_x((P + xw - 1) / xw, a1.b < 0 ? 2 : 1);
     CUtensorMap m1, m2;
     if (int r = make_piece_map(&m1, ws + lay.xq, g.H, P, NMAX)) return r;
     if (int r = make_piece_map(&m2, ws + lay.hq, g.I, P, NMAX)) return r;
-    prep_x_kernel<true><<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
+    prep_x_kernel<true><<<grid_x, 32 * xw, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
                                                (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, a1.gu_out, g.I);
     MOE_LAUNCH_CHECK();
     if (int r = launch_decode_gemm<NMAX, 1>(m1, a1, decode_blocks<NMAX>(ctx, a1.b, shared, units1), false, s)) return r;
