@@ -907,6 +907,76 @@ __global__ void __launch_bounds__(256) prep_h_kernel(BankLists L0, BankLists L1,
     }
 }
 
+constexpr int kHLaneCols = 12;   // 8-value columns of an h row a lane keeps (I <= 3072)
+
+// prep_h for prefill-sized steps: one warp per pick, the row in the lanes'
+// registers, the maximum a warp reduction; the same values and rounding as
+// prep_h_kernel.
+template <bool PERM>
+__global__ void __launch_bounds__(32 * kPrepWarps) prep_h_warp_kernel(BankLists L0, BankLists L1, int b0, int P, int I,
+                                                                     const float *__restrict__ h32,
+                                                                     const float *__restrict__ gu32,
+                                                                     uint8_t *__restrict__ hq,
+                                                                     int32_t *__restrict__ hexp,
+                                                                     float *__restrict__ y32, int H) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int p = blockIdx.x * (int)(blockDim.x >> 5) + warp, b = b0 >= 0 ? b0 : (int)blockIdx.y;
+    const BankLists &L = b ? L1 : L0;
+    if (p >= L.hdr[kHdrNPicks + b]) return;   // warp-uniform
+    const int g = bank_offset(L, b, P) + p;
+    const int n8 = I / 8;
+    const bool keep = n8 <= 32 * kHLaneCols;
+    float kf[kHLaneCols][8];
+    float mx = 0.0f;
+    if (keep) {
+#pragma unroll
+        for (int c = 0; c < kHLaneCols; ++c) {
+            const int i = lane + 32 * c;
+            if (i < n8) {
+                h_values(h32, gu32, g, I, i, kf[c]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(kf[c][q]));
+            }
+        }
+    } else {
+        for (int i = lane; i < n8; i += 32) {
+            float f[8];
+            h_values(h32, gu32, g, I, i, f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(f[q]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const int e = row_exponent(mx);
+    uint8_t *dst = hq + (int64_t)g * I * 2;
+    if (keep) {
+#pragma unroll
+        for (int c = 0; c < kHLaneCols; ++c) {
+            const int i = lane + 32 * c;
+            if (i < n8) {
+                float f[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) f[q] = ldexpf(kf[c][q], -e);
+                store_pieces<PERM>(dst, i, f);
+            }
+        }
+    } else {
+        for (int i = lane; i < n8; i += 32) {
+            float f[8];
+            h_values(h32, gu32, g, I, i, f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] = ldexpf(f[q], -e);
+            store_pieces<PERM>(dst, i, f);
+        }
+    }
+    if (lane == 0) hexp[g] = e;
+    if (y32) {
+        float4 *z = (float4 *)(y32 + (int64_t)L.picks[p] * H);
+        for (int i = lane; i < H / 4; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
 // Split units: this bank's down-GEMM sums (fp32, by slot) -> the bf16 rows of Y.
 __global__ void __launch_bounds__(256) round_y_kernel(BankLists L0, BankLists L1, int b0, int H,
                                                       const float *__restrict__ y32, uint16_t *__restrict__ Y) {
@@ -1180,7 +1250,7 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
                                                  ws + lay.hq, (int32_t *)(ws + lay.hexp),
                                                  (const int32_t *)(ws + lay.tile_off), ws + lay.sfh, lay.max_tiles);
     } else {
-        prep_h_kernel<false><<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I,
+        prep_h_warp_kernel<false><<<grid_x, 32 * xw, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I,
                                                     (const float *)(ws + lay.h32), a1.gu_out, ws + lay.hq,
                                                     (int32_t *)(ws + lay.hexp), a2.y_out, g.H);
     }
