@@ -390,11 +390,8 @@ __global__ void __launch_bounds__(256) route_tokens(const float *__restrict__ lo
     }
 }
 
-// Large steps, stage 2 (one CTA): the active-row scan over the per-expert
-// counts, then for each active expert the first place of each 32-token
-// chunk's picks in its bank list (its list start plus the earlier chunks'
-// counts: one warp scan per expert), written over the chunk counts.
-__global__ void __launch_bounds__(1024) split_scan(const int32_t *__restrict__ ecnt, int32_t *ccnt, int nch, int E,
+// Large steps, stage 2 (one CTA): the active-row scan over the per-expert counts.
+__global__ void __launch_bounds__(1024) split_scan(const int32_t *__restrict__ ecnt, int E,
                                                    const int32_t *__restrict__ rowmap, int n_hot,
                                                    int n_cold, WsPtrs ws) {
     extern __shared__ int32_t sm[];
@@ -410,27 +407,33 @@ __global__ void __launch_bounds__(1024) split_scan(const int32_t *__restrict__ e
     }
     __syncthreads();
     if (warp < 2) warp_scan_bank(warp, warp == 0 ? n_hot : n_cold, E, rowexp, cnt, ws.epos, ws, lane);
-    __syncthreads();   // every active expert's list start is in ws.epos
-    for (int e = warp; e < E; e += (int)(blockDim.x >> 5)) {
-        int base = ws.epos[e];
-        if (base < 0) continue;   // no picks (warp-uniform)
-        int32_t *row = ccnt + (size_t)e * nch;
-        for (int c0 = 0; c0 < nch; c0 += 32) {
-            const int c = c0 + lane;
-            const int v = c < nch ? row[c] : 0;
-            int inc = v;
+}
+
+// Large steps, stage 3: one warp per active expert turns its chunk counts
+// into the first place of each 32-token chunk's picks in its bank list (the
+// expert's list start plus the earlier chunks' counts), over the counts.
+__global__ void __launch_bounds__(256) split_chunks(int32_t *ccnt, int nch, int E, WsPtrs ws) {
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (e >= E) return;
+    int base = ws.epos[e];
+    if (base < 0) return;   // no picks
+    int32_t *row = ccnt + (size_t)e * nch;
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+        const int c = c0 + lane;
+        const int v = c < nch ? row[c] : 0;
+        int inc = v;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, inc, off);
-                if (lane >= off) inc += o;
-            }
-            if (c < nch) row[c] = base + inc - v;
-            base += __shfl_sync(0xffffffffu, inc, 31);
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += o;
         }
+        if (c < nch) row[c] = base + inc - v;
+        base += __shfl_sync(0xffffffffu, inc, 31);
     }
 }
 
-// Large steps, stage 3: one warp per 32-token chunk places the chunk's picks,
+// Large steps, stage 4: one warp per 32-token chunk places the chunk's picks,
 // 32 slots at a time in slot order: the lanes holding the same expert
 // (__match_any_sync) take consecutive places from that expert's cursor for
 // this chunk, lower slots first, so each expert's picks stay in slot order.
@@ -483,8 +486,9 @@ int launch_route_km(const moe_ctx *ctx, const Layer &L, const float *logits, int
     MOE_CUDA_TRY(cudaMemsetAsync(ccnt, 0, sizeof(int32_t) * g.E * nch, s));
     route_tokens<KM, NV><<<(T + 7) / 8, 256, 0, s>>>(logits, T, g.E, g.k, counts, ids, w, ecnt, ccnt);
     MOE_LAUNCH_CHECK();
-    split_scan<<<1, 1024, sizeof(int32_t) * 3 * (size_t)g.E, s>>>(ecnt, ccnt, nch, g.E, L.rowmap_dev, L.n_hot,
-                                                                   L.n_cold, ws);
+    split_scan<<<1, 1024, sizeof(int32_t) * 3 * (size_t)g.E, s>>>(ecnt, g.E, L.rowmap_dev, L.n_hot, L.n_cold, ws);
+    MOE_LAUNCH_CHECK();
+    split_chunks<<<(g.E + 7) / 8, 256, 0, s>>>(ccnt, nch, g.E, ws);
     MOE_LAUNCH_CHECK();
     split_place<<<nch, 32, sizeof(int32_t) * (size_t)g.E, s>>>(ids, T, g.k, g.E, ccnt, L.rowmap_dev, ws);
     MOE_LAUNCH_CHECK();
