@@ -1072,8 +1072,10 @@ __device__ __forceinline__ int sfb_byte(int r, int kblk) {
 template <class Load8>
 __device__ __forceinline__ void mx8_row(int n8, Load8 load8, uint8_t *__restrict__ dst, uint8_t *__restrict__ slab,
                                         int r) {
-    for (int i0 = 0; i0 < n8; i0 += blockDim.x) {   // every thread takes part in each pass (warp shuffles)
-        const int i = i0 + threadIdx.x;
+    // one warp per row: every lane takes part in each pass (warp shuffles)
+    const int lane = threadIdx.x & 31;
+    for (int i0 = 0; i0 < n8; i0 += 32) {
+        const int i = i0 + lane;
         float v[8];
         if (i < n8) {
             load8(i, v);
@@ -1090,14 +1092,15 @@ __device__ __forceinline__ void mx8_row(int n8, Load8 load8, uint8_t *__restrict
     }
 }
 
+// One warp per pick, blockDim.x / 32 picks per block.
 __global__ void __launch_bounds__(256) prep_x_mx8_kernel(const uint16_t *__restrict__ x, int H, int k, BankLists L0,
                                                          BankLists L1, int b0, int P, uint8_t *__restrict__ xq,
                                                          int32_t *__restrict__ xgexp, int32_t *sched, int32_t *claim,
                                                          const int32_t *__restrict__ tile_off, uint8_t *__restrict__ sfx,
                                                          int max_tiles) {
-    const int p = blockIdx.x, b = b0 >= 0 ? b0 : (int)blockIdx.y;
+    const int p = blockIdx.x * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5), b = b0 >= 0 ? b0 : (int)blockIdx.y;
     const BankLists &L = b ? L1 : L0;
-    if (p == 0 && blockIdx.y == 0) {
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
         if (threadIdx.x < 4 && (b0 < 0 || (int)threadIdx.x / 2 == b0)) sched[threadIdx.x] = 0;
         if (claim)
             for (int i = threadIdx.x; i < 2 * 1024; i += blockDim.x) claim[i] = 0;
@@ -1118,14 +1121,15 @@ __global__ void __launch_bounds__(256) prep_x_mx8_kernel(const uint16_t *__restr
             v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
         }
     }, xq + (int64_t)g * H, slab, r);
-    if (threadIdx.x == 0) xgexp[g] = 0;   // the block scales carry the magnitudes
+    if ((threadIdx.x & 31) == 0) xgexp[g] = 0;   // the block scales carry the magnitudes
 }
 
 __global__ void __launch_bounds__(256) prep_h_mx8_kernel(BankLists L0, BankLists L1, int b0, int P, int I,
                                                          const float *__restrict__ h32, uint8_t *__restrict__ hq,
                                                          int32_t *__restrict__ hexp, const int32_t *__restrict__ tile_off,
                                                          uint8_t *__restrict__ sfh, int max_tiles) {
-    const int p = blockIdx.x, b = b0 >= 0 ? b0 : (int)blockIdx.y;
+    // one warp per pick, blockDim.x / 32 picks per block
+    const int p = blockIdx.x * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5), b = b0 >= 0 ? b0 : (int)blockIdx.y;
     const BankLists &L = b ? L1 : L0;
     if (p >= L.hdr[kHdrNPicks + b]) return;
     const int g = bank_offset(L, b, P) + p;
@@ -1138,7 +1142,7 @@ __global__ void __launch_bounds__(256) prep_h_mx8_kernel(BankLists L0, BankLists
         const float4 a = row[2 * i], c = row[2 * i + 1];
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
     }, hq + (int64_t)g * I, slab, r);
-    if (threadIdx.x == 0) hexp[g] = 0;
+    if ((threadIdx.x & 31) == 0) hexp[g] = 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -1232,7 +1236,7 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
         a2.sf_groups = gh;
         tile_scan_kernel<<<1, 64, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, tile_off);
         MOE_LAUNCH_CHECK();
-        prep_x_mx8_kernel<<<grid_p, 256, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
+        prep_x_mx8_kernel<<<grid_x, 32 * xw, 0, s>>>(x, g.H, g.k, a1.lists[0], a1.lists[1], a1.b, P, ws + lay.xq,
                                                  (int32_t *)(ws + lay.xgexp), a1.sched, a1.claim, tile_off, ws + lay.sfx,
                                                  lay.max_tiles);
     } else {
@@ -1246,7 +1250,7 @@ int launch_bank(moe_ctx *ctx, const Layer &layer, bool shared, TcArgs a1, TcArgs
     const CUtensorMap &sm2 = ctx->stage_pool ? ctx->stage_map[1] : layer.wmap[1][1];
     if (int r = launch_gemm<NMAX, 1, MX>(m1, layer.wmap[0][0], layer.wmap[1][0], sm1, a1, blocks1, s)) return r;
     if (MX) {
-        prep_h_mx8_kernel<<<grid_p, 256, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
+        prep_h_mx8_kernel<<<grid_x, 32 * xw, 0, s>>>(a1.lists[0], a1.lists[1], a1.b, P, g.I, (const float *)(ws + lay.h32),
                                                  ws + lay.hq, (int32_t *)(ws + lay.hexp),
                                                  (const int32_t *)(ws + lay.tile_off), ws + lay.sfh, lay.max_tiles);
     } else {
