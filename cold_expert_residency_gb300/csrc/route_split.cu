@@ -15,11 +15,14 @@
 // Decode steps (at most 256 tokens) build the lists in one CTA of 512 threads
 // whose work is sized by the step's picks, not by the experts: one
 // block-wide scan over the per-row pick counts gives every active row its
-// list position and offset, and each pick finds its place by counting the
-// earlier picks of its expert.  Steps of at most 32 tokens route in the same
-// CTA; larger decode steps route with one warp per token across CTAs first.
-// Larger steps (prefill) route the same way and build the lists from
-// per-expert counts in two more kernels.
+// list position and offset, and each pick's place adds the number of earlier
+// picks of its expert (read from the expert's token mask up to 32 tokens,
+// counted beyond).  Steps of at most 32 tokens route in the same CTA; larger
+// decode steps route with one warp per token across CTAs first.  Larger
+// steps (prefill) route the same way, counting picks per expert and per
+// (expert, 32-token chunk), then build the lists in three more kernels: the
+// active-row scan, each chunk's first place per expert, and the placement of
+// each chunk's picks in slot order.
 #include "moe_internal.cuh"
 
 #include <climits>
