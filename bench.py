@@ -842,11 +842,12 @@ def measure_prefill(S, ctx, pcfg, args, layer, fmt=0):
     if fmt == 0:
         peak, src = S.tf_burst, (f"{S.peak_src} bf16 dense burst ('of measured'): rows carry bf16-class precision "
                                  "as two e4m3 pieces, two fp8-rate MMAs per product = the bf16 rate")
-        kern = "ffn_tc_kernel<192,1,hot,false> + <192,2,hot,false> with prep_x, prep_h"
+        kern = f"ffn_tc_kernel<{kPrefillTile},1,hot,false> + <{kPrefillTile},2,hot,false> with prep_x, prep_h"
     else:
         peak, src = 2.0 * S.tf_burst, (f"{S.peak_src} bf16 dense burst x 2 (the nominal fp8 : bf16 dense ratio, "
                                        "4.5 : 2.25 PFLOP/s; 'of measured'): one fp8-rate MMA per product")
-        kern = "ffn_tc_kernel<192,1,hot,true> + <192,2,hot,true> with tile_scan, prep_x_mx8, prep_h_mx8"
+        kern = (f"ffn_tc_kernel<{kPrefillTileMx},1,hot,true> + <{kPrefillTileMx},2,hot,true> with tile_scan, "
+                "prep_x_mx8, prep_h_mx8")
     return {
         "workload": WORKLOADS["prefill"], "tokens_per_step": T, "steps": steps,
         "activations": "two e4m3 pieces per value (bf16-class)" if fmt == 0 else "MXFP8 (e4m3, e8m0 per 32)",
@@ -864,7 +865,7 @@ def measure_prefill_shift(S, ctx, args, layer=0, slots=16):
     """An 8192-token prefill chunk on split context layer `layer` (295 hot /
     89 cold by the first ranking) right after the domain shift: the logits
     follow the redrawn ranking, so the new domain's popular experts are
-    still cold and draw several 192-token tiles each.  Timed with the cold
+    still cold and draw several 144-token tiles each.  Timed with the cold
     staging pool off and on (`slots` rows)."""
     acfg = synth.get_config("adaptive")
     scfg = dataclasses.replace(acfg, name="prefill_shift", T=8192, shift_at=0, steps=1)
@@ -906,7 +907,11 @@ def measure_prefill_shift(S, ctx, args, layer=0, slots=16):
     return out
 
 
-kPrefillTile = 192
+# Token rows per tile of the prefill FFN on steps of more than 256 tokens:
+# two-piece rows (the default format), MXFP8 rows.  The library's own widths;
+# the link-byte accounting of the shifted prefill chunk counts tiles with them.
+kPrefillTile = 144
+kPrefillTileMx = 160
 
 
 def line_for(S, name, cfg, m, args, cpu):
