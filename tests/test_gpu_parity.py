@@ -210,15 +210,19 @@ def test_restore_round_trip_is_lossless(impl):
 
 
 def test_workspace_serves_every_smaller_step():
-    """A workspace sized for T_max serves every step of at most T_max tokens:
-    the size is non-decreasing in T although steps of at most 256 tokens hold
-    extra fp32 partial-sum rows that larger steps do not."""
+    """A workspace (and a host-buffer step's scratch area) sized for T_max
+    serves every step of at most T_max tokens: the size is non-decreasing in T
+    although steps of at most 256 tokens hold extra fp32 partial-sum rows that
+    larger steps do not."""
     import cold_expert_residency_gb300 as moe
     for name in ("tiny", "decode1"):
         cfg = synth.get_config(name)
         ctx = moe.moe_create(1, cfg.E, cfg.k, cfg.H, cfg.I, 600)
         try:
             sizes = [moe.moe_workspace_bytes(ctx, T) for T in range(0, 601)]
+            assert all(b >= a for a, b in zip(sizes, sizes[1:])), name
+            # the host-buffer step's scratch area likewise
+            sizes = [moe.moe_step_scratch_bytes(ctx, T) for T in range(0, 601)]
             assert all(b >= a for a, b in zip(sizes, sizes[1:])), name
         finally:
             moe.moe_destroy(ctx)
