@@ -306,16 +306,17 @@ def source_sha():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config):
-    """DRAM bytes per launch of the hot-bank FFN from a committed ncu summary,
-    if it was taken on the current kernel source; else None."""
+def profiled_traffic(config, key="bytes_per_hot_expert"):
+    """DRAM bytes of an FFN call per unit of work (per distinct hot expert for
+    the decode calls, per routed pick for the prefill calls) from a committed
+    ncu summary, if it was taken on the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         e = d.get(config)
         if e and e.get("source_sha") == source_sha():
-            return e.get("bytes_per_hot_expert")
+            return e.get(key)
     except Exception:
         pass
     return None
@@ -848,6 +849,13 @@ def measure_prefill(S, ctx, pcfg, args, layer, fmt=0):
                                        "4.5 : 2.25 PFLOP/s; 'of measured'): one fp8-rate MMA per product")
         kern = (f"ffn_tc_kernel<{kPrefillTileMx},1,hot,true> + <{kPrefillTileMx},2,hot,true> with tile_scan, "
                 "prep_x_mx8, prep_h_mx8")
+    # DRAM bytes of the FFN call (prep kernels and both GEMMs), captured on the
+    # 64-expert profiling case (about 128 picks per expert, as here) and scaled
+    # by the routed picks: weights and token rows both grow with them
+    per_pick = profiled_traffic("prefill_mxfp8" if fmt else "prefill", "bytes_per_pick")
+    traffic = per_pick * picks if per_pick is not None else None
+    traffic_src = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the FFN call's launches on the 64-expert "
+                   f"profiling case, per routed pick x {picks} picks") if per_pick is not None else None
     return {
         "workload": WORKLOADS["prefill"], "tokens_per_step": T, "steps": steps,
         "activations": "two e4m3 pieces per value (bf16-class)" if fmt == 0 else "MXFP8 (e4m3, e8m0 per 32)",
@@ -855,8 +863,8 @@ def measure_prefill(S, ctx, pcfg, args, layer, fmt=0):
         "step_us_pct": pct(step_ms),
         "roofline": {"kernel": f"FFN call inside the step ({kern})", "bound": "tensor", "achieved": tf, "peak": peak,
                      "unit": "TFLOP/s", "frac": tf / peak, "flops_per_launch": flops, "peak_source": src,
-                     "hbm_gbs_achieved": 384 * eb / (float(np.mean(ffn)) * 1e-3) / 1e9,
-                     "traffic": None, "us_per_launch": float(np.mean(ffn)) * 1e3},
+                     "hbm_gbs_achieved": pcfg.E * eb / (float(np.mean(ffn)) * 1e-3) / 1e9,
+                     "traffic": traffic, "traffic_source": traffic_src, "us_per_launch": float(np.mean(ffn)) * 1e3},
         "clocks": clocks, "launches_per_step": run.launches_per_step,
     }
 
