@@ -599,6 +599,38 @@ class StepRunner:
             ts.append(ea[0].elapsed_time(ea[1]) * 1e3)
         return ts
 
+    def call_repeated_us(self, call, reps, n):
+        """µs per call of `reps` calls back to back inside one replayed graph
+        (events around the whole run, after an L2 flush): the first call reads
+        its inputs from DRAM, the rest from L2, as a call right after the
+        kernel that wrote them would.  Eager calls between plain stream events
+        when graphs cannot hold events."""
+        S, torch = self.S, self.S.torch
+        ea = (S.event(), S.event())
+        g = None
+        if self.graph is not None and S.in_graph_events:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=S.main):
+                ea[0].record(S.main)
+                for _ in range(reps):
+                    call()
+                ea[1].record(S.main)
+        ts = []
+        for i in range(n):
+            self.load_inputs(i, S.main)
+            with torch.cuda.stream(S.main):
+                S.flush.zero_()
+                if g is not None:
+                    g.replay()
+                else:
+                    ea[0].record(S.main)
+                    for _ in range(reps):
+                        call()
+                    ea[1].record(S.main)
+            S.main.synchronize()
+            ts.append(ea[0].elapsed_time(ea[1]) * 1e3 / reps)
+        return ts
+
     def bank_alone_ms(self, layer_idx, bank, n):
         """One FFN call over `bank` of one layer after its routing, with events
         around the call inside a replayed graph; returns (ms list, distinct
@@ -729,12 +761,22 @@ def measure_decode1(S, ctx, cfg, masks, args, layer=0, want_breakdown=True):
         bias = S.torch.from_numpy(synth.router_bias(cfg, 0)).to(S.dev)
         lo = S.torch.empty((T, cfg.E), dtype=S.torch.float32, device=S.dev)
         router_us = run.call_alone_us(lambda: moe.moe_router_logits(ctx, b.x, wr, bias, T, cfg.E, cfg.H, lo, S.main), n)
+        route_rep = run.call_repeated_us(lambda: moe.moe_route_split_count(
+            ctx, layer, b.logits, T, run.count_on, b.ids, b.w, b.ws_ptr, S.main), 32, 5)
+        router_rep = run.call_repeated_us(
+            lambda: moe.moe_router_logits(ctx, b.x, wr, bias, T, cfg.E, cfg.H, lo, S.main), 32, 5)
         cold_ms = run.bank_alone_ms(0, moe.MOE_BANK_COLD, n)
         out["breakdown"] = {"route_us": float(np.mean(route_us)), "router_gemm_us": float(np.mean(router_us)),
                             "hot_alone_us": float(np.mean(hot_ms)) * 1e3, "cold_alone_us": float(np.mean(cold_ms)) * 1e3,
                             "note": "in-graph events after an L2 flush: the routing call alone, the router GEMM "
                                     "(hidden states -> logits, outside the step) alone, each bank's FFN call "
-                                    "alone after routing"}
+                                    "alone after routing",
+                            "back_to_back": {
+                                "route_us": float(np.median(route_rep)),
+                                "router_gemm_us": float(np.median(router_rep)),
+                                "note": "per call of 32 calls back to back in one replayed graph after an L2 flush "
+                                        "(median of 5): inputs come from L2 after the first call, as right after "
+                                        "the kernel that wrote them, and one event pair spans all 32"}}
         if run.count_on:
             t_on = run.replay_graph_us(lambda: run.enqueue(count=True), n)
             t_off = run.replay_graph_us(lambda: run.enqueue(count=False), n)
