@@ -1,6 +1,7 @@
 """The bench's host-side helpers, on the CPU: the distinct-expert count behind
-the bytes roofline, the peaks it divides by, the profiled-traffic lookup and
-the workload table."""
+the bytes roofline, the peaks it divides by, the profiled-traffic lookups
+(per hot expert for decode calls, per routed pick for prefill calls), the
+workload table and the library's prefill tile widths."""
 import json
 import os
 import sys
@@ -51,3 +52,31 @@ def test_every_workload_is_a_generator_config():
     for name in bench.WORKLOADS:
         cfg = synth.get_config(name)
         assert cfg.E == 384 and cfg.k == 6 and cfg.H == 4096 and cfg.I == 2880
+
+
+def test_prefill_traffic_is_per_routed_pick_of_the_profiled_source():
+    d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for name in ("prefill", "prefill_mxfp8"):
+        rec = d[name]
+        got = bench.profiled_traffic(name, "bytes_per_pick")
+        if rec["source_sha"] != bench.source_sha():
+            assert got is None
+            continue
+        # the per-launch reads and writes add up to the captured step, and the
+        # per-pick figure is that over the captured picks
+        tot = sum(rec["dram_read_bytes"].values()) + sum(rec["dram_write_bytes"].values())
+        assert tot == rec["dram_bytes_captured_step"]
+        assert got == round(tot / rec["picks_captured_step"])
+        # a pick's share of the weights at about 128 picks per expert, within
+        # the rows it adds: 18.8 MB / 128 = 147 KB plus at most ~80 KB of rows
+        assert 140e3 < got < 230e3
+
+
+def test_prefill_tile_widths_match_the_library():
+    # the shifted-prefill link-byte accounting counts tiles with the library's
+    # token-tile widths; read them from the library's source
+    import re
+    src = open(os.path.join(ROOT, "cold_expert_residency_gb300", "csrc", "moe_internal.cuh")).read()
+    two = int(re.search(r"constexpr int kPrefillTile = (\d+);", src).group(1))
+    mx = int(re.search(r"constexpr int kPrefillTileMx = (\d+);", src).group(1))
+    assert (bench.kPrefillTile, bench.kPrefillTileMx) == (two, mx)
