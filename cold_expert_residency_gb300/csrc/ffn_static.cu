@@ -72,8 +72,7 @@ int moe_expert_ffn_bank_static(moe_ctx *ctx, int layer, int bank, const uint16_t
     const int rows = bank == MOE_BANK_HOT ? L.n_hot : (bank == MOE_BANK_COLD ? L.n_cold : L.n_hot + L.n_cold);
     if (T == 0 || rows == 0) return MOE_OK;
 
-    DeviceGuard guard(ctx->device);
-    if (guard.status() != cudaSuccess) return cuda_error(guard.status(), "cudaSetDevice(context device)");
+    MOE_ON_DEVICE(ctx->device);
     uint8_t *scratch = nullptr;
     if (int r = scratch_for_device(ctx->device, &scratch)) return r;
     cudaStream_t s = (cudaStream_t)stream;

@@ -260,7 +260,7 @@ int moe_create(const moe_geom *geom, int device, moe_ctx **out) {
     int ndev = 0;
     MOE_CUDA_TRY(cudaGetDeviceCount(&ndev));
     if (device < 0 || device >= ndev) return set_error(MOE_EINVAL, "no such CUDA device");
-    DeviceGuard guard(device);
+    MOE_ON_DEVICE(device);
     moe_ctx *ctx = new moe_ctx();
     ctx->g = make_geom(g);
     ctx->device = device;
@@ -318,8 +318,7 @@ int moe_set_ffn_impl(moe_ctx *ctx, int impl) {
 int moe_set_cold_staging(moe_ctx *ctx, int slots) {
     if (int r = check_ctx(ctx)) return r;
     if (slots < 0 || slots > kMaxStageSlots) return set_error(MOE_EINVAL, "staging slots out of range (0..64)");
-    DeviceGuard guard(ctx->device);
-    if (guard.status() != cudaSuccess) return cuda_error(guard.status(), "cudaSetDevice(context device)");
+    MOE_ON_DEVICE(ctx->device);
     MOE_CUDA_TRY(cudaDeviceSynchronize());   // no call in flight may still read the old pool
     dev_free(ctx->stage_pool);
     ctx->stage_pool = nullptr;
@@ -341,7 +340,7 @@ int moe_set_cold_staging(moe_ctx *ctx, int slots) {
 int moe_read_stage(moe_ctx *ctx, const void *ws, int T, int32_t *rows, void *stream) {
     if (int r = check_ctx(ctx)) return r;
     if (!ws || !rows || T < 0 || T > ctx->g.Tmax) return set_error(MOE_EINVAL, "bad moe_read_stage arguments");
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     cudaStream_t s = (cudaStream_t)stream;
     const WsLayout lay = ws_layout(ctx->g, T);
     MOE_CUDA_TRY(cudaMemcpyAsync(rows, (const uint8_t *)ws + lay.stage_src, sizeof(int32_t) * kMaxStageSlots,
@@ -361,7 +360,7 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
                    const uint8_t *w2_q, const uint8_t *w2_s, const uint8_t *is_hot, void *stream) {
     if (int r = check_layer(ctx, layer, false)) return r;
     if (!w13_q || !w13_s || !w2_q || !w2_s || !is_hot) return set_error(MOE_EINVAL, "null weight pointer");
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     cudaStream_t s = (cudaStream_t)stream;
     const Geom &g = ctx->g;
     Layer &L = ctx->layers[layer];
@@ -467,7 +466,7 @@ int moe_route_split_count(moe_ctx *ctx, int layer, const float *logits, int T, i
     if (T > 0 && (!logits || !ids || !w || !ws)) return set_error(MOE_EINVAL, "null pointer");
     if (!ws) return set_error(MOE_EINVAL, "null workspace");
     if ((uintptr_t)ws % 256) return set_error(MOE_EINVAL, "workspace must be 256-byte aligned");
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     return launch_route_split(ctx, layer, logits, T, count_on, ids, w, (uint8_t *)ws, (cudaStream_t)stream);
 }
 
@@ -477,7 +476,7 @@ int moe_read_split(moe_ctx *ctx, const void *ws, int T, int bank, int32_t *n_act
     if (!ws || T < 0 || T > ctx->g.Tmax || (bank != 0 && bank != 1) || !n_act || !n_picks || !act_row ||
         !act_off || !picks)
         return set_error(MOE_EINVAL, "bad moe_read_split arguments");
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     cudaStream_t s = (cudaStream_t)stream;
     const WsLayout lay = ws_layout(ctx->g, T);
     const size_t P = (size_t)T * ctx->g.k;
@@ -513,7 +512,7 @@ int moe_expert_ffn_bank(moe_ctx *ctx, int layer, int bank, const uint16_t *x, in
     if (bank == MOE_BANK_BOTH && (L.n_hot == 0 || L.n_cold == 0)) bank = L.n_hot ? MOE_BANK_HOT : MOE_BANK_COLD;
     const int rows = bank == MOE_BANK_HOT ? L.n_hot : (bank == MOE_BANK_COLD ? L.n_cold : L.n_hot + L.n_cold);
     if (T == 0 || rows == 0) return MOE_OK;
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     cudaStream_t s = (cudaStream_t)stream;
     if (ctx->ffn_impl == MOE_FFN_SIMT) {
         for (int bk = 0; bk < 2; ++bk) {
@@ -589,7 +588,7 @@ int moe_layer_step_host(moe_ctx *ctx, int layer, const float *logits, const uint
     uint16_t *d_x = (uint16_t *)(base + p.x), *d_Y = (uint16_t *)(base + p.Y), *d_out = (uint16_t *)(base + p.out);
     int32_t *d_ids = (int32_t *)(base + p.ids);
     float *d_w = (float *)(base + p.w);
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     cudaStream_t s = (cudaStream_t)stream;
     MOE_CUDA_TRY(cudaMemcpyAsync(d_logits, logits, (size_t)T * g.E * 4, cudaMemcpyHostToDevice, s));
     MOE_CUDA_TRY(cudaMemcpyAsync(d_x, x, (size_t)T * g.H * 2, cudaMemcpyHostToDevice, s));
@@ -609,7 +608,7 @@ int moe_router_logits(moe_ctx *ctx, const uint16_t *x, const uint16_t *w_router,
     if (!x || !w_router || !logits) return set_error(MOE_EINVAL, "null pointer");
     if (((uintptr_t)x | (uintptr_t)w_router) % 16 || (uintptr_t)logits % 4 || (uintptr_t)bias % 4)
         return set_error(MOE_EINVAL, "x and w_router must be 16-byte aligned, logits and bias 4-byte aligned");
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     return launch_router(x, w_router, bias, T, E, H, logits, ctx->status_dev, ctx->sms, (cudaStream_t)stream);
 }
 
@@ -617,7 +616,7 @@ int moe_swap_rows(moe_ctx *ctx, int layer, int n, const int32_t *promote, const 
                   int32_t *applied, void *stream) {
     if (int r = check_layer(ctx, layer, true)) return r;
     if (n < 0 || (n > 0 && (!promote || !demote))) return set_error(MOE_EINVAL, "bad swap list");
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     cudaStream_t s = (cudaStream_t)stream;
     Layer &L = ctx->layers[layer];
     const Geom &g = ctx->g;
@@ -692,7 +691,7 @@ int moe_swap_rows(moe_ctx *ctx, int layer, int n, const int32_t *promote, const 
 int moe_read_counts(moe_ctx *ctx, int32_t *host_out, void *stream) {
     if (int r = check_ctx(ctx)) return r;
     if (!host_out) return set_error(MOE_EINVAL, "null output");
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     cudaStream_t s = (cudaStream_t)stream;
     MOE_CUDA_TRY(cudaMemcpyAsync(host_out, ctx->counts_dev, sizeof(int32_t) * ctx->g.L * ctx->g.E,
                                  cudaMemcpyDeviceToHost, s));
@@ -702,7 +701,7 @@ int moe_read_counts(moe_ctx *ctx, int32_t *host_out, void *stream) {
 
 int moe_reset_counts(moe_ctx *ctx, void *stream) {
     if (int r = check_ctx(ctx)) return r;
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     MOE_CUDA_TRY(cudaMemsetAsync(ctx->counts_dev, 0, sizeof(int32_t) * ctx->g.L * ctx->g.E, (cudaStream_t)stream));
     return MOE_OK;
 }
@@ -724,7 +723,7 @@ int moe_get_rowmap(moe_ctx *ctx, int layer, int32_t *host_out) {
 int moe_read_rowmap_device(moe_ctx *ctx, int layer, int32_t *host_out, void *stream) {
     if (int r = check_layer(ctx, layer, true)) return r;
     if (!host_out) return set_error(MOE_EINVAL, "null output");
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     cudaStream_t s = (cudaStream_t)stream;
     MOE_CUDA_TRY(cudaMemcpyAsync(host_out, ctx->layers[layer].rowmap_dev, sizeof(int32_t) * ctx->g.E,
                                  cudaMemcpyDeviceToHost, s));
@@ -737,7 +736,7 @@ int moe_read_bank_row(moe_ctx *ctx, int layer, int bank, int row, uint8_t *host_
     Layer &L = ctx->layers[layer];
     int rows = bank == MOE_BANK_HOT ? L.n_hot : (bank == MOE_BANK_COLD ? L.n_cold : -1);
     if (row < 0 || row >= rows || !host_out) return set_error(MOE_EINVAL, "bank/row out of range");
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     cudaStream_t s = (cudaStream_t)stream;
     MOE_CUDA_TRY(cudaStreamSynchronize(s));
     if (bank == MOE_BANK_HOT) {
@@ -753,7 +752,7 @@ int moe_probe_link(moe_ctx *ctx, size_t bytes, int iters, double *gbps, double *
     if (int r = check_ctx(ctx)) return r;
     if (!gbps || bytes < (1 << 20) || iters < 1) return set_error(MOE_EINVAL, "bad probe arguments");
     bytes &= ~size_t(4095);
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     if (ctx->probe_bytes < bytes) {
         pinned_free(ctx->probe_host);
         dev_free(ctx->probe_dev);
@@ -797,7 +796,7 @@ int moe_probe_link(moe_ctx *ctx, size_t bytes, int iters, double *gbps, double *
 
 int moe_device_status(moe_ctx *ctx, int32_t *status) {
     if (int r = check_ctx(ctx)) return r;
-    DeviceGuard guard(ctx->device);
+    MOE_ON_DEVICE(ctx->device);
     int32_t v[4] = {0, 0, 0, 0};
     MOE_CUDA_TRY(cudaDeviceSynchronize());
     MOE_CUDA_TRY(cudaMemcpy(v, ctx->status_dev, sizeof v, cudaMemcpyDeviceToHost));

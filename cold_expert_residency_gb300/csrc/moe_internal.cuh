@@ -279,6 +279,12 @@ struct DeviceGuard {
         if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
     }
 };
+// An entry point's device switch: the context's device is current for the
+// rest of the enclosing function, or the function returns the failure.
+#define MOE_ON_DEVICE(dev)                                  \
+    moe::DeviceGuard moe_dev_guard_(dev);                    \
+    if (moe_dev_guard_.status() != cudaSuccess)              \
+    return moe::cuda_error(moe_dev_guard_.status(), "cudaSetDevice(context device)")
 #define MOE_CUDA_TRY(call)                                   \
     do {                                                     \
         cudaError_t e_ = (call);                             \
