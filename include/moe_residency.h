@@ -269,7 +269,10 @@ int moe_router_logits(moe_ctx *ctx, const uint16_t *x, const uint16_t *w_router,
  * token's k bf16 expert rows in fp32 with fma in the original k order and
  * cast once:  out[t][c] = bf16(fma(w[t][k-1], Y[t][k-1][c], ... fma(w[t][0],
  * Y[t][0][c], 0.0f))).  Y device bf16 [T][k][H], w device fp32 [T][k],
- * out device bf16 [T][H]. */
+ * out device bf16 [T][H], all caller-owned; Y and out 16-byte aligned.
+ * Takes no context: it runs on the calling thread's current device, which
+ * must hold the three buffers.  1 <= k <= 16, H % 8 == 0; T == 0 is a no-op.
+ * MOE_EINVAL on a bad shape or a null or misaligned pointer. */
 int moe_finalize(const uint16_t *Y, const float *w, int T, int k, int H, uint16_t *out,
                  void *stream);
 
