@@ -8,6 +8,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <sys/mman.h>
 #include <thread>
 #include <unordered_map>
@@ -81,21 +82,26 @@ static void pinned_free(void *p) {
     cudaFreeHost(p);
 }
 
-// Run f(i) for i in [0, n) on up to `threads` host threads.
+// Run f(i) for i in [0, n) on up to 32 host threads, the calling one
+// included.  If a thread cannot be started, the ones that did (and the
+// caller) take its share: nothing throws out of here.
 template <class F>
 static void parallel_for(int n, F f) {
     int threads = (int)std::max(1u, std::min(32u, std::thread::hardware_concurrency()));
     threads = std::min(threads, n);
-    if (threads <= 1) {
-        for (int i = 0; i < n; ++i) f(i);
-        return;
-    }
     std::atomic<int> next{0};
+    auto work = [&]() {
+        for (int i = next.fetch_add(1); i < n; i = next.fetch_add(1)) f(i);
+    };
     std::vector<std::thread> pool;
-    for (int t = 0; t < threads; ++t)
-        pool.emplace_back([&]() {
-            for (int i = next.fetch_add(1); i < n; i = next.fetch_add(1)) f(i);
-        });
+    for (int t = 1; t < threads; ++t) {
+        try {
+            pool.emplace_back(work);
+        } catch (...) {
+            break;
+        }
+    }
+    work();
     for (auto &th : pool) th.join();
 }
 
@@ -261,10 +267,16 @@ int moe_create(const moe_geom *geom, int device, moe_ctx **out) {
     MOE_CUDA_TRY(cudaGetDeviceCount(&ndev));
     if (device < 0 || device >= ndev) return set_error(MOE_EINVAL, "no such CUDA device");
     MOE_ON_DEVICE(device);
-    moe_ctx *ctx = new moe_ctx();
+    moe_ctx *ctx = new (std::nothrow) moe_ctx();
+    if (!ctx) return set_error(MOE_ENOMEM, "out of host memory");
     ctx->g = make_geom(g);
     ctx->device = device;
-    ctx->layers.resize(g.layers);
+    try {
+        ctx->layers.resize(g.layers);
+    } catch (const std::bad_alloc &) {
+        delete ctx;
+        return set_error(MOE_ENOMEM, "out of host memory");
+    }
     cudaDeviceProp prop;
     cudaError_t e = cudaGetDeviceProperties(&prop, device);
     if (e == cudaSuccess) ctx->sms = prop.multiProcessorCount;

@@ -49,8 +49,13 @@ int moe_policy_create(int experts, double read_every, double half_life, double h
     p->hysteresis = hysteresis;
     p->min_avg = min_avg;
     p->max_pairs = max_pairs;
-    p->last.assign(experts, 0u);
-    p->acc.assign(experts, 0.0);
+    try {
+        p->last.assign(experts, 0u);
+        p->acc.assign(experts, 0.0);
+    } catch (const std::bad_alloc &) {
+        delete p;
+        return set_error(MOE_ENOMEM, "out of host memory");
+    }
     if (counts_now)
         for (int e = 0; e < experts; ++e) p->last[e] = (uint32_t)counts_now[e];
     *out = p;
@@ -62,9 +67,8 @@ int moe_policy_destroy(moe_policy *p) {
     return MOE_OK;
 }
 
-int moe_policy_read(moe_policy *p, const int32_t *counts, const int32_t *row_map, int32_t *promote,
-                    int32_t *demote) {
-    if (!p || !counts || !row_map || !promote || !demote) return set_error(MOE_EINVAL, "null argument");
+static int policy_read(moe_policy *p, const int32_t *counts, const int32_t *row_map, int32_t *promote,
+                       int32_t *demote) {
     const int E = p->E;
     for (int e = 0; e < E; ++e) {
         const uint32_t now = (uint32_t)counts[e];
@@ -96,10 +100,8 @@ int moe_policy_read(moe_policy *p, const int32_t *counts, const int32_t *row_map
     return n;
 }
 
-int moe_plan_restore(int experts, const int32_t *row_map, const int32_t *target, int max_pairs,
-                     int32_t *promote, int32_t *demote) {
-    if (experts < 1 || !row_map || !target || max_pairs < 0 || ((!promote || !demote) && max_pairs > 0))
-        return set_error(MOE_EINVAL, "invalid argument");
+static int plan_restore(int experts, const int32_t *row_map, const int32_t *target, int max_pairs,
+                        int32_t *promote, int32_t *demote) {
     std::vector<int> in, out;       // experts to bring into HBM, experts to move out
     for (int e = 0; e < experts; ++e) {
         const bool hot = row_map[e] >= 0, want = target[e] >= 0;
@@ -113,6 +115,27 @@ int moe_plan_restore(int experts, const int32_t *row_map, const int32_t *target,
         demote[i] = out[i];
     }
     return n;
+}
+
+int moe_policy_read(moe_policy *p, const int32_t *counts, const int32_t *row_map, int32_t *promote,
+                    int32_t *demote) {
+    if (!p || !counts || !row_map || !promote || !demote) return set_error(MOE_EINVAL, "null argument");
+    try {
+        return policy_read(p, counts, row_map, promote, demote);
+    } catch (const std::bad_alloc &) {
+        return set_error(MOE_ENOMEM, "out of host memory");
+    }
+}
+
+int moe_plan_restore(int experts, const int32_t *row_map, const int32_t *target, int max_pairs,
+                     int32_t *promote, int32_t *demote) {
+    if (experts < 1 || !row_map || !target || max_pairs < 0 || ((!promote || !demote) && max_pairs > 0))
+        return set_error(MOE_EINVAL, "invalid argument");
+    try {
+        return plan_restore(experts, row_map, target, max_pairs, promote, demote);
+    } catch (const std::bad_alloc &) {
+        return set_error(MOE_ENOMEM, "out of host memory");
+    }
 }
 
 }  // extern "C"

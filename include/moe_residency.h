@@ -19,8 +19,9 @@
  *    gives a message for the calling thread.  Nothing throws across the ABI.
  *  - "device" pointers are CUDA device (or mapped) addresses on the context's
  *    device; "host" pointers are ordinary CPU memory.  The caller owns every
- *    pointer it passes; the library owns the banks, row maps, usage table and
- *    swap staging row it allocates in moe_create / moe_init_banks.
+ *    pointer it passes; the library owns the banks, row maps, usage table,
+ *    swap staging rows and swap stream it allocates in moe_create /
+ *    moe_init_banks.
  *  - stream: a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  Calls marked "async" only enqueue work on it.
  *  - bf16 tensors are passed as uint16_t bit patterns.
@@ -96,14 +97,19 @@ int moe_pack_expert(int32_t hidden, int32_t inter, const uint8_t *w13_q, const u
                     const uint8_t *w2_q, const uint8_t *w2_s, uint8_t *out);
 
 /* Create a context on CUDA device `device`: validates the geometry and
- * allocates the [L x E] int32 usage table (zeroed) and one HBM staging row
- * for swaps.  *out receives the context. */
+ * allocates the [L x E] int32 usage table (zeroed), two HBM staging rows for
+ * swaps, and the swap stream with its events.  *out receives the context.
+ * MOE_EINVAL on a bad geometry (the rules above), a null argument or no such
+ * device; on a failed allocation the error of that call, with nothing left
+ * allocated. */
 int moe_create(const moe_geom *geom, int device, moe_ctx **out);
 
-/* Free everything the context allocated.  Synchronizes the device. */
+/* Free everything the context allocated (its banks included).  Synchronizes
+ * the device.  NULL is a no-op. */
 int moe_destroy(moe_ctx *ctx);
 
-/* Select the FFN kernel implementation (MOE_FFN_*) for later calls. */
+/* Select the FFN kernel implementation (MOE_FFN_*) for later calls.
+ * MOE_EINVAL for another value. */
 int moe_set_ffn_impl(moe_ctx *ctx, int impl);
 
 /* Activation format of the tensor-core FFN on prefill-sized steps (more
@@ -136,7 +142,8 @@ int moe_init_banks(moe_ctx *ctx, int layer, const uint8_t *w13_q, const uint8_t 
 
 /* Bytes of the caller-owned device workspace that serves every step of at
  * most T tokens (split lists, per-bank scratch for the FFN's intermediate
- * rows); non-decreasing in T. */
+ * rows); non-decreasing in T.  MOE_EINVAL unless 0 <= T <= T_max and bytes
+ * is non-null. */
 int moe_workspace_bytes(const moe_ctx *ctx, int T, size_t *bytes);
 
 /* Big-batch cold staging ("We Built the Counter", section 6: copying an
@@ -175,7 +182,10 @@ int moe_read_stage(moe_ctx *ctx, const void *ws, int T, int32_t *rows, void *str
  *   ws:     device workspace (moe_workspace_bytes) receiving both banks'
  *           pick lists grouped by (bank row, slot t*k+j).
  *   count_on: nonzero adds 1 per pick to usage[layer][id] when
- *           T <= count_tmax. */
+ *           T <= count_tmax.
+ * T == 0 writes empty lists.  MOE_EINVAL on a layer or T outside [0, T_max],
+ * a null pointer or a workspace not 256-byte aligned; MOE_ESTATE if the
+ * layer has no banks. */
 int moe_route_split_count(moe_ctx *ctx, int layer, const float *logits, int T, int count_on,
                           int32_t *ids, float *w, void *ws, void *stream);
 
@@ -200,7 +210,12 @@ int moe_read_split(moe_ctx *ctx, const void *ws, int T, int bank, int32_t *n_act
  *   runs out.  The rows equal those of the two one-bank calls bit for bit.
  *   Do not run a MOE_BANK_BOTH call concurrently with a one-bank call on the
  *   same workspace.
- *   x: device bf16 [T][H];  Y: device bf16 [T][k][H] out;  ws as routed. */
+ *   x: device bf16 [T][H];  Y: device bf16 [T][k][H] out (x and Y 16-byte
+ *   aligned);  ws as routed, 256-byte aligned.
+ * T == 0 is a no-op.  MOE_EINVAL on a bad bank, layer or T, a null or
+ * misaligned pointer; MOE_ESTATE if the layer has no banks.  A device wait
+ * that runs out (moe_set_wait_limit) is reported by moe_device_status as
+ * MOE_ETIMEOUT, not by this call's return value. */
 int moe_expert_ffn_bank(moe_ctx *ctx, int layer, int bank, const uint16_t *x, int T, void *ws,
                         uint16_t *Y, void *stream);
 
