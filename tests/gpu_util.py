@@ -52,6 +52,26 @@ def assert_rows_close_bf16(got_bits, ref_bits, what="", rel=REL_L2):
     return worst
 
 
+def tile_edge_slots(ids, widths):
+    """Slots s = t*k + j of the first and last pick of each token tile of
+    each expert: an expert's picks in slot order (the order of its bank
+    list), cut into tiles of each width in `widths` (the FFN's token tiles).
+    Rows at these slots exercise every (expert, token tile) unit of both
+    GEMMs and every tile's first and last token row."""
+    flat = np.asarray(ids).reshape(-1)
+    order = np.argsort(flat, kind="stable")          # grouped by expert, slot order within
+    e_sorted = flat[order]
+    starts = np.flatnonzero(np.r_[True, e_sorted[1:] != e_sorted[:-1]])
+    ends = np.r_[starts[1:], flat.size]
+    sel = set()
+    for a, b in zip(starts.tolist(), ends.tolist()):
+        for W in widths:
+            for t0 in range(a, b, W):
+                sel.add(int(order[t0]))
+                sel.add(int(order[min(t0 + W, b) - 1]))
+    return np.array(sorted(sel), np.int32)
+
+
 def bf16_ulp(v):
     """Spacing of bf16 numbers at |v| (8 significant bits)."""
     a = np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)

@@ -5,16 +5,18 @@
   output is bitwise equal to an all-HBM (unsplit) layer, the policy takes the
   oracle policy's decisions on the GPU's counts, and counts and row maps match
   the oracle's bookkeeping exactly;
-- 16-stream decode (112 tokens, the 256-wide token tile) on a split layer and
-  an all-HBM layer: routing/split bit-exact, sampled rows within tolerance;
+- 16-stream decode (112 tokens, 32-token tiles) on a split layer and an
+  all-HBM layer: routing/split bit-exact, every expert row within tolerance;
 - prefill (8192 tokens, the multi-kernel routing path, no counting): routing
-  and split bit-exact, sampled rows within tolerance."""
+  and split bit-exact; within tolerance, the first and last pick of every
+  token tile of every expert (so every (expert, tile) unit of both GEMMs and
+  every ragged tile end is checked)."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from gpu_util import Harness, assert_close_bf16
+from gpu_util import Harness, assert_close_bf16, assert_rows_close_bf16, tile_edge_slots
 
 torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -87,14 +89,13 @@ def test_adaptive_domain_shift_swaps_are_bit_identical():
         unsplit.close()
 
 
-def _sampled_rows(h, layer, lg, x, res, n_slots=18, seed=0):
-    cfg = h.cfg
-    T = lg.shape[0]
-    rng = np.random.default_rng(seed)
-    slots = np.sort(rng.choice(T * cfg.k, size=min(n_slots, T * cfg.k), replace=False)).astype(np.int32)
+def _rows(h, layer, x, res, slots):
+    """The GPU's expert rows of `slots` against the oracle's: within tolerance
+    over the rows together and in every row."""
     ref = oracle.rows_for_slots(h.weights[layer], res["ids"], x, slots)
-    got = res["Y"].reshape(-1, cfg.H)[slots]
-    assert_close_bf16(got, ref, f"layer {layer} sampled rows")
+    got = res["Y"].reshape(-1, h.cfg.H)[slots]
+    assert_close_bf16(got, ref, f"layer {layer}: {slots.size} rows")
+    assert_rows_close_bf16(got, ref, f"layer {layer}: {slots.size} rows")
 
 
 def test_decode16_split_and_hbm_layers():
@@ -108,7 +109,7 @@ def test_decode16_split_and_hbm_layers():
             ids_ref, w_ref = oracle.route(lg, cfg.k)
             assert np.array_equal(res["ids"], ids_ref)
             _check_split(h, layer, ids_ref, cfg.T)
-            _sampled_rows(h, layer, lg, x, res)
+            _rows(h, layer, x, res, np.arange(cfg.T * cfg.k, dtype=np.int32))    # every row
             assert np.array_equal(res["out"], oracle.finalize(res["Y"], res["w"]))
         counts = h.moe.moe_read_counts(h.ctx, 2, cfg.E)
         assert counts.sum(axis=1).tolist() == [cfg.T * cfg.k] * 2
@@ -128,7 +129,8 @@ def test_prefill_chunk_sampled():
         assert np.allclose(res["w"], w_ref, rtol=4e-7, atol=0)
         _check_split(h, 0, ids_ref, cfg.T)
         assert h.moe.moe_read_counts(h.ctx, 1, cfg.E).sum() == 0      # 8192 tokens > 256: not counted
-        _sampled_rows(h, 0, lg, x, res, n_slots=24)
+        # both formats' tile widths: two-piece rows 144 tokens, MXFP8 rows 160
+        _rows(h, 0, x, res, tile_edge_slots(res["ids"], (144, 160)))
         # finalize bit-exact on a slice of tokens
         assert np.array_equal(res["out"][:64], oracle.finalize(res["Y"][:64], res["w"][:64]))
     finally:
