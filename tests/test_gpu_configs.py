@@ -117,7 +117,7 @@ def test_decode16_split_and_hbm_layers():
         h.close()
 
 
-def test_prefill_chunk_sampled():
+def test_prefill_chunk_every_tile_end():
     cfg = synth.get_config("prefill")
     h = Harness(cfg)
     try:
