@@ -80,3 +80,31 @@ def test_prefill_tile_widths_match_the_library():
     two = int(re.search(r"constexpr int kPrefillTile = (\d+);", src).group(1))
     mx = int(re.search(r"constexpr int kPrefillTileMx = (\d+);", src).group(1))
     assert (bench.kPrefillTile, bench.kPrefillTileMx) == (two, mx)
+
+
+def test_bytes_roofline_on_a_hand_example():
+    # two steps of two layers; an expert of 1e9 bytes, HBM 1000 GB/s (1 ms per
+    # expert), link 100 GB/s (10 ms per expert)
+    dh = [[3, 2], [1, 0]]
+    dc = [[0, 1], [1, 0]]
+    r = bench.bytes_roofline(dh, dc, [40.0, 20.0], 1e9, 1000.0, 100.0)
+    # per layer-step: max(hot, cold) = 3, 10, 10, 0 ms; sums 3, 12, 11, 0 ms
+    assert abs(r["frac_max"] - 23.0 / 60.0) < 1e-12
+    assert abs(r["frac_sum"] - 26.0 / 60.0) < 1e-12
+    assert abs(r["t_roof_max_us"] - 11.5e3) < 1e-6 and abs(r["t_roof_sum_us"] - 13.0e3) < 1e-6
+    assert abs(r["t_step_us"] - 30.0e3) < 1e-6
+    assert r["distinct_hot"] == 3.0 and r["distinct_cold"] == 1.0
+    # the max form never exceeds the sum form
+    assert r["frac_max"] <= r["frac_sum"]
+
+
+def test_ffn_roofline_and_whole_job_rate():
+    import types
+    S = types.SimpleNamespace(hbm_peak=5000.0, peak_src="measured")
+    r = bench.ffn_roofline(S, "k", [10, 30], [2.0, 2.0], 1e8, traffic_per_expert=1.01e8)
+    # 20 experts of 0.1 GB in 2 ms: 1000 GB/s, 0.2 of the peak; traffic 20 x 1.01e8
+    assert abs(r["achieved"] - 1000.0) < 1e-9 and abs(r["frac"] - 0.2) < 1e-12
+    assert abs(r["traffic"] - 2.02e9) < 1e-3 and r["algorithmic_bytes"] == 2e9
+    assert bench.ffn_roofline(S, "k", [10], [1.0], 1e8)["traffic"] is None
+    # 2 ranks x 112 tokens x 10 steps over the slowest rank's 70 ms
+    assert abs(bench.job_tokens_per_s(2, 112, 10, 70.0) - 32000.0) < 1e-9
