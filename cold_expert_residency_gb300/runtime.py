@@ -3,13 +3,13 @@
 One layer-step ("vLLM: Pin Hot Experts", Results):
     [router GEMM                     (moe_router_logits, optional)]
     route + split + count            (moe_route_split_count, main stream)
-    hot-bank FFN   || cold-bank FFN  (moe_expert_ffn_bank on the main stream
-                                      and on a second stream, joined by events)
+    expert FFN over both banks       (moe_expert_ffn_bank with MOE_BANK_BOTH:
+                                      one launch per GEMM, main stream)
     finalize                         (moe_finalize, main stream)
 The hot bank streams HBM and the cold bank streams the host link, so the two
-run concurrently.  One call with MOE_BANK_BOTH (one launch per GEMM over both
-banks) and the two calls one after the other give bit-identical rows.
-PyTorch provides the device buffers and streams.
+run concurrently: inside the one call by default, or as two calls on two
+streams joined by events.  Both forms, and the two calls one after the other,
+give bit-identical rows.  PyTorch provides the device buffers and streams.
 """
 from __future__ import annotations
 
