@@ -296,13 +296,39 @@ def run_reference(args):
 
 # ------------------------------------------------------------- profiles
 
+def code_only(text):
+    """C++/CUDA source without its comments, all white space collapsed to
+    single blanks: what the compiler reads of it (string and character
+    literals are kept whole)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_sha():
-    """Hash of the FFN kernels' sources (a stored profile is used only while
-    they are unchanged)."""
+    """Hash of the FFN kernels' code, comments and layout aside (a stored
+    profile is used only while the code is unchanged)."""
     h = hashlib.sha256()
     for name in ("ffn_tc.cu", "ffn_tc_decode.cuh"):
-        with open(os.path.join(ROOT, "cold_expert_residency_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "cold_expert_residency_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -31,10 +31,13 @@
 //             HBM for the hot bank, over the host link from the mapped pinned
 //             host bank for the cold bank.  All into a ring of stages with one
 //             mbarrier each; one thread issues them.
-//   MMA       One thread: tcgen05.cp of the stage's scale atom into its
-//             tensor-memory scale slot, the group's MMAs (four K blocks, two
-//             for a half group), tcgen05.commit to free the stage; after a
-//             token tile's last group, a commit hands its accumulator over.
+//   MMA       One warp runs the loop and one elected lane issues: per landed
+//             stage, tcgen05.cp of its scale atom into the stage's
+//             tensor-memory scale slot, the group's MMAs (four K blocks per
+//             e4m3 piece, two for a half group), tcgen05.commit to free the
+//             stage; it goes on through every following stage that has
+//             landed too (one burst) before it waits again.  After a token
+//             tile's last group, a commit hands its accumulator over.
 //   epilogue  Four warps (thread m = accumulator row m): tcgen05.ld of D, the
 //             row's power of two undone, then SwiGLU (gate and up rows meet
 //             in lanes l and l^16) or the bf16 row.  Two accumulators, so a

@@ -108,3 +108,13 @@ def test_ffn_roofline_and_whole_job_rate():
     assert bench.ffn_roofline(S, "k", [10], [1.0], 1e8)["traffic"] is None
     # 2 ranks x 112 tokens x 10 steps over the slowest rank's 70 ms
     assert abs(bench.job_tokens_per_s(2, 112, 10, 70.0) - 32000.0) < 1e-9
+
+
+def test_profile_key_ignores_comments_but_not_code():
+    src = 'int f(int a) {  // the first\n  /* two\n lines */ return a + 1; }\nconst char *s = "x // y";\n'
+    same = '// a header\nint f(int a)\n{\n    return a + 1;  /* once */\n}\nconst char *s = "x // y";'
+    assert bench.code_only(src) == bench.code_only(same)
+    assert bench.code_only(src) != bench.code_only(src.replace("a + 1", "a + 2"))
+    # text inside a string literal is code, even when it looks like a comment
+    assert bench.code_only(src) != bench.code_only(src.replace('"x // y"', '"x // z"'))
+    assert bench.code_only("char c = '/'; // c\nint d;") == "char c = '/'; int d;"
