@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(TcCfg<NMAX, MX>::kThreads, 1)
     // slot free again).  ACCREADY / ACCFREE: accumulator handover.
     const int FULL = 0, DONE = S, ACCREADY = 2 * S, ACCFREE = ACCREADY + DB, UQFULL = ACCFREE + DB,
               UQEMPTY = UQFULL + kQ;
-    constexpr int kQueueReaders = 128 + 1;   // the epilogue warps and the MMA thread
+    constexpr int kQueueReaders = 128 + 1;   // the epilogue warps and the MMA warp's lane 0
     constexpr bool SUSP = false;             // one CTA per SM: plain polling
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

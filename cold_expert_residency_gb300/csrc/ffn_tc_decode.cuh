@@ -385,7 +385,9 @@ __global__ void __launch_bounds__(DecCfg<NMAX>::kThreads, DecCfg<NMAX>::kPerSm)
         }
         if (!ok && ci > 0) {
             // wait until the MMAs already issued have retired (bounded); the
-            // last chunk's commit covers every earlier MMA of this thread
+            // last chunk's commit covers every earlier MMA of the issuing
+            // lane (elect.sync over the converged warp elects the same lane
+            // each time)
             const uint32_t last = ci - 1;
             for (uint32_t t = 0; t < kWaitLimit; ++t)
                 if (ptx::mbar_try_wait(bar(ADONE + (last % NA)), (last / NA) & 1)) break;
